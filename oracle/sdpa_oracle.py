@@ -1,0 +1,182 @@
+"""fp64 CPU oracle of fused scaled-dot-product attention, forward and backward.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this module; the
+product path never does, and this module imports nothing from the product.
+
+What it computes is the equation block at the head of CK tile's
+``fmha_bwd_kernel.hpp`` (the comment that opens the file, S = Q K^T through
+dQ = dS K * scale), with the parameter set of PyTorch cudnn ``MHA.cpp``
+``run_cudnn_SDP_fprop`` / ``run_cudnn_SDP_bprop`` (fp32 softmax statistics of
+shape [b, h, s_q], BHSD tensors, optional bias, dropout by seed and offset).
+Every matrix is materialised; there is no tiling and no online softmax. Matrix
+products are numpy ``@`` in float64.
+
+Readings taken where the pages are silent (each is listed in the design doc):
+
+* The saved statistic is the natural-log logsumexp of the scaled, biased,
+  masked scores, taken before dropout: LSE_i = m_i + ln(sum_j exp(s_ij - m_i)).
+* Causal masking is top-left aligned: key j is visible to query i iff j <= i.
+* A row with no visible key (possible only through a -inf bias) has P = 0,
+  O = 0, LSE = -inf and contributes nothing to any gradient.
+* Dropout multiplies P by Z = keep / (1 - p) before the product with V; the
+  row sum and LSE are those of P before dropout. The keep bits come from
+  ``oracle.philox``.
+* D_i = sum_d dO_id * O_id uses the dropout-applied output O, which equals
+  sum_j P_ij Z_ij dP_ij; dS = P * (dP * Z - D) with dP = dO V^T.
+* dBias has shape [1, H, S_q, S_kv] and is the sum over the batch of dS.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import philox
+
+
+@dataclass(frozen=True)
+class Problem:
+    """Sizes and scalar parameters of one attention call (BHSD layout)."""
+
+    B: int
+    H: int
+    S_q: int
+    S_kv: int
+    D_qk: int
+    D_v: int
+    scale: float
+    is_causal: bool = False
+    dropout_p: float = 0.0
+    seed: int = 0
+    offset: int = 0
+
+
+def _f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor on the CPU
+        x = x.detach().to(dtype=__import__("torch").float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def scores(prob: Problem, q_h: np.ndarray, k_h: np.ndarray, bias_h, rows: np.ndarray,
+           cols: np.ndarray) -> np.ndarray:
+    """S'' = (Q K^T) * scale + Bias on the (rows, cols) block, -inf where masked.
+
+    CK tile fmha_bwd_kernel.hpp header: S = Q K^T, S' = S * Scale, S'' = S' + Bias.
+    """
+    s = prob.scale * (q_h[rows] @ k_h[cols].T)
+    if bias_h is not None:
+        s = s + bias_h[np.ix_(rows, cols)]
+    if prob.is_causal:
+        s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
+    return s
+
+
+def softmax_rows(s: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """P = softmax over each row of s, and LSE = ln(sum exp(s)) per row.
+
+    CK tile fmha_bwd_kernel.hpp header: P = Softmax(S''). Rows whose entries are
+    all -inf give P = 0 and LSE = -inf.
+    """
+    m = s.max(axis=1)
+    m0 = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - m0[:, None])
+    l = e.sum(axis=1)
+    alive = l > 0
+    p = np.where(alive[:, None], e / np.where(alive, l, 1.0)[:, None], 0.0)
+    lse = np.where(alive, m0 + np.log(np.where(alive, l, 1.0)), -np.inf)
+    return p, lse
+
+
+def dropout_scale(prob: Problem, b: int, h: int, rows: np.ndarray, cols: np.ndarray):
+    """Z = keep / (1 - p) on the (rows, cols) block, or 1.0 without dropout."""
+    if prob.dropout_p == 0.0:
+        return 1.0
+    keep = philox.keep_mask(prob.B, prob.H, prob.S_q, prob.S_kv, prob.dropout_p, prob.seed,
+                            prob.offset, b, h, rows)[:, cols]
+    return keep.astype(np.float64) / (1.0 - prob.dropout_p)
+
+
+def forward_head(prob: Problem, b: int, h: int, q, k, v, bias=None, rows=None):
+    """O and LSE of the (b, h) slice for the query rows ``rows`` (default: all).
+
+    q, k, v: [B, H, S, D] arrays; bias: [1, H, S_q, S_kv] or None.
+    Returns O [len(rows), D_v] and LSE [len(rows)].
+    """
+    rows = np.arange(prob.S_q) if rows is None else np.asarray(rows)
+    cols = np.arange(prob.S_kv)
+    q_h, k_h, v_h = _f64(q[b, h]), _f64(k[b, h]), _f64(v[b, h])
+    bias_h = None if bias is None else _f64(bias[0, h])
+    p, lse = softmax_rows(scores(prob, q_h, k_h, bias_h, rows, cols))
+    z = dropout_scale(prob, b, h, rows, cols)
+    return (p * z) @ v_h, lse
+
+
+def forward(prob: Problem, q, k, v, bias=None):
+    """O [B, H, S_q, D_v] and LSE [B, H, S_q] of the whole problem."""
+    o = np.zeros((prob.B, prob.H, prob.S_q, prob.D_v))
+    lse = np.zeros((prob.B, prob.H, prob.S_q))
+    for b in range(prob.B):
+        for h in range(prob.H):
+            o[b, h], lse[b, h] = forward_head(prob, b, h, q, k, v, bias)
+    return o, lse
+
+
+def backward_head(prob: Problem, b: int, h: int, q, k, v, do, bias=None, rows=None,
+                  cols=None, row_chunk=None):
+    """Gradients of the (b, h) slice.
+
+    Returns (dQ[rows], dK[cols], dV[cols], dS[rows][:, cols]) with rows / cols
+    defaulting to all queries / keys. dQ and dS on a query row need only that
+    row; dK and dV of a key sum over every query row, which is taken
+    ``row_chunk`` rows at a time when given (to bound memory at long sequence
+    lengths) and all at once otherwise.
+
+    CK tile fmha_bwd_kernel.hpp header: dV = P^T dO, dP = dO V^T,
+    D = rowsum(dO * O), dS = P * (dP - D), dK = dS^T Q * Scale,
+    dQ = dS K * Scale; dropout enters through Z as described in the module text.
+    """
+    all_rows = np.arange(prob.S_q)
+    all_cols = np.arange(prob.S_kv)
+    rows = all_rows if rows is None else np.asarray(rows)
+    cols = all_cols if cols is None else np.asarray(cols)
+    q_h, k_h, v_h, do_h = _f64(q[b, h]), _f64(k[b, h]), _f64(v[b, h]), _f64(do[b, h])
+    bias_h = None if bias is None else _f64(bias[0, h])
+
+    def grads_of_rows(rr, want_dq):
+        p, _ = softmax_rows(scores(prob, q_h, k_h, bias_h, rr, all_cols))
+        z = dropout_scale(prob, b, h, rr, all_cols)
+        pz = p * z
+        o = pz @ v_h
+        d = (do_h[rr] * o).sum(axis=1)
+        dp = do_h[rr] @ v_h.T
+        ds = p * (dp * z - d[:, None])
+        dq = prob.scale * (ds @ k_h) if want_dq else None
+        return pz, ds, dq
+
+    _, ds_rows, dq = grads_of_rows(rows, True)
+    ds_block = ds_rows[:, cols]
+
+    dk = np.zeros((len(cols), prob.D_qk))
+    dv = np.zeros((len(cols), prob.D_v))
+    step = prob.S_q if row_chunk is None else int(row_chunk)
+    for r0 in range(0, prob.S_q, step):
+        rr = all_rows[r0:r0 + step]
+        pz, ds, _ = grads_of_rows(rr, False)
+        dv += pz[:, cols].T @ do_h[rr]
+        dk += prob.scale * (ds[:, cols].T @ q_h[rr])
+    return dq, dk, dv, ds_block
+
+
+def backward(prob: Problem, q, k, v, do, bias=None):
+    """dQ, dK, dV [B, H, S, D] and dBias [1, H, S_q, S_kv] (None without bias)."""
+    dq = np.zeros((prob.B, prob.H, prob.S_q, prob.D_qk))
+    dk = np.zeros((prob.B, prob.H, prob.S_kv, prob.D_qk))
+    dv = np.zeros((prob.B, prob.H, prob.S_kv, prob.D_v))
+    dbias = None if bias is None else np.zeros((1, prob.H, prob.S_q, prob.S_kv))
+    for b in range(prob.B):
+        for h in range(prob.H):
+            dq[b, h], dk[b, h], dv[b, h], ds = backward_head(prob, b, h, q, k, v, do, bias)
+            if dbias is not None:
+                dbias[0, h] += ds
+    return dq, dk, dv, dbias
