@@ -1,0 +1,146 @@
+/*
+ * sdpa.h — C ABI of the GB300 fused scaled-dot-product attention library
+ * (libsdpa.so, sm_103a only).
+ *
+ * What is computed is the equation block that opens CK tile's
+ * fmha_bwd_kernel.hpp (page "Composable Kernel: fmha_bwd_kernel.hpp Source
+ * File", header comment):
+ *     S = Q K^T,  S' = S * scale,  S'' = S' + Bias,  P = softmax(S''),  O = P V
+ *     dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+ *     dBias = dS,  dK = dS^T Q * scale,  dQ = dS K * scale
+ * with the parameter set of PyTorch's cuDNN attention glue
+ * (page "aten/src/ATen/native/cudnn/MHA.cpp", run_cudnn_SDP_fprop and
+ * run_cudnn_SDP_bprop): b, h, s_q, s_kv, d_qk, d_v, a scale passed by value,
+ * a causal flag, a dropout probability with seed and offset, an optional
+ * bias, and an fp32 per-row softmax statistic of shape [b, h, s_q].
+ *
+ * Conventions shared by every entry point
+ *   Layout      Contiguous BHSD: Q [b,h,s_q,d_qk], K [b,h,s_kv,d_qk],
+ *               V [b,h,s_kv,d_v], O and dO [b,h,s_q,d_v], LSE [b,h,s_q] fp32,
+ *               Bias and dBias [1,h,s_q,s_kv] fp32 (one bias shared by the
+ *               batch; dBias is the sum over the batch of dS).
+ *   Types       Q, K, V, O, dO, dQ, dK, dV are bf16 or fp16 (dtype argument);
+ *               accumulation and softmax are fp32.
+ *   Head sizes  (d_qk, d_v) in {(64,64), (128,128), (192,128)}.
+ *   Causal      Top-left: key j is visible to query i iff j <= i.
+ *   LSE         Natural-log logsumexp of the scaled, biased, masked scores
+ *               before dropout; -inf for a row that sees no key (its O row
+ *               is 0 and it adds nothing to any gradient).
+ *   Dropout     p in [0, 1); p == 0 disables it and seed/offset are ignored.
+ *               Element (b,h,i,j) has linear index L = ((b*h_n+h)*s_q+i)*s_kv+j;
+ *               its 32-bit draw r is word L%4 of Philox4x32-10 with key
+ *               (lo32 seed, hi32 seed) and counter (lo32 offset, hi32 offset,
+ *               lo32 L/4, hi32 L/4); it is kept iff r >= floor(p * 2^32), and
+ *               kept values of P are scaled by 1/(1-p). Needs s_kv % 4 == 0.
+ *   Pointers    Device pointers, 16-byte aligned, owned by the caller; the
+ *               library never allocates, frees or retains them.
+ *   Streams     `stream` is a cudaStream_t (NULL = legacy default stream).
+ *               Every call is asynchronous on that stream; nothing is
+ *               synchronised unless stated.
+ *   Errors      Every call returns a status and never throws or aborts.
+ *               Arguments are validated before any CUDA call; a rejected call
+ *               launches nothing. Zero-sized problems (any of b, h, s_q, s_kv
+ *               equal to 0) return SDPA_OK and launch nothing, as the cuDNN
+ *               glue does for 0-element tensors.
+ *   Devices     The current CUDA device must be a compute capability 10.3
+ *               GPU (GB300); the library holds one 4-byte error word per
+ *               device in its static device memory.
+ */
+#ifndef SDPA_H_
+#define SDPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, p outside [0,1) */
+  SDPA_ERR_UNSUPPORTED = 2,   /* head sizes, dtype, or dropout with s_kv % 4 != 0 */
+  SDPA_ERR_MISALIGNED = 3,    /* a pointer that is not 16-byte aligned */
+  SDPA_ERR_WORKSPACE = 4,     /* workspace null or smaller than sdpa_bwd_workspace_size */
+  SDPA_ERR_CUDA = 5,          /* a CUDA runtime / driver call failed */
+  SDPA_ERR_DEVICE_TIMEOUT = 6 /* a kernel gave up waiting (see sdpa_device_error) */
+} sdpa_status_t;
+
+typedef enum { SDPA_BF16 = 0, SDPA_FP16 = 1 } sdpa_dtype_t;
+
+/*
+ * Forward pass (the S .. O lines of the CK header equations; output set of
+ * run_cudnn_SDP_fprop with the softmax statistics requested).
+ *   q, k, v   inputs (dtype), BHSD.
+ *   bias      optional fp32 [1,h,s_q,s_kv] added after scaling; NULL for none.
+ *   o         output [b,h,s_q,d_v] (dtype), O = (P * Z) V with Z the dropout
+ *             factor (1 without dropout).
+ *   lse       output fp32 [b,h,s_q].
+ */
+sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
+                       int64_t d_v, float scale, int is_causal, float dropout_p, uint64_t seed,
+                       uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
+                       const void* v, const float* bias, void* o, float* lse, void* stream);
+
+/*
+ * Bytes of device workspace sdpa_bwd needs: D (fp32 [b,h,s_q]) followed, at
+ * the next 256-byte boundary, by the fp32 dQ accumulator [b,h,s_q,d_qk]
+ * (the f32 scratchpad of oneDNN's sdpa micro.cpp and the dq_acc buffer of the
+ * CK page play the same role). Returns 0 for invalid sizes.
+ */
+size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
+                               int64_t d_v);
+
+/*
+ * Backward pass (the dV .. dQ lines of the CK header equations; argument set
+ * of run_cudnn_SDP_bprop plus the bias gradient).
+ *   o, lse    the forward outputs for the same inputs and parameters.
+ *   dout      upstream gradient dO [b,h,s_q,d_v] (dtype).
+ *   dq, dk, dv  outputs (dtype), shapes of q, k, v.
+ *   dbias     fp32 [1,h,s_q,s_kv] output (overwritten with sum_b dS); must be
+ *             non-NULL iff bias is non-NULL.
+ *   workspace caller-owned device memory of at least
+ *             sdpa_bwd_workspace_size(...) bytes, 256-byte aligned; its
+ *             contents on entry are ignored and on exit are unspecified.
+ * Runs three kernels on `stream`: preprocess (D, zero dQ_acc and dBias), the
+ * fused dQ/dK/dV/dBias kernel, and the dQ convert. dQ is accumulated with
+ * fp32 additions whose order varies from run to run (not bitwise
+ * deterministic); dK, dV and, for b <= 2, dBias are deterministic.
+ */
+sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
+                       int64_t d_v, float scale, int is_causal, float dropout_p, uint64_t seed,
+                       uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
+                       const void* v, const float* bias, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, float* dbias,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Test hook: the packed dropout keep bits of a whole problem, drawn by the
+ * same device Philox function the fused kernels use. Bit (L % 32) of word
+ * bits[L / 32] is element L's keep flag (L as in "Dropout" above); bits past
+ * the last element of the final word are 0. bits must hold
+ * ceil(b*h*s_q*s_kv / 32) words. p == 0 gives all ones.
+ */
+sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, float dropout_p,
+                                uint64_t seed, uint64_t offset, uint32_t* bits, void* stream);
+
+/*
+ * Reads the current device's error word (synchronising the device) and, when
+ * `clear` is non-zero, resets it. A non-zero word means a kernel's bounded
+ * wait ran out: the kernel recorded which role gave up (bit mask), released
+ * its resources and returned without completing its outputs. Returns
+ * SDPA_ERR_DEVICE_TIMEOUT when the word is non-zero, SDPA_OK otherwise.
+ */
+sdpa_status_t sdpa_device_error(uint32_t* word, int clear);
+
+/* Static, human-readable name of a status code. */
+const char* sdpa_status_string(sdpa_status_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int sdpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_H_ */

@@ -1,0 +1,10 @@
+"""GB300-native fused scaled-dot-product attention (forward and backward).
+
+The compute path is libsdpa.so (hand-written sm_103a CUDA behind the C ABI in
+include/sdpa.h); this package is its PyTorch binding.
+"""
+from .api import (sdpa_bwd, sdpa_bwd_workspace_size, sdpa_device_error, sdpa_dropout_mask,
+                  sdpa_fwd, sdpa_status_string)
+
+__all__ = ["sdpa_fwd", "sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_dropout_mask",
+           "sdpa_device_error", "sdpa_status_string"]

@@ -1,0 +1,126 @@
+"""PyTorch-facing binding of the C ABI (same names as include/sdpa.h).
+
+PyTorch provides device memory and the stream; every step of the attention
+computation runs in libsdpa.so's kernels. The functions here only check
+tensor properties, allocate outputs with torch and pass raw pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _native
+
+_DTYPE_CODE = {torch.bfloat16: _native.SDPA_BF16, torch.float16: _native.SDPA_FP16}
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check_io(name: str, t: torch.Tensor, shape, dtype) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (BHSD)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0,
+             bias=None, out=None, lse=None, stream=None):
+    """Forward pass. Returns (o [b,h,s_q,d_v], lse fp32 [b,h,s_q])."""
+    b, h, s_q, d_qk = q.shape
+    s_kv, d_v = k.shape[2], v.shape[3]
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("q, k, v must be bf16 or fp16")
+    _check_io("q", q, (b, h, s_q, d_qk), dt)
+    _check_io("k", k, (b, h, s_kv, d_qk), dt)
+    _check_io("v", v, (b, h, s_kv, d_v), dt)
+    if bias is not None:
+        _check_io("bias", bias, (1, h, s_q, s_kv), torch.float32)
+    scale = 1.0 / math.sqrt(d_qk) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((b, h, s_q, d_v), dtype=dt, device=q.device)
+    if lse is None:
+        lse = torch.empty((b, h, s_q), dtype=torch.float32, device=q.device)
+    _check_io("out", out, (b, h, s_q, d_v), dt)
+    _check_io("lse", lse, (b, h, s_q), torch.float32)
+    st = _native.lib().sdpa_fwd(b, h, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
+                                float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse),
+                                ctypes.c_void_p(_stream_ptr(stream)))
+    _native.check(st, "sdpa_fwd")
+    return out, lse
+
+
+def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v) -> int:
+    return int(_native.lib().sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v))
+
+
+def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
+             offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None, dbias=None,
+             stream=None):
+    """Backward pass. Returns (dq, dk, dv, dbias or None)."""
+    b, h, s_q, d_qk = q.shape
+    s_kv, d_v = k.shape[2], v.shape[3]
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("q, k, v must be bf16 or fp16")
+    for name, t, shp in (("q", q, (b, h, s_q, d_qk)), ("k", k, (b, h, s_kv, d_qk)),
+                         ("v", v, (b, h, s_kv, d_v)), ("o", o, (b, h, s_q, d_v)),
+                         ("dout", dout, (b, h, s_q, d_v))):
+        _check_io(name, t, shp, dt)
+    _check_io("lse", lse, (b, h, s_q), torch.float32)
+    if bias is not None:
+        _check_io("bias", bias, (1, h, s_q, s_kv), torch.float32)
+    scale = 1.0 / math.sqrt(d_qk) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if bias is not None and dbias is None:
+        dbias = torch.empty_like(bias)
+    need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = _native.lib().sdpa_bwd(b, h, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
+                                float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o), _ptr(dout),
+                                _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+                                _ptr(workspace), workspace.numel(),
+                                ctypes.c_void_p(_stream_ptr(stream)))
+    _native.check(st, "sdpa_bwd")
+    return dq, dk, dv, dbias
+
+
+def sdpa_dropout_mask(b, h, s_q, s_kv, dropout_p, seed, offset, device="cuda", stream=None):
+    """Packed keep bits as an int32 tensor of ceil(b*h*s_q*s_kv/32) words."""
+    words = (b * h * s_q * s_kv + 31) // 32
+    bits = torch.empty(max(words, 1), dtype=torch.int32, device=device)
+    st = _native.lib().sdpa_dropout_mask(b, h, s_q, s_kv, float(dropout_p), int(seed), int(offset),
+                                         _ptr(bits), ctypes.c_void_p(_stream_ptr(stream)))
+    _native.check(st, "sdpa_dropout_mask")
+    return bits[:words]
+
+
+def sdpa_device_error(clear: bool = True) -> int:
+    """The device error word (synchronises); 0 when every kernel completed."""
+    w = ctypes.c_uint32(0)
+    st = _native.lib().sdpa_device_error(ctypes.byref(w), int(bool(clear)))
+    if st not in (_native.SDPA_OK, _native.SDPA_ERR_DEVICE_TIMEOUT):
+        _native.check(st, "sdpa_device_error")
+    return int(w.value)
+
+
+def sdpa_status_string(status: int) -> str:
+    return _native.status_string(status)

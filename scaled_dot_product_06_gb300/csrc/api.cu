@@ -1,0 +1,272 @@
+// C ABI of libsdpa.so: argument validation, TMA descriptor encoding and kernel
+// launches. Mirrors the parameter set of PyTorch cudnn MHA.cpp
+// run_cudnn_SDP_fprop / run_cudnn_SDP_bprop (sizes, scale by value, causal
+// flag, dropout probability with seed and offset, optional bias, fp32 softmax
+// statistics) with plain pointers and a status return instead of exceptions,
+// the way oneDNN's sdpa micro.cpp reports failures through status codes.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/sdpa.h"
+#include "common.cuh"
+
+namespace {
+
+using namespace sdpa;
+
+// One error word per device, in this library's static device memory.
+__device__ uint32_t g_sdpa_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+sdpa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
+
+// Device-side error word of the current device (looked up once per device).
+sdpa_status_t error_word_ptr(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_err_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_sdpa_error_word) != cudaSuccess) return SDPA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<uint32_t*>(ptr);
+  }
+  *out = g_err_ptr[dev];
+  return SDPA_OK;
+}
+
+sdpa_status_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        fn == nullptr || q != cudaDriverEntryPointSuccess)
+      return SDPA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = g_encode;
+  return SDPA_OK;
+}
+
+// 3-D map over a [outer][rows][inner] tensor, box {64, box_rows, 1}.
+sdpa_status_t make_map(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* ptr,
+                       int64_t inner, int64_t rows, int64_t outer, uint32_t box_rows, bool swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (sdpa_status_t s = encoder(&enc)) return s;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * elem_bytes),
+                           static_cast<cuuint64_t>(inner * rows * elem_bytes)};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, type, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_sizes_ok(int64_t d_qk, int64_t d_v) {
+  return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128);
+}
+
+constexpr int64_t kMaxSeq = (int64_t{1} << 31) - 256;
+
+// Checks shared by fwd and bwd that need no pointer. Sets *empty for a
+// zero-sized problem.
+sdpa_status_t check_sizes(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
+                          float dropout_p, int dtype, bool* empty) {
+  if (b < 0 || h < 0 || s_q < 0 || s_kv < 0 || d_qk < 0 || d_v < 0) return SDPA_ERR_INVALID_ARG;
+  if (!(dropout_p >= 0.0f && dropout_p < 1.0f)) return SDPA_ERR_INVALID_ARG;
+  if (dtype != SDPA_BF16 && dtype != SDPA_FP16) return SDPA_ERR_UNSUPPORTED;
+  if (!head_sizes_ok(d_qk, d_v)) return SDPA_ERR_UNSUPPORTED;
+  if (s_q > kMaxSeq || s_kv > kMaxSeq || b * h > (int64_t{1} << 24)) return SDPA_ERR_UNSUPPORTED;
+  if (dropout_p > 0.0f && (s_kv % 4) != 0) return SDPA_ERR_UNSUPPORTED;
+  *empty = (b == 0 || h == 0 || s_q == 0 || s_kv == 0);
+  return SDPA_OK;
+}
+
+uint32_t drop_threshold(float p) {
+  return static_cast<uint32_t>(std::floor(static_cast<double>(p) * 4294967296.0));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sdpa_status_string(sdpa_status_t s) {
+  switch (s) {
+    case SDPA_OK: return "SDPA_OK";
+    case SDPA_ERR_INVALID_ARG: return "SDPA_ERR_INVALID_ARG: invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED: unsupported configuration";
+    case SDPA_ERR_MISALIGNED: return "SDPA_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case SDPA_ERR_WORKSPACE: return "SDPA_ERR_WORKSPACE: workspace missing or too small";
+    case SDPA_ERR_CUDA: return "SDPA_ERR_CUDA: CUDA call failed";
+    case SDPA_ERR_DEVICE_TIMEOUT: return "SDPA_ERR_DEVICE_TIMEOUT: a kernel wait ran out";
+  }
+  return "unknown sdpa status";
+}
+
+int sdpa_version(void) { return 10000; }
+
+sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
+                       float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
+                       sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
+                       const float* bias, void* o, float* lse, void* stream) {
+  bool empty = false;
+  if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (empty) return SDPA_OK;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (bias && !aligned16(bias)))
+    return SDPA_ERR_MISALIGNED;
+
+  const bool bf16 = dtype == SDPA_BF16;
+  const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv;
+  if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
+
+  FwdParams p{};
+  p.B = static_cast<int>(b);
+  p.H = static_cast<int>(h);
+  p.S_q = static_cast<int>(s_q);
+  p.S_kv = static_cast<int>(s_kv);
+  p.scale_log2 = scale * kLog2e;
+  p.causal = is_causal ? 1 : 0;
+  p.bias = bias;
+  p.dropout = dropout_p > 0.0f ? 1 : 0;
+  p.drop_threshold = drop_threshold(dropout_p);
+  p.keep_scale = 1.0f / (1.0f - dropout_p);
+  p.seed_lo = static_cast<uint32_t>(seed);
+  p.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.offset_lo = static_cast<uint32_t>(offset);
+  p.offset_hi = static_cast<uint32_t>(offset >> 32);
+  p.o = o;
+  p.lse = lse;
+  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = bf16 ? launch_fwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st)
+                             : launch_fwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st);
+  return cuda_status(e);
+}
+
+size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
+                               int64_t d_v) {
+  bool empty = false;
+  if (check_sizes(b, h, s_q, s_kv, d_qk, d_v, 0.0f, SDPA_BF16, &empty) != SDPA_OK) return 0;
+  const size_t rows = static_cast<size_t>(b) * h * s_q;
+  const size_t d_bytes = (rows * sizeof(float) + 255) & ~size_t(255);
+  return d_bytes + rows * static_cast<size_t>(d_qk) * sizeof(float);
+}
+
+sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
+                       float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
+                       sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
+                       const float* bias, const void* o, const void* dout, const float* lse,
+                       void* dq, void* dk, void* dv, float* dbias, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  bool empty = false;
+  if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (empty) return SDPA_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
+  if ((bias == nullptr) != (dbias == nullptr)) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (bias && !aligned16(bias)) || (dbias && !aligned16(dbias)))
+    return SDPA_ERR_MISALIGNED;
+  const size_t need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v);
+  if (workspace == nullptr || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SDPA_ERR_MISALIGNED;
+
+  const bool bf16 = dtype == SDPA_BF16;
+  const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const size_t rows = static_cast<size_t>(b) * h * s_q;
+  float* delta = static_cast<float*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           ((rows * sizeof(float) + 255) & ~size_t(255)));
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 64, true)) return s;
+  if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, 64, true)) return s;
+  if (sdpa_status_t s = make_map(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, d_qk, s_q, b * h, 64,
+                                 false))
+    return s;
+
+  BwdParams p{};
+  p.B = static_cast<int>(b);
+  p.H = static_cast<int>(h);
+  p.S_q = static_cast<int>(s_q);
+  p.S_kv = static_cast<int>(s_kv);
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = is_causal ? 1 : 0;
+  p.bias = bias;
+  p.dbias = dbias;
+  p.dropout = dropout_p > 0.0f ? 1 : 0;
+  p.drop_threshold = drop_threshold(dropout_p);
+  p.keep_scale = 1.0f / (1.0f - dropout_p);
+  p.seed_lo = static_cast<uint32_t>(seed);
+  p.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.offset_lo = static_cast<uint32_t>(offset);
+  p.offset_hi = static_cast<uint32_t>(offset >> 32);
+  p.lse = lse;
+  p.delta = delta;
+  p.dq_acc = dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
+  cudaError_t e = launch_bwd_pre(bf16, o, dout, delta, dq_acc, dbias, static_cast<int64_t>(rows),
+                                 static_cast<int>(d_v), static_cast<int64_t>(rows) * d_qk, dbias_elems, st);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  e = bf16 ? launch_bwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st)
+           : launch_bwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  e = launch_dq_convert(bf16, dq_acc, dq, scale, static_cast<int64_t>(rows) * d_qk, st);
+  return cuda_status(e);
+}
+
+sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, float dropout_p,
+                                uint64_t seed, uint64_t offset, uint32_t* bits, void* stream) {
+  if (b < 0 || h < 0 || s_q < 0 || s_kv < 0) return SDPA_ERR_INVALID_ARG;
+  if (!(dropout_p >= 0.0f && dropout_p < 1.0f)) return SDPA_ERR_INVALID_ARG;
+  const int64_t total = b * h * s_q * s_kv;
+  if (total == 0) return SDPA_OK;
+  if (bits == nullptr) return SDPA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(bits) & 3u) != 0) return SDPA_ERR_MISALIGNED;
+  return cuda_status(launch_dropout_mask(total, drop_threshold(dropout_p), static_cast<uint32_t>(seed),
+                                         static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(offset),
+                                         static_cast<uint32_t>(offset >> 32), bits,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+sdpa_status_t sdpa_device_error(uint32_t* word, int clear) {
+  uint32_t* dev_word = nullptr;
+  if (sdpa_status_t s = error_word_ptr(&dev_word)) return s;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SDPA_ERR_CUDA;
+  uint32_t host = 0;
+  if (cudaMemcpy(&host, dev_word, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (clear && host != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(dev_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SDPA_ERR_CUDA;
+  }
+  if (word) *word = host;
+  return host ? SDPA_ERR_DEVICE_TIMEOUT : SDPA_OK;
+}
+
+}  // extern "C"

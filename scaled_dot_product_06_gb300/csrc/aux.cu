@@ -1,0 +1,134 @@
+// Memory-bound helper kernels of the backward pass and the dropout-mask hook.
+//
+// * bwd_pre: D = rowsum(dO * O) in fp32 (CK tile fmha_bwd_kernel.hpp,
+//   FmhaBwdOGradDotOKernel; the D line of the header equations), and zeroing
+//   of the fp32 dQ accumulator and of dBias, which the main kernel
+//   accumulates into (oneDNN sdpa micro.cpp, execute_backward: preprocess and
+//   fill of the f32 intermediates).
+// * dq_convert: dQ = scale * dQ_acc rounded to the io dtype (CK tile
+//   FmhaBwdConvertQGradKernel; oneDNN postprocess).
+// * dropout_mask: the packed keep bits of the whole problem, drawn by the same
+//   device Philox function the fused kernels use (oneDNN's dropout mask output
+//   and CK's stored random values serve the same purpose).
+#include "common.cuh"
+
+namespace sdpa {
+
+constexpr int kAuxThreads = 256;
+
+static int aux_grid(int64_t work_items) {
+  int64_t g = (work_items + kAuxThreads - 1) / kAuxThreads;
+  const int64_t cap = 152 * 16;  // a few waves over 152 SMs, grid-stride beyond
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+// One group of DV/8 consecutive threads per row; each thread takes 8 elements.
+template <bool BF16>
+__global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __restrict__ o,
+                                                              const uint4* __restrict__ dout,
+                                                              float* __restrict__ delta,
+                                                              float4* __restrict__ dq_acc,
+                                                              float4* __restrict__ dbias,
+                                                              int64_t rows, int d_v,
+                                                              int64_t dq_vec, int64_t dbias_elems) {
+  const int group = d_v / 8;  // 8 or 16 threads per row (power of two)
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31, sub = lane % group;
+  const int64_t rows_per_warp = 32 / group;
+  const int64_t warp_id = tid / 32, nwarps = nthreads / 32;
+  // wbase is uniform across the warp, so every lane reaches every shuffle
+  for (int64_t wbase = warp_id * rows_per_warp; wbase < rows; wbase += nwarps * rows_per_warp) {
+    const int64_t row = wbase + lane / group;
+    const bool live = row < rows;
+    float acc = 0.f;
+    if (live) {
+      const uint4 a = o[row * group + sub];
+      const uint4 c = dout[row * group + sub];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack2<BF16>(aw[e]), y = unpack2<BF16>(cw[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+    for (int off = group / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, group);
+    if (live && sub == 0) delta[row] = acc;
+  }
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = tid; i < dq_vec; i += nthreads) dq_acc[i] = z;
+  const int64_t dbias_vec = dbias_elems / 4;
+  for (int64_t i = tid; i < dbias_vec; i += nthreads) dbias[i] = z;
+  if (tid < (dbias_elems & 3)) reinterpret_cast<float*>(dbias)[dbias_vec * 4 + tid] = 0.f;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const float4* __restrict__ acc,
+                                                                 uint4* __restrict__ dq, float scale,
+                                                                 int64_t n8) {
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += nthreads) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    dq[i] = make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
+                       pack2<BF16>(b.x * scale, b.y * scale), pack2<BF16>(b.z * scale, b.w * scale));
+  }
+}
+
+// Word w holds the keep bits of elements 32w .. 32w+31 (bit e = element 32w+e).
+__global__ void __launch_bounds__(kAuxThreads) dropout_mask_kernel(int64_t total, uint32_t thr,
+                                                                   uint32_t seed_lo, uint32_t seed_hi,
+                                                                   uint32_t off_lo, uint32_t off_hi,
+                                                                   uint32_t* __restrict__ bits) {
+  const int64_t words = (total + 31) / 32;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < words; w += nthreads) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint64_t grp = static_cast<uint64_t>(w) * 8 + g;
+      const uint4 d = dropout_draws(grp, seed_lo, seed_hi, off_lo, off_hi);
+      const uint32_t k = static_cast<uint32_t>(d.x >= thr) | (static_cast<uint32_t>(d.y >= thr) << 1) |
+                         (static_cast<uint32_t>(d.z >= thr) << 2) | (static_cast<uint32_t>(d.w >= thr) << 3);
+      out |= k << (4 * g);
+    }
+    const int64_t valid = total - w * 32;
+    if (valid < 32) out &= (1u << valid) - 1u;
+    bits[w] = out;
+  }
+}
+
+cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta, float* dq_acc,
+                           float* dbias, int64_t rows, int d_v, int64_t dq_elems, int64_t dbias_elems,
+                           cudaStream_t st) {
+  const int group = d_v / 8;
+  const int64_t work = rows * group;
+  const int64_t zero_work = (dq_elems + dbias_elems) / 4;
+  const int grid = aux_grid(work > zero_work ? work : zero_work);
+  auto kern = bf16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
+  kern<<<grid, kAuxThreads, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta,
+                                      reinterpret_cast<float4*>(dq_acc), reinterpret_cast<float4*>(dbias),
+                                      rows, d_v, dq_elems / 4, dbias_elems);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(bool bf16, const float* dq_acc, void* dq, float scale, int64_t elems,
+                              cudaStream_t st) {
+  const int64_t n8 = elems / 8;
+  auto kern = bf16 ? dq_convert_kernel<true> : dq_convert_kernel<false>;
+  kern<<<aux_grid(n8), kAuxThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
+                                              static_cast<uint4*>(dq), scale, n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dropout_mask(int64_t total, uint32_t threshold, uint32_t seed_lo, uint32_t seed_hi,
+                                uint32_t off_lo, uint32_t off_hi, uint32_t* bits, cudaStream_t st) {
+  const int64_t words = (total + 31) / 32;
+  dropout_mask_kernel<<<aux_grid(words), kAuxThreads, 0, st>>>(total, threshold, seed_lo, seed_hi, off_lo,
+                                                                off_hi, bits);
+  return cudaGetLastError();
+}
+
+}  // namespace sdpa

@@ -1,0 +1,145 @@
+// Device helpers and launch parameters shared by the attention kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace sdpa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+#define SDPA_NEG_INF (-__int_as_float(0x7f800000))
+
+// Error-word site codes (bitwise OR of the sites whose wait ran out).
+enum : uint32_t {
+  kSiteFwdLoad = 1u << 0,
+  kSiteFwdMma = 1u << 1,
+  kSiteFwdSoftmax = 1u << 2,
+  kSiteBwdLoad = 1u << 4,
+  kSiteBwdMma = 1u << 5,
+  kSiteBwdCompute = 1u << 6,
+  kSiteBwdDq = 1u << 7,
+  kSiteDrain = 1u << 8,
+};
+
+struct FwdParams {
+  int B, H, S_q, S_kv;
+  float scale_log2;        // softmax scale * log2(e)
+  int causal;              // top-left: key j visible to query i iff j <= i
+  const float* bias;       // [1, H, S_q, S_kv] fp32 or null
+  int dropout;             // 0 / 1
+  uint32_t drop_threshold; // drop iff draw < threshold
+  float keep_scale;        // 1 / (1 - p)
+  uint32_t seed_lo, seed_hi, offset_lo, offset_hi;
+  void* o;                 // [B, H, S_q, D_v] io dtype
+  float* lse;              // [B, H, S_q] natural-log logsumexp
+  uint32_t* err;           // device error word
+};
+
+struct BwdParams {
+  int B, H, S_q, S_kv;
+  float scale;             // softmax scale
+  float scale_log2;        // scale * log2(e)
+  int causal;
+  const float* bias;       // [1, H, S_q, S_kv] or null
+  float* dbias;            // [1, H, S_q, S_kv] or null (accumulated with atomics)
+  int dropout;
+  uint32_t drop_threshold;
+  float keep_scale;
+  uint32_t seed_lo, seed_hi, offset_lo, offset_hi;
+  const float* lse;        // [B, H, S_q]
+  const float* delta;      // D = rowsum(dO * O)  [B, H, S_q]
+  float* dq_acc;           // [B, H, S_q, D_qk] fp32, zeroed before the main kernel
+  void* dk;                // [B, H, S_kv, D_qk]
+  void* dv;                // [B, H, S_kv, D_v]
+  uint32_t* err;
+};
+
+// ---------------------------------------------------------------- Philox4x32-10
+// Restated from Salmon et al., "Parallel random numbers: as easy as 1, 2, 3"
+// (SC'11): ten rounds of two 32x32->64 multiplies mixed into the counter,
+// with the key bumped by the two Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
+    const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// The four draws of linear-index group g (elements 4g .. 4g+3).
+__device__ __forceinline__ uint4 dropout_draws(uint64_t g, uint32_t seed_lo, uint32_t seed_hi,
+                                               uint32_t off_lo, uint32_t off_hi) {
+  return philox4x32_10(make_uint4(off_lo, off_hi, static_cast<uint32_t>(g),
+                                  static_cast<uint32_t>(g >> 32)),
+                       seed_lo, seed_hi);
+}
+
+// ---------------------------------------------------------------- arithmetic
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w);
+    return __bfloat1622float2(v);
+  } else {
+    __half2 v = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(v);
+  }
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// ---------------------------------------------------------------- launchers
+// Defined in the per-dtype kernel translation units; return a CUDA error
+// (cudaErrorInvalidValue for a head-size pair that has no kernel).
+cudaError_t launch_fwd_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const FwdParams& p, cudaStream_t st);
+cudaError_t launch_fwd_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const FwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
+                            const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
+                            const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta,
+                           float* dq_acc, float* dbias, int64_t rows, int d_v, int64_t dq_elems,
+                           int64_t dbias_elems, cudaStream_t st);
+cudaError_t launch_dq_convert(bool bf16, const float* dq_acc, void* dq, float scale,
+                              int64_t elems, cudaStream_t st);
+cudaError_t launch_dropout_mask(int64_t total, uint32_t threshold, uint32_t seed_lo,
+                                uint32_t seed_hi, uint32_t off_lo, uint32_t off_hi,
+                                uint32_t* bits, cudaStream_t st);
+
+}  // namespace sdpa

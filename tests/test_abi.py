@@ -1,0 +1,111 @@
+"""The C ABI loads, exports every function include/sdpa.h declares, and
+rejects bad arguments with the documented status before touching CUDA (so
+these run without a GPU: validation happens before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from scaled_dot_product_06_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_native.LIB_PATH):
+        from scaled_dot_product_06_gb300 import build
+        build.build()
+    return _native.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdpa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("sdpa_fwd", "sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_dropout_mask",
+                 "sdpa_device_error", "sdpa_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(_native.SIGNATURES), \
+        "binding signatures and header disagree"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert _native.status_string(code).startswith("SDPA_")
+    assert lib.sdpa_version() >= 10000
+
+
+NULL = None
+P = ctypes.c_void_p(1 << 20)        # a 16-byte aligned non-null value (never dereferenced)
+MIS = ctypes.c_void_p((1 << 20) + 8)
+
+
+def fwd(lib, b=1, h=1, sq=128, skv=128, dqk=64, dv=64, p=0.0, dtype=0, q=P, k=P, v=P, bias=NULL,
+        o=P, lse=P):
+    return lib.sdpa_fwd(b, h, sq, skv, dqk, dv, 0.125, 0, p, 0, 0, dtype, q, k, v, bias, o, lse,
+                        None)
+
+
+def test_fwd_argument_errors(lib):
+    assert fwd(lib, b=-1) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(lib, dqk=96, dv=96) == _native.SDPA_ERR_UNSUPPORTED
+    assert fwd(lib, dqk=128, dv=64) == _native.SDPA_ERR_UNSUPPORTED
+    assert fwd(lib, dtype=7) == _native.SDPA_ERR_UNSUPPORTED
+    assert fwd(lib, p=1.0) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(lib, p=-0.1) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(lib, p=float("nan")) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(lib, p=0.1, skv=130) == _native.SDPA_ERR_UNSUPPORTED
+    assert fwd(lib, q=NULL) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(lib, lse=NULL) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(lib, k=MIS) == _native.SDPA_ERR_MISALIGNED
+    assert fwd(lib, bias=MIS) == _native.SDPA_ERR_MISALIGNED
+    # zero-sized problems are a no-op even with null pointers
+    assert fwd(lib, sq=0, q=NULL, o=NULL, lse=NULL) == _native.SDPA_OK
+    assert fwd(lib, b=0, q=NULL) == _native.SDPA_OK
+
+
+def bwd(lib, b=1, h=1, sq=128, skv=128, dqk=64, dv=64, p=0.0, bias=NULL, dbias=NULL, ws=P,
+        ws_bytes=None, dout=P, q=P):
+    if ws_bytes is None:
+        ws_bytes = lib.sdpa_bwd_workspace_size(b, h, sq, skv, dqk, dv)
+    return lib.sdpa_bwd(b, h, sq, skv, dqk, dv, 0.125, 1, p, 0, 0, 0, q, P, P, bias, P, dout, P,
+                        P, P, P, dbias, ws, ws_bytes, None)
+
+
+def test_workspace_size(lib):
+    b, h, sq, dqk = 2, 3, 100, 128
+    rows = b * h * sq
+    want = ((rows * 4 + 255) // 256) * 256 + rows * dqk * 4
+    assert lib.sdpa_bwd_workspace_size(b, h, sq, 50, dqk, 128) == want
+    assert lib.sdpa_bwd_workspace_size(1, 1, 8, 8, 80, 80) == 0
+
+
+def test_bwd_argument_errors(lib):
+    assert bwd(lib, dout=NULL) == _native.SDPA_ERR_INVALID_ARG
+    assert bwd(lib, bias=P, dbias=NULL) == _native.SDPA_ERR_INVALID_ARG
+    assert bwd(lib, bias=NULL, dbias=P) == _native.SDPA_ERR_INVALID_ARG
+    assert bwd(lib, ws=NULL) == _native.SDPA_ERR_WORKSPACE
+    assert bwd(lib, ws_bytes=16) == _native.SDPA_ERR_WORKSPACE
+    assert bwd(lib, ws=ctypes.c_void_p((1 << 20) + 16)) == _native.SDPA_ERR_MISALIGNED
+    assert bwd(lib, q=MIS) == _native.SDPA_ERR_MISALIGNED
+    assert bwd(lib, dqk=192, dv=192) == _native.SDPA_ERR_UNSUPPORTED
+    assert bwd(lib, skv=0, q=NULL) == _native.SDPA_OK
+
+
+def test_dropout_mask_argument_errors(lib):
+    f = lib.sdpa_dropout_mask
+    assert f(1, 1, 4, 4, 1.5, 0, 0, P, None) == _native.SDPA_ERR_INVALID_ARG
+    assert f(1, 1, 4, 4, 0.5, 0, 0, NULL, None) == _native.SDPA_ERR_INVALID_ARG
+    assert f(0, 1, 4, 4, 0.5, 0, 0, NULL, None) == _native.SDPA_OK

@@ -1,0 +1,60 @@
+"""GPU parity against the fp64 oracle on whole small problems (every element).
+
+Sizes span several 128-row tiles and ragged tails; every feature alone and
+combined; bf16 and fp16; every supported head-size pair.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import philox
+from parity_util import Case, check_full
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # the small configuration: b1 h2 s128 d64, scale 1/8, no mask / bias / dropout
+    Case(1, 2, 128, 128, 64, 64, scale=0.125),
+    Case(2, 2, 256, 384, 64, 64),
+    Case(1, 2, 256, 256, 128, 128, causal=True),
+    Case(2, 1, 384, 384, 128, 128, causal=True, dtype="fp16"),
+    Case(1, 2, 256, 256, 192, 128, causal=True, bias=True),
+    Case(2, 2, 128, 256, 64, 64, dtype="fp16", p=0.1),
+    Case(2, 2, 256, 256, 128, 128, causal=True, bias=True, p=0.2),
+    # ragged tails and s_q != s_kv
+    Case(1, 1, 1, 1, 64, 64),
+    Case(1, 1, 17, 17, 64, 64, causal=True),
+    Case(1, 2, 100, 260, 128, 128, p=0.15),
+    Case(1, 1, 129, 257, 128, 128, causal=True, bias=True),
+    Case(2, 1, 257, 129, 192, 128, causal=True),
+    Case(1, 2, 200, 72, 64, 64, causal=True, bias=True, dtype="fp16"),
+    Case(1, 1, 300, 300, 192, 128, bias=True, p=0.3),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: (
+    f"b{c.B}h{c.H}q{c.S_q}k{c.S_kv}d{c.D_qk}-{c.D_v}-{c.dtype}"
+    f"{'-causal' if c.causal else ''}{'-bias' if c.bias else ''}{f'-p{c.p}' if c.p else ''}"))
+def test_fwd_bwd_match_oracle(case):
+    check_full(case)
+
+
+@pytest.mark.parametrize("shape,p,seed,offset", [
+    ((1, 2, 16, 32), 0.1, 0x1234, 0),
+    ((2, 3, 17, 20), 0.5, 7, 2**33 + 5),
+    ((1, 1, 1, 36), 0.9, 2**63 + 11, 123),
+])
+def test_dropout_mask_bit_exact(shape, p, seed, offset):
+    from scaled_dot_product_06_gb300 import sdpa_dropout_mask
+    B, H, S_q, S_kv = shape
+    got = sdpa_dropout_mask(B, H, S_q, S_kv, p, seed, offset).cpu().numpy().view(np.uint32)
+    ref = philox.packed_mask_words(B, H, S_q, S_kv, p, seed, offset)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_zero_sized_problem_is_noop():
+    from scaled_dot_product_06_gb300 import sdpa_fwd
+    q = torch.zeros(1, 1, 0, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16, device="cuda")
+    o, lse = sdpa_fwd(q, k, k)
+    assert o.shape == (1, 1, 0, 64) and lse.shape == (1, 1, 0)
