@@ -133,6 +133,11 @@ sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
  */
 sdpa_status_t sdpa_device_error(uint32_t* word, int clear);
 
+/* Detail of the calling thread's most recent failure (the step and, for
+ * SDPA_ERR_CUDA, the CUDA error string); "" if none. Valid until the thread's
+ * next call into the library. */
+const char* sdpa_last_error(void);
+
 /* Static, human-readable name of a status code. */
 const char* sdpa_status_string(sdpa_status_t status);
 

@@ -32,6 +32,7 @@ SIGNATURES = {
                         _sz, _ptr]),
     "sdpa_dropout_mask": (_int, [_i64, _i64, _i64, _i64, _f32, _u64, _u64, _ptr, _ptr]),
     "sdpa_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
+    "sdpa_last_error": (ctypes.c_char_p, []),
     "sdpa_status_string": (ctypes.c_char_p, [_int]),
     "sdpa_version": (_int, []),
 }
@@ -68,4 +69,5 @@ def status_string(status: int) -> str:
 
 def check(status: int, what: str) -> None:
     if status != SDPA_OK:
-        raise SdpaError(status, what)
+        detail = lib().sdpa_last_error().decode()
+        raise SdpaError(status, f"{what} ({detail})" if detail else what)

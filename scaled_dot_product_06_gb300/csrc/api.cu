@@ -5,6 +5,7 @@
 // statistics) with plain pointers and a status return instead of exceptions,
 // the way oneDNN's sdpa micro.cpp reports failures through status codes.
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -25,16 +26,30 @@ std::mutex g_mutex;
 uint32_t* g_err_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-sdpa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
+thread_local char g_last_error[256] = "";
+
+sdpa_status_t fail(sdpa_status_t s, const char* what, cudaError_t e = cudaSuccess) {
+  if (e != cudaSuccess)
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, cudaGetErrorString(e));
+  else
+    snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+  return s;
+}
+
+sdpa_status_t cuda_status(cudaError_t e, const char* what) {
+  return e == cudaSuccess ? SDPA_OK : fail(SDPA_ERR_CUDA, what, e);
+}
 
 // Device-side error word of the current device (looked up once per device).
 sdpa_status_t error_word_ptr(uint32_t** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDPA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(SDPA_ERR_CUDA, "cudaGetDevice");
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_err_ptr[dev] == nullptr) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_sdpa_error_word) != cudaSuccess) return SDPA_ERR_CUDA;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_sdpa_error_word);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "cudaGetSymbolAddress(error word)", e);
     g_err_ptr[dev] = static_cast<uint32_t*>(ptr);
   }
   *out = g_err_ptr[dev];
@@ -49,7 +64,7 @@ sdpa_status_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         fn == nullptr || q != cudaDriverEntryPointSuccess)
-      return SDPA_ERR_CUDA;
+      return fail(SDPA_ERR_CUDA, "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   *out = g_encode;
@@ -71,7 +86,12 @@ sdpa_status_t make_map(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes,
                    CU_TENSOR_MAP_INTERLEAVE_NONE,
                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_CUDA;
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (CUresult %d)",
+             static_cast<int>(r));
+    return SDPA_ERR_CUDA;
+  }
+  return SDPA_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -119,6 +139,8 @@ const char* sdpa_status_string(sdpa_status_t s) {
 
 int sdpa_version(void) { return 10000; }
 
+const char* sdpa_last_error(void) { return g_last_error; }
+
 sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
                        float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
                        sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
@@ -159,7 +181,7 @@ sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t e = bf16 ? launch_fwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st)
                              : launch_fwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st);
-  return cuda_status(e);
+  return cuda_status(e, "forward kernel launch");
 }
 
 size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
@@ -233,12 +255,12 @@ sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
   const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
   cudaError_t e = launch_bwd_pre(bf16, o, dout, delta, dq_acc, dbias, static_cast<int64_t>(rows),
                                  static_cast<int>(d_v), static_cast<int64_t>(rows) * d_qk, dbias_elems, st);
-  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
   e = bf16 ? launch_bwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st)
            : launch_bwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st);
-  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward main kernel launch", e);
   e = launch_dq_convert(bf16, dq_acc, dq, scale, static_cast<int64_t>(rows) * d_qk, st);
-  return cuda_status(e);
+  return cuda_status(e, "dQ convert launch");
 }
 
 sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, float dropout_p,
@@ -252,18 +274,22 @@ sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
   return cuda_status(launch_dropout_mask(total, drop_threshold(dropout_p), static_cast<uint32_t>(seed),
                                          static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(offset),
                                          static_cast<uint32_t>(offset >> 32), bits,
-                                         static_cast<cudaStream_t>(stream)));
+                                         static_cast<cudaStream_t>(stream)),
+                     "dropout mask launch");
 }
 
 sdpa_status_t sdpa_device_error(uint32_t* word, int clear) {
   uint32_t* dev_word = nullptr;
   if (sdpa_status_t s = error_word_ptr(&dev_word)) return s;
-  if (cudaDeviceSynchronize() != cudaSuccess) return SDPA_ERR_CUDA;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "cudaDeviceSynchronize", e);
   uint32_t host = 0;
-  if (cudaMemcpy(&host, dev_word, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return SDPA_ERR_CUDA;
+  e = cudaMemcpy(&host, dev_word, sizeof(host), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "reading the error word", e);
   if (clear && host != 0) {
     const uint32_t zero = 0;
-    if (cudaMemcpy(dev_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SDPA_ERR_CUDA;
+    e = cudaMemcpy(dev_word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "clearing the error word", e);
   }
   if (word) *word = host;
   return host ? SDPA_ERR_DEVICE_TIMEOUT : SDPA_OK;

@@ -96,7 +96,7 @@ __device__ __forceinline__ void bwd_keep_bits(uint64_t lin_tile, int S_kv, int t
 }
 
 template <int DQK, int DV, bool BF16>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(320, 1)
     sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
@@ -413,38 +413,39 @@ __global__ void __maxnreg__(200)
       mbar_arrive(bar(BB_P));
       if (!(ok = mbar_wait(bar(BB_DP), i & 1, ec, kSiteBwdCompute))) break;
       tc_fence_after();
-      float dp[64];
-      {
-        uint32_t a0[32], a1[32];
-        tmem_ld32(tbase + C::T_DP + lane_off, a0);
-        tmem_ld32(tbase + C::T_DP + lane_off + 32, a1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) dp[c] = __uint_as_float(a0[c]);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) dp[32 + c] = __uint_as_float(a1[c]);
-      }
       float* dbias_col =
           (p.dbias != nullptr && kv_ok) ? p.dbias + (static_cast<size_t>(h) * p.S_q + q0) * p.S_kv + kv
                                         : nullptr;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w[4];
+      for (int half = 0; half < 2; ++half) {
+        float dp[32];
+        {
+          uint32_t a0[32];
+          tmem_ld32(tbase + C::T_DP + lane_off + half * 32, a0);
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = ch * 8 + e * 2 + u;
-            const float z = ((km[c & 3] >> (c >> 2)) & 1u) ? zk : 0.f;
-            const float ds = pr[c] * fmaf(dp[c], z, -dd[c]);
-            if (dbias_col != nullptr && q0 + c < p.S_q)
-              atomicAdd(dbias_col + static_cast<size_t>(c) * p.S_kv, ds);
-            v2[u] = ds;
-          }
-          w[e] = pack2<BF16>(v2[0], v2[1]);
+          for (int c = 0; c < 32; ++c) dp[c] = __uint_as_float(a0[c]);
         }
-        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int chh = 0; chh < 4; ++chh) {
+          const int ch = half * 4 + chh;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int c = ch * 8 + e * 2 + u;
+              const float z = ((km[c & 3] >> (c >> 2)) & 1u) ? zk : 0.f;
+              const float ds = pr[c] * fmaf(dp[c - half * 32], z, -dd[c]);
+              if (dbias_col != nullptr && q0 + c < p.S_q)
+                atomicAdd(dbias_col + static_cast<size_t>(c) * p.S_kv, ds);
+              v2[u] = ds;
+            }
+            w[e] = pack2<BF16>(v2[0], v2[1]);
+          }
+          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
