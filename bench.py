@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Throughput of fused scaled-dot-product attention forward + backward on GB300.
+
+One step = sdpa_fwd + the three sdpa_bwd phases on one batch of synthetic,
+seeded inputs resident in HBM. The default workload is the long-context
+causal case: b1 h32 s16384 d128 bf16 (inputs of 537 MB, far larger than L2,
+so no flush is needed between steps).
+
+FLOP convention: forward = 4*b*h*s_q*s_kv*(d_qk+d_v)/2, halved for causal;
+backward = 2.5x forward; a step = 3.5x forward.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       python bench.py --impl reference ...   (the fp64 CPU oracle on a bounded sample)
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SDPA fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+
+WORKLOADS = {
+    "b1h2-s128-d64": dict(B=1, H=2, S_q=128, S_kv=128, D_qk=64, D_v=64, dtype="bf16",
+                          causal=False, bias=False, p=0.0, scale=0.125),
+    "b4h16-s2048-d128-causal": dict(B=4, H=16, S_q=2048, S_kv=2048, D_qk=128, D_v=128,
+                                    dtype="bf16", causal=True, bias=False, p=0.0, scale=None),
+    "b2h16-s4096-d192x128-causal-bias": dict(B=2, H=16, S_q=4096, S_kv=4096, D_qk=192, D_v=128,
+                                             dtype="bf16", causal=True, bias=True, p=0.0,
+                                             scale=None),
+    "b8h16-s1024x2048-d64-fp16-dropout0.1": dict(B=8, H=16, S_q=1024, S_kv=2048, D_qk=64, D_v=64,
+                                                 dtype="fp16", causal=False, bias=False, p=0.1,
+                                                 scale=None),
+    "b1h32-s16384-d128-causal": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
+                                     dtype="bf16", causal=True, bias=False, p=0.0, scale=None),
+}
+DEFAULT_WORKLOAD = "b1h32-s16384-d128-causal"
+DROP_SEED, DROP_OFFSET = 0x1234, 0
+
+# Kernel sources whose ncu DRAM counters are recorded in profiles/traffic.json.
+KERNEL_SOURCES = {
+    "bwd_main": ["scaled_dot_product_06_gb300/csrc/bwd_kernel.cuh",
+                 "scaled_dot_product_06_gb300/csrc/common.cuh",
+                 "scaled_dot_product_06_gb300/csrc/ptx.cuh"],
+    "fwd": ["scaled_dot_product_06_gb300/csrc/fwd_kernel.cuh",
+            "scaled_dot_product_06_gb300/csrc/common.cuh",
+            "scaled_dot_product_06_gb300/csrc/ptx.cuh"],
+}
+
+
+def fwd_flops(w: dict) -> float:
+    f = 4.0 * w["B"] * w["H"] * w["S_q"] * w["S_kv"] * (w["D_qk"] + w["D_v"]) / 2.0
+    return f / 2.0 if w["causal"] else f
+
+
+def source_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+def oracle_sample(w: dict, s_sample: int) -> tuple[float, float]:
+    """fp64 oracle fwd+bwd on one head restricted to the first s_sample
+    positions of the workload. Returns (seconds, FLOPs by the convention)."""
+    import oracle
+    from scaled_dot_product_06_gb300.inputs import Shape, make_inputs
+    s_q = min(s_sample, w["S_q"])
+    s_kv = min(s_sample * w["S_kv"] // w["S_q"], w["S_kv"])
+    shp = Shape(1, 1, s_q, s_kv, w["D_qk"], w["D_v"])
+    x = make_inputs(shp, w["dtype"], with_bias=w["bias"])
+    scale = w["scale"] if w["scale"] is not None else 1.0 / math.sqrt(w["D_qk"])
+    pr = oracle.Problem(1, 1, s_q, s_kv, w["D_qk"], w["D_v"], scale, w["causal"], w["p"],
+                        DROP_SEED, DROP_OFFSET)
+    t0 = time.perf_counter()
+    oracle.forward(pr, x["q"], x["k"], x["v"], x["bias"])
+    oracle.backward(pr, x["q"], x["k"], x["v"], x["do"], x["bias"])
+    dt = time.perf_counter() - t0
+    ws = dict(w, B=1, H=1, S_q=s_q, S_kv=s_kv)
+    return dt, 3.5 * fwd_flops(ws)
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, w, rank):
+    """The reference arm: the oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    s_sample = args.ref_sample
+    for _ in range(args.warmup):
+        oracle_sample(w, s_sample)
+    secs, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, f = oracle_sample(w, s_sample)
+        secs += dt
+        flops += f
+    value = flops / secs / 1e12
+    sample = (f"one head, first {min(s_sample, w['S_q'])} query positions of {args.workload} "
+              f"(fp64 numpy oracle, fwd+bwd, FLOPs by the same convention)")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normal)",
+           "config": {"workload": args.workload, **{k: w[k] for k in ("B", "H", "S_q", "S_kv",
+                                                                      "D_qk", "D_v")}},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-sample", type=int, default=4096,
+                    help="query positions of the one-head oracle sample (cpu_baseline)")
+    ap.add_argument("--ref-sample", type=int, default=2048,
+                    help="query positions of the one-head oracle sample per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from scaled_dot_product_06_gb300 import (SDPA_BWD_DQ_CONVERT, SDPA_BWD_MAIN,
+                                             SDPA_BWD_PREPROCESS, sdpa_bwd_phases,
+                                             sdpa_bwd_workspace_size, sdpa_device_error, sdpa_fwd)
+    from scaled_dot_product_06_gb300.inputs import Shape, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    shp = Shape(w["B"], w["H"], w["S_q"], w["S_kv"], w["D_qk"], w["D_v"])
+    x = make_inputs(shp, w["dtype"], with_bias=w["bias"], seed_base=rank, device=dev)
+    q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
+    scale = w["scale"] if w["scale"] is not None else 1.0 / math.sqrt(w["D_qk"])
+    kw = dict(scale=scale, is_causal=w["causal"], dropout_p=w["p"], seed=DROP_SEED,
+              offset=DROP_OFFSET, bias=bias)
+    o = torch.empty(shp.B, shp.H, shp.S_q, shp.D_v, dtype=q.dtype, device=dev)
+    lse = torch.empty(shp.B, shp.H, shp.S_q, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbias = torch.empty_like(bias) if bias is not None else None
+    ws = torch.empty(sdpa_bwd_workspace_size(shp.B, shp.H, shp.S_q, shp.S_kv, shp.D_qk, shp.D_v),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    names = ["fwd", "bwd_pre", "bwd_main", "dq_convert"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sdpa_fwd(q, k, v, out=o, lse=lse, **kw)
+        if ev is not None:
+            ev[1].record(stream)
+        for i, ph in enumerate((SDPA_BWD_PREPROCESS, SDPA_BWD_MAIN, SDPA_BWD_DQ_CONVERT)):
+            sdpa_bwd_phases(ph, q, k, v, o, do, lse, workspace=ws, dq=dq, dk=dk, dv=dv,
+                            dbias=dbias, **kw)
+            if ev is not None:
+                ev[2 + i].record(stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if sdpa_device_error() != 0:
+        raise SystemExit("a kernel wait ran out during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    if sdpa_device_error() != 0:
+        raise SystemExit("a kernel wait ran out during the timed steps")
+    total_ms = t_start.elapsed_time(t_end)
+    per_kernel = {n: 0.0 for n in names}
+    for e in evs:
+        for i, n in enumerate(names):
+            per_kernel[n] += e[i].elapsed_time(e[i + 1])
+    per_kernel = {n: t / args.steps for n, t in per_kernel.items()}
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    ff = fwd_flops(w)
+    step_flops = 3.5 * ff
+    value = world * step_flops / (ms * 1e-3) / 1e12
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+
+    # dominant kernel and its roofline
+    dom = max(per_kernel, key=per_kernel.get)
+    kernel_flops = {"fwd": ff, "bwd_main": 2.5 * ff}
+    roof = None
+    if dom in kernel_flops:
+        achieved = kernel_flops[dom] / (per_kernel[dom] * 1e-3) / 1e12
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tpath):
+            with open(tpath) as f:
+                tr = json.load(f).get(args.workload, {}).get(dom)
+            if tr and tr.get("source_sha") == source_sha(dom):
+                traffic = tr.get("bytes_per_launch")
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_kind} bf16 dense (burst)"}
+    else:
+        hbm = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": hbm, "unit": "GB/s",
+                "frac": None, "traffic": None, "peak_source": f"{peak_kind} HBM copy"}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hin = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("do", do))}
+        if bias is not None:
+            hin["bias"] = bias.cpu().pin_memory()
+        hout = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        if dbias is not None:
+            hout["dbias"] = torch.empty(dbias.shape, dtype=dbias.dtype).pin_memory()
+        dbuf = {"q": q, "k": k, "v": v, "do": do, "bias": bias, "o": o, "lse": lse, "dq": dq,
+                "dk": dk, "dv": dv, "dbias": dbias}
+        h2d = sum(t.numel() * t.element_size() for t in hin.values())
+        d2h = sum(t.numel() * t.element_size() for t in hout.values())
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            for n, t in hin.items():
+                dbuf[n].copy_(t, non_blocking=True)
+            step()
+            for n, t in hout.items():
+                t.copy_(dbuf[n], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, flops = oracle_sample(w, args.cpu_sample)
+        cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": cpu_threads(),
+               "kind": "oracle",
+               "sample": (f"one head, first {min(args.cpu_sample, w['S_q'])} query positions of "
+                          f"the workload, fp64 numpy oracle fwd+bwd ({secs:.1f} s)")}
+
+    if rank == 0:
+        kt = {n: {"ms": t} for n, t in per_kernel.items()}
+        kt["fwd"]["tflops"] = ff / (per_kernel["fwd"] * 1e-3) / 1e12
+        kt["bwd_main"]["tflops"] = 2.5 * ff / (per_kernel["bwd_main"] * 1e-3) / 1e12
+        bwd_ms = per_kernel["bwd_pre"] + per_kernel["bwd_main"] + per_kernel["dq_convert"]
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w["dtype"], "data": "synthetic (seeded normal inputs, no dataset)",
+            "config": {"workload": args.workload, "B": w["B"], "H": w["H"], "S_q": w["S_q"],
+                       "S_kv": w["S_kv"], "D_qk": w["D_qk"], "D_v": w["D_v"],
+                       "causal": w["causal"], "bias": w["bias"], "dropout_p": w["p"],
+                       "l2": "inputs larger than L2, no flush",
+                       "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "fwd_tflops": ff / (per_kernel["fwd"] * 1e-3) / 1e12,
+            "bwd_tflops": 2.5 * ff / (bwd_ms * 1e-3) / 1e12,
+            "kernels": kt,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": 4 * args.steps,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -114,6 +114,31 @@ sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
                        const float* lse, void* dq, void* dk, void* dv, float* dbias,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Phases of the backward pass, in the order they must run. */
+typedef enum {
+  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O); zero the dQ accumulator and dBias */
+  SDPA_BWD_MAIN = 2,       /* fused dK, dV, dBias and fp32 dQ accumulation */
+  SDPA_BWD_DQ_CONVERT = 4, /* dQ = scale * accumulator, rounded to dtype */
+  SDPA_BWD_ALL = 7
+} sdpa_bwd_phase_t;
+
+/*
+ * sdpa_bwd restricted to the phases set in `phases` (a non-empty subset of
+ * SDPA_BWD_ALL), with identical arguments and validation. Issuing the three
+ * phases in order, with the same arguments, on one stream is exactly
+ * sdpa_bwd; they are separate so a caller can time or overlap them one by one
+ * (the CK page runs the same split as three kernels: dot_do_o, dq_dk_dv and
+ * convert_dq). A later phase reads what the earlier ones left in `workspace`
+ * and `dbias`.
+ */
+sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
+                              int64_t d_qk, int64_t d_v, float scale, int is_causal,
+                              float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+                              const void* q, const void* k, const void* v, const float* bias,
+                              const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                              void* dv, float* dbias, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /*
  * Test hook: the packed dropout keep bits of a whole problem, drawn by the
  * same device Philox function the fused kernels use. Bit (L % 32) of word

@@ -17,6 +17,10 @@ SDPA_ERR_MISALIGNED = 3
 SDPA_ERR_WORKSPACE = 4
 SDPA_ERR_CUDA = 5
 SDPA_ERR_DEVICE_TIMEOUT = 6
+SDPA_BWD_PREPROCESS = 1
+SDPA_BWD_MAIN = 2
+SDPA_BWD_DQ_CONVERT = 4
+SDPA_BWD_ALL = 7
 SDPA_BF16 = 0
 SDPA_FP16 = 1
 
@@ -30,6 +34,9 @@ SIGNATURES = {
     "sdpa_bwd": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64, _int,
                         _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                         _sz, _ptr]),
+    "sdpa_bwd_phases": (_int, [_int, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64,
+                               _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                               _ptr, _ptr, _ptr, _sz, _ptr]),
     "sdpa_dropout_mask": (_int, [_i64, _i64, _i64, _i64, _f32, _u64, _u64, _ptr, _ptr]),
     "sdpa_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
     "sdpa_last_error": (ctypes.c_char_p, []),

@@ -72,6 +72,16 @@ def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.
              offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None, dbias=None,
              stream=None):
     """Backward pass. Returns (dq, dk, dv, dbias or None)."""
+    return sdpa_bwd_phases(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, scale=scale,
+                           is_causal=is_causal, dropout_p=dropout_p, seed=seed, offset=offset,
+                           bias=bias, workspace=workspace, dq=dq, dk=dk, dv=dv, dbias=dbias,
+                           stream=stream)
+
+
+def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0,
+                    seed=0, offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None,
+                    dbias=None, stream=None):
+    """The backward phases selected by ``phases`` (SDPA_BWD_* bit mask)."""
     b, h, s_q, d_qk = q.shape
     s_kv, d_v = k.shape[2], v.shape[3]
     dt = q.dtype
@@ -93,13 +103,12 @@ def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.
     need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    st = _native.lib().sdpa_bwd(b, h, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
-                                float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
-                                _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o), _ptr(dout),
-                                _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
-                                _ptr(workspace), workspace.numel(),
-                                ctypes.c_void_p(_stream_ptr(stream)))
-    _native.check(st, "sdpa_bwd")
+    st = _native.lib().sdpa_bwd_phases(
+        int(phases), b, h, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)), float(dropout_p),
+        int(seed), int(offset), _DTYPE_CODE[dt], _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o),
+        _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
+        workspace.numel(), ctypes.c_void_p(_stream_ptr(stream)))
+    _native.check(st, "sdpa_bwd_phases")
     return dq, dk, dv, dbias
 
 

@@ -193,12 +193,14 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
   return d_bytes + rows * static_cast<size_t>(d_qk) * sizeof(float);
 }
 
-sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
-                       float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
-                       sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
-                       const float* bias, const void* o, const void* dout, const float* lse,
-                       void* dq, void* dk, void* dv, float* dbias, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
+                              int64_t d_qk, int64_t d_v, float scale, int is_causal,
+                              float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+                              const void* q, const void* k, const void* v, const float* bias,
+                              const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                              void* dv, float* dbias, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (phases <= 0 || (phases & ~SDPA_BWD_ALL) != 0) return fail(SDPA_ERR_INVALID_ARG, "phases");
   bool empty = false;
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
   if (empty) return SDPA_OK;
@@ -253,14 +255,33 @@ sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
-  cudaError_t e = launch_bwd_pre(bf16, o, dout, delta, dq_acc, dbias, static_cast<int64_t>(rows),
-                                 static_cast<int>(d_v), static_cast<int64_t>(rows) * d_qk, dbias_elems, st);
-  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
-  e = bf16 ? launch_bwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st)
-           : launch_bwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st);
-  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward main kernel launch", e);
-  e = launch_dq_convert(bf16, dq_acc, dq, scale, static_cast<int64_t>(rows) * d_qk, st);
-  return cuda_status(e, "dQ convert launch");
+  cudaError_t e = cudaSuccess;
+  if (phases & SDPA_BWD_PREPROCESS) {
+    e = launch_bwd_pre(bf16, o, dout, delta, dq_acc, dbias, static_cast<int64_t>(rows),
+                       static_cast<int>(d_v), static_cast<int64_t>(rows) * d_qk, dbias_elems, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
+  }
+  if (phases & SDPA_BWD_MAIN) {
+    e = bf16 ? launch_bwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st)
+             : launch_bwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward main kernel launch", e);
+  }
+  if (phases & SDPA_BWD_DQ_CONVERT) {
+    e = launch_dq_convert(bf16, dq_acc, dq, scale, static_cast<int64_t>(rows) * d_qk, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "dQ convert launch", e);
+  }
+  return SDPA_OK;
+}
+
+sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
+                       float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
+                       sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
+                       const float* bias, const void* o, const void* dout, const float* lse,
+                       void* dq, void* dk, void* dv, float* dbias, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return sdpa_bwd_phases(SDPA_BWD_ALL, b, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed,
+                         offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias, workspace,
+                         workspace_bytes, stream);
 }
 
 sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, float dropout_p,
