@@ -19,17 +19,23 @@
 //   dQ_i^T = K^T dS^T       [128 x 64]   A = K (MN-major), B = dS^T (MN-major),
 //                                        one product per 128-wide slice of Dk
 // Roles:
-//   warps 0-3  compute: thread t owns key row t. Recomputes P^T, writes P~^T
-//              into TMEM, forms dS^T, adds it into dBias (fp32 atomics) and
-//              stores it to shared memory (bf16, 128-byte swizzle).
-//   warps 4-7  dQ drain: thread t owns TMEM lane t (a column of dQ); stages the
+//   warps 0-7  compute, two warpgroups: warp w owns key rows 32*(w%4)..+31
+//              (its TMEM lanes) and query columns [32*(w/4), +32) of each
+//              tile. Recomputes P^T, writes P~^T into TMEM, forms dS^T, adds
+//              it into dBias (fp32 atomics) and stores it to shared memory
+//              (io dtype, 128-byte swizzle). Two warps per scheduler hide
+//              each other's latencies.
+//   warps 8-11 dQ drain: thread t owns TMEM lane t (a column of dQ); stages the
 //              dQ_i^T slice in shared memory and reduce-adds it into the fp32
 //              dQ accumulator with a TMA tensor reduce.
-//   warp 8     TMA producer (K, V once; Q_i and dO_i through a 2-stage ring).
-//   warp 9     MMA issuer (one lane).
-// Tensor memory (512 columns): S^T [0,64) with P~^T over [0,32), dP^T
+//   warp 12    TMA producer (K, V once; Q_i and dO_i through a 2-stage ring).
+//   warp 13    MMA issuer (one lane).
+// Tensor memory (512 columns): S^T [0,64) with P~^T over [0,16) and [32,48)
+// (each warpgroup overwrites only columns it has already read), dP^T
 // [64,128), dV [128,128+Dv), dK next, dQ^T slices after that.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sdpa {
@@ -56,7 +62,7 @@ struct BwdCfg {
   static constexpr int OFF_ROW = OFF_DQ + DQ_STAGE_BYTES;  // 2 x 64 (-LSE log2e), 2 x 64 D
   static constexpr int OFF_BAR = OFF_ROW + 1024;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 448;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 64, T_DV = 128, T_DK = 128 + DV, T_DQ = T_DK + DQK;
   static_assert(T_DQ + DQ_BUFS * 64 <= 512, "tensor memory overflow");
@@ -64,39 +70,39 @@ struct BwdCfg {
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128 && DQK <= 192, "head size");
 };
 
+constexpr int kLoadWarp = 12, kMmaWarp = 13;
+
 enum : int { BB_KV = 0, BB_QF, BB_DOF = BB_QF + 2, BB_QE = BB_DOF + 2, BB_S = BB_QE + 2, BB_P,
              BB_DP, BB_DS, BB_DQF, BB_DQE = BB_DQF + 2, BB_DKDV = BB_DQE + 2, BB_DRAIN,
              BB_COUNT };
 
-// Keep bits of key row (k0 + t) for the 64 query rows of a tile, gathered from
-// the Philox blocks computed by the four threads of t's quad. One Philox block
-// covers four consecutive keys of one query row (the four lanes of a quad), so
-// lane (4g + w) draws the blocks of query rows 4r + w and the quad exchanges
-// the bits. Returns m[src]: bit r = keep flag of query row 4r + src.
-__device__ __forceinline__ void bwd_keep_bits(uint64_t lin_tile, int S_kv, int t, uint32_t thr,
+// Keep bits of key row k for the 32 query rows [row0, row0 + 32) of a tile.
+// One Philox block covers four consecutive keys of one query row, i.e. the
+// four lanes of a quad (lane 4g + w owns key 4g + w), so lane 4g + w draws the
+// blocks of query rows row0 + 4r + w (r < 8) and the quad exchanges the bits.
+// Returns m[src]: bit r = keep flag of query row row0 + 4r + src.
+// lin_quad is the linear index of (query row row0, first key of the quad).
+__device__ __forceinline__ void bwd_keep_bits(uint64_t lin_quad, int S_kv, int lane, uint32_t thr,
                                               uint32_t seed_lo, uint32_t seed_hi, uint32_t off_lo,
                                               uint32_t off_hi, uint32_t (&m)[4]) {
-  const int w = t & 3, g = t >> 2;
-  uint32_t a = 0, bb = 0;
+  const int w = lane & 3;
+  uint32_t a = 0;
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const uint64_t L = lin_tile + static_cast<uint64_t>(4 * r + w) * S_kv + 4 * g;
+  for (int r = 0; r < 8; ++r) {
+    const uint64_t L = lin_quad + static_cast<uint64_t>(4 * r + w) * S_kv;
     const uint4 d = dropout_draws(L >> 2, seed_lo, seed_hi, off_lo, off_hi);
-    a |= (static_cast<uint32_t>(d.x >= thr) << r) | (static_cast<uint32_t>(d.y >= thr) << (16 + r));
-    bb |= (static_cast<uint32_t>(d.z >= thr) << r) | (static_cast<uint32_t>(d.w >= thr) << (16 + r));
+    a |= (static_cast<uint32_t>(d.x >= thr) << r) | (static_cast<uint32_t>(d.y >= thr) << (8 + r)) |
+         (static_cast<uint32_t>(d.z >= thr) << (16 + r)) | (static_cast<uint32_t>(d.w >= thr) << (24 + r));
   }
-  const int lane = t & 31;
 #pragma unroll
   for (int src = 0; src < 4; ++src) {
-    const int sl = (lane & ~3) | src;
-    const uint32_t xa = __shfl_sync(0xffffffffu, a, sl);
-    const uint32_t xb = __shfl_sync(0xffffffffu, bb, sl);
-    m[src] = (((w < 2) ? xa : xb) >> (16 * (w & 1))) & 0xFFFFu;
+    const uint32_t x = __shfl_sync(0xffffffffu, a, (lane & ~3) | src);
+    m[src] = (x >> (8 * w)) & 0xFFu;
   }
 }
 
 template <int DQK, int DV, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
@@ -114,11 +120,13 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- key tile of this CTA: most query work first (causal), batch fastest
-  const int n_bh = p.B * p.H;
-  const int kt = static_cast<int>(blockIdx.x / n_bh);
-  const int r = static_cast<int>(blockIdx.x % n_bh);
-  const int b = r % p.B, h = r / p.B;
+  // ---- key tile of this CTA: head-major (one head's Q / dO / dQ stay in L2),
+  // then key tiles with the most query work first, batch fastest (the batches
+  // of one head share Bias and dBias rows)
+  const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
+  const int b = static_cast<int>(blockIdx.x % p.B);
+  const int rest = static_cast<int>(blockIdx.x / p.B);
+  const int kt = rest % n_kt, h = rest / n_kt;
   const int bh = b * p.H + h;
   const int k0 = kt * C::BN;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
@@ -127,17 +135,18 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < BB_COUNT; ++i) {
-      const bool many = (i == BB_P || i == BB_DS || i == BB_DQE || i == BB_DQE + 1);
-      mbar_init(bar(i), many ? 128u : 1u);
+      const uint32_t count = (i == BB_P || i == BB_DS) ? 256u
+                             : (i == BB_DQE || i == BB_DQE + 1) ? 128u : 1u;
+      mbar_init(bar(i), count);
     }
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kLoadWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tbase = *tmem_slot;
   const ErrCtx ec{p.err, abort_flag};
 
-  if (warp == 8) {
+  if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     int issued = 0;
     if (n_it > 0) {
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_wait(bar(BB_DOF + (i & 1)), ph, ec, kSiteDrain, false);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_f16(128, 64, BF16, false, false);
     constexpr uint32_t kIdDV = idesc_f16(128, DV, BF16, false, true);
@@ -242,8 +251,8 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t ob = sdO + s * C::DO_BYTES;
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          umma_ts(tDV, tS + kk * 8, sdesc_sw128(ob + kk * 2048, C::BM * 128, 1024), kIdDV,
-                  (i > 0 || kk > 0));
+          umma_ts(tDV, tS + (kk >> 1) * 32 + (kk & 1) * 8,
+                  sdesc_sw128(ob + kk * 2048, C::BM * 128, 1024), kIdDV, (i > 0 || kk > 0));
       }
       __syncwarp();
       if (i + 1 < n_it) {
@@ -300,9 +309,9 @@ __global__ void __launch_bounds__(320, 1)
     }
     __syncwarp();
     mbar_wait(bar(BB_DRAIN), 0, ec, kSiteDrain, false);
-  } else if (warp >= 4) {
+  } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ drain
-    const int t = threadIdx.x - 128;  // TMEM lane
+    const int t = threadIdx.x - 256;  // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* stage = reinterpret_cast<float*>(smem + C::OFF_DQ);
     bool ok = true;
@@ -347,164 +356,183 @@ __global__ void __launch_bounds__(320, 1)
     if (t == 0) bulk_wait_group0();
   } else {
     // ------------------------------------------------------------ compute
-    const int t = threadIdx.x;  // key row within the tile = TMEM lane
-    const int kv = k0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // Two warpgroups: warp w owns key rows 32*(w%4) .. +31 (its TMEM lanes)
+    // and query columns [32*hf, 32*hf + 32) of each tile, hf = w / 4.
+    const int t = threadIdx.x;
+    const int row = t & 127;           // key row within the tile = TMEM lane
+    const int hf = t >> 7;             // query-column half
+    const int kv = k0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const bool kv_ok = kv < p.S_kv;
     float* nl2_buf = rowbuf;        // [2][64]  -LSE * log2(e) (-inf for rows without keys)
     float* d_buf = rowbuf + 128;    // [2][64]  D
-    uint8_t* ds_row = smem + C::OFF_DS + t * 128;
-    bool ok = true;
-    for (int i = 0; ok && i < n_it; ++i) {
-      const int q0 = (it0 + i) * C::BM;
-      float* nl2 = nl2_buf + (i & 1) * 64;
-      float* dd = d_buf + (i & 1) * 64;
+    uint8_t* ds_row = smem + C::OFF_DS + row * 128;
+    // Row statistics of query tile i: threads 0-63 read -LSE*log2e, threads
+    // 64-127 read D. Tile i+1's values are fetched during tile i.
+    auto fetch_row_stat = [&](int i) -> float {
+      const int qr = (it0 + i) * C::BM + (t & 63);
+      const size_t idx = static_cast<size_t>(bh) * p.S_q + qr;
       if (t < 64) {
-        const int qr = q0 + t;
-        const size_t idx = static_cast<size_t>(bh) * p.S_q + qr;
         const float L = (qr < p.S_q) ? p.lse[idx] : SDPA_NEG_INF;
-        nl2[t] = (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
-        dd[t] = (qr < p.S_q) ? p.delta[idx] : 0.f;
+        return (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
       }
-      named_bar_sync(2, 128);
-      uint32_t km[4] = {0xFFFFu, 0xFFFFu, 0xFFFFu, 0xFFFFu};
-      if (p.dropout)
-        bwd_keep_bits((static_cast<uint64_t>(bh) * p.S_q + q0) * p.S_kv + k0, p.S_kv, t,
-                      p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi, km);
-      const float zk = p.dropout ? p.keep_scale : 1.0f;
-      if (!(ok = mbar_wait(bar(BB_S), i & 1, ec, kSiteBwdCompute))) break;
-      tc_fence_after();
-      float pr[64];
-      {
-        uint32_t a0[32], a1[32];
-        tmem_ld32(tbase + C::T_S + lane_off, a0);
-        tmem_ld32(tbase + C::T_S + lane_off + 32, a1);
-        tmem_wait_ld();
+      return (qr < p.S_q) ? p.delta[idx] : 0.f;
+    };
+    auto store_row_stat = [&](int i, float v) {
+      if (t < 128) rowbuf[(t < 64 ? 0 : 128) + (i & 1) * 64 + (t & 63)] = v;
+    };
+    bool ok = true;
+    auto body = [&](auto drop_tag) {
+      constexpr bool DROP = decltype(drop_tag)::value;
+      const float zk = p.keep_scale;
+      if (n_it > 0) store_row_stat(0, t < 128 ? fetch_row_stat(0) : 0.f);
+      for (int i = 0; ok && i < n_it; ++i) {
+        const int q0 = (it0 + i) * C::BM;
+        const int qc0 = q0 + 32 * hf;  // first query row of this thread's columns
+        named_bar_sync(2, 256);  // tile i's statistics are in shared memory
+        const float4* nl2 = reinterpret_cast<const float4*>(nl2_buf + (i & 1) * 64 + 32 * hf);
+        const float4* dd = reinterpret_cast<const float4*>(d_buf + (i & 1) * 64 + 32 * hf);
+        const float next_stat = (t < 128 && i + 1 < n_it) ? fetch_row_stat(i + 1) : 0.f;
+        uint32_t km[4] = {0xFFu, 0xFFu, 0xFFu, 0xFFu};
+        if constexpr (DROP)
+          bwd_keep_bits((static_cast<uint64_t>(bh) * p.S_q + qc0) * p.S_kv + k0 + (row & ~3), p.S_kv, lane,
+                        p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi, km);
+        auto zf = [&](int c) -> float {
+          if constexpr (DROP) return ((km[c & 3] >> (c >> 2)) & 1u) ? zk : 0.f;
+          return 1.0f;
+        };
+        if (!(ok = mbar_wait(bar(BB_S), i & 1, ec, kSiteBwdCompute))) break;
+        tc_fence_after();
+        float pr[32];
+        {
+          uint32_t a0[32];
+          tmem_ld32(tbase + C::T_S + lane_off + 32 * hf, a0);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pr[c] = __uint_as_float(a0[c]);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pr[32 + c] = __uint_as_float(a1[c]);
-      }
-      const bool need_mask = (p.causal && q0 < k0 + C::BN - 1) || (q0 + C::BM > p.S_q) || !kv_ok ||
-                             (k0 + C::BN > p.S_kv);
-      const float* bias_col =
-          (p.bias != nullptr && kv_ok) ? p.bias + (static_cast<size_t>(h) * p.S_q + q0) * p.S_kv + kv
-                                       : nullptr;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x = fmaf(pr[c], p.scale_log2, nl2[c]);
-        if (bias_col != nullptr && q0 + c < p.S_q)
-          x = fmaf(__ldg(bias_col + static_cast<size_t>(c) * p.S_kv), kLog2e, x);
-        if (need_mask && (!kv_ok || q0 + c >= p.S_q || (p.causal && kv > q0 + c))) x = SDPA_NEG_INF;
-        pr[c] = ex2(x);
-      }
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float z0 = ((km[(2 * c) & 3] >> ((2 * c) >> 2)) & 1u) ? zk : 0.f;
-          const float z1 = ((km[(2 * c + 1) & 3] >> ((2 * c + 1) >> 2)) & 1u) ? zk : 0.f;
-          pk[c] = pack2<BF16>(pr[2 * c] * z0, pr[2 * c + 1] * z1);
+          for (int c = 0; c < 32; ++c) pr[c] = __uint_as_float(a0[c]);
         }
-        tmem_st32(tbase + C::T_S + lane_off, pk);
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      mbar_arrive(bar(BB_P));
-      if (!(ok = mbar_wait(bar(BB_DP), i & 1, ec, kSiteBwdCompute))) break;
-      tc_fence_after();
-      float* dbias_col =
-          (p.dbias != nullptr && kv_ok) ? p.dbias + (static_cast<size_t>(h) * p.S_q + q0) * p.S_kv + kv
-                                        : nullptr;
+        const bool need_mask = (p.causal && qc0 < k0 + C::BN - 1) || (qc0 + 32 > p.S_q) ||
+                               !kv_ok || (k0 + C::BN > p.S_kv);
+        const float* bias_col =
+            (p.bias != nullptr && kv_ok)
+                ? p.bias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
+                : nullptr;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 n4 = nl2[c4];
+          const float nv[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            float x = fmaf(pr[c], p.scale_log2, nv[e]);
+            if (bias_col != nullptr && qc0 + c < p.S_q)
+              x = fmaf(__ldg(bias_col + static_cast<size_t>(c) * p.S_kv), kLog2e, x);
+            if (need_mask && (!kv_ok || qc0 + c >= p.S_q || (p.causal && kv > qc0 + c)))
+              x = SDPA_NEG_INF;
+            pr[c] = ex2(x);
+          }
+        }
+        {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack2<BF16>(pr[2 * c] * zf(2 * c), pr[2 * c + 1] * zf(2 * c + 1));
+          tmem_st16(tbase + C::T_S + lane_off + 32 * hf, pk);  // P~^T over [32hf, 32hf+16)
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(BB_P));
+        if (!(ok = mbar_wait(bar(BB_DP), i & 1, ec, kSiteBwdCompute))) break;
+        tc_fence_after();
         float dp[32];
         {
           uint32_t a0[32];
-          tmem_ld32(tbase + C::T_DP + lane_off + half * 32, a0);
+          tmem_ld32(tbase + C::T_DP + lane_off + 32 * hf, a0);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) dp[c] = __uint_as_float(a0[c]);
         }
+        float* dbias_col =
+            (p.dbias != nullptr && kv_ok)
+                ? p.dbias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
+                : nullptr;
 #pragma unroll
         for (int chh = 0; chh < 4; ++chh) {
-          const int ch = half * 4 + chh;
-          uint32_t w[4];
+          float ds[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float v2[2];
+          for (int g = 0; g < 2; ++g) {
+            const float4 d4 = dd[chh * 2 + g];
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int c = ch * 8 + e * 2 + u;
-              const float z = ((km[c & 3] >> (c >> 2)) & 1u) ? zk : 0.f;
-              const float ds = pr[c] * fmaf(dp[c - half * 32], z, -dd[c]);
-              if (dbias_col != nullptr && q0 + c < p.S_q)
-                atomicAdd(dbias_col + static_cast<size_t>(c) * p.S_kv, ds);
-              v2[u] = ds;
+            for (int e = 0; e < 4; ++e) {
+              const int c = chh * 8 + g * 4 + e;
+              ds[g * 4 + e] = pr[c] * (DROP ? fmaf(dp[c], zf(c), -dv4[e]) : dp[c] - dv4[e]);
             }
-            w[e] = pack2<BF16>(v2[0], v2[1]);
           }
-          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          if (dbias_col != nullptr) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (qc0 + chh * 8 + e < p.S_q)
+                atomicAdd(dbias_col + static_cast<size_t>(chh * 8 + e) * p.S_kv, ds[e]);
+          }
+          const int ch = 4 * hf + chh;  // 16-byte chunk = query columns 8ch .. 8ch+7
+          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(pack2<BF16>(ds[0], ds[1]), pack2<BF16>(ds[2], ds[3]),
+                         pack2<BF16>(ds[4], ds[5]), pack2<BF16>(ds[6], ds[7]));
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(BB_DS));
+        if (i + 1 < n_it) store_row_stat(i + 1, next_stat);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(BB_DS));
-    }
-    // ---- epilogue: dV, dK * scale (zeros for a key tile no query sees)
+    };
+    if (p.dropout)
+      body(std::true_type{});
+    else
+      body(std::false_type{});
+    // ---- epilogue: warps 0-3 write dV, warps 4-7 write dK * scale (zeros for
+    // a key tile that no query sees)
     const bool have = n_it > 0;
     bool ready = have && ok && mbar_wait(bar(BB_DKDV), 0, ec, kSiteBwdCompute);
     if (have && !ready) ok = false;
     if (ok) {
       if (ready) tc_fence_after();
       const size_t rowi = static_cast<size_t>(bh) * p.S_kv + (kv_ok ? kv : 0);
-      uint8_t* dvrow = static_cast<uint8_t*>(p.dv) + rowi * DV * 2;
-      uint8_t* dkrow = static_cast<uint8_t*>(p.dk) + rowi * DQK * 2;
+      auto write_rows = [&](auto width_tag, uint32_t tcol, void* base, float mul) {
+        constexpr int W = decltype(width_tag)::value;
+        uint8_t* dst_row = static_cast<uint8_t*>(base) + rowi * W * 2;
 #pragma unroll
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t a[32];
-        if (ready) {
-          tmem_ld32(tbase + C::T_DV + lane_off + c * 32, a);
-          tmem_wait_ld();
-        } else {
+        for (int c = 0; c < W / 32; ++c) {
+          uint32_t a[32];
+          if (ready) {
+            tmem_ld32(tbase + tcol + lane_off + c * 32, a);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = 0u;
+            for (int e = 0; e < 32; ++e) a[e] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+          if (kv_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
         }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-        if (kv_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dvrow + c * 64);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < DQK / 32; ++c) {
-        uint32_t a[32];
-        if (ready) {
-          tmem_ld32(tbase + C::T_DK + lane_off + c * 32, a);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
-        if (kv_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dkrow + c * 64);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
-      }
+      };
+      if (hf == 0)
+        write_rows(std::integral_constant<int, DV>{}, C::T_DV, p.dv, 1.0f);
+      else
+        write_rows(std::integral_constant<int, DQK>{}, C::T_DK, p.dk, p.scale);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
