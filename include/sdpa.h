@@ -140,6 +140,32 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
                               void* stream);
 
 /*
+ * sdpa_bwd for callers that cannot allocate device memory when they run the
+ * backward pass (a host framework that owns all GPU memory through its own
+ * pool, or a latency-critical loop that cannot afford cudaMalloc's implicit
+ * synchronisation). There is no counterpart on the pages; it exists for such
+ * callers. Same arguments and results as sdpa_bwd minus the workspace: the
+ * scratch lives in a 16 MiB static device array inside the library, which
+ * every GPU that loads the library holds until the process exits. The call
+ * allocates nothing.
+ *   Limit    problems with sdpa_bwd_workspace_size(...) > 16 MiB are rejected
+ *            with SDPA_ERR_WORKSPACE (detail in sdpa_last_error).
+ *   Sharing  all calls on a device use the same array and leave their data in
+ *            it; each call re-zeroes what must start at zero, but calls whose
+ *            kernels overlap on the GPU (e.g. on two streams) race: serialise
+ *            them.
+ *   Set-up   the first call on each device looks up the array's device
+ *            address (cudaGetSymbolAddress) with that device current; make
+ *            that first call before any stream capture begins.
+ */
+sdpa_status_t sdpa_bwd_noalloc(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
+                               int64_t d_v, float scale, int is_causal, float dropout_p,
+                               uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
+                               const void* k, const void* v, const float* bias, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               float* dbias, void* stream);
+
+/*
  * Test hook: the packed dropout keep bits of a whole problem, drawn by the
  * same device Philox function the fused kernels use. Bit (L % 32) of word
  * bits[L / 32] is element L's keep flag (L as in "Dropout" above); bits past

@@ -37,6 +37,9 @@ SIGNATURES = {
     "sdpa_bwd_phases": (_int, [_int, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64,
                                _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                _ptr, _ptr, _ptr, _sz, _ptr]),
+    "sdpa_bwd_noalloc": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64,
+                                _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                                _ptr, _ptr]),
     "sdpa_dropout_mask": (_int, [_i64, _i64, _i64, _i64, _f32, _u64, _u64, _ptr, _ptr]),
     "sdpa_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
     "sdpa_last_error": (ctypes.c_char_p, []),

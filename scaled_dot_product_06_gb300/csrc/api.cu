@@ -122,6 +122,10 @@ uint32_t drop_threshold(float p) {
 
 }  // namespace
 
+namespace sdpa {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace sdpa
+
 extern "C" {
 
 const char* sdpa_status_string(sdpa_status_t s) {

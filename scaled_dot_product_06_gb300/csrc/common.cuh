@@ -120,6 +120,9 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// Records a failure detail for sdpa_last_error() on the calling thread.
+void set_last_error(const char* msg);
+
 // ---------------------------------------------------------------- launchers
 // Defined in the per-dtype kernel translation units; return a CUDA error
 // (cudaErrorInvalidValue for a head-size pair that has no kernel).
