@@ -1,0 +1,114 @@
+"""GPU parity at the five workloads' full sizes, in the launch configuration
+bench.py times (whole-problem sdpa_fwd + sdpa_bwd calls).
+
+The oracle cannot materialise every head at these sizes in seconds, so each
+check compares sampled outputs it computes one by one (whole (b, h) slices,
+or sampled query rows and key columns of one head), plus invariants that hold
+at any size: with no dropout every row of dS sums to zero, so the key-sum of
+dK vanishes and the key-sum of dV equals the query-sum of dO.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import philox
+from parity_util import Case, assert_close, assert_lse, run_gpu
+from scaled_dot_product_06_gb300 import sdpa_dropout_mask
+from scaled_dot_product_06_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def slice_check(case, x, outs, b, h):
+    o, lse, dq, dk, dv, _ = outs
+    pr = case.problem()
+    o_ref, lse_ref = oracle.forward_head(pr, b, h, x["q"], x["k"], x["v"], x["bias"])
+    assert_close(f"o[{b},{h}]", o[b, h], o_ref)
+    assert_lse(lse[b, h], lse_ref)
+    dq_r, dk_r, dv_r, ds = oracle.backward_head(pr, b, h, x["q"], x["k"], x["v"], x["do"],
+                                                x["bias"])
+    assert_close(f"dq[{b},{h}]", dq[b, h], dq_r)
+    assert_close(f"dk[{b},{h}]", dk[b, h], dk_r)
+    assert_close(f"dv[{b},{h}]", dv[b, h], dv_r)
+    return ds
+
+
+def key_sum_invariants(case, outs, x):
+    """No dropout: sum over keys of dK is 0 and of dV equals sum over queries of dO."""
+    _, _, _, dk, dv, _ = outs
+    dk64 = dk.double()
+    rel = dk64.sum(dim=2).abs().max().item() / dk64.abs().sum(dim=2).max().item()
+    assert rel < 2e-2, f"key-sum of dK is not ~0 (relative {rel:.3e})"
+    dv_sum = dv.double().sum(dim=2).cpu().numpy()
+    do_sum = x["do"].double().sum(dim=2).numpy()
+    assert_close("sum_j dV", torch.from_numpy(dv_sum), do_sum, rel=3e-2)
+
+
+def test_small_configuration_every_element():
+    from parity_util import check_full
+    check_full(Case(1, 2, 128, 128, 64, 64, scale=0.125))
+
+
+def test_b4h16_s2048_d128_causal():
+    case = Case(4, 16, 2048, 2048, 128, 128, causal=True)
+    x = make_inputs(case.shape, case.dtype)
+    outs = run_gpu(case, x)
+    for b, h in ((0, 0), (3, 15), (2, 7)):
+        slice_check(case, x, outs, b, h)
+    key_sum_invariants(case, outs, x)
+
+
+def test_b2h16_s4096_d192x128_causal_bias():
+    case = Case(2, 16, 4096, 4096, 192, 128, causal=True, bias=True)
+    x = make_inputs(case.shape, case.dtype, with_bias=True)
+    outs = run_gpu(case, x)
+    dbias = outs[5]
+    for h in (0, 11):  # dBias sums over the batch, so sample whole heads
+        ds_sum = 0.0
+        for b in range(case.B):
+            ds_sum = ds_sum + slice_check(case, x, outs, b, h)
+        assert_close(f"dbias[{h}]", dbias[0, h], ds_sum)
+    key_sum_invariants(case, outs, x)
+
+
+def test_b8h16_s1024x2048_d64_fp16_dropout():
+    case = Case(8, 16, 1024, 2048, 64, 64, dtype="fp16", p=0.1)
+    x = make_inputs(case.shape, case.dtype)
+    outs = run_gpu(case, x)
+    for b, h in ((0, 0), (7, 15), (3, 9)):
+        slice_check(case, x, outs, b, h)
+    # keep bits of the sampled slices, bit-exact
+    bits = sdpa_dropout_mask(case.B, case.H, case.S_q, case.S_kv, case.p, case.seed,
+                             case.offset).cpu().numpy().view(np.uint32)
+    flat = np.unpackbits(bits.view(np.uint8), bitorder="little")
+    per_head = case.S_q * case.S_kv
+    for b, h in ((0, 0), (7, 15), (5, 2)):
+        start = (b * case.H + h) * per_head
+        got = flat[start:start + per_head].reshape(case.S_q, case.S_kv).astype(bool)
+        want = philox.keep_mask(case.B, case.H, case.S_q, case.S_kv, case.p, case.seed,
+                                case.offset, b, h)
+        np.testing.assert_array_equal(got, want)
+
+
+def test_b1h32_s16384_d128_causal_sampled():
+    case = Case(1, 32, 16384, 16384, 128, 128, causal=True)
+    x = make_inputs(case.shape, case.dtype)
+    o, lse, dq, dk, dv, _ = outs = run_gpu(case, x)
+    pr = case.problem()
+    rng = np.random.default_rng(3)
+    h = 17
+    rows = np.unique(np.concatenate([np.arange(0, 130), np.arange(16384 - 130, 16384),
+                                     rng.integers(0, 16384, 120)]))
+    cols = np.unique(np.concatenate([np.arange(0, 66), np.arange(16384 - 66, 16384),
+                                     rng.integers(0, 16384, 60)]))
+    r_t, c_t = torch.as_tensor(rows, device=o.device), torch.as_tensor(cols, device=o.device)
+    o_ref, lse_ref = oracle.forward_head(pr, 0, h, x["q"], x["k"], x["v"], rows=rows)
+    assert_close("o rows", o[0, h][r_t], o_ref)
+    assert_lse(lse[0, h][r_t], lse_ref)
+    dq_r, dk_c, dv_c, _ = oracle.backward_head(pr, 0, h, x["q"], x["k"], x["v"], x["do"],
+                                               rows=rows, cols=cols, row_chunk=2048)
+    assert_close("dq rows", dq[0, h][r_t], dq_r)
+    assert_close("dk cols", dk[0, h][c_t], dk_c)
+    assert_close("dv cols", dv[0, h][c_t], dv_c)
+    key_sum_invariants(case, outs, x)
