@@ -51,9 +51,12 @@ DROP_SEED, DROP_OFFSET = 0x1234, 0
 
 # Kernel sources whose ncu DRAM counters are recorded in profiles/traffic.json.
 KERNEL_SOURCES = {
-    "bwd_main": ["scaled_dot_product_06_gb300/csrc/bwd_kernel.cuh",
+    "bwd_dkdv": ["scaled_dot_product_06_gb300/csrc/bwd_dkdv_kernel.cuh",
                  "scaled_dot_product_06_gb300/csrc/common.cuh",
                  "scaled_dot_product_06_gb300/csrc/ptx.cuh"],
+    "bwd_dq": ["scaled_dot_product_06_gb300/csrc/bwd_dq_kernel.cuh",
+               "scaled_dot_product_06_gb300/csrc/common.cuh",
+               "scaled_dot_product_06_gb300/csrc/ptx.cuh"],
     "fwd": ["scaled_dot_product_06_gb300/csrc/fwd_kernel.cuh",
             "scaled_dot_product_06_gb300/csrc/common.cuh",
             "scaled_dot_product_06_gb300/csrc/ptx.cuh"],
@@ -220,8 +223,8 @@ def main():
     import torch
     import torch.distributed as dist
 
-    from scaled_dot_product_06_gb300 import (SDPA_BWD_DQ_CONVERT, SDPA_BWD_MAIN,
-                                             SDPA_BWD_PREPROCESS, sdpa_bwd_phases,
+    from scaled_dot_product_06_gb300 import (SDPA_BWD_DKDV, SDPA_BWD_DQ, SDPA_BWD_PREPROCESS,
+                                             sdpa_bwd_phases,
                                              sdpa_bwd_workspace_size, sdpa_device_error, sdpa_fwd)
     from scaled_dot_product_06_gb300.inputs import Shape, make_inputs
 
@@ -249,7 +252,7 @@ def main():
     ws = torch.empty(sdpa_bwd_workspace_size(shp.B, shp.H, shp.S_q, shp.S_kv, shp.D_qk, shp.D_v),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    names = ["fwd", "bwd_pre", "bwd_main", "dq_convert"]
+    names = ["fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"]
 
     def step(ev=None):
         if ev is not None:
@@ -257,7 +260,7 @@ def main():
         sdpa_fwd(q, k, v, out=o, lse=lse, **kw)
         if ev is not None:
             ev[1].record(stream)
-        for i, ph in enumerate((SDPA_BWD_PREPROCESS, SDPA_BWD_MAIN, SDPA_BWD_DQ_CONVERT)):
+        for i, ph in enumerate((SDPA_BWD_PREPROCESS, SDPA_BWD_DKDV, SDPA_BWD_DQ)):
             sdpa_bwd_phases(ph, q, k, v, o, do, lse, workspace=ws, dq=dq, dk=dk, dv=dv,
                             dbias=dbias, **kw)
             if ev is not None:
@@ -305,7 +308,11 @@ def main():
 
     # dominant kernel and its roofline
     dom = max(per_kernel, key=per_kernel.get)
-    kernel_flops = {"fwd": ff, "bwd_main": 2.5 * ff}
+    # algorithmic FLOPs per launch: the dK/dV kernel forms S^T, dP^T, dV, dK
+    # (2x the forward); the dQ kernel's algorithmic share is the dQ product
+    # alone (its recomputed S and dP are not counted)
+    dq_share = 2.0 * w["D_qk"] / (w["D_qk"] + w["D_v"]) * 0.5 * ff
+    kernel_flops = {"fwd": ff, "bwd_dkdv": 2.0 * ff, "bwd_dq": dq_share}
     roof = None
     if dom in kernel_flops:
         achieved = kernel_flops[dom] / (per_kernel[dom] * 1e-3) / 1e12
@@ -371,8 +378,10 @@ def main():
     if rank == 0:
         kt = {n: {"ms": t} for n, t in per_kernel.items()}
         kt["fwd"]["tflops"] = ff / (per_kernel["fwd"] * 1e-3) / 1e12
-        kt["bwd_main"]["tflops"] = 2.5 * ff / (per_kernel["bwd_main"] * 1e-3) / 1e12
-        bwd_ms = per_kernel["bwd_pre"] + per_kernel["bwd_main"] + per_kernel["dq_convert"]
+        kt["bwd_dkdv"]["tflops"] = 2.0 * ff / (per_kernel["bwd_dkdv"] * 1e-3) / 1e12
+        kt["bwd_dq"]["tflops_algorithmic"] = dq_share / (per_kernel["bwd_dq"] * 1e-3) / 1e12
+        kt["bwd_dq"]["tflops_executed"] = (dq_share + ff) / (per_kernel["bwd_dq"] * 1e-3) / 1e12
+        bwd_ms = per_kernel["bwd_pre"] + per_kernel["bwd_dkdv"] + per_kernel["bwd_dq"]
         out = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

@@ -83,10 +83,9 @@ sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
                        const void* v, const float* bias, void* o, float* lse, void* stream);
 
 /*
- * Bytes of device workspace sdpa_bwd needs: D (fp32 [b,h,s_q]) followed, at
- * the next 256-byte boundary, by the fp32 dQ accumulator [b,h,s_q,d_qk]
- * (the f32 scratchpad of oneDNN's sdpa micro.cpp and the dq_acc buffer of the
- * CK page play the same role). Returns 0 for invalid sizes.
+ * Bytes of device workspace sdpa_bwd needs: D = rowsum(dO * O), fp32
+ * [b,h,s_q], rounded up to 256 bytes (oneDNN's sdpa micro.cpp books the same
+ * buffer in its scratchpad). Returns 0 for invalid sizes.
  */
 size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v);
@@ -102,10 +101,10 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
  *   workspace caller-owned device memory of at least
  *             sdpa_bwd_workspace_size(...) bytes, 256-byte aligned; its
  *             contents on entry are ignored and on exit are unspecified.
- * Runs three kernels on `stream`: preprocess (D, zero dQ_acc and dBias), the
- * fused dQ/dK/dV/dBias kernel, and the dQ convert. dQ is accumulated with
- * fp32 additions whose order varies from run to run (not bitwise
- * deterministic); dK, dV and, for b <= 2, dBias are deterministic.
+ * Runs three kernels on `stream`: preprocess (D; zero dBias), the
+ * key/value-stationary kernel (dK, dV, dBias) and the query-stationary kernel
+ * (dQ). dQ, dK and dV are bitwise reproducible; dBias sums the batch with
+ * fp32 atomics, reproducible for b <= 2.
  */
 sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                        int64_t d_v, float scale, int is_causal, float dropout_p, uint64_t seed,
@@ -116,9 +115,9 @@ sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
 
 /* Phases of the backward pass, in the order they must run. */
 typedef enum {
-  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O); zero the dQ accumulator and dBias */
-  SDPA_BWD_MAIN = 2,       /* fused dK, dV, dBias and fp32 dQ accumulation */
-  SDPA_BWD_DQ_CONVERT = 4, /* dQ = scale * accumulator, rounded to dtype */
+  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O); zero dBias */
+  SDPA_BWD_DKDV = 2,       /* key/value-stationary kernel: dK, dV, dBias */
+  SDPA_BWD_DQ = 4,         /* query-stationary kernel: dQ */
   SDPA_BWD_ALL = 7
 } sdpa_bwd_phase_t;
 
@@ -126,10 +125,10 @@ typedef enum {
  * sdpa_bwd restricted to the phases set in `phases` (a non-empty subset of
  * SDPA_BWD_ALL), with identical arguments and validation. Issuing the three
  * phases in order, with the same arguments, on one stream is exactly
- * sdpa_bwd; they are separate so a caller can time or overlap them one by one
- * (the CK page runs the same split as three kernels: dot_do_o, dq_dk_dv and
- * convert_dq). A later phase reads what the earlier ones left in `workspace`
- * and `dbias`.
+ * sdpa_bwd; they are separate so a caller can time them one by one (the CK
+ * page also splits its backward into three kernels). The dK/dV and dQ phases
+ * both read D from `workspace`, and the dK/dV phase adds into `dbias`, so the
+ * preprocess phase must run first.
  */
 sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int is_causal,

@@ -18,8 +18,8 @@ SDPA_ERR_WORKSPACE = 4
 SDPA_ERR_CUDA = 5
 SDPA_ERR_DEVICE_TIMEOUT = 6
 SDPA_BWD_PREPROCESS = 1
-SDPA_BWD_MAIN = 2
-SDPA_BWD_DQ_CONVERT = 4
+SDPA_BWD_DKDV = 2
+SDPA_BWD_DQ = 4
 SDPA_BWD_ALL = 7
 SDPA_BF16 = 0
 SDPA_FP16 = 1

@@ -193,8 +193,7 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
   bool empty = false;
   if (check_sizes(b, h, s_q, s_kv, d_qk, d_v, 0.0f, SDPA_BF16, &empty) != SDPA_OK) return 0;
   const size_t rows = static_cast<size_t>(b) * h * s_q;
-  const size_t d_bytes = (rows * sizeof(float) + 255) & ~size_t(255);
-  return d_bytes + rows * static_cast<size_t>(d_qk) * sizeof(float);
+  return (rows * sizeof(float) + 255) & ~size_t(255);
 }
 
 sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
@@ -222,16 +221,7 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
   const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const size_t rows = static_cast<size_t>(b) * h * s_q;
   float* delta = static_cast<float*>(workspace);
-  float* dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                           ((rows * sizeof(float) + 255) & ~size_t(255)));
-  CUtensorMap mq, mk, mv, mdo, mdq;
-  if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 64, true)) return s;
-  if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
-  if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
-  if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, 64, true)) return s;
-  if (sdpa_status_t s = make_map(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, d_qk, s_q, b * h, 64,
-                                 false))
-    return s;
+  const int di = static_cast<int>(d_qk), dvi = static_cast<int>(d_v);
 
   BwdParams p{};
   p.B = static_cast<int>(b);
@@ -252,27 +242,39 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
   p.offset_hi = static_cast<uint32_t>(offset >> 32);
   p.lse = lse;
   p.delta = delta;
-  p.dq_acc = dq_acc;
+  p.dq = dq;
   p.dk = dk;
   p.dv = dv;
   if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
   cudaError_t e = cudaSuccess;
   if (phases & SDPA_BWD_PREPROCESS) {
-    e = launch_bwd_pre(bf16, o, dout, delta, dq_acc, dbias, static_cast<int64_t>(rows),
-                       static_cast<int>(d_v), static_cast<int64_t>(rows) * d_qk, dbias_elems, st);
+    const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
+    e = launch_bwd_pre(bf16, o, dout, delta, dbias, static_cast<int64_t>(rows), dvi, dbias_elems, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
   }
-  if (phases & SDPA_BWD_MAIN) {
-    e = bf16 ? launch_bwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st)
-             : launch_bwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, mdo, mdq, p, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward main kernel launch", e);
+  if (phases & SDPA_BWD_DKDV) {
+    // key/value-stationary kernel: query tiles of 128 rows (64 at d_qk = 192)
+    const uint32_t q_rows = d_qk <= 128 ? 128 : 64;
+    CUtensorMap mq, mk, mv, mdo;
+    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, q_rows, true)) return s;
+    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, q_rows, true)) return s;
+    e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st)
+             : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dK/dV kernel launch", e);
   }
-  if (phases & SDPA_BWD_DQ_CONVERT) {
-    e = launch_dq_convert(bf16, dq_acc, dq, scale, static_cast<int64_t>(rows) * d_qk, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "dQ convert launch", e);
+  if (phases & SDPA_BWD_DQ) {
+    CUtensorMap mq, mk, mv, mdo;
+    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, 128, true)) return s;
+    e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, p, st)
+             : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, p, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dQ kernel launch", e);
   }
   return SDPA_OK;
 }

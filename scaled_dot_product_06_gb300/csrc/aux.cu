@@ -2,11 +2,9 @@
 //
 // * bwd_pre: D = rowsum(dO * O) in fp32 (CK tile fmha_bwd_kernel.hpp,
 //   FmhaBwdOGradDotOKernel; the D line of the header equations), and zeroing
-//   of the fp32 dQ accumulator and of dBias, which the main kernel
-//   accumulates into (oneDNN sdpa micro.cpp, execute_backward: preprocess and
-//   fill of the f32 intermediates).
-// * dq_convert: dQ = scale * dQ_acc rounded to the io dtype (CK tile
-//   FmhaBwdConvertQGradKernel; oneDNN postprocess).
+//   of dBias, which the key/value-stationary kernel accumulates into (oneDNN
+//   sdpa micro.cpp, execute_backward: preprocess and fill of the f32
+//   intermediates).
 // * dropout_mask: the packed keep bits of the whole problem, drawn by the same
 //   device Philox function the fused kernels use (oneDNN's dropout mask output
 //   and CK's stored random values serve the same purpose).
@@ -29,10 +27,9 @@ template <bool BF16>
 __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __restrict__ o,
                                                               const uint4* __restrict__ dout,
                                                               float* __restrict__ delta,
-                                                              float4* __restrict__ dq_acc,
                                                               float4* __restrict__ dbias,
                                                               int64_t rows, int d_v,
-                                                              int64_t dq_vec, int64_t dbias_elems) {
+                                                              int64_t dbias_elems) {
   const int group = d_v / 8;  // 8 or 16 threads per row (power of two)
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -59,22 +56,9 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
     if (live && sub == 0) delta[row] = acc;
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t i = tid; i < dq_vec; i += nthreads) dq_acc[i] = z;
   const int64_t dbias_vec = dbias_elems / 4;
   for (int64_t i = tid; i < dbias_vec; i += nthreads) dbias[i] = z;
   if (tid < (dbias_elems & 3)) reinterpret_cast<float*>(dbias)[dbias_vec * 4 + tid] = 0.f;
-}
-
-template <bool BF16>
-__global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const float4* __restrict__ acc,
-                                                                 uint4* __restrict__ dq, float scale,
-                                                                 int64_t n8) {
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += nthreads) {
-    const float4 a = acc[2 * i], b = acc[2 * i + 1];
-    dq[i] = make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
-                       pack2<BF16>(b.x * scale, b.y * scale), pack2<BF16>(b.z * scale, b.w * scale));
-  }
 }
 
 // Word w holds the keep bits of elements 32w .. 32w+31 (bit e = element 32w+e).
@@ -100,26 +84,15 @@ __global__ void __launch_bounds__(kAuxThreads) dropout_mask_kernel(int64_t total
   }
 }
 
-cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta, float* dq_acc,
-                           float* dbias, int64_t rows, int d_v, int64_t dq_elems, int64_t dbias_elems,
-                           cudaStream_t st) {
+cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta, float* dbias,
+                           int64_t rows, int d_v, int64_t dbias_elems, cudaStream_t st) {
   const int group = d_v / 8;
   const int64_t work = rows * group;
-  const int64_t zero_work = (dq_elems + dbias_elems) / 4;
+  const int64_t zero_work = dbias_elems / 4;
   const int grid = aux_grid(work > zero_work ? work : zero_work);
   auto kern = bf16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
   kern<<<grid, kAuxThreads, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta,
-                                      reinterpret_cast<float4*>(dq_acc), reinterpret_cast<float4*>(dbias),
-                                      rows, d_v, dq_elems / 4, dbias_elems);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dq_convert(bool bf16, const float* dq_acc, void* dq, float scale, int64_t elems,
-                              cudaStream_t st) {
-  const int64_t n8 = elems / 8;
-  auto kern = bf16 ? dq_convert_kernel<true> : dq_convert_kernel<false>;
-  kern<<<aux_grid(n8), kAuxThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
-                                              static_cast<uint4*>(dq), scale, n8);
+                                      reinterpret_cast<float4*>(dbias), rows, d_v, dbias_elems);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,492 @@
+// Attention backward, key/value-stationary half: dK, dV and dBias (sm_103a).
+//
+// Computes the dV, dS, dBias and dK lines of the equation block that opens CK
+// tile's fmha_bwd_kernel.hpp: dV = P^T dO, dP = dO V^T, dS = P * (dP - D),
+// dBias = dS, dK = dS^T Q * scale, with dropout entering as P~ = P * Z
+// (Z = keep / (1 - p)) in dV and dS = P * (dP * Z - D). P is recomputed from
+// the saved logsumexp, P = exp(S * scale + Bias - LSE), and D = rowsum(dO * O)
+// comes from the preprocess kernel. dQ is produced by the query-stationary
+// kernel in bwd_dq_kernel.cuh, so this kernel has no cross-CTA accumulation
+// other than dBias.
+//
+// One CTA owns 128 key rows of one (b, h) (K_j and V_j stay in shared memory)
+// and loops over query tiles of BM rows (128, or 64 at d_qk = 192 where tensor
+// memory is short). Every product keeps the 128 keys in the MMA's M dimension
+// (the TMEM lanes):
+//   S^T  = K Q_i^T      [128 x BM]  A = K (smem, K-major),  B = Q_i (K-major)
+//   dP^T = V dO_i^T     [128 x BM]  A = V (smem, K-major),  B = dO_i (K-major)
+//   dV  += P~^T dO_i    [128 x Dv]  A = P~^T (TMEM),        B = dO_i (MN-major)
+//   dK  += dS^T Q_i     [128 x Dk]  A = dS^T (TMEM),        B = Q_i (MN-major)
+// With BM = 128 every shared-memory operand pair stays within the shared
+// memory read rate (an M=128 product with both operands in shared memory
+// needs N >= 128), and the two products with an operand in TMEM read only B.
+// Roles (320 threads):
+//   warps 0-7  compute, two warpgroups: warp w owns key rows 32*(w%4)..+31 (its
+//              TMEM lanes) and query columns [hf*BM/2, (hf+1)*BM/2), hf = w/4.
+//              Recomputes P^T and writes P~^T (io dtype) over the first half
+//              of the S^T columns it has read; forms dS^T, adds it into dBias
+//              (fp32 atomics) and writes it (io dtype) over the dP^T columns
+//              it has read.
+//   warp 8     TMA producer (K, V once; Q_i and dO_i through a 2-stage ring).
+//   warp 9     MMA issuer (one lane), order per tile i: dV(i), S^T(i+1),
+//              dK(i), dP^T(i+1), so the softmax of tile i+1 overlaps dK(i)
+//              and dP^T(i+1), and dS of tile i overlaps dV(i) and S^T(i+1).
+// Tensor memory (512 columns): S^T [0,BM), dP^T [BM,2BM), dV [2BM,2BM+Dv),
+// dK [2BM+Dv, 2BM+Dv+Dk).
+#pragma once
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace sdpa {
+
+template <int DQK, int DV>
+struct DkdvCfg {
+  static constexpr int BN = 128;                      // key rows per CTA
+  static constexpr int BM = (DQK <= 128) ? 128 : 64;  // query rows per tile
+  static constexpr int CW = BM / 2;                   // query columns per compute thread
+  static constexpr int STAGES = 2;
+  static constexpr int K_BYTES = BN * DQK * 2;
+  static constexpr int V_BYTES = BN * DV * 2;
+  static constexpr int Q_BYTES = BM * DQK * 2;
+  static constexpr int DO_BYTES = BM * DV * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + K_BYTES;
+  static constexpr int OFF_Q = OFF_V + V_BYTES;
+  static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
+  static constexpr int OFF_ROW = OFF_DO + STAGES * DO_BYTES;  // [2][BM] -LSE log2e, [2][BM] D
+  static constexpr int OFF_BAR = OFF_ROW + 4 * BM * 4;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_S = 0, T_DP = BM, T_DV = 2 * BM, T_DK = 2 * BM + DV;
+  static_assert(T_DK + DQK <= 512, "tensor memory overflow");
+  static_assert(SMEM <= 227 * 1024, "shared memory overflow");
+  static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128 && DQK <= 192, "head size");
+};
+
+enum : int { AB_KV = 0, AB_QF, AB_DOF = AB_QF + 2, AB_QE = AB_DOF + 2, AB_S = AB_QE + 2, AB_P,
+             AB_DP, AB_DS, AB_DKDV, AB_DRAIN, AB_COUNT };
+
+// Keep bits of key row k for the 32 query rows [row0, row0 + 32) of a tile.
+// One Philox block covers four consecutive keys of one query row, i.e. the
+// four lanes of a quad (lane 4g + w owns key 4g + w), so lane 4g + w draws the
+// blocks of query rows row0 + 4r + w (r < 8) and the quad exchanges the bits.
+// lin_quad is the linear index of (query row row0, first key of the quad).
+// Returns m[src]: bit r = keep flag of query row row0 + 4r + src.
+__device__ __forceinline__ void keep_bits_transposed(uint64_t lin_quad, int S_kv, int lane,
+                                                     uint32_t thr, uint32_t seed_lo,
+                                                     uint32_t seed_hi, uint32_t off_lo,
+                                                     uint32_t off_hi, uint32_t (&m)[4]) {
+  const int w = lane & 3;
+  uint32_t a = 0;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const uint64_t L = lin_quad + static_cast<uint64_t>(4 * r + w) * S_kv;
+    const uint4 d = dropout_draws(L >> 2, seed_lo, seed_hi, off_lo, off_hi);
+    a |= (static_cast<uint32_t>(d.x >= thr) << r) | (static_cast<uint32_t>(d.y >= thr) << (8 + r)) |
+         (static_cast<uint32_t>(d.z >= thr) << (16 + r)) | (static_cast<uint32_t>(d.w >= thr) << (24 + r));
+  }
+#pragma unroll
+  for (int src = 0; src < 4; ++src) {
+    const uint32_t x = __shfl_sync(0xffffffffu, a, (lane & ~3) | src);
+    m[src] = (x >> (8 * w)) & 0xFFu;
+  }
+}
+
+template <int DQK, int DV, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+  using C = DkdvCfg<DQK, DV>;
+  constexpr int BM = C::BM, CW = C::CW;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+  const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
+  float* rowbuf = reinterpret_cast<float*>(smem + C::OFF_ROW);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + AB_COUNT);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kLoadWarp = 8, kMmaWarp = 9;
+
+  // ---- key tile of this CTA: head-major (one head's Q / dO stay in L2), then
+  // the key tiles with the most query work first, batch fastest (the batches
+  // of one head share Bias and dBias rows)
+  const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
+  const int b = static_cast<int>(blockIdx.x % p.B);
+  const int rest = static_cast<int>(blockIdx.x / p.B);
+  const int kt = rest % n_kt, h = rest / n_kt;
+  const int bh = b * p.H + h;
+  const int k0 = kt * C::BN;
+  const int n_qt = (p.S_q + BM - 1) / BM;
+  const int it0 = p.causal ? min(n_qt, k0 / BM) : 0;  // first query tile that sees a key here
+  const int n_it = n_qt - it0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < AB_COUNT; ++i)
+      mbar_init(bar(i), (i == AB_P || i == AB_DS) ? 256u : 1u);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const ErrCtx ec{p.err, abort_flag};
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    if (n_it > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(AB_KV), C::K_BYTES + C::V_BYTES);
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          tma_load_3d(sK + c * C::BN * 128, &tmK, bar(AB_KV), c * 64, k0, bh);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(sV + c * C::BN * 128, &tmV, bar(AB_KV), c * 64, k0, bh);
+      }
+      for (int i = 0; i < n_it; ++i) {
+        const int s = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad)) break;
+        const int q0 = (it0 + i) * BM;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(AB_QF + s), C::Q_BYTES);
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            tma_load_3d(sQ + s * C::Q_BYTES + c * BM * 128, &tmQ, bar(AB_QF + s), c * 64, q0, bh);
+          mbar_arrive_expect_tx(bar(AB_DOF + s), C::DO_BYTES);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_3d(sdO + s * C::DO_BYTES + c * BM * 128, &tmdO, bar(AB_DOF + s), c * 64, q0, bh);
+        }
+        issued = i + 1;
+      }
+    }
+    __syncwarp();
+    if (*abort_flag && n_it > 0) {
+      mbar_wait(bar(AB_KV), 0, ec, kSiteDrain, false);
+      for (int i = 0; i < issued; ++i) {
+        const uint32_t ph = (i >> 1) & 1;
+        mbar_wait(bar(AB_QF + (i & 1)), ph, ec, kSiteDrain, false);
+        mbar_wait(bar(AB_DOF + (i & 1)), ph, ec, kSiteDrain, false);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16(128, BM, BF16, false, false);
+    constexpr uint32_t kIdDV = idesc_f16(128, DV, BF16, false, true);
+    constexpr uint32_t kIdDK = idesc_f16(128, DQK, BF16, false, true);
+    const uint32_t tS = tbase + C::T_S, tDP = tbase + C::T_DP, tDV = tbase + C::T_DV,
+                   tDK = tbase + C::T_DK;
+    // Packed io-dtype operand columns of query rows [16kk, 16kk+16): each
+    // compute half wrote its CW columns, packed two per TMEM column, at the
+    // start of the CW columns it read.
+    auto packed_col = [](int kk) -> uint32_t {
+      return static_cast<uint32_t>(((kk * 16) / CW) * CW + ((kk * 16) % CW) / 2);
+    };
+    auto issue_s = [&](int s) {  // S^T = K Q^T
+      const uint32_t qb = sQ + s * C::Q_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < DQK / 16; ++kk)
+        umma_ss(tS, sdesc_sw128(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024),
+                sdesc_sw128(qb + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024), kIdS, kk > 0);
+    };
+    auto issue_dp = [&](int s) {  // dP^T = V dO^T
+      const uint32_t ob = sdO + s * C::DO_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < DV / 16; ++kk)
+        umma_ss(tDP, sdesc_sw128(sV + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024),
+                sdesc_sw128(ob + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024), kIdS, kk > 0);
+    };
+    bool ok = n_it > 0;
+    if (ok) ok = mbar_wait(bar(AB_KV), 0, ec, kSiteBwdMma);
+    if (ok) ok = mbar_wait(bar(AB_QF), 0, ec, kSiteBwdMma);
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0);
+        umma_commit(bar(AB_S));
+      }
+      __syncwarp();
+      ok = mbar_wait(bar(AB_DOF), 0, ec, kSiteBwdMma);
+    }
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_dp(0);
+        umma_commit(bar(AB_DP));
+      }
+      __syncwarp();
+    }
+    for (int i = 0; ok && i < n_it; ++i) {
+      const int s = i & 1, s1 = (i + 1) & 1;
+      const uint32_t ph1 = ((i + 1) >> 1) & 1;
+      if (!(ok = mbar_wait(bar(AB_P), i & 1, ec, kSiteBwdMma))) break;
+      tc_fence_after();
+      if (lane == 0) {  // dV += P~^T dO_i
+        const uint32_t ob = sdO + s * C::DO_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ts(tDV, tS + packed_col(kk), sdesc_sw128(ob + kk * 2048, BM * 128, 1024), kIdDV,
+                  (i > 0 || kk > 0));
+      }
+      __syncwarp();
+      if (i + 1 < n_it) {
+        if (!(ok = mbar_wait(bar(AB_QF + s1), ph1, ec, kSiteBwdMma))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(s1);
+          umma_commit(bar(AB_S));
+        }
+        __syncwarp();
+      }
+      if (!(ok = mbar_wait(bar(AB_DS), i & 1, ec, kSiteBwdMma))) break;
+      tc_fence_after();
+      if (lane == 0) {  // dK += dS^T Q_i
+        const uint32_t qb = sQ + s * C::Q_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          umma_ts(tDK, tDP + packed_col(kk), sdesc_sw128(qb + kk * 2048, BM * 128, 1024), kIdDK,
+                  (i > 0 || kk > 0));
+        umma_commit(bar(AB_QE + s));  // Q_i and dO_i are no longer read
+      }
+      __syncwarp();
+      if (i + 1 < n_it) {
+        if (!(ok = mbar_wait(bar(AB_DOF + s1), ph1, ec, kSiteBwdMma))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_dp(s1);
+          umma_commit(bar(AB_DP));
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      if (ok) umma_commit(bar(AB_DKDV));
+      umma_commit(bar(AB_DRAIN));
+    }
+    __syncwarp();
+    mbar_wait(bar(AB_DRAIN), 0, ec, kSiteDrain, false);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int t = threadIdx.x;
+    const int row = t & 127;  // key row within the tile = TMEM lane
+    const int hf = t >> 7;    // query-column half
+    const int kv = k0 + row;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool kv_ok = kv < p.S_kv;
+    float* nl2_buf = rowbuf;          // [2][BM]  -LSE * log2(e) (-inf for rows without keys)
+    float* d_buf = rowbuf + 2 * BM;   // [2][BM]  D
+    // Row statistics of query tile i: threads 0..BM-1 read -LSE*log2e, threads
+    // BM..2BM-1 read D. Tile i+1's values are fetched during tile i.
+    auto fetch_row_stat = [&](int i) -> float {
+      const int qr = (it0 + i) * BM + (t % BM);
+      const size_t idx = static_cast<size_t>(bh) * p.S_q + qr;
+      if (t < BM) {
+        const float L = (qr < p.S_q) ? p.lse[idx] : SDPA_NEG_INF;
+        return (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
+      }
+      return (qr < p.S_q) ? p.delta[idx] : 0.f;
+    };
+    auto store_row_stat = [&](int i, float v) {
+      if (t < 2 * BM) rowbuf[(t < BM ? 0 : 2 * BM) + (i & 1) * BM + (t % BM)] = v;
+    };
+    bool ok = true;
+    auto body = [&](auto drop_tag) {
+      constexpr bool DROP = decltype(drop_tag)::value;
+      const float zk = p.keep_scale;
+      if (n_it > 0) store_row_stat(0, t < 2 * BM ? fetch_row_stat(0) : 0.f);
+      for (int i = 0; ok && i < n_it; ++i) {
+        const int q0 = (it0 + i) * BM;
+        const int qc0 = q0 + CW * hf;  // first query row of this thread's columns
+        named_bar_sync(2, 256);        // tile i's statistics are in shared memory
+        const float4* nl2 = reinterpret_cast<const float4*>(nl2_buf + (i & 1) * BM + CW * hf);
+        const float4* dd = reinterpret_cast<const float4*>(d_buf + (i & 1) * BM + CW * hf);
+        const float next_stat = (t < 2 * BM && i + 1 < n_it) ? fetch_row_stat(i + 1) : 0.f;
+        uint32_t km[CW / 32][4];
+#pragma unroll
+        for (int g = 0; g < CW / 32; ++g) {
+          km[g][0] = km[g][1] = km[g][2] = km[g][3] = 0xFFu;
+          if constexpr (DROP)
+            keep_bits_transposed(
+                (static_cast<uint64_t>(bh) * p.S_q + qc0 + 32 * g) * p.S_kv + k0 + (row & ~3),
+                p.S_kv, lane, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi,
+                km[g]);
+        }
+        auto zf = [&](int c) -> float {  // dropout factor of local column c
+          if constexpr (DROP) return ((km[c >> 5][c & 3] >> ((c & 31) >> 2)) & 1u) ? zk : 0.f;
+          return 1.0f;
+        };
+        if (!(ok = mbar_wait(bar(AB_S), i & 1, ec, kSiteBwdCompute))) break;
+        tc_fence_after();
+        float pr[CW];
+#pragma unroll
+        for (int c = 0; c < CW / 32; ++c) {
+          uint32_t a0[32];
+          tmem_ld32(tbase + C::T_S + lane_off + CW * hf + 32 * c, a0);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pr[32 * c + e] = __uint_as_float(a0[e]) * p.scale_log2;
+        }
+        if (p.bias != nullptr && kv_ok) {
+          const float* bias_col = p.bias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv;
+          const int lim = min(CW, p.S_q - qc0);
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            if (c < lim) pr[c] = fmaf(__ldg(bias_col + static_cast<size_t>(c) * p.S_kv), kLog2e, pr[c]);
+        }
+        const bool need_mask = (p.causal && qc0 < k0 + C::BN - 1) || (qc0 + CW > p.S_q) || !kv_ok;
+        if (need_mask) {
+          // visible iff the key exists, the query exists and (causal) key <= query
+          const int first = p.causal ? kv - qc0 : 0;  // first visible local column
+          const int lim = kv_ok ? min(CW, p.S_q - qc0) : 0;
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            if (c < first || c >= lim) pr[c] = SDPA_NEG_INF;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < CW / 4; ++c4) {
+          const float4 n4 = nl2[c4];
+          pr[4 * c4 + 0] = ex2(pr[4 * c4 + 0] + n4.x);
+          pr[4 * c4 + 1] = ex2(pr[4 * c4 + 1] + n4.y);
+          pr[4 * c4 + 2] = ex2(pr[4 * c4 + 2] + n4.z);
+          pr[4 * c4 + 3] = ex2(pr[4 * c4 + 3] + n4.w);
+        }
+#pragma unroll
+        for (int c = 0; c < CW / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int cc = 32 * c + 2 * e;
+            pk[e] = pack2<BF16>(pr[cc] * zf(cc), pr[cc + 1] * zf(cc + 1));
+          }
+          tmem_st16(tbase + C::T_S + lane_off + CW * hf + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(AB_P));
+        if (!(ok = mbar_wait(bar(AB_DP), i & 1, ec, kSiteBwdCompute))) break;
+        tc_fence_after();
+        float* dbias_col = (p.dbias != nullptr && kv_ok)
+                               ? p.dbias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
+                               : nullptr;
+#pragma unroll
+        for (int c = 0; c < CW / 32; ++c) {
+          uint32_t a0[32];
+          tmem_ld32(tbase + C::T_DP + lane_off + CW * hf + 32 * c, a0);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 d4 = dd[8 * c + e4];
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float ds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cc = 32 * c + 4 * e4 + e;
+              const float dpv = __uint_as_float(a0[4 * e4 + e]);
+              ds[e] = pr[cc] * (DROP ? fmaf(dpv, zf(cc), -dv4[e]) : dpv - dv4[e]);
+            }
+            if (dbias_col != nullptr) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int cc = 32 * c + 4 * e4 + e;
+                if (qc0 + cc < p.S_q) atomicAdd(dbias_col + static_cast<size_t>(cc) * p.S_kv, ds[e]);
+              }
+            }
+            pk[2 * e4] = pack2<BF16>(ds[0], ds[1]);
+            pk[2 * e4 + 1] = pack2<BF16>(ds[2], ds[3]);
+          }
+          // dS^T over the first half of the dP^T columns this thread has read
+          tmem_st16(tbase + C::T_DP + lane_off + CW * hf + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(AB_DS));
+        if (i + 1 < n_it) store_row_stat(i + 1, next_stat);
+      }
+    };
+    if (p.dropout)
+      body(std::true_type{});
+    else
+      body(std::false_type{});
+    // ---- epilogue: warps 0-3 write dV, warps 4-7 write dK * scale (zeros for
+    // a key tile that no query sees)
+    const bool have = n_it > 0;
+    const bool ready = have && ok && mbar_wait(bar(AB_DKDV), 0, ec, kSiteBwdCompute);
+    if (!have || ready) {
+      if (ready) tc_fence_after();
+      const size_t rowi = static_cast<size_t>(bh) * p.S_kv + (kv_ok ? kv : 0);
+      auto write_rows = [&](auto width_tag, uint32_t tcol, void* base, float mul) {
+        constexpr int W = decltype(width_tag)::value;
+        uint8_t* dst_row = static_cast<uint8_t*>(base) + rowi * W * 2;
+#pragma unroll
+        for (int c = 0; c < W / 32; ++c) {
+          uint32_t a[32];
+          if (ready) {
+            tmem_ld32(tbase + tcol + lane_off + c * 32, a);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+          if (kv_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+      };
+      if (hf == 0)
+        write_rows(std::integral_constant<int, DV>{}, C::T_DV, p.dv, 1.0f);
+      else
+        write_rows(std::integral_constant<int, DQK>{}, C::T_DK, p.dk, p.scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int DQK, int DV, bool BF16>
+cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                              const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
+  using C = DkdvCfg<DQK, DV>;
+  auto kern = sdpa_bwd_dkdv_kernel<DQK, DV, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
+  const long long grid = static_cast<long long>(n_kt) * p.B * p.H;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, p);
+  return cudaGetLastError();
+}
+
+}  // namespace sdpa

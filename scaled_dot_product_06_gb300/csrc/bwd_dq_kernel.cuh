@@ -1,0 +1,403 @@
+// Attention backward, query-stationary half: dQ (sm_103a).
+//
+// Computes the dQ line of the equation block that opens CK tile's
+// fmha_bwd_kernel.hpp, dQ = dS K * scale with dS = P * (dP * Z - D),
+// dP = dO V^T and P = exp(S * scale + Bias - LSE) recomputed from the saved
+// logsumexp. Each CTA owns 128 query rows of one (b, h) and sums over the key
+// tiles in a fixed order inside tensor memory, so dQ needs no cross-CTA
+// accumulation and is bitwise reproducible. This trades the two extra
+// products per tile (S and dP are also formed by the key/value-stationary
+// kernel) for the fp32 atomics, accumulator buffer and convert kernel a fused
+// backward needs.
+//
+// Per key tile j of 128 rows (keys in the N dimension, queries in the TMEM
+// lanes):
+//   S   = Q K_j^T     [128 x 128]  A = Q (smem, K-major),  B = K_j (K-major)
+//   dP  = dO V_j^T    [128 x 128]  A = dO (smem, K-major), B = V_j (K-major)
+//   dQ += dS K_j      [128 x Dk]   A = dS (TMEM),          B = K_j (MN-major)
+// Roles (320 threads):
+//   warps 0-7  compute, two warpgroups: warp w owns query rows 32*(w%4)..+31
+//              (its TMEM lanes) and key columns [64*(w/4), +64) of each tile:
+//              P from S, then dS (io dtype) written over the first half of the
+//              dP columns it has read.
+//   warp 8     TMA producer (Q, dO once; K_j and V_j through a ring).
+//   warp 9     MMA issuer (one lane).
+// Tensor memory (512 columns): S [0,128), dP [128,256), dQ [256, 256+Dk).
+#pragma once
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace sdpa {
+
+template <int DQK, int DV>
+struct DqCfg {
+  static constexpr int BM = 128, BN = 128, CW = 64;
+  static constexpr int STAGES = (DQK <= 128) ? 2 : 1;
+  static constexpr int Q_BYTES = BM * DQK * 2;
+  static constexpr int DO_BYTES = BM * DV * 2;
+  static constexpr int K_BYTES = BN * DQK * 2;
+  static constexpr int V_BYTES = BN * DV * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_DO + DO_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * V_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+  static_assert(T_DQ + DQK <= 512, "tensor memory overflow");
+  static_assert(SMEM <= 227 * 1024, "shared memory overflow");
+};
+
+enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_VF + 2,
+             QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DS, QB_DONE, QB_DRAIN, QB_COUNT };
+
+template <int DQK, int DV, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    sdpa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+  using C = DqCfg<DQK, DV>;
+  constexpr int BM = C::BM, BN = C::BN, CW = C::CW, ST = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
+  const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + QB_COUNT);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kLoadWarp = 8, kMmaWarp = 9;
+
+  // ---- query tile of this CTA: heaviest causal tiles first, batch fastest
+  const int n_qt = (p.S_q + BM - 1) / BM;
+  const int n_bh = p.B * p.H;
+  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / n_bh);
+  const int r = static_cast<int>(blockIdx.x % n_bh);
+  const int b = r % p.B, h = r / p.B;
+  const int bh = b * p.H + h;
+  const int q0 = qt * BM;
+  const int n_kv_all = (p.S_kv + BN - 1) / BN;
+  const int n_kv = p.causal ? min(n_kv_all, (q0 + BM - 1) / BN + 1) : n_kv_all;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < QB_COUNT; ++i)
+      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS) ? 256u : 1u);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const ErrCtx ec{p.err, abort_flag};
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(QB_Q), C::Q_BYTES + C::DO_BYTES);
+#pragma unroll
+      for (int c = 0; c < DQK / 64; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, bar(QB_Q), c * 64, q0, bh);
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c) tma_load_3d(sdO + c * BM * 128, &tmdO, bar(QB_Q), c * 64, q0, bh);
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j % ST;
+      const uint32_t ph = (j / ST) & 1;
+      if (!mbar_wait(bar(QB_KE + s), ph ^ 1, ec, kSiteBwdLoad)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(QB_KF + s), C::K_BYTES);
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, j * BN, bh);
+      }
+      if (!mbar_wait(bar(QB_VE + s), ph ^ 1, ec, kSiteBwdLoad)) {
+        issued = 2 * j + 1;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(QB_VF + s), C::V_BYTES);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, j * BN, bh);
+      }
+      issued = 2 * j + 2;
+    }
+    __syncwarp();
+    if (*abort_flag) {
+      mbar_wait(bar(QB_Q), 0, ec, kSiteDrain, false);
+      for (int i = 0; i < issued; ++i) {
+        const int j = i >> 1, s = j % ST;
+        mbar_wait(bar(((i & 1) ? QB_VF : QB_KF) + s), (j / ST) & 1, ec, kSiteDrain, false);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_f16(128, BN, BF16, false, false);
+    constexpr uint32_t kIdDQ = idesc_f16(128, DQK, BF16, false, true);
+    const uint32_t tS = tbase + C::T_S, tDP = tbase + C::T_DP, tDQ = tbase + C::T_DQ;
+    auto issue_s = [&](int j) {  // S = Q K_j^T
+      const uint32_t kb = sK + (j % ST) * C::K_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < DQK / 16; ++kk) {
+        const uint32_t qa = sQ + (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+        const uint32_t kb2 = kb + (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+        umma_ss(tS, sdesc_sw128(qa, 16, 1024), sdesc_sw128(kb2, 16, 1024), kIdS, kk > 0);
+      }
+    };
+    auto issue_dp = [&](int j) {  // dP = dO V_j^T
+      const uint32_t vb = sV + (j % ST) * C::V_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < DV / 16; ++kk) {
+        const uint32_t oa = sdO + (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+        const uint32_t vb2 = vb + (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+        umma_ss(tDP, sdesc_sw128(oa, 16, 1024), sdesc_sw128(vb2, 16, 1024), kIdS, kk > 0);
+      }
+    };
+    auto issue_dq = [&](int j) {  // dQ += dS K_j, dS packed two per column
+      const uint32_t kb = sK + (j % ST) * C::K_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        umma_ts(tDQ, tDP + (kk >> 2) * CW + (kk & 3) * 8,
+                sdesc_sw128(kb + kk * 2048, BN * 128, 1024), kIdDQ, (j > 0 || kk > 0));
+    };
+    auto wait_kv = [&](int which, int j) {
+      return mbar_wait(bar(which + j % ST), (j / ST) & 1, ec, kSiteBwdMma);
+    };
+    bool ok = mbar_wait(bar(QB_Q), 0, ec, kSiteBwdMma) && wait_kv(QB_KF, 0);
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0);
+        umma_commit(bar(QB_S));
+      }
+      __syncwarp();
+      ok = wait_kv(QB_VF, 0);
+    }
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_dp(0);
+        umma_commit(bar(QB_DP));
+        umma_commit(bar(QB_VE + 0));
+      }
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const bool more = j + 1 < n_kv;
+      // With two stages the next S is formed while the compute warps work on
+      // tile j; with one stage K_{j+1} cannot land before dQ(j) frees K_j.
+      if constexpr (ST > 1) {
+        if (more) {
+          if (!(ok = mbar_wait(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            issue_s(j + 1);
+            umma_commit(bar(QB_S));
+          }
+          __syncwarp();
+        }
+      }
+      if (!(ok = mbar_wait(bar(QB_DS), j & 1, ec, kSiteBwdMma))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_dq(j);
+        umma_commit(bar(QB_KE + j % ST));
+      }
+      __syncwarp();
+      if constexpr (ST == 1) {
+        if (more) {
+          if (!(ok = mbar_wait(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            issue_s(j + 1);
+            umma_commit(bar(QB_S));
+          }
+          __syncwarp();
+        }
+      }
+      if (more) {
+        if (!(ok = wait_kv(QB_VF, j + 1))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_dp(j + 1);
+          umma_commit(bar(QB_DP));
+          umma_commit(bar(QB_VE + (j + 1) % ST));
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      if (ok) umma_commit(bar(QB_DONE));
+      umma_commit(bar(QB_DRAIN));
+    }
+    __syncwarp();
+    mbar_wait(bar(QB_DRAIN), 0, ec, kSiteDrain, false);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int t = threadIdx.x;
+    const int row = t & 127;  // query row within the tile = TMEM lane
+    const int hf = t >> 7;    // key-column half
+    const int qr = q0 + row;
+    const bool row_ok = qr < p.S_q;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const size_t ridx = static_cast<size_t>(bh) * p.S_q + (row_ok ? qr : 0);
+    const float L = row_ok ? p.lse[ridx] : SDPA_NEG_INF;
+    const float nl2 = (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
+    const float Drow = row_ok ? p.delta[ridx] : 0.f;
+    const float* bias_row =
+        (p.bias != nullptr && row_ok) ? p.bias + (static_cast<size_t>(h) * p.S_q + qr) * p.S_kv : nullptr;
+    const bool bias_vec = (p.S_kv & 3) == 0;
+    const uint64_t lin_row = (static_cast<uint64_t>(bh) * p.S_q + qr) * p.S_kv;
+    bool ok = true;
+    auto body = [&](auto drop_tag) {
+      constexpr bool DROP = decltype(drop_tag)::value;
+      const float zk = p.keep_scale;
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int kc0 = j * BN + CW * hf;  // first key of this thread's columns
+        uint32_t keep[CW / 32] = {};
+        if constexpr (DROP) {
+#pragma unroll
+          for (int g = 0; g < CW / 4; ++g) {
+            const uint4 d = dropout_draws((lin_row + kc0) / 4 + g, p.seed_lo, p.seed_hi,
+                                          p.offset_lo, p.offset_hi);
+            const uint32_t k4 = static_cast<uint32_t>(d.x >= p.drop_threshold) |
+                                (static_cast<uint32_t>(d.y >= p.drop_threshold) << 1) |
+                                (static_cast<uint32_t>(d.z >= p.drop_threshold) << 2) |
+                                (static_cast<uint32_t>(d.w >= p.drop_threshold) << 3);
+            keep[g / 8] |= k4 << (4 * (g % 8));
+          }
+        }
+        auto zf = [&](int c) -> float {
+          if constexpr (DROP) return ((keep[c >> 5] >> (c & 31)) & 1u) ? zk : 0.f;
+          return 1.0f;
+        };
+        if (!(ok = mbar_wait(bar(QB_S), j & 1, ec, kSiteBwdCompute))) break;
+        tc_fence_after();
+        float pr[CW];
+#pragma unroll
+        for (int c = 0; c < CW / 32; ++c) {
+          uint32_t a0[32];
+          tmem_ld32(tbase + C::T_S + lane_off + CW * hf + 32 * c, a0);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pr[32 * c + e] = __uint_as_float(a0[e]) * p.scale_log2;
+        }
+        tc_fence_before();
+        mbar_arrive(bar(QB_SFREE));
+        if (bias_row != nullptr) {
+          if (bias_vec && kc0 + CW <= p.S_kv) {
+            const float4* b4 = reinterpret_cast<const float4*>(bias_row + kc0);
+#pragma unroll
+            for (int i = 0; i < CW / 4; ++i) {
+              const float4 v = __ldg(b4 + i);
+              pr[4 * i + 0] = fmaf(v.x, kLog2e, pr[4 * i + 0]);
+              pr[4 * i + 1] = fmaf(v.y, kLog2e, pr[4 * i + 1]);
+              pr[4 * i + 2] = fmaf(v.z, kLog2e, pr[4 * i + 2]);
+              pr[4 * i + 3] = fmaf(v.w, kLog2e, pr[4 * i + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < CW; ++c)
+              if (kc0 + c < p.S_kv) pr[c] = fmaf(__ldg(bias_row + kc0 + c), kLog2e, pr[c]);
+          }
+        }
+        const bool need_mask = (kc0 + CW > p.S_kv) || (p.causal && kc0 + CW - 1 > q0) || !row_ok;
+        if (need_mask) {
+          const int last = row_ok ? (p.causal ? min(p.S_kv - 1, qr) : p.S_kv - 1) : -1;
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            if (kc0 + c > last) pr[c] = SDPA_NEG_INF;
+        }
+#pragma unroll
+        for (int c = 0; c < CW; ++c) pr[c] = ex2(pr[c] + nl2);
+        if (!(ok = mbar_wait(bar(QB_DP), j & 1, ec, kSiteBwdCompute))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < CW / 32; ++c) {
+          uint32_t a0[32];
+          tmem_ld32(tbase + C::T_DP + lane_off + CW * hf + 32 * c, a0);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int cc = 32 * c + 2 * e;
+            const float d0 = __uint_as_float(a0[2 * e]), d1 = __uint_as_float(a0[2 * e + 1]);
+            const float s0 = pr[cc] * (DROP ? fmaf(d0, zf(cc), -Drow) : d0 - Drow);
+            const float s1 = pr[cc + 1] * (DROP ? fmaf(d1, zf(cc + 1), -Drow) : d1 - Drow);
+            pk[e] = pack2<BF16>(s0, s1);
+          }
+          // dS over the first half of the dP columns this thread has read
+          tmem_st16(tbase + C::T_DP + lane_off + CW * hf + 16 * c, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(QB_DS));
+      }
+    };
+    if (p.dropout)
+      body(std::true_type{});
+    else
+      body(std::false_type{});
+    // ---- epilogue: dQ * scale; each half writes half of the columns
+    if (ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute)) {
+      tc_fence_after();
+      constexpr int HW = DQK / 2;  // columns per thread
+      uint8_t* dst_row = static_cast<uint8_t*>(p.dq) + ridx * DQK * 2 + hf * HW * 2;
+#pragma unroll
+      for (int c = 0; c < HW / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tbase + C::T_DQ + lane_off + hf * HW + c * 32, a);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int DQK, int DV, bool BF16>
+cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
+  using C = DqCfg<DQK, DV>;
+  auto kern = sdpa_bwd_dq_kernel<DQK, DV, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (p.S_q + C::BM - 1) / C::BM;
+  const long long grid = static_cast<long long>(n_qt) * p.B * p.H;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, p);
+  return cudaGetLastError();
+}
+
+}  // namespace sdpa

@@ -22,7 +22,6 @@ enum : uint32_t {
   kSiteBwdLoad = 1u << 4,
   kSiteBwdMma = 1u << 5,
   kSiteBwdCompute = 1u << 6,
-  kSiteBwdDq = 1u << 7,
   kSiteDrain = 1u << 8,
 };
 
@@ -53,7 +52,7 @@ struct BwdParams {
   uint32_t seed_lo, seed_hi, offset_lo, offset_hi;
   const float* lse;        // [B, H, S_q]
   const float* delta;      // D = rowsum(dO * O)  [B, H, S_q]
-  float* dq_acc;           // [B, H, S_q, D_qk] fp32, zeroed before the main kernel
+  void* dq;                // [B, H, S_q, D_qk]
   void* dk;                // [B, H, S_kv, D_qk]
   void* dv;                // [B, H, S_kv, D_v]
   uint32_t* err;
@@ -130,17 +129,20 @@ cudaError_t launch_fwd_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUten
                             const CUtensorMap& v, const FwdParams& p, cudaStream_t st);
 cudaError_t launch_fwd_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
                             const CUtensorMap& v, const FwdParams& p, cudaStream_t st);
-cudaError_t launch_bwd_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
-                            const BwdParams& p, cudaStream_t st);
-cudaError_t launch_bwd_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                            const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dq,
-                            const BwdParams& p, cudaStream_t st);
-cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta,
-                           float* dq_acc, float* dbias, int64_t rows, int d_v, int64_t dq_elems,
-                           int64_t dbias_elems, cudaStream_t st);
-cudaError_t launch_dq_convert(bool bf16, const float* dq_acc, void* dq, float scale,
-                              int64_t elems, cudaStream_t st);
+cudaError_t launch_bwd_dkdv_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                                 const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                                 cudaStream_t st);
+cudaError_t launch_bwd_dkdv_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                                 const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                                 cudaStream_t st);
+cudaError_t launch_bwd_dq_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                               cudaStream_t st);
+cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                               cudaStream_t st);
+cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta, float* dbias,
+                           int64_t rows, int d_v, int64_t dbias_elems, cudaStream_t st);
 cudaError_t launch_dropout_mask(int64_t total, uint32_t threshold, uint32_t seed_lo,
                                 uint32_t seed_hi, uint32_t off_lo, uint32_t off_hi,
                                 uint32_t* bits, cudaStream_t st);

@@ -5,16 +5,17 @@
 // pool and forbids allocations from outside it, or a latency-critical loop
 // where cudaMalloc's implicit device synchronisation and unbounded latency are
 // not acceptable. For them this entry point keeps the backward scratch (the
-// per-row D values and the fp32 dQ accumulator) in a fixed, file-scope device
-// array that exists for as long as the library is loaded, on every GPU that
-// loads it. It calls no cudaMalloc, cudaFree or other allocating routine.
+// per-row D = rowsum(dO * O) values the backward kernels share) in a fixed,
+// file-scope device array that exists for as long as the library is loaded,
+// on every GPU that loads it. It calls no cudaMalloc, cudaFree or other
+// allocating routine.
 //
 // Limits and sharing:
 // * The array holds kNoAllocScratchBytes (16 MiB). A problem whose scratch
 //   (sdpa_bwd_workspace_size) is larger is rejected with SDPA_ERR_WORKSPACE.
 // * Every call on a device uses the same array and leaves its contents behind;
-//   the preprocess kernel of each call overwrites D and zeroes the dQ
-//   accumulator before the main kernel reads them, so nothing carries over.
+//   the preprocess kernel of each call overwrites D before the other kernels
+//   read it, so nothing carries over.
 //   Calls whose kernels overlap on the GPU (for example on two streams at
 //   once) race on the array and give wrong gradients: serialise them.
 // * Host code cannot use the array's name as a device address. The first call
