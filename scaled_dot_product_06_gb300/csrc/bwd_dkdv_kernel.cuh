@@ -9,17 +9,17 @@
 // kernel in bwd_dq_kernel.cuh, so this kernel has no cross-CTA accumulation
 // other than dBias.
 //
-// One CTA owns 128 key rows of one (b, h) (K_j and V_j stay in shared memory)
-// and loops over query tiles of BM rows (128, or 64 at d_qk = 192 where tensor
+// One CTA owns 128 key rows of one (b, h) (K_j and V_j stay resident) and
+// loops over query tiles of BM rows (128, or 64 at d_qk = 192 where tensor
 // memory is short). Every product keeps the 128 keys in the MMA's M dimension
 // (the TMEM lanes):
-//   S^T  = K Q_i^T      [128 x BM]  A = K (smem, K-major),  B = Q_i (K-major)
-//   dP^T = V dO_i^T     [128 x BM]  A = V (smem, K-major),  B = dO_i (K-major)
-//   dV  += P~^T dO_i    [128 x Dv]  A = P~^T (TMEM),        B = dO_i (MN-major)
-//   dK  += dS^T Q_i     [128 x Dk]  A = dS^T (TMEM),        B = Q_i (MN-major)
-// With BM = 128 every shared-memory operand pair stays within the shared
-// memory read rate (an M=128 product with both operands in shared memory
-// needs N >= 128), and the two products with an operand in TMEM read only B.
+//   S^T  = K Q_i^T      [128 x BM]  A = K,              B = Q_i (smem, K-major)
+//   dP^T = V dO_i^T     [128 x BM]  A = V,              B = dO_i (smem, K-major)
+//   dV  += P~^T dO_i    [128 x Dv]  A = P~^T (TMEM),    B = dO_i (smem, MN-major)
+//   dK  += dS^T Q_i     [128 x Dk]  A = dS^T (TMEM),    B = Q_i (smem, MN-major)
+// K and V are read from shared memory, or, when tensor memory has room for
+// them next to the accumulators (d_qk = 64), copied once per CTA into TMEM so
+// that S^T and dP^T read only their B operand from shared memory.
 // Roles (320 threads):
 //   warps 0-7  compute, two warpgroups: warp w owns key rows 32*(w%4)..+31 (its
 //              TMEM lanes) and query columns [hf*BM/2, (hf+1)*BM/2), hf = w/4.
@@ -32,7 +32,7 @@
 //              dK(i), dP^T(i+1), so the softmax of tile i+1 overlaps dK(i)
 //              and dP^T(i+1), and dS of tile i overlaps dV(i) and S^T(i+1).
 // Tensor memory (512 columns): S^T [0,BM), dP^T [BM,2BM), dV [2BM,2BM+Dv),
-// dK [2BM+Dv, 2BM+Dv+Dk).
+// dK [2BM+Dv, 2BM+Dv+Dk), then K and V (two elements per column) if they fit.
 #pragma once
 #include <type_traits>
 
@@ -60,13 +60,17 @@ struct DkdvCfg {
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = BM, T_DV = 2 * BM, T_DK = 2 * BM + DV;
+  // K and V, the operands every tile reuses, live in TMEM when they fit, so
+  // S^T and dP^T take A from TMEM and read only Q_i / dO_i from shared memory.
+  static constexpr uint32_t T_K = T_DK + DQK, T_V = T_K + DQK / 2;
+  static constexpr bool OPS_IN_TMEM = T_V + DV / 2 <= 512;
   static_assert(T_DK + DQK <= 512, "tensor memory overflow");
   static_assert(SMEM <= 227 * 1024, "shared memory overflow");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128 && DQK <= 192, "head size");
 };
 
 enum : int { AB_KV = 0, AB_QF, AB_DOF = AB_QF + 2, AB_QE = AB_DOF + 2, AB_S = AB_QE + 2, AB_P,
-             AB_DP, AB_DS, AB_DKDV, AB_DRAIN, AB_COUNT };
+             AB_DP, AB_DS, AB_DKDV, AB_DRAIN, AB_OPS, AB_COUNT };
 
 // Keep bits of key row k for the 32 query rows [row0, row0 + 32) of a tile.
 // One Philox block covers four consecutive keys of one query row, i.e. the
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AB_COUNT; ++i)
-      mbar_init(bar(i), (i == AB_P || i == AB_DS) ? 256u : 1u);
+      mbar_init(bar(i), (i == AB_P || i == AB_DS || i == AB_OPS) ? 256u : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -203,22 +207,35 @@ __global__ void __launch_bounds__(320, 1)
     auto packed_col = [](int kk) -> uint32_t {
       return static_cast<uint32_t>(((kk * 16) / CW) * CW + ((kk * 16) % CW) / 2);
     };
+    // base descriptors, advanced by constant offsets per instruction
+    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dV0 = sdesc_sw128(sV, 16, 1024);
+    const uint64_t dQk0 = sdesc_sw128(sQ, 16, 1024), dOk0 = sdesc_sw128(sdO, 16, 1024);
+    const uint64_t dQm0 = sdesc_sw128(sQ, BM * 128, 1024), dOm0 = sdesc_sw128(sdO, BM * 128, 1024);
     auto issue_s = [&](int s) {  // S^T = K Q^T
-      const uint32_t qb = sQ + s * C::Q_BYTES;
+      const uint64_t dq = desc_adv(dQk0, s * C::Q_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < DQK / 16; ++kk)
-        umma_ss(tS, sdesc_sw128(sK + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024),
-                sdesc_sw128(qb + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024), kIdS, kk > 0);
+      for (int kk = 0; kk < DQK / 16; ++kk) {
+        const uint64_t bq = desc_adv(dq, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
+        if constexpr (C::OPS_IN_TMEM)
+          umma_ts(tS, tbase + C::T_K + kk * 8, bq, kIdS, kk > 0);
+        else
+          umma_ss(tS, desc_adv(dK0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bq, kIdS, kk > 0);
+      }
     };
     auto issue_dp = [&](int s) {  // dP^T = V dO^T
-      const uint32_t ob = sdO + s * C::DO_BYTES;
+      const uint64_t dob = desc_adv(dOk0, s * C::DO_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < DV / 16; ++kk)
-        umma_ss(tDP, sdesc_sw128(sV + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024),
-                sdesc_sw128(ob + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024), kIdS, kk > 0);
+      for (int kk = 0; kk < DV / 16; ++kk) {
+        const uint64_t bo = desc_adv(dob, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
+        if constexpr (C::OPS_IN_TMEM)
+          umma_ts(tDP, tbase + C::T_V + kk * 8, bo, kIdS, kk > 0);
+        else
+          umma_ss(tDP, desc_adv(dV0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bo, kIdS, kk > 0);
+      }
     };
     bool ok = n_it > 0;
     if (ok) ok = mbar_wait(bar(AB_KV), 0, ec, kSiteBwdMma);
+    if (C::OPS_IN_TMEM && ok) ok = mbar_wait(bar(AB_OPS), 0, ec, kSiteBwdMma);
     if (ok) ok = mbar_wait(bar(AB_QF), 0, ec, kSiteBwdMma);
     if (ok) {
       tc_fence_after();
@@ -243,11 +260,10 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = mbar_wait(bar(AB_P), i & 1, ec, kSiteBwdMma))) break;
       tc_fence_after();
       if (lane == 0) {  // dV += P~^T dO_i
-        const uint32_t ob = sdO + s * C::DO_BYTES;
+        const uint64_t dob = desc_adv(dOm0, s * C::DO_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(tDV, tS + packed_col(kk), sdesc_sw128(ob + kk * 2048, BM * 128, 1024), kIdDV,
-                  (i > 0 || kk > 0));
+          umma_ts(tDV, tS + packed_col(kk), desc_adv(dob, kk * 2048), kIdDV, (i > 0 || kk > 0));
       }
       __syncwarp();
       if (i + 1 < n_it) {
@@ -262,11 +278,10 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = mbar_wait(bar(AB_DS), i & 1, ec, kSiteBwdMma))) break;
       tc_fence_after();
       if (lane == 0) {  // dK += dS^T Q_i
-        const uint32_t qb = sQ + s * C::Q_BYTES;
+        const uint64_t dqb = desc_adv(dQm0, s * C::Q_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(tDK, tDP + packed_col(kk), sdesc_sw128(qb + kk * 2048, BM * 128, 1024), kIdDK,
-                  (i > 0 || kk > 0));
+          umma_ts(tDK, tDP + packed_col(kk), desc_adv(dqb, kk * 2048), kIdDK, (i > 0 || kk > 0));
         umma_commit(bar(AB_QE + s));  // Q_i and dO_i are no longer read
       }
       __syncwarp();
@@ -311,6 +326,18 @@ __global__ void __launch_bounds__(320, 1)
       if (t < 2 * BM) rowbuf[(t < BM ? 0 : 2 * BM) + (i & 1) * BM + (t % BM)] = v;
     };
     bool ok = true;
+    if (C::OPS_IN_TMEM && n_it > 0) {  // K and V rows into this thread's TMEM lane
+      ok = mbar_wait(bar(AB_KV), 0, ec, kSiteBwdCompute);
+      if (ok) {
+        smem_row_to_tmem<DQK / 2>(smem + C::OFF_K, C::BN, row, hf * (DQK / 2),
+                                  tbase + lane_off + C::T_K + hf * (DQK / 4));
+        smem_row_to_tmem<DV / 2>(smem + C::OFF_V, C::BN, row, hf * (DV / 2),
+                                 tbase + lane_off + C::T_V + hf * (DV / 4));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(AB_OPS));
+      }
+    }
     auto body = [&](auto drop_tag) {
       constexpr bool DROP = decltype(drop_tag)::value;
       const float zk = p.keep_scale;

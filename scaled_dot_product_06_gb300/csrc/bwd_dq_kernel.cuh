@@ -22,7 +22,10 @@
 //              dP columns it has read.
 //   warp 8     TMA producer (Q, dO once; K_j and V_j through a ring).
 //   warp 9     MMA issuer (one lane).
-// Tensor memory (512 columns): S [0,128), dP [128,256), dQ [256, 256+Dk).
+// Tensor memory (512 columns): S [0,128), dP [128,256), dQ [256, 256+Dk),
+// then Q and dO (two elements per column) when they fit (d_qk <= 128): the S
+// and dP products then take A from TMEM and read only K_j / V_j from shared
+// memory, which keeps the tensor core within the shared-memory read rate.
 #pragma once
 #include <type_traits>
 
@@ -47,12 +50,16 @@ struct DqCfg {
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+  // Q and dO, the operands every tile reuses, live in TMEM when they fit, so
+  // the S and dP products read only K_j / V_j from shared memory.
+  static constexpr bool OPS_IN_TMEM = DQK + DQK / 2 + DV / 2 <= 256;
+  static constexpr uint32_t T_Q = T_DQ + DQK, T_DO = T_Q + DQK / 2;
   static_assert(T_DQ + DQK <= 512, "tensor memory overflow");
   static_assert(SMEM <= 227 * 1024, "shared memory overflow");
 };
 
 enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_VF + 2,
-             QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DS, QB_DONE, QB_DRAIN, QB_COUNT };
+             QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DS, QB_DONE, QB_DRAIN, QB_OPS, QB_COUNT };
 
 template <int DQK, int DV, bool BF16>
 __global__ void __launch_bounds__(320, 1)
@@ -87,7 +94,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_COUNT; ++i)
-      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS) ? 256u : 1u);
+      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS || i == QB_OPS) ? 256u : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -152,35 +159,44 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t kIdS = idesc_f16(128, BN, BF16, false, false);
     constexpr uint32_t kIdDQ = idesc_f16(128, DQK, BF16, false, true);
     const uint32_t tS = tbase + C::T_S, tDP = tbase + C::T_DP, tDQ = tbase + C::T_DQ;
+    // base descriptors, advanced by constant offsets per instruction
+    const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dO0 = sdesc_sw128(sdO, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dV0 = sdesc_sw128(sV, 16, 1024);
+    const uint64_t dKm0 = sdesc_sw128(sK, BN * 128, 1024);
     auto issue_s = [&](int j) {  // S = Q K_j^T
-      const uint32_t kb = sK + (j % ST) * C::K_BYTES;
+      const uint64_t dk = desc_adv(dK0, (j % ST) * C::K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < DQK / 16; ++kk) {
-        const uint32_t qa = sQ + (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-        const uint32_t kb2 = kb + (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-        umma_ss(tS, sdesc_sw128(qa, 16, 1024), sdesc_sw128(kb2, 16, 1024), kIdS, kk > 0);
+        const uint64_t bk = desc_adv(dk, (kk >> 2) * (BN * 128) + (kk & 3) * 32);
+        if constexpr (C::OPS_IN_TMEM)
+          umma_ts(tS, tbase + C::T_Q + kk * 8, bk, kIdS, kk > 0);
+        else
+          umma_ss(tS, desc_adv(dQ0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bk, kIdS, kk > 0);
       }
     };
     auto issue_dp = [&](int j) {  // dP = dO V_j^T
-      const uint32_t vb = sV + (j % ST) * C::V_BYTES;
+      const uint64_t dv = desc_adv(dV0, (j % ST) * C::V_BYTES);
 #pragma unroll
       for (int kk = 0; kk < DV / 16; ++kk) {
-        const uint32_t oa = sdO + (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-        const uint32_t vb2 = vb + (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-        umma_ss(tDP, sdesc_sw128(oa, 16, 1024), sdesc_sw128(vb2, 16, 1024), kIdS, kk > 0);
+        const uint64_t bv = desc_adv(dv, (kk >> 2) * (BN * 128) + (kk & 3) * 32);
+        if constexpr (C::OPS_IN_TMEM)
+          umma_ts(tDP, tbase + C::T_DO + kk * 8, bv, kIdS, kk > 0);
+        else
+          umma_ss(tDP, desc_adv(dO0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bv, kIdS, kk > 0);
       }
     };
     auto issue_dq = [&](int j) {  // dQ += dS K_j, dS packed two per column
-      const uint32_t kb = sK + (j % ST) * C::K_BYTES;
+      const uint64_t dk = desc_adv(dKm0, (j % ST) * C::K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
-        umma_ts(tDQ, tDP + (kk >> 2) * CW + (kk & 3) * 8,
-                sdesc_sw128(kb + kk * 2048, BN * 128, 1024), kIdDQ, (j > 0 || kk > 0));
+        umma_ts(tDQ, tDP + (kk >> 2) * CW + (kk & 3) * 8, desc_adv(dk, kk * 2048), kIdDQ,
+                (j > 0 || kk > 0));
     };
     auto wait_kv = [&](int which, int j) {
       return mbar_wait(bar(which + j % ST), (j / ST) & 1, ec, kSiteBwdMma);
     };
     bool ok = mbar_wait(bar(QB_Q), 0, ec, kSiteBwdMma) && wait_kv(QB_KF, 0);
+    if (C::OPS_IN_TMEM && ok) ok = mbar_wait(bar(QB_OPS), 0, ec, kSiteBwdMma);
     if (ok) {
       tc_fence_after();
       if (lane == 0) {
@@ -266,6 +282,18 @@ __global__ void __launch_bounds__(320, 1)
     const bool bias_vec = (p.S_kv & 3) == 0;
     const uint64_t lin_row = (static_cast<uint64_t>(bh) * p.S_q + qr) * p.S_kv;
     bool ok = true;
+    if constexpr (C::OPS_IN_TMEM) {  // Q and dO rows into this thread's TMEM lane
+      ok = mbar_wait(bar(QB_Q), 0, ec, kSiteBwdCompute);
+      if (ok) {
+        smem_row_to_tmem<DQK / 2>(smem + C::OFF_Q, BM, row, hf * (DQK / 2),
+                                  tbase + lane_off + C::T_Q + hf * (DQK / 4));
+        smem_row_to_tmem<DV / 2>(smem + C::OFF_DO, BM, row, hf * (DV / 2),
+                                 tbase + lane_off + C::T_DO + hf * (DV / 4));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(QB_OPS));
+      }
+    }
     auto body = [&](auto drop_tag) {
       constexpr bool DROP = decltype(drop_tag)::value;
       const float zk = p.keep_scale;

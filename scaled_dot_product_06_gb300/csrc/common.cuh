@@ -119,6 +119,34 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// Copies elements [e0, e0 + N) of row `row` of a 128-byte-swizzled K-major
+// shared-memory tile (64-element boxes of `rows_per_box` rows, as TMA writes
+// them) into the calling thread's TMEM lane at `taddr`, two elements per
+// 32-bit column: the layout of an MMA A operand read from tensor memory.
+// taddr must address column e0 / 2 of the thread's own lane. Caller waits with
+// tmem_wait_st() before signalling the MMA issuer.
+template <int N>
+__device__ __forceinline__ void smem_row_to_tmem(const uint8_t* tile, int rows_per_box, int row,
+                                                 int e0, uint32_t taddr) {
+  static_assert(N % 32 == 0, "whole 16-column stores");
+#pragma unroll
+  for (int c = 0; c < N / 32; ++c) {
+    uint32_t r[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = e0 + c * 32 + q * 8;
+      const int chunk = (e & 63) >> 3;
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + (e >> 6) * rows_per_box * 128 +
+                                                      row * 128 + ((chunk ^ (row & 7)) << 4));
+      r[4 * q + 0] = v.x;
+      r[4 * q + 1] = v.y;
+      r[4 * q + 2] = v.z;
+      r[4 * q + 3] = v.w;
+    }
+    tmem_st16(taddr + c * 16, r);
+  }
+}
+
 // Records a failure detail for sdpa_last_error() on the calling thread.
 void set_last_error(const char* msg);
 

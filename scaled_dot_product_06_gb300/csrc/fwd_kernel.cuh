@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
     constexpr uint32_t kIdO = idesc_f16(128, DV, BF16, false, true);
+    const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(sV, C::BN * 128, 1024);
     bool ok = mbar_wait(bar(FB_Q), 0, ec, kSiteFwdMma);
     for (int j = 0; ok && j < n_kv; ++j) {
       const int s = j % C::STAGES;
@@ -153,12 +156,11 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
       if (!(ok = mbar_wait(bar(FB_KF + s), ph, ec, kSiteFwdMma))) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t kb = sK + s * C::K_BYTES;
+        const uint64_t dK = desc_adv(dK0, s * C::K_BYTES);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          umma_ss(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdS,
-                  kk > 0);
+          umma_ss(tS, desc_adv(dQ0, off), desc_adv(dK, off), kIdS, kk > 0);
         }
         umma_commit(bar(FB_S));
         umma_commit(bar(FB_KE + s));
@@ -168,11 +170,10 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
       if (!(ok = mbar_wait(bar(FB_VF + s), ph, ec, kSiteFwdMma))) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t vb = sV + s * C::V_BYTES;
+        const uint64_t dV = desc_adv(dV0, s * C::V_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(tO, tS + kk * 8, sdesc_sw128(vb + kk * 2048, C::BN * 128, 1024), kIdO,
-                  (j > 0 || kk > 0));
+          umma_ts(tO, tS + kk * 8, desc_adv(dV, kk * 2048), kIdO, (j > 0 || kk > 0));
         umma_commit(bar(FB_VE + s));
       }
       __syncwarp();

@@ -160,6 +160,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the same operand `bytes` further on in shared memory
+// (the start-address field counts 16-byte units). MMA issue loops build each
+// base descriptor once and advance it with constant offsets: a tcgen05.mma
+// takes 64 cycles of tensor-core time at M=128, N=128, so the issuing thread
+// must spend far fewer than that per instruction.
+__device__ __forceinline__ uint64_t desc_adv(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 //   ab_bf16: operands are bf16 (else fp16); a_mn / b_mn: operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, bool ab_bf16, bool a_mn,
