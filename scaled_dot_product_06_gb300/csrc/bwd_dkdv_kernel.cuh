@@ -20,15 +20,16 @@
 // K and V are read from shared memory, or, when tensor memory has room for
 // them next to the accumulators (d_qk = 64), copied once per CTA into TMEM so
 // that S^T and dP^T read only their B operand from shared memory.
-// Roles (320 threads):
-//   warps 0-7  compute, two warpgroups: warp w owns key rows 32*(w%4)..+31 (its
-//              TMEM lanes) and query columns [hf*BM/2, (hf+1)*BM/2), hf = w/4.
+// Roles (BM/32 compute warpgroups, a producer warp and an MMA warp):
+//   compute    warp w owns key rows 32*(w%4)..+31 (its TMEM lanes) and query
+//              columns [32*hf, 32*hf + 32), hf = w/4, so each scheduler runs
+//              BM/32 compute warps whose latencies hide one another.
 //              Recomputes P^T and writes P~^T (io dtype) over the first half
 //              of the S^T columns it has read; forms dS^T, adds it into dBias
 //              (fp32 atomics) and writes it (io dtype) over the dP^T columns
 //              it has read.
-//   warp 8     TMA producer (K, V once; Q_i and dO_i through a 2-stage ring).
-//   warp 9     MMA issuer (one lane), order per tile i: dV(i), S^T(i+1),
+//   producer   TMA for K, V once and Q_i, dO_i through a 2-stage ring.
+//   MMA        one lane issues, order per tile i: dV(i), S^T(i+1),
 //              dK(i), dP^T(i+1), so the softmax of tile i+1 overlaps dK(i)
 //              and dP^T(i+1), and dS of tile i overlaps dV(i) and S^T(i+1).
 // Tensor memory (512 columns): S^T [0,BM), dP^T [BM,2BM), dV [2BM,2BM+Dv),
@@ -44,7 +45,9 @@ template <int DQK, int DV>
 struct DkdvCfg {
   static constexpr int BN = 128;                      // key rows per CTA
   static constexpr int BM = (DQK <= 128) ? 128 : 64;  // query rows per tile
-  static constexpr int CW = BM / 2;                   // query columns per compute thread
+  static constexpr int NQ = BM / 32;                  // compute warpgroups (32 query columns each)
+  static constexpr int CW = BM / NQ;                  // query columns per compute thread
+  static constexpr int NCT = 128 * NQ;                // compute threads
   static constexpr int STAGES = 2;
   static constexpr int K_BYTES = BN * DQK * 2;
   static constexpr int V_BYTES = BN * DV * 2;
@@ -57,7 +60,7 @@ struct DkdvCfg {
   static constexpr int OFF_ROW = OFF_DO + STAGES * DO_BYTES;  // [2][BM] -LSE log2e, [2][BM] D
   static constexpr int OFF_BAR = OFF_ROW + 4 * BM * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = NCT + 64;            // + producer warp + MMA warp
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = BM, T_DV = 2 * BM, T_DK = 2 * BM + DV;
   // K and V, the operands every tile reuses, live in TMEM when they fit, so
@@ -99,13 +102,13 @@ __device__ __forceinline__ void keep_bits_transposed(uint64_t lin_quad, int S_kv
 }
 
 template <int DQK, int DV, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
   using C = DkdvCfg<DQK, DV>;
-  constexpr int BM = C::BM, CW = C::CW;
+  constexpr int BM = C::BM, CW = C::CW, NCT = C::NCT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(320, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kLoadWarp = 8, kMmaWarp = 9;
+  constexpr int kLoadWarp = NCT / 32, kMmaWarp = NCT / 32 + 1;
 
   // ---- key tile of this CTA: head-major (one head's Q / dO stay in L2), then
   // the key tiles with the most query work first, batch fastest (the batches
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AB_COUNT; ++i)
-      mbar_init(bar(i), (i == AB_P || i == AB_DS || i == AB_OPS) ? 256u : 1u);
+      mbar_init(bar(i), (i == AB_P || i == AB_DS || i == AB_OPS) ? static_cast<uint32_t>(NCT) : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ compute
     const int t = threadIdx.x;
     const int row = t & 127;  // key row within the tile = TMEM lane
-    const int hf = t >> 7;    // query-column half
+    const int hf = t >> 7;    // query-column group
     const int kv = k0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const bool kv_ok = kv < p.S_kv;
@@ -328,15 +331,15 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     if (C::OPS_IN_TMEM && n_it > 0) {  // K and V rows into this thread's TMEM lane
       ok = mbar_wait(bar(AB_KV), 0, ec, kSiteBwdCompute);
-      if (ok) {
+      if (ok && hf < 2) {  // the first two groups copy one half of the columns each
         smem_row_to_tmem<DQK / 2>(smem + C::OFF_K, C::BN, row, hf * (DQK / 2),
                                   tbase + lane_off + C::T_K + hf * (DQK / 4));
         smem_row_to_tmem<DV / 2>(smem + C::OFF_V, C::BN, row, hf * (DV / 2),
                                  tbase + lane_off + C::T_V + hf * (DV / 4));
         tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(AB_OPS));
       }
+      tc_fence_before();
+      if (ok) mbar_arrive(bar(AB_OPS));
     }
     auto body = [&](auto drop_tag) {
       constexpr bool DROP = decltype(drop_tag)::value;
@@ -345,7 +348,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; ok && i < n_it; ++i) {
         const int q0 = (it0 + i) * BM;
         const int qc0 = q0 + CW * hf;  // first query row of this thread's columns
-        named_bar_sync(2, 256);        // tile i's statistics are in shared memory
+        named_bar_sync(2, NCT);        // tile i's statistics are in shared memory
         const float4* nl2 = reinterpret_cast<const float4*>(nl2_buf + (i & 1) * BM + CW * hf);
         const float4* dd = reinterpret_cast<const float4*>(d_buf + (i & 1) * BM + CW * hf);
         const float next_stat = (t < 2 * BM && i + 1 < n_it) ? fetch_row_stat(i + 1) : 0.f;
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(320, 1)
       };
       if (hf == 0)
         write_rows(std::integral_constant<int, DV>{}, C::T_DV, p.dv, 1.0f);
-      else
+      else if (hf == 1)
         write_rows(std::integral_constant<int, DQK>{}, C::T_DK, p.dk, p.scale);
     }
   }
