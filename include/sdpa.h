@@ -83,9 +83,11 @@ sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
                        const void* v, const float* bias, void* o, float* lse, void* stream);
 
 /*
- * Bytes of device workspace sdpa_bwd needs: D = rowsum(dO * O), fp32
- * [b,h,s_q], rounded up to 256 bytes (oneDNN's sdpa micro.cpp books the same
- * buffer in its scratchpad). Returns 0 for invalid sizes.
+ * Bytes of device workspace sdpa_bwd needs: two fp32 row statistics per query
+ * row, D = rowsum(dO * O) (oneDNN's sdpa micro.cpp books the same buffer in
+ * its scratchpad) and -LSE * log2(e), with s_q padded up to a multiple of 128
+ * for each (b, h): 8 * b * h * ceil(s_q / 128) * 128 bytes, rounded up to 256.
+ * Returns 0 for invalid sizes.
  */
 size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v);
@@ -101,7 +103,7 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
  *   workspace caller-owned device memory of at least
  *             sdpa_bwd_workspace_size(...) bytes, 256-byte aligned; its
  *             contents on entry are ignored and on exit are unspecified.
- * Runs three kernels on `stream`: preprocess (D; zero dBias), the
+ * Runs three kernels on `stream`: preprocess (row statistics; zero dBias), the
  * key/value-stationary kernel (dK, dV, dBias) and the query-stationary kernel
  * (dQ). dQ, dK and dV are bitwise reproducible; dBias sums the batch with
  * fp32 atomics, reproducible for b <= 2.
@@ -115,7 +117,7 @@ sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
 
 /* Phases of the backward pass, in the order they must run. */
 typedef enum {
-  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O); zero dBias */
+  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O) and -LSE*log2e; zero dBias */
   SDPA_BWD_DKDV = 2,       /* key/value-stationary kernel: dK, dV, dBias */
   SDPA_BWD_DQ = 4,         /* query-stationary kernel: dQ */
   SDPA_BWD_ALL = 7
@@ -127,8 +129,9 @@ typedef enum {
  * phases in order, with the same arguments, on one stream is exactly
  * sdpa_bwd; they are separate so a caller can time them one by one (the CK
  * page also splits its backward into three kernels). The dK/dV and dQ phases
- * both read D from `workspace`, and the dK/dV phase adds into `dbias`, so the
- * preprocess phase must run first.
+ * both read the row statistics the preprocess phase leaves in `workspace`,
+ * and the dK/dV phase adds into `dbias`, so the preprocess phase must run
+ * first.
  */
 sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int is_causal,

@@ -192,8 +192,9 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
                                int64_t d_v) {
   bool empty = false;
   if (check_sizes(b, h, s_q, s_kv, d_qk, d_v, 0.0f, SDPA_BF16, &empty) != SDPA_OK) return 0;
-  const size_t rows = static_cast<size_t>(b) * h * s_q;
-  return (rows * sizeof(float) + 255) & ~size_t(255);
+  // two floats (-LSE*log2e, D) per query row, rows padded to 128 per (b, h)
+  const size_t prows = static_cast<size_t>(b) * h * static_cast<size_t>(sdpa::stat_pad(static_cast<int>(s_q)));
+  return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
 }
 
 sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
@@ -219,8 +220,7 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
 
   const bool bf16 = dtype == SDPA_BF16;
   const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const size_t rows = static_cast<size_t>(b) * h * s_q;
-  float* delta = static_cast<float*>(workspace);
+  float* stats = static_cast<float*>(workspace);
   const int di = static_cast<int>(d_qk), dvi = static_cast<int>(d_v);
 
   BwdParams p{};
@@ -240,8 +240,8 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
   p.seed_hi = static_cast<uint32_t>(seed >> 32);
   p.offset_lo = static_cast<uint32_t>(offset);
   p.offset_hi = static_cast<uint32_t>(offset >> 32);
-  p.lse = lse;
-  p.delta = delta;
+  p.stats = stats;
+  p.S_pad = stat_pad(static_cast<int>(s_q));
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -251,7 +251,7 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
   cudaError_t e = cudaSuccess;
   if (phases & SDPA_BWD_PREPROCESS) {
     const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
-    e = launch_bwd_pre(bf16, o, dout, delta, dbias, static_cast<int64_t>(rows), dvi, dbias_elems, st);
+    e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, b * h, static_cast<int>(s_q), dvi, dbias_elems, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
   }
   if (phases & SDPA_BWD_DKDV) {

@@ -1,7 +1,8 @@
 // Memory-bound helper kernels of the backward pass and the dropout-mask hook.
 //
 // * bwd_pre: D = rowsum(dO * O) in fp32 (CK tile fmha_bwd_kernel.hpp,
-//   FmhaBwdOGradDotOKernel; the D line of the header equations), and zeroing
+//   FmhaBwdOGradDotOKernel; the D line of the header equations) next to
+//   -LSE * log2(e), in the tiled row-statistics layout of stat_index, and zeroing
 //   of dBias, which the key/value-stationary kernel accumulates into (oneDNN
 //   sdpa micro.cpp, execute_backward: preprocess and fill of the f32
 //   intermediates).
@@ -23,23 +24,30 @@ static int aux_grid(int64_t work_items) {
 }
 
 // One group of DV/8 consecutive threads per row; each thread takes 8 elements.
+// Walks the padded rows (S_pad per (b, h)) so the padding of the statistics is
+// written too: -inf and 0 there, as for a query row that sees no key.
 template <bool BF16>
 __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __restrict__ o,
                                                               const uint4* __restrict__ dout,
-                                                              float* __restrict__ delta,
+                                                              const float* __restrict__ lse,
+                                                              float* __restrict__ stats,
                                                               float4* __restrict__ dbias,
-                                                              int64_t rows, int d_v,
-                                                              int64_t dbias_elems) {
+                                                              int64_t bh_count, int s_q, int s_pad,
+                                                              int d_v, int64_t dbias_elems) {
   const int group = d_v / 8;  // 8 or 16 threads per row (power of two)
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x & 31, sub = lane % group;
   const int64_t rows_per_warp = 32 / group;
   const int64_t warp_id = tid / 32, nwarps = nthreads / 32;
+  const int64_t prow_count = bh_count * s_pad;
   // wbase is uniform across the warp, so every lane reaches every shuffle
-  for (int64_t wbase = warp_id * rows_per_warp; wbase < rows; wbase += nwarps * rows_per_warp) {
-    const int64_t row = wbase + lane / group;
-    const bool live = row < rows;
+  for (int64_t wbase = warp_id * rows_per_warp; wbase < prow_count; wbase += nwarps * rows_per_warp) {
+    const int64_t prow = wbase + lane / group;  // padded row
+    const int64_t bh = prow / s_pad;
+    const int q = static_cast<int>(prow - bh * s_pad);
+    const bool live = prow < prow_count && q < s_q;
+    const int64_t row = bh * s_q + q;  // row of O, dO and LSE
     float acc = 0.f;
     if (live) {
       const uint4 a = o[row * group + sub];
@@ -53,7 +61,12 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
       }
     }
     for (int off = group / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, group);
-    if (live && sub == 0) delta[row] = acc;
+    if (prow < prow_count && sub == 0) {
+      const float L = live ? lse[row] : SDPA_NEG_INF;
+      const size_t si = stat_index(static_cast<size_t>(bh), s_pad, q);
+      stats[si] = (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
+      stats[si + 64] = acc;
+    }
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t dbias_vec = dbias_elems / 4;
@@ -84,15 +97,17 @@ __global__ void __launch_bounds__(kAuxThreads) dropout_mask_kernel(int64_t total
   }
 }
 
-cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta, float* dbias,
-                           int64_t rows, int d_v, int64_t dbias_elems, cudaStream_t st) {
+cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
+                           float* dbias, int64_t bh, int s_q, int d_v, int64_t dbias_elems,
+                           cudaStream_t st) {
   const int group = d_v / 8;
-  const int64_t work = rows * group;
+  const int s_pad = stat_pad(s_q);
+  const int64_t work = bh * s_pad * group;
   const int64_t zero_work = dbias_elems / 4;
   const int grid = aux_grid(work > zero_work ? work : zero_work);
   auto kern = bf16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
-  kern<<<grid, kAuxThreads, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), delta,
-                                      reinterpret_cast<float4*>(dbias), rows, d_v, dbias_elems);
+  kern<<<grid, kAuxThreads, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, stats,
+                                      reinterpret_cast<float4*>(dbias), bh, s_q, s_pad, d_v, dbias_elems);
   return cudaGetLastError();
 }
 

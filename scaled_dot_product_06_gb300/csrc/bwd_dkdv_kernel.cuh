@@ -24,14 +24,24 @@
 //   compute    warp w owns key rows 32*(w%4)..+31 (its TMEM lanes) and query
 //              columns [32*hf, 32*hf + 32), hf = w/4, so each scheduler runs
 //              BM/32 compute warps whose latencies hide one another.
-//              Recomputes P^T and writes P~^T (io dtype) over the first half
-//              of the S^T columns it has read; forms dS^T, adds it into dBias
-//              (fp32 atomics) and writes it (io dtype) over the dP^T columns
-//              it has read.
-//   producer   TMA for K, V once and Q_i, dO_i through a 2-stage ring.
-//   MMA        one lane issues, order per tile i: dV(i), S^T(i+1),
-//              dK(i), dP^T(i+1), so the softmax of tile i+1 overlaps dK(i)
-//              and dP^T(i+1), and dS of tile i overlaps dV(i) and S^T(i+1).
+//              Recomputes P^T, releasing the S^T columns as soon as they are
+//              in registers; once dP^T is in registers too, writes P~^T and
+//              then dS^T (io dtype, two per column) over the 32 dP^T columns
+//              it has read, P~^T in the second 16 and dS^T in the first 16,
+//              and adds dS into dBias (fp32 atomics).
+//   producer   TMA for K, V once and Q_i, dO_i through a 2-stage ring; the
+//              row statistics of tile i (-LSE*log2e and D, one bulk copy)
+//              ride with Q_i on its barrier and in its ring slot.
+//   MMA        one lane issues, order per tile i: S^T(i+1) once S^T(i) is
+//              in registers, dV(i), dK(i), dP^T(i+1). Tensor memory has no
+//              room for a second S^T buffer, so P~^T must not stay in the S^T
+//              columns (it would hold S^T(i+1) back until dV(i) had read it,
+//              putting dV(i) + S^T(i+1) + the whole softmax on the per-tile
+//              critical path). In the dP^T columns it is free of that: the
+//              in-order tensor pipe finishes dV(i) before dP^T(i+1)
+//              overwrites them. So the softmax of tile i overlaps S^T(i+1),
+//              dS(i) overlaps dV(i), and the next softmax overlaps dK(i) and
+//              dP^T(i+1).
 // Tensor memory (512 columns): S^T [0,BM), dP^T [BM,2BM), dV [2BM,2BM+Dv),
 // dK [2BM+Dv, 2BM+Dv+Dk), then K and V (two elements per column) if they fit.
 #pragma once
@@ -57,8 +67,9 @@ struct DkdvCfg {
   static constexpr int OFF_V = OFF_K + K_BYTES;
   static constexpr int OFF_Q = OFF_V + V_BYTES;
   static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
-  static constexpr int OFF_ROW = OFF_DO + STAGES * DO_BYTES;  // [2][BM] -LSE log2e, [2][BM] D
-  static constexpr int OFF_BAR = OFF_ROW + 4 * BM * 4;
+  static constexpr int STAT_BYTES = 2 * BM * 4;       // -LSE log2e and D of BM query rows
+  static constexpr int OFF_ROW = OFF_DO + STAGES * DO_BYTES;  // [STAGES] row statistics
+  static constexpr int OFF_BAR = OFF_ROW + STAGES * STAT_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int THREADS = NCT + 64;            // + producer warp + MMA warp
   static constexpr uint32_t TMEM_COLS = 512;
@@ -70,10 +81,11 @@ struct DkdvCfg {
   static_assert(T_DK + DQK <= 512, "tensor memory overflow");
   static_assert(SMEM <= 227 * 1024, "shared memory overflow");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128 && DQK <= 192, "head size");
+  static_assert(CW == 32, "one 32-column TMEM load per compute thread and tile");
 };
 
-enum : int { AB_KV = 0, AB_QF, AB_DOF = AB_QF + 2, AB_QE = AB_DOF + 2, AB_S = AB_QE + 2, AB_P,
-             AB_DP, AB_DS, AB_DKDV, AB_DRAIN, AB_OPS, AB_COUNT };
+enum : int { AB_KV = 0, AB_QF, AB_DOF = AB_QF + 2, AB_QE = AB_DOF + 2, AB_S = AB_QE + 2, AB_SFREE,
+             AB_P, AB_DP, AB_DS, AB_DKDV, AB_DRAIN, AB_OPS, AB_COUNT };
 
 // Keep bits of key row k for the 32 query rows [row0, row0 + 32) of a tile.
 // One Philox block covers four consecutive keys of one query row, i.e. the
@@ -137,7 +149,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AB_COUNT; ++i)
-      mbar_init(bar(i), (i == AB_P || i == AB_DS || i == AB_OPS) ? static_cast<uint32_t>(NCT) : 1u);
+      mbar_init(bar(i), (i == AB_SFREE || i == AB_P || i == AB_DS || i == AB_OPS)
+                            ? static_cast<uint32_t>(NCT)
+                            : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -176,10 +190,12 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad)) break;
         const int q0 = (it0 + i) * BM;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(AB_QF + s), C::Q_BYTES);
+          mbar_arrive_expect_tx(bar(AB_QF + s), C::Q_BYTES + C::STAT_BYTES);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
             tma_load_3d(sQ + s * C::Q_BYTES + c * BM * 128, &tmQ, bar(AB_QF + s), c * 64, q0, bh);
+          bulk_load(smem_u32(rowbuf) + s * C::STAT_BYTES, p.stats + stat_index(bh, p.S_pad, q0),
+                    C::STAT_BYTES, bar(AB_QF + s));
           mbar_arrive_expect_tx(bar(AB_DOF + s), C::DO_BYTES);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
@@ -204,9 +220,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     constexpr uint32_t kIdDK = idesc_f16(128, DQK, BF16, false, true);
     const uint32_t tS = tbase + C::T_S, tDP = tbase + C::T_DP, tDV = tbase + C::T_DV,
                    tDK = tbase + C::T_DK;
-    // Packed io-dtype operand columns of query rows [16kk, 16kk+16): each
-    // compute half wrote its CW columns, packed two per TMEM column, at the
-    // start of the CW columns it read.
+    // Packed io-dtype operand columns of query rows [16kk, 16kk+16) within
+    // the dP^T columns: each compute group wrote its CW queries, two per TMEM
+    // column, dS^T at the start of the CW columns it read and P~^T CW/2 after.
     auto packed_col = [](int kk) -> uint32_t {
       return static_cast<uint32_t>(((kk * 16) / CW) * CW + ((kk * 16) % CW) / 2);
     };
@@ -220,9 +236,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
       for (int kk = 0; kk < DQK / 16; ++kk) {
         const uint64_t bq = desc_adv(dq, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
         if constexpr (C::OPS_IN_TMEM)
-          umma_ts(tS, tbase + C::T_K + kk * 8, bq, kIdS, kk > 0);
+          umma_ts_w(tS, tbase + C::T_K + kk * 8, bq, kIdS, kk > 0);
         else
-          umma_ss(tS, desc_adv(dK0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bq, kIdS, kk > 0);
+          umma_ss_w(tS, desc_adv(dK0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bq, kIdS, kk > 0);
       }
     };
     auto issue_dp = [&](int s) {  // dP^T = V dO^T
@@ -231,78 +247,63 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
       for (int kk = 0; kk < DV / 16; ++kk) {
         const uint64_t bo = desc_adv(dob, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
         if constexpr (C::OPS_IN_TMEM)
-          umma_ts(tDP, tbase + C::T_V + kk * 8, bo, kIdS, kk > 0);
+          umma_ts_w(tDP, tbase + C::T_V + kk * 8, bo, kIdS, kk > 0);
         else
-          umma_ss(tDP, desc_adv(dV0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bo, kIdS, kk > 0);
+          umma_ss_w(tDP, desc_adv(dV0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bo, kIdS, kk > 0);
       }
     };
+    // the whole warp runs the issue loop; one elected lane issues (umma_*_w)
     bool ok = n_it > 0;
-    if (ok) ok = mbar_wait(bar(AB_KV), 0, ec, kSiteBwdMma);
-    if (C::OPS_IN_TMEM && ok) ok = mbar_wait(bar(AB_OPS), 0, ec, kSiteBwdMma);
-    if (ok) ok = mbar_wait(bar(AB_QF), 0, ec, kSiteBwdMma);
+    if (ok) ok = mbar_wait_w(bar(AB_KV), 0, ec, kSiteBwdMma);
+    if (C::OPS_IN_TMEM && ok) ok = mbar_wait_w(bar(AB_OPS), 0, ec, kSiteBwdMma);
+    if (ok) ok = mbar_wait_w(bar(AB_QF), 0, ec, kSiteBwdMma);
     if (ok) {
       tc_fence_after();
-      if (lane == 0) {
-        issue_s(0);
-        umma_commit(bar(AB_S));
-      }
-      __syncwarp();
-      ok = mbar_wait(bar(AB_DOF), 0, ec, kSiteBwdMma);
+      issue_s(0);
+      umma_commit_w(bar(AB_S));
+      ok = mbar_wait_w(bar(AB_DOF), 0, ec, kSiteBwdMma);
     }
     if (ok) {
       tc_fence_after();
-      if (lane == 0) {
-        issue_dp(0);
-        umma_commit(bar(AB_DP));
-      }
-      __syncwarp();
+      issue_dp(0);
+      umma_commit_w(bar(AB_DP));
     }
     for (int i = 0; ok && i < n_it; ++i) {
       const int s = i & 1, s1 = (i + 1) & 1;
       const uint32_t ph1 = ((i + 1) >> 1) & 1;
-      if (!(ok = mbar_wait(bar(AB_P), i & 1, ec, kSiteBwdMma))) break;
+      if (i + 1 < n_it) {  // S^T(i+1) once the compute warps hold S^T(i) in registers
+        if (!(ok = mbar_wait_w(bar(AB_SFREE), i & 1, ec, kSiteBwdMma))) break;
+        if (!(ok = mbar_wait_w(bar(AB_QF + s1), ph1, ec, kSiteBwdMma))) break;
+        tc_fence_after();
+        issue_s(s1);
+        umma_commit_w(bar(AB_S));
+      }
+      if (!(ok = mbar_wait_w(bar(AB_P), i & 1, ec, kSiteBwdMma))) break;
       tc_fence_after();
-      if (lane == 0) {  // dV += P~^T dO_i
+      {  // dV += P~^T dO_i
         const uint64_t dob = desc_adv(dOm0, s * C::DO_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(tDV, tS + packed_col(kk), desc_adv(dob, kk * 2048), kIdDV, (i > 0 || kk > 0));
+          umma_ts_w(tDV, tDP + packed_col(kk) + CW / 2, desc_adv(dob, kk * 2048), kIdDV, (i > 0 || kk > 0));
       }
-      __syncwarp();
-      if (i + 1 < n_it) {
-        if (!(ok = mbar_wait(bar(AB_QF + s1), ph1, ec, kSiteBwdMma))) break;
-        tc_fence_after();
-        if (lane == 0) {
-          issue_s(s1);
-          umma_commit(bar(AB_S));
-        }
-        __syncwarp();
-      }
-      if (!(ok = mbar_wait(bar(AB_DS), i & 1, ec, kSiteBwdMma))) break;
+      if (!(ok = mbar_wait_w(bar(AB_DS), i & 1, ec, kSiteBwdMma))) break;
       tc_fence_after();
-      if (lane == 0) {  // dK += dS^T Q_i
+      {  // dK += dS^T Q_i
         const uint64_t dqb = desc_adv(dQm0, s * C::Q_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts(tDK, tDP + packed_col(kk), desc_adv(dqb, kk * 2048), kIdDK, (i > 0 || kk > 0));
-        umma_commit(bar(AB_QE + s));  // Q_i and dO_i are no longer read
+          umma_ts_w(tDK, tDP + packed_col(kk), desc_adv(dqb, kk * 2048), kIdDK, (i > 0 || kk > 0));
+        umma_commit_w(bar(AB_QE + s));  // Q_i and dO_i are no longer read
       }
-      __syncwarp();
       if (i + 1 < n_it) {
-        if (!(ok = mbar_wait(bar(AB_DOF + s1), ph1, ec, kSiteBwdMma))) break;
+        if (!(ok = mbar_wait_w(bar(AB_DOF + s1), ph1, ec, kSiteBwdMma))) break;
         tc_fence_after();
-        if (lane == 0) {
-          issue_dp(s1);
-          umma_commit(bar(AB_DP));
-        }
-        __syncwarp();
+        issue_dp(s1);
+        umma_commit_w(bar(AB_DP));
       }
     }
-    if (lane == 0) {
-      if (ok) umma_commit(bar(AB_DKDV));
-      umma_commit(bar(AB_DRAIN));
-    }
-    __syncwarp();
+    if (ok) umma_commit_w(bar(AB_DKDV));
+    umma_commit_w(bar(AB_DRAIN));
     mbar_wait(bar(AB_DRAIN), 0, ec, kSiteDrain, false);
   } else {
     // ------------------------------------------------------------ compute
@@ -312,22 +313,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     const int kv = k0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const bool kv_ok = kv < p.S_kv;
-    float* nl2_buf = rowbuf;          // [2][BM]  -LSE * log2(e) (-inf for rows without keys)
-    float* d_buf = rowbuf + 2 * BM;   // [2][BM]  D
-    // Row statistics of query tile i: threads 0..BM-1 read -LSE*log2e, threads
-    // BM..2BM-1 read D. Tile i+1's values are fetched during tile i.
-    auto fetch_row_stat = [&](int i) -> float {
-      const int qr = (it0 + i) * BM + (t % BM);
-      const size_t idx = static_cast<size_t>(bh) * p.S_q + qr;
-      if (t < BM) {
-        const float L = (qr < p.S_q) ? p.lse[idx] : SDPA_NEG_INF;
-        return (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
-      }
-      return (qr < p.S_q) ? p.delta[idx] : 0.f;
-    };
-    auto store_row_stat = [&](int i, float v) {
-      if (t < 2 * BM) rowbuf[(t < BM ? 0 : 2 * BM) + (i & 1) * BM + (t % BM)] = v;
-    };
+    // This thread's 32 query columns lie in one 64-row block of the statistics
+    // slot: 64 values -LSE*log2e (-inf for rows without keys), then 64 D.
+    const int stat_off = ((CW * hf) / 64) * 128 + (CW * hf) % 64;
     bool ok = true;
     if (C::OPS_IN_TMEM && n_it > 0) {  // K and V rows into this thread's TMEM lane
       ok = mbar_wait(bar(AB_KV), 0, ec, kSiteBwdCompute);
@@ -344,14 +332,12 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     auto body = [&](auto drop_tag) {
       constexpr bool DROP = decltype(drop_tag)::value;
       const float zk = p.keep_scale;
-      if (n_it > 0) store_row_stat(0, t < 2 * BM ? fetch_row_stat(0) : 0.f);
       for (int i = 0; ok && i < n_it; ++i) {
         const int q0 = (it0 + i) * BM;
         const int qc0 = q0 + CW * hf;  // first query row of this thread's columns
-        named_bar_sync(2, NCT);        // tile i's statistics are in shared memory
-        const float4* nl2 = reinterpret_cast<const float4*>(nl2_buf + (i & 1) * BM + CW * hf);
-        const float4* dd = reinterpret_cast<const float4*>(d_buf + (i & 1) * BM + CW * hf);
-        const float next_stat = (t < 2 * BM && i + 1 < n_it) ? fetch_row_stat(i + 1) : 0.f;
+        const float* stat = rowbuf + (i & 1) * (2 * BM) + stat_off;
+        const float4* nl2 = reinterpret_cast<const float4*>(stat);
+        const float4* dd = reinterpret_cast<const float4*>(stat + 64);
         uint32_t km[CW / 32][4];
 #pragma unroll
         for (int g = 0; g < CW / 32; ++g) {
@@ -367,7 +353,11 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
           return 1.0f;
         };
         if (!(ok = mbar_wait(bar(AB_S), i & 1, ec, kSiteBwdCompute))) break;
+        // S^T(i) was issued after Q_i and the statistics landed; the wait on the
+        // same barrier makes the statistics visible to this thread too
+        if (!(ok = mbar_wait(bar(AB_QF + (i & 1)), (i >> 1) & 1, ec, kSiteBwdCompute))) break;
         tc_fence_after();
+        // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)
         float pr[CW];
 #pragma unroll
         for (int c = 0; c < CW / 32; ++c) {
@@ -375,8 +365,16 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
           tmem_ld32(tbase + C::T_S + lane_off + CW * hf + 32 * c, a0);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pr[32 * c + e] = __uint_as_float(a0[e]) * p.scale_log2;
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 n4 = nl2[8 * c + e4];
+            pr[32 * c + 4 * e4 + 0] = fmaf(__uint_as_float(a0[4 * e4 + 0]), p.scale_log2, n4.x);
+            pr[32 * c + 4 * e4 + 1] = fmaf(__uint_as_float(a0[4 * e4 + 1]), p.scale_log2, n4.y);
+            pr[32 * c + 4 * e4 + 2] = fmaf(__uint_as_float(a0[4 * e4 + 2]), p.scale_log2, n4.z);
+            pr[32 * c + 4 * e4 + 3] = fmaf(__uint_as_float(a0[4 * e4 + 3]), p.scale_log2, n4.w);
+          }
         }
+        tc_fence_before();
+        mbar_arrive(bar(AB_SFREE));  // S^T(i) is in registers: S^T(i+1) may overwrite it
         if (p.bias != nullptr && kv_ok) {
           const float* bias_col = p.bias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv;
           const int lim = min(CW, p.S_q - qc0);
@@ -394,36 +392,37 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
             if (c < first || c >= lim) pr[c] = SDPA_NEG_INF;
         }
 #pragma unroll
-        for (int c4 = 0; c4 < CW / 4; ++c4) {
-          const float4 n4 = nl2[c4];
-          pr[4 * c4 + 0] = ex2(pr[4 * c4 + 0] + n4.x);
-          pr[4 * c4 + 1] = ex2(pr[4 * c4 + 1] + n4.y);
-          pr[4 * c4 + 2] = ex2(pr[4 * c4 + 2] + n4.z);
-          pr[4 * c4 + 3] = ex2(pr[4 * c4 + 3] + n4.w);
-        }
+        for (int c = 0; c < CW; ++c) pr[c] = ex2(pr[c]);
+        if (!(ok = mbar_wait(bar(AB_DP), i & 1, ec, kSiteBwdCompute))) break;
+        tc_fence_after();
+        // dP^T of this thread's 32 columns, the upper 16 first: P~^T goes over
+        // them as soon as they are in registers, then the lower 16 follow
+        uint32_t dpw[CW];
+        {
+          uint32_t hi[16], lo[16], pw[16];
+          const uint32_t tcol = tbase + C::T_DP + lane_off + CW * hf;
+          tmem_ld16(tcol + 16, hi);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < CW / 32; ++c) {
-          uint32_t pk[16];
+          for (int e = 0; e < 16; ++e) pw[e] = pack2<BF16>(pr[2 * e] * zf(2 * e), pr[2 * e + 1] * zf(2 * e + 1));
+          tmem_st16(tcol + 16, pw);
+          tmem_ld16(tcol, lo);
+          tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int cc = 32 * c + 2 * e;
-            pk[e] = pack2<BF16>(pr[cc] * zf(cc), pr[cc + 1] * zf(cc + 1));
+            dpw[e] = lo[e];
+            dpw[16 + e] = hi[e];
           }
-          tmem_st16(tbase + C::T_S + lane_off + CW * hf + 16 * c, pk);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(AB_P));
-        if (!(ok = mbar_wait(bar(AB_DP), i & 1, ec, kSiteBwdCompute))) break;
-        tc_fence_after();
         float* dbias_col = (p.dbias != nullptr && kv_ok)
                                ? p.dbias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
                                : nullptr;
 #pragma unroll
         for (int c = 0; c < CW / 32; ++c) {
-          uint32_t a0[32];
-          tmem_ld32(tbase + C::T_DP + lane_off + CW * hf + 32 * c, a0);
-          tmem_wait_ld();
+          const uint32_t* a0 = dpw + 32 * c;
           uint32_t pk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
@@ -452,7 +451,6 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(AB_DS));
-        if (i + 1 < n_it) store_row_stat(i + 1, next_stat);
       }
     };
     if (p.dropout)

@@ -169,9 +169,9 @@ __global__ void __launch_bounds__(320, 1)
       for (int kk = 0; kk < DQK / 16; ++kk) {
         const uint64_t bk = desc_adv(dk, (kk >> 2) * (BN * 128) + (kk & 3) * 32);
         if constexpr (C::OPS_IN_TMEM)
-          umma_ts(tS, tbase + C::T_Q + kk * 8, bk, kIdS, kk > 0);
+          umma_ts_w(tS, tbase + C::T_Q + kk * 8, bk, kIdS, kk > 0);
         else
-          umma_ss(tS, desc_adv(dQ0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bk, kIdS, kk > 0);
+          umma_ss_w(tS, desc_adv(dQ0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bk, kIdS, kk > 0);
       }
     };
     auto issue_dp = [&](int j) {  // dP = dO V_j^T
@@ -180,40 +180,35 @@ __global__ void __launch_bounds__(320, 1)
       for (int kk = 0; kk < DV / 16; ++kk) {
         const uint64_t bv = desc_adv(dv, (kk >> 2) * (BN * 128) + (kk & 3) * 32);
         if constexpr (C::OPS_IN_TMEM)
-          umma_ts(tDP, tbase + C::T_DO + kk * 8, bv, kIdS, kk > 0);
+          umma_ts_w(tDP, tbase + C::T_DO + kk * 8, bv, kIdS, kk > 0);
         else
-          umma_ss(tDP, desc_adv(dO0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bv, kIdS, kk > 0);
+          umma_ss_w(tDP, desc_adv(dO0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bv, kIdS, kk > 0);
       }
     };
     auto issue_dq = [&](int j) {  // dQ += dS K_j, dS packed two per column
       const uint64_t dk = desc_adv(dKm0, (j % ST) * C::K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
-        umma_ts(tDQ, tDP + (kk >> 2) * CW + (kk & 3) * 8, desc_adv(dk, kk * 2048), kIdDQ,
+        umma_ts_w(tDQ, tDP + (kk >> 2) * CW + (kk & 3) * 8, desc_adv(dk, kk * 2048), kIdDQ,
                 (j > 0 || kk > 0));
     };
     auto wait_kv = [&](int which, int j) {
-      return mbar_wait(bar(which + j % ST), (j / ST) & 1, ec, kSiteBwdMma);
+      return mbar_wait_w(bar(which + j % ST), (j / ST) & 1, ec, kSiteBwdMma);
     };
-    bool ok = mbar_wait(bar(QB_Q), 0, ec, kSiteBwdMma) && wait_kv(QB_KF, 0);
-    if (C::OPS_IN_TMEM && ok) ok = mbar_wait(bar(QB_OPS), 0, ec, kSiteBwdMma);
+    // the whole warp runs the issue loop; one elected lane issues (umma_*_w)
+    bool ok = mbar_wait_w(bar(QB_Q), 0, ec, kSiteBwdMma) && wait_kv(QB_KF, 0);
+    if (C::OPS_IN_TMEM && ok) ok = mbar_wait_w(bar(QB_OPS), 0, ec, kSiteBwdMma);
     if (ok) {
       tc_fence_after();
-      if (lane == 0) {
-        issue_s(0);
-        umma_commit(bar(QB_S));
-      }
-      __syncwarp();
+      issue_s(0);
+      umma_commit_w(bar(QB_S));
       ok = wait_kv(QB_VF, 0);
     }
     if (ok) {
       tc_fence_after();
-      if (lane == 0) {
-        issue_dp(0);
-        umma_commit(bar(QB_DP));
-        umma_commit(bar(QB_VE + 0));
-      }
-      __syncwarp();
+      issue_dp(0);
+      umma_commit_w(bar(QB_DP));
+      umma_commit_w(bar(QB_VE + 0));
     }
     for (int j = 0; ok && j < n_kv; ++j) {
       const bool more = j + 1 < n_kv;
@@ -221,49 +216,34 @@ __global__ void __launch_bounds__(320, 1)
       // tile j; with one stage K_{j+1} cannot land before dQ(j) frees K_j.
       if constexpr (ST > 1) {
         if (more) {
-          if (!(ok = mbar_wait(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
+          if (!(ok = mbar_wait_w(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
           tc_fence_after();
-          if (lane == 0) {
-            issue_s(j + 1);
-            umma_commit(bar(QB_S));
-          }
-          __syncwarp();
+          issue_s(j + 1);
+          umma_commit_w(bar(QB_S));
         }
       }
-      if (!(ok = mbar_wait(bar(QB_DS), j & 1, ec, kSiteBwdMma))) break;
+      if (!(ok = mbar_wait_w(bar(QB_DS), j & 1, ec, kSiteBwdMma))) break;
       tc_fence_after();
-      if (lane == 0) {
-        issue_dq(j);
-        umma_commit(bar(QB_KE + j % ST));
-      }
-      __syncwarp();
+      issue_dq(j);
+      umma_commit_w(bar(QB_KE + j % ST));
       if constexpr (ST == 1) {
         if (more) {
-          if (!(ok = mbar_wait(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
+          if (!(ok = mbar_wait_w(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
           tc_fence_after();
-          if (lane == 0) {
-            issue_s(j + 1);
-            umma_commit(bar(QB_S));
-          }
-          __syncwarp();
+          issue_s(j + 1);
+          umma_commit_w(bar(QB_S));
         }
       }
       if (more) {
         if (!(ok = wait_kv(QB_VF, j + 1))) break;
         tc_fence_after();
-        if (lane == 0) {
-          issue_dp(j + 1);
-          umma_commit(bar(QB_DP));
-          umma_commit(bar(QB_VE + (j + 1) % ST));
-        }
-        __syncwarp();
+        issue_dp(j + 1);
+        umma_commit_w(bar(QB_DP));
+        umma_commit_w(bar(QB_VE + (j + 1) % ST));
       }
     }
-    if (lane == 0) {
-      if (ok) umma_commit(bar(QB_DONE));
-      umma_commit(bar(QB_DRAIN));
-    }
-    __syncwarp();
+    if (ok) umma_commit_w(bar(QB_DONE));
+    umma_commit_w(bar(QB_DRAIN));
     mbar_wait(bar(QB_DRAIN), 0, ec, kSiteDrain, false);
   } else {
     // ------------------------------------------------------------ compute
@@ -274,9 +254,11 @@ __global__ void __launch_bounds__(320, 1)
     const bool row_ok = qr < p.S_q;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const size_t ridx = static_cast<size_t>(bh) * p.S_q + (row_ok ? qr : 0);
-    const float L = row_ok ? p.lse[ridx] : SDPA_NEG_INF;
-    const float nl2 = (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
-    const float Drow = row_ok ? p.delta[ridx] : 0.f;
+    // -LSE*log2e and D of this row (-inf and 0 past S_q: the tile never
+    // reaches beyond the statistics' padding to 128 rows)
+    const size_t sidx = stat_index(static_cast<size_t>(bh), p.S_pad, qr);
+    const float nl2 = p.stats[sidx];
+    const float Drow = p.stats[sidx + 64];
     const float* bias_row =
         (p.bias != nullptr && row_ok) ? p.bias + (static_cast<size_t>(h) * p.S_q + qr) * p.S_kv : nullptr;
     const bool bias_vec = (p.S_kv & 3) == 0;

@@ -39,6 +39,16 @@ struct FwdParams {
   uint32_t* err;           // device error word
 };
 
+// Row statistics the backward kernels share, written by the preprocess kernel:
+// for each (b, h) and each block of 64 query rows (S_q padded to a multiple
+// of 128), 64 floats -LSE * log2(e) followed by 64 floats D = rowsum(dO * O).
+// A tile of 64 or 128 query rows is thus one contiguous run of 512 or 1024
+// bytes, fetched with one bulk copy. Rows past S_q hold -inf and 0.
+__host__ __device__ __forceinline__ size_t stat_index(size_t bh, int S_pad, int q) {
+  return (bh * static_cast<size_t>(S_pad) + static_cast<size_t>(q & ~63)) * 2 + static_cast<size_t>(q & 63);
+}
+__host__ __device__ __forceinline__ int stat_pad(int S_q) { return (S_q + 127) & ~127; }
+
 struct BwdParams {
   int B, H, S_q, S_kv;
   float scale;             // softmax scale
@@ -50,8 +60,8 @@ struct BwdParams {
   uint32_t drop_threshold;
   float keep_scale;
   uint32_t seed_lo, seed_hi, offset_lo, offset_hi;
-  const float* lse;        // [B, H, S_q]
-  const float* delta;      // D = rowsum(dO * O)  [B, H, S_q]
+  const float* stats;      // row statistics, see stat_index
+  int S_pad;               // S_q rounded up to a multiple of 128
   void* dq;                // [B, H, S_q, D_qk]
   void* dk;                // [B, H, S_kv, D_qk]
   void* dv;                // [B, H, S_kv, D_v]
@@ -169,8 +179,9 @@ cudaError_t launch_bwd_dq_bf16(int d_qk, int d_v, const CUtensorMap& q, const CU
 cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
                                const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
                                cudaStream_t st);
-cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, float* delta, float* dbias,
-                           int64_t rows, int d_v, int64_t dbias_elems, cudaStream_t st);
+cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
+                           float* dbias, int64_t bh, int s_q, int d_v, int64_t dbias_elems,
+                           cudaStream_t st);
 cudaError_t launch_dropout_mask(int64_t total, uint32_t threshold, uint32_t seed_lo,
                                 uint32_t seed_hi, uint32_t off_lo, uint32_t off_hi,
                                 uint32_t* bits, cudaStream_t st);

@@ -149,40 +149,36 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
     const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
     const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
     const uint64_t dV0 = sdesc_sw128(sV, C::BN * 128, 1024);
-    bool ok = mbar_wait(bar(FB_Q), 0, ec, kSiteFwdMma);
+    // the whole warp runs the issue loop; one elected lane issues (umma_*_w)
+    bool ok = mbar_wait_w(bar(FB_Q), 0, ec, kSiteFwdMma);
     for (int j = 0; ok && j < n_kv; ++j) {
       const int s = j % C::STAGES;
       const uint32_t ph = (j / C::STAGES) & 1;
-      if (!(ok = mbar_wait(bar(FB_KF + s), ph, ec, kSiteFwdMma))) break;
+      if (!(ok = mbar_wait_w(bar(FB_KF + s), ph, ec, kSiteFwdMma))) break;
       tc_fence_after();
-      if (lane == 0) {
+      {
         const uint64_t dK = desc_adv(dK0, s * C::K_BYTES);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          umma_ss(tS, desc_adv(dQ0, off), desc_adv(dK, off), kIdS, kk > 0);
+          umma_ss_w(tS, desc_adv(dQ0, off), desc_adv(dK, off), kIdS, kk > 0);
         }
-        umma_commit(bar(FB_S));
-        umma_commit(bar(FB_KE + s));
+        umma_commit_w(bar(FB_S));
+        umma_commit_w(bar(FB_KE + s));
       }
-      __syncwarp();
-      if (!(ok = mbar_wait(bar(FB_P), j & 1, ec, kSiteFwdMma))) break;
-      if (!(ok = mbar_wait(bar(FB_VF + s), ph, ec, kSiteFwdMma))) break;
+      if (!(ok = mbar_wait_w(bar(FB_P), j & 1, ec, kSiteFwdMma))) break;
+      if (!(ok = mbar_wait_w(bar(FB_VF + s), ph, ec, kSiteFwdMma))) break;
       tc_fence_after();
-      if (lane == 0) {
+      {
         const uint64_t dV = desc_adv(dV0, s * C::V_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(tO, tS + kk * 8, desc_adv(dV, kk * 2048), kIdO, (j > 0 || kk > 0));
-        umma_commit(bar(FB_VE + s));
+          umma_ts_w(tO, tS + kk * 8, desc_adv(dV, kk * 2048), kIdO, (j > 0 || kk > 0));
+        umma_commit_w(bar(FB_VE + s));
       }
-      __syncwarp();
     }
-    if (lane == 0) {
-      if (ok) umma_commit(bar(FB_O));
-      umma_commit(bar(FB_DRAIN));
-    }
-    __syncwarp();
+    if (ok) umma_commit_w(bar(FB_O));
+    umma_commit_w(bar(FB_DRAIN));
     mbar_wait(bar(FB_DRAIN), 0, ec, kSiteDrain, false);
   } else {
     // ------------------------------------------------------------ softmax

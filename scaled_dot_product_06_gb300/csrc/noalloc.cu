@@ -5,7 +5,8 @@
 // pool and forbids allocations from outside it, or a latency-critical loop
 // where cudaMalloc's implicit device synchronisation and unbounded latency are
 // not acceptable. For them this entry point keeps the backward scratch (the
-// per-row D = rowsum(dO * O) values the backward kernels share) in a fixed,
+// per-row statistics D = rowsum(dO * O) and -LSE*log2e that the backward
+// kernels share) in a fixed,
 // file-scope device array that exists for as long as the library is loaded,
 // on every GPU that loads it. It calls no cudaMalloc, cudaFree or other
 // allocating routine.
@@ -14,7 +15,7 @@
 // * The array holds kNoAllocScratchBytes (16 MiB). A problem whose scratch
 //   (sdpa_bwd_workspace_size) is larger is rejected with SDPA_ERR_WORKSPACE.
 // * Every call on a device uses the same array and leaves its contents behind;
-//   the preprocess kernel of each call overwrites D before the other kernels
+//   the preprocess kernel of each call overwrites the statistics before the other kernels
 //   read it, so nothing carries over.
 //   Calls whose kernels overlap on the GPU (for example on two streams at
 //   once) race on the array and give wrong gradients: serialise them.

@@ -87,6 +87,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, const Er
   }
 }
 
+// mbar_wait by a whole converged warp; the result is the same in every lane
+// (false if any lane gave up), so the warp stays converged for the
+// warp-issued MMA forms below.
+__device__ __forceinline__ bool mbar_wait_w(uint32_t bar, uint32_t phase, const ErrCtx& e,
+                                            uint32_t site, bool honor_abort = true) {
+  const bool ok = mbar_wait(bar, phase, e, site, honor_abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -209,6 +218,42 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// Warp-issued forms: the whole converged warp executes the call and the lane
+// that elect.sync picks inside the instruction block issues. This keeps the
+// issuing loop's control flow warp-uniform. Issued from a one-lane branch
+// instead, every MMA costs many issue slots of its scheduler, and when the
+// other warps on that scheduler are busy the tensor pipe starves: measured on
+// GB300 with four FFMA-bound warps beside the issuer, a 128x128x16 MMA took
+// 248 cycles from a lane-0 branch and 67 in this form (64 with idle
+// neighbours).
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 

@@ -86,8 +86,8 @@ def bwd(lib, b=1, h=1, sq=128, skv=128, dqk=64, dv=64, p=0.0, bias=NULL, dbias=N
 
 def test_workspace_size(lib):
     b, h, sq, dqk = 2, 3, 100, 128
-    rows = b * h * sq
-    want = ((rows * 4 + 255) // 256) * 256  # D = rowsum(dO * O), fp32 per query row
+    s_pad = (sq + 127) // 128 * 128  # query rows padded to whole 128-row tiles
+    want = ((b * h * s_pad * 2 * 4 + 255) // 256) * 256  # -LSE*log2e and D, fp32 per row
     assert lib.sdpa_bwd_workspace_size(b, h, sq, 50, dqk, 128) == want
     assert lib.sdpa_bwd_workspace_size(1, 1, 8, 8, 80, 80) == 0
 
