@@ -25,10 +25,10 @@
 //              columns [32*hf, 32*hf + 32), hf = w/4, so each scheduler runs
 //              BM/32 compute warps whose latencies hide one another.
 //              Recomputes P^T, releasing the S^T columns as soon as they are
-//              in registers; once dP^T is in registers too, writes P~^T and
-//              then dS^T (io dtype, two per column) over the 32 dP^T columns
-//              it has read, P~^T in the second 16 and dS^T in the first 16,
-//              and adds dS into dBias (fp32 atomics).
+//              in registers; then writes P~^T and dS^T (io dtype, two per
+//              column) over the 32 dP^T columns it reads, P~^T in the first
+//              16 and dS^T in the second 16, and adds dS into dBias (fp32
+//              atomics).
 //   producer   TMA for K, V once and Q_i, dO_i through a 2-stage ring; the
 //              row statistics of tile i (-LSE*log2e and D, one bulk copy)
 //              ride with Q_i on its barrier and in its ring slot.
@@ -113,7 +113,11 @@ __device__ __forceinline__ void keep_bits_transposed(uint64_t lin_quad, int S_kv
   }
 }
 
-template <int DQK, int DV, bool BF16>
+// DROP is a template parameter (not a runtime branch) so the kernel without
+// dropout is compiled alone: at 96 registers a thread (18 warps, five on some
+// schedulers) the dropout body's keep bits would otherwise push the common
+// path into spilling.
+template <int DQK, int DV, bool BF16, bool DROP>
 __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
                    tDK = tbase + C::T_DK;
     // Packed io-dtype operand columns of query rows [16kk, 16kk+16) within
     // the dP^T columns: each compute group wrote its CW queries, two per TMEM
-    // column, dS^T at the start of the CW columns it read and P~^T CW/2 after.
+    // column, P~^T at the start of the CW columns it read and dS^T CW/2 after.
     auto packed_col = [](int kk) -> uint32_t {
       return static_cast<uint32_t>(((kk * 16) / CW) * CW + ((kk * 16) % CW) / 2);
     };
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         const uint64_t dob = desc_adv(dOm0, s * C::DO_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts_w(tDV, tDP + packed_col(kk) + CW / 2, desc_adv(dob, kk * 2048), kIdDV, (i > 0 || kk > 0));
+          umma_ts_w(tDV, tDP + packed_col(kk), desc_adv(dob, kk * 2048), kIdDV, (i > 0 || kk > 0));
       }
       if (!(ok = mbar_wait_w(bar(AB_DS), i & 1, ec, kSiteBwdMma))) break;
       tc_fence_after();
@@ -292,7 +296,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         const uint64_t dqb = desc_adv(dQm0, s * C::Q_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          umma_ts_w(tDK, tDP + packed_col(kk), desc_adv(dqb, kk * 2048), kIdDK, (i > 0 || kk > 0));
+          umma_ts_w(tDK, tDP + packed_col(kk) + CW / 2, desc_adv(dqb, kk * 2048), kIdDK, (i > 0 || kk > 0));
         umma_commit_w(bar(AB_QE + s));  // Q_i and dO_i are no longer read
       }
       if (i + 1 < n_it) {
@@ -329,8 +333,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
       tc_fence_before();
       if (ok) mbar_arrive(bar(AB_OPS));
     }
-    auto body = [&](auto drop_tag) {
-      constexpr bool DROP = decltype(drop_tag)::value;
+    {
       const float zk = p.keep_scale;
       for (int i = 0; ok && i < n_it; ++i) {
         const int q0 = (it0 + i) * BM;
@@ -395,68 +398,65 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         for (int c = 0; c < CW; ++c) pr[c] = ex2(pr[c]);
         if (!(ok = mbar_wait(bar(AB_DP), i & 1, ec, kSiteBwdCompute))) break;
         tc_fence_after();
-        // dP^T of this thread's 32 columns, the upper 16 first: P~^T goes over
-        // them as soon as they are in registers, then the lower 16 follow
-        uint32_t dpw[CW];
-        {
-          uint32_t hi[16], lo[16], pw[16];
-          const uint32_t tcol = tbase + C::T_DP + lane_off + CW * hf;
-          tmem_ld16(tcol + 16, hi);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) pw[e] = pack2<BF16>(pr[2 * e] * zf(2 * e), pr[2 * e + 1] * zf(2 * e + 1));
-          tmem_st16(tcol + 16, pw);
-          tmem_ld16(tcol, lo);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            dpw[e] = lo[e];
-            dpw[16 + e] = hi[e];
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(AB_P));
+        // The thread's 32 dP^T columns are handled in halves of 16 so that at
+        // most half of dP^T is in registers next to P: the lower half is read,
+        // P~^T (io dtype, two per column) goes over it at once, and dS of the
+        // lower queries is formed; then the upper half is read and dS^T of all
+        // 32 queries goes over it. dV reads P~^T from the first 16 columns of
+        // each 32, dK reads dS^T from the second 16.
+        const uint32_t tcol = tbase + C::T_DP + lane_off + CW * hf;
         float* dbias_col = (p.dbias != nullptr && kv_ok)
                                ? p.dbias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
                                : nullptr;
+        // dS = P * (dP * Z - D) of local columns [c0, c0 + 16) into 8 packed words
+        auto ds_half = [&](const uint32_t (&dp)[16], int c0, uint32_t* out) {
 #pragma unroll
-        for (int c = 0; c < CW / 32; ++c) {
-          const uint32_t* a0 = dpw + 32 * c;
-          uint32_t pk[16];
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 d4 = dd[8 * c + e4];
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 d4 = dd[c0 / 4 + e4];
             const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
             float ds[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int cc = 32 * c + 4 * e4 + e;
-              const float dpv = __uint_as_float(a0[4 * e4 + e]);
+              const int cc = c0 + 4 * e4 + e;
+              const float dpv = __uint_as_float(dp[4 * e4 + e]);
               ds[e] = pr[cc] * (DROP ? fmaf(dpv, zf(cc), -dv4[e]) : dpv - dv4[e]);
             }
             if (dbias_col != nullptr) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int cc = 32 * c + 4 * e4 + e;
+                const int cc = c0 + 4 * e4 + e;
                 if (qc0 + cc < p.S_q) atomicAdd(dbias_col + static_cast<size_t>(cc) * p.S_kv, ds[e]);
               }
             }
-            pk[2 * e4] = pack2<BF16>(ds[0], ds[1]);
-            pk[2 * e4 + 1] = pack2<BF16>(ds[2], ds[3]);
+            out[2 * e4] = pack2<BF16>(ds[0], ds[1]);
+            out[2 * e4 + 1] = pack2<BF16>(ds[2], ds[3]);
           }
-          // dS^T over the first half of the dP^T columns this thread has read
-          tmem_st16(tbase + C::T_DP + lane_off + CW * hf + 16 * c, pk);
+        };
+        uint32_t pk[16];  // dS^T, packed
+        {
+          uint32_t lo[16], pw[16];
+          tmem_ld16(tcol, lo);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pw[e] = pack2<BF16>(pr[2 * e] * zf(2 * e), pr[2 * e + 1] * zf(2 * e + 1));
+          tmem_st16(tcol, pw);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(AB_P));
+          ds_half(lo, 0, pk);
         }
+        {
+          uint32_t hi[16];
+          tmem_ld16(tcol + 16, hi);
+          tmem_wait_ld();
+          ds_half(hi, 16, pk + 8);
+        }
+        tmem_st16(tcol + 16, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(AB_DS));
       }
-    };
-    if (p.dropout)
-      body(std::true_type{});
-    else
-      body(std::false_type{});
+    }
     // ---- epilogue: warps 0-3 write dV, warps 4-7 write dK * scale (zeros for
     // a key tile that no query sees)
     const bool have = n_it > 0;
@@ -508,7 +508,7 @@ template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                               const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
   using C = DkdvCfg<DQK, DV>;
-  auto kern = sdpa_bwd_dkdv_kernel<DQK, DV, BF16>;
+  auto kern = p.dropout ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true> : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
