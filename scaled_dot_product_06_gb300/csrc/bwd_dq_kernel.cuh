@@ -15,13 +15,14 @@
 //   S   = Q K_j^T     [128 x 128]  A = Q (smem, K-major),  B = K_j (K-major)
 //   dP  = dO V_j^T    [128 x 128]  A = dO (smem, K-major), B = V_j (K-major)
 //   dQ += dS K_j      [128 x Dk]   A = dS (TMEM),          B = K_j (MN-major)
-// Roles (320 threads):
-//   warps 0-7  compute, two warpgroups: warp w owns query rows 32*(w%4)..+31
-//              (its TMEM lanes) and key columns [64*(w/4), +64) of each tile:
-//              P from S, then dS (io dtype) written over the first half of the
-//              dP columns it has read.
-//   warp 8     TMA producer (Q, dO once; K_j and V_j through a ring).
-//   warp 9     MMA issuer (one lane).
+// Roles (four compute warpgroups, a producer warp and an MMA warp):
+//   compute    warp w owns query rows 32*(w%4)..+31 (its TMEM lanes) and key
+//              columns [32*(w/4), +32) of each tile, so each scheduler runs
+//              four compute warps whose latencies hide one another: P from S,
+//              then dS (io dtype) written over the second half of the dP
+//              columns it has read.
+//   producer   TMA for Q, dO once and K_j, V_j through a ring.
+//   MMA        the whole warp runs the issue loop, one elected lane issues.
 // Tensor memory (512 columns): S [0,128), dP [128,256), dQ [256, 256+Dk),
 // then Q and dO (two elements per column) when they fit (d_qk <= 128): the S
 // and dP products then take A from TMEM and read only K_j / V_j from shared
@@ -35,7 +36,10 @@ namespace sdpa {
 
 template <int DQK, int DV>
 struct DqCfg {
-  static constexpr int BM = 128, BN = 128, CW = 64;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int NQ = 4;             // compute warpgroups
+  static constexpr int CW = BN / NQ;       // key columns per compute thread
+  static constexpr int NCT = 128 * NQ;     // compute threads
   static constexpr int STAGES = (DQK <= 128) ? 2 : 1;
   static constexpr int Q_BYTES = BM * DQK * 2;
   static constexpr int DO_BYTES = BM * DV * 2;
@@ -47,7 +51,7 @@ struct DqCfg {
   static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * V_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = NCT + 64;  // + producer warp + MMA warp
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
   // Q and dO, the operands every tile reuses, live in TMEM when they fit, so
@@ -56,19 +60,22 @@ struct DqCfg {
   static constexpr uint32_t T_Q = T_DQ + DQK, T_DO = T_Q + DQK / 2;
   static_assert(T_DQ + DQK <= 512, "tensor memory overflow");
   static_assert(SMEM <= 227 * 1024, "shared memory overflow");
+  static_assert(CW == 32, "one 32-column TMEM load per compute thread and tile");
 };
 
 enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_VF + 2,
              QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DS, QB_DONE, QB_DRAIN, QB_OPS, QB_COUNT };
 
-template <int DQK, int DV, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+// DROP is a template parameter so the kernel without dropout is compiled
+// alone and stays within 96 registers a thread without spilling.
+template <int DQK, int DV, bool BF16, bool DROP>
+__global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
   using C = DqCfg<DQK, DV>;
-  constexpr int BM = C::BM, BN = C::BN, CW = C::CW, ST = C::STAGES;
+  constexpr int BM = C::BM, BN = C::BN, CW = C::CW, ST = C::STAGES, NCT = C::NCT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
@@ -79,7 +86,7 @@ __global__ void __launch_bounds__(320, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kLoadWarp = 8, kMmaWarp = 9;
+  constexpr int kLoadWarp = NCT / 32, kMmaWarp = NCT / 32 + 1;
 
   // ---- query tile of this CTA: heaviest causal tiles first, batch fastest
   const int n_qt = (p.S_q + BM - 1) / BM;
@@ -94,7 +101,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_COUNT; ++i)
-      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS || i == QB_OPS) ? 256u : 1u);
+      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS || i == QB_OPS) ? static_cast<uint32_t>(NCT) : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -185,12 +192,16 @@ __global__ void __launch_bounds__(320, 1)
           umma_ss_w(tDP, desc_adv(dO0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bv, kIdS, kk > 0);
       }
     };
-    auto issue_dq = [&](int j) {  // dQ += dS K_j, dS packed two per column
+    // dS of keys [16kk, 16kk+16), packed two per column in the second half of
+    // the CW dP columns each compute group read
+    auto ds_col = [](int kk) -> uint32_t {
+      return static_cast<uint32_t>(((kk * 16) / CW) * CW + CW / 2 + ((kk * 16) % CW) / 2);
+    };
+    auto issue_dq = [&](int j) {  // dQ += dS K_j
       const uint64_t dk = desc_adv(dKm0, (j % ST) * C::K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
-        umma_ts_w(tDQ, tDP + (kk >> 2) * CW + (kk & 3) * 8, desc_adv(dk, kk * 2048), kIdDQ,
-                (j > 0 || kk > 0));
+        umma_ts_w(tDQ, tDP + ds_col(kk), desc_adv(dk, kk * 2048), kIdDQ, (j > 0 || kk > 0));
     };
     auto wait_kv = [&](int which, int j) {
       return mbar_wait_w(bar(which + j % ST), (j / ST) & 1, ec, kSiteBwdMma);
@@ -266,107 +277,110 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     if constexpr (C::OPS_IN_TMEM) {  // Q and dO rows into this thread's TMEM lane
       ok = mbar_wait(bar(QB_Q), 0, ec, kSiteBwdCompute);
-      if (ok) {
+      if (ok && hf < 2) {  // the first two groups copy one half of the columns each
         smem_row_to_tmem<DQK / 2>(smem + C::OFF_Q, BM, row, hf * (DQK / 2),
                                   tbase + lane_off + C::T_Q + hf * (DQK / 4));
         smem_row_to_tmem<DV / 2>(smem + C::OFF_DO, BM, row, hf * (DV / 2),
                                  tbase + lane_off + C::T_DO + hf * (DV / 4));
         tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(QB_OPS));
       }
+      tc_fence_before();
+      if (ok) mbar_arrive(bar(QB_OPS));
     }
-    auto body = [&](auto drop_tag) {
-      constexpr bool DROP = decltype(drop_tag)::value;
-      const float zk = p.keep_scale;
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int kc0 = j * BN + CW * hf;  // first key of this thread's columns
-        uint32_t keep[CW / 32] = {};
-        if constexpr (DROP) {
+    const float zk = p.keep_scale;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int kc0 = j * BN + CW * hf;  // first key of this thread's columns
+      uint32_t keep = 0;                 // bit c: keep flag of local column c
+      if constexpr (DROP) {
 #pragma unroll
-          for (int g = 0; g < CW / 4; ++g) {
-            const uint4 d = dropout_draws((lin_row + kc0) / 4 + g, p.seed_lo, p.seed_hi,
-                                          p.offset_lo, p.offset_hi);
-            const uint32_t k4 = static_cast<uint32_t>(d.x >= p.drop_threshold) |
-                                (static_cast<uint32_t>(d.y >= p.drop_threshold) << 1) |
-                                (static_cast<uint32_t>(d.z >= p.drop_threshold) << 2) |
-                                (static_cast<uint32_t>(d.w >= p.drop_threshold) << 3);
-            keep[g / 8] |= k4 << (4 * (g % 8));
+        for (int g = 0; g < CW / 4; ++g) {
+          const uint4 d = dropout_draws((lin_row + kc0) / 4 + g, p.seed_lo, p.seed_hi,
+                                        p.offset_lo, p.offset_hi);
+          const uint32_t k4 = static_cast<uint32_t>(d.x >= p.drop_threshold) |
+                              (static_cast<uint32_t>(d.y >= p.drop_threshold) << 1) |
+                              (static_cast<uint32_t>(d.z >= p.drop_threshold) << 2) |
+                              (static_cast<uint32_t>(d.w >= p.drop_threshold) << 3);
+          keep |= k4 << (4 * g);
+        }
+      }
+      auto zf = [&](int c) -> float {
+        if constexpr (DROP) return ((keep >> c) & 1u) ? zk : 0.f;
+        return 1.0f;
+      };
+      if (!(ok = mbar_wait(bar(QB_S), j & 1, ec, kSiteBwdCompute))) break;
+      tc_fence_after();
+      // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)
+      float pr[CW];
+      {
+        uint32_t a0[32];
+        tmem_ld32(tbase + C::T_S + lane_off + CW * hf, a0);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pr[e] = fmaf(__uint_as_float(a0[e]), p.scale_log2, nl2);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(QB_SFREE));
+      if (bias_row != nullptr) {
+        if (bias_vec && kc0 + CW <= p.S_kv) {
+          const float4* b4 = reinterpret_cast<const float4*>(bias_row + kc0);
+#pragma unroll
+          for (int i = 0; i < CW / 4; ++i) {
+            const float4 v = __ldg(b4 + i);
+            pr[4 * i + 0] = fmaf(v.x, kLog2e, pr[4 * i + 0]);
+            pr[4 * i + 1] = fmaf(v.y, kLog2e, pr[4 * i + 1]);
+            pr[4 * i + 2] = fmaf(v.z, kLog2e, pr[4 * i + 2]);
+            pr[4 * i + 3] = fmaf(v.w, kLog2e, pr[4 * i + 3]);
           }
-        }
-        auto zf = [&](int c) -> float {
-          if constexpr (DROP) return ((keep[c >> 5] >> (c & 31)) & 1u) ? zk : 0.f;
-          return 1.0f;
-        };
-        if (!(ok = mbar_wait(bar(QB_S), j & 1, ec, kSiteBwdCompute))) break;
-        tc_fence_after();
-        float pr[CW];
-#pragma unroll
-        for (int c = 0; c < CW / 32; ++c) {
-          uint32_t a0[32];
-          tmem_ld32(tbase + C::T_S + lane_off + CW * hf + 32 * c, a0);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pr[32 * c + e] = __uint_as_float(a0[e]) * p.scale_log2;
-        }
-        tc_fence_before();
-        mbar_arrive(bar(QB_SFREE));
-        if (bias_row != nullptr) {
-          if (bias_vec && kc0 + CW <= p.S_kv) {
-            const float4* b4 = reinterpret_cast<const float4*>(bias_row + kc0);
-#pragma unroll
-            for (int i = 0; i < CW / 4; ++i) {
-              const float4 v = __ldg(b4 + i);
-              pr[4 * i + 0] = fmaf(v.x, kLog2e, pr[4 * i + 0]);
-              pr[4 * i + 1] = fmaf(v.y, kLog2e, pr[4 * i + 1]);
-              pr[4 * i + 2] = fmaf(v.z, kLog2e, pr[4 * i + 2]);
-              pr[4 * i + 3] = fmaf(v.w, kLog2e, pr[4 * i + 3]);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < CW; ++c)
-              if (kc0 + c < p.S_kv) pr[c] = fmaf(__ldg(bias_row + kc0 + c), kLog2e, pr[c]);
-          }
-        }
-        const bool need_mask = (kc0 + CW > p.S_kv) || (p.causal && kc0 + CW - 1 > q0) || !row_ok;
-        if (need_mask) {
-          const int last = row_ok ? (p.causal ? min(p.S_kv - 1, qr) : p.S_kv - 1) : -1;
+        } else {
 #pragma unroll
           for (int c = 0; c < CW; ++c)
-            if (kc0 + c > last) pr[c] = SDPA_NEG_INF;
+            if (kc0 + c < p.S_kv) pr[c] = fmaf(__ldg(bias_row + kc0 + c), kLog2e, pr[c]);
         }
-#pragma unroll
-        for (int c = 0; c < CW; ++c) pr[c] = ex2(pr[c] + nl2);
-        if (!(ok = mbar_wait(bar(QB_DP), j & 1, ec, kSiteBwdCompute))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < CW / 32; ++c) {
-          uint32_t a0[32];
-          tmem_ld32(tbase + C::T_DP + lane_off + CW * hf + 32 * c, a0);
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int cc = 32 * c + 2 * e;
-            const float d0 = __uint_as_float(a0[2 * e]), d1 = __uint_as_float(a0[2 * e + 1]);
-            const float s0 = pr[cc] * (DROP ? fmaf(d0, zf(cc), -Drow) : d0 - Drow);
-            const float s1 = pr[cc + 1] * (DROP ? fmaf(d1, zf(cc + 1), -Drow) : d1 - Drow);
-            pk[e] = pack2<BF16>(s0, s1);
-          }
-          // dS over the first half of the dP columns this thread has read
-          tmem_st16(tbase + C::T_DP + lane_off + CW * hf + 16 * c, pk);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(QB_DS));
       }
-    };
-    if (p.dropout)
-      body(std::true_type{});
-    else
-      body(std::false_type{});
-    // ---- epilogue: dQ * scale; each half writes half of the columns
-    if (ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute)) {
+      const bool need_mask = (kc0 + CW > p.S_kv) || (p.causal && kc0 + CW - 1 > q0) || !row_ok;
+      if (need_mask) {
+        const int last = row_ok ? (p.causal ? min(p.S_kv - 1, qr) : p.S_kv - 1) : -1;
+#pragma unroll
+        for (int c = 0; c < CW; ++c)
+          if (kc0 + c > last) pr[c] = SDPA_NEG_INF;
+      }
+#pragma unroll
+      for (int c = 0; c < CW; ++c) pr[c] = ex2(pr[c]);
+      if (!(ok = mbar_wait(bar(QB_DP), j & 1, ec, kSiteBwdCompute))) break;
+      tc_fence_after();
+      // dP in two halves of 16 columns (at most half of dP in registers next
+      // to P); dS of all 32 keys goes over the upper half once it is read
+      const uint32_t tcol = tbase + C::T_DP + lane_off + CW * hf;
+      auto ds_half = [&](const uint32_t (&dp)[16], int c0, uint32_t* out) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int cc = c0 + 2 * e;
+          const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
+          const float s0 = pr[cc] * (DROP ? fmaf(d0, zf(cc), -Drow) : d0 - Drow);
+          const float s1 = pr[cc + 1] * (DROP ? fmaf(d1, zf(cc + 1), -Drow) : d1 - Drow);
+          out[e] = pack2<BF16>(s0, s1);
+        }
+      };
+      uint32_t pk[16];
+      {
+        uint32_t lo[16];
+        tmem_ld16(tcol, lo);
+        tmem_wait_ld();
+        ds_half(lo, 0, pk);
+      }
+      {
+        uint32_t hi[16];
+        tmem_ld16(tcol + 16, hi);
+        tmem_wait_ld();
+        ds_half(hi, 16, pk + 8);
+      }
+      tmem_st16(tcol + 16, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(QB_DS));
+    }
+    // ---- epilogue: dQ * scale; the first two groups write half of the columns each
+    if (hf < 2 && ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute)) {
       tc_fence_after();
       constexpr int HW = DQK / 2;  // columns per thread
       uint8_t* dst_row = static_cast<uint8_t*>(p.dq) + ridx * DQK * 2 + hf * HW * 2;
@@ -401,7 +415,7 @@ template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
   using C = DqCfg<DQK, DV>;
-  auto kern = sdpa_bwd_dq_kernel<DQK, DV, BF16>;
+  auto kern = p.dropout ? sdpa_bwd_dq_kernel<DQK, DV, BF16, true> : sdpa_bwd_dq_kernel<DQK, DV, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
