@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
       const float L = live ? lse[row] : SDPA_NEG_INF;
       const size_t si = stat_index(static_cast<size_t>(bh), s_pad, q);
       stats[si] = (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
-      stats[si + 64] = acc;
+      stats[si + 64] = -acc;
     }
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);

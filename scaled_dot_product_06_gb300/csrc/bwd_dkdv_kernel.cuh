@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const bool kv_ok = kv < p.S_kv;
     // This thread's 32 query columns lie in one 64-row block of the statistics
-    // slot: 64 values -LSE*log2e (-inf for rows without keys), then 64 D.
+    // slot: 64 values -LSE*log2e (-inf for rows without keys), then 64 -D.
     const int stat_off = ((CW * hf) / 64) * 128 + (CW * hf) % 64;
     bool ok = true;
     if (C::OPS_IN_TMEM && n_it > 0) {  // K and V rows into this thread's TMEM lane
@@ -367,13 +367,18 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
           uint32_t a0[32];
           tmem_ld32(tbase + C::T_S + lane_off + CW * hf + 32 * c, a0);
           tmem_wait_ld();
+          const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 n4 = nl2[8 * c + e4];
-            pr[32 * c + 4 * e4 + 0] = fmaf(__uint_as_float(a0[4 * e4 + 0]), p.scale_log2, n4.x);
-            pr[32 * c + 4 * e4 + 1] = fmaf(__uint_as_float(a0[4 * e4 + 1]), p.scale_log2, n4.y);
-            pr[32 * c + 4 * e4 + 2] = fmaf(__uint_as_float(a0[4 * e4 + 2]), p.scale_log2, n4.z);
-            pr[32 * c + 4 * e4 + 3] = fmaf(__uint_as_float(a0[4 * e4 + 3]), p.scale_log2, n4.w);
+            const float2 x01 = f2split(fma2(f2(__uint_as_float(a0[4 * e4 + 0]), __uint_as_float(a0[4 * e4 + 1])),
+                                            sc2, f2(n4.x, n4.y)));
+            const float2 x23 = f2split(fma2(f2(__uint_as_float(a0[4 * e4 + 2]), __uint_as_float(a0[4 * e4 + 3])),
+                                            sc2, f2(n4.z, n4.w)));
+            pr[32 * c + 4 * e4 + 0] = x01.x;
+            pr[32 * c + 4 * e4 + 1] = x01.y;
+            pr[32 * c + 4 * e4 + 2] = x23.x;
+            pr[32 * c + 4 * e4 + 3] = x23.y;
           }
         }
         tc_fence_before();
@@ -408,18 +413,22 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         float* dbias_col = (p.dbias != nullptr && kv_ok)
                                ? p.dbias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
                                : nullptr;
-        // dS = P * (dP * Z - D) of local columns [c0, c0 + 16) into 8 packed words
+        // dS = P * (dP * Z - D) of local columns [c0, c0 + 16) into 8 packed
+        // words, two columns per f32x2 instruction (dd holds -D)
         auto ds_half = [&](const uint32_t (&dp)[16], int c0, uint32_t* out) {
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 d4 = dd[c0 / 4 + e4];
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            const float4 nd4 = dd[c0 / 4 + e4];
             float ds[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int cc = c0 + 4 * e4 + e;
-              const float dpv = __uint_as_float(dp[4 * e4 + e]);
-              ds[e] = pr[cc] * (DROP ? fmaf(dpv, zf(cc), -dv4[e]) : dpv - dv4[e]);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int cc = c0 + 4 * e4 + 2 * h2;
+              const uint64_t dp2 = f2(__uint_as_float(dp[4 * e4 + 2 * h2]), __uint_as_float(dp[4 * e4 + 2 * h2 + 1]));
+              const uint64_t nd2 = h2 ? f2(nd4.z, nd4.w) : f2(nd4.x, nd4.y);
+              const uint64_t t2 = fma2(dp2, f2(zf(cc), zf(cc + 1)), nd2);
+              const float2 r = f2split(mul2(f2(pr[cc], pr[cc + 1]), t2));
+              ds[2 * h2] = r.x;
+              ds[2 * h2 + 1] = r.y;
             }
             if (dbias_col != nullptr) {
 #pragma unroll

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     // reaches beyond the statistics' padding to 128 rows)
     const size_t sidx = stat_index(static_cast<size_t>(bh), p.S_pad, qr);
     const float nl2 = p.stats[sidx];
-    const float Drow = p.stats[sidx + 64];
+    const float nDrow = p.stats[sidx + 64];  // -D
     const float* bias_row =
         (p.bias != nullptr && row_ok) ? p.bias + (static_cast<size_t>(h) * p.S_q + qr) * p.S_kv : nullptr;
     const bool bias_vec = (p.S_kv & 3) == 0;
@@ -315,8 +315,13 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         uint32_t a0[32];
         tmem_ld32(tbase + C::T_S + lane_off + CW * hf, a0);
         tmem_wait_ld();
+        const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nl22 = f2(nl2, nl2);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pr[e] = fmaf(__uint_as_float(a0[e]), p.scale_log2, nl2);
+        for (int e = 0; e < 16; ++e) {
+          const float2 x = f2split(fma2(f2(__uint_as_float(a0[2 * e]), __uint_as_float(a0[2 * e + 1])), sc2, nl22));
+          pr[2 * e] = x.x;
+          pr[2 * e + 1] = x.y;
+        }
       }
       tc_fence_before();
       mbar_arrive(bar(QB_SFREE));
@@ -351,14 +356,14 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       // dP in two halves of 16 columns (at most half of dP in registers next
       // to P); dS of all 32 keys goes over the upper half once it is read
       const uint32_t tcol = tbase + C::T_DP + lane_off + CW * hf;
+      const uint64_t nD2 = f2(nDrow, nDrow);
       auto ds_half = [&](const uint32_t (&dp)[16], int c0, uint32_t* out) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int cc = c0 + 2 * e;
           const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
-          const float s0 = pr[cc] * (DROP ? fmaf(d0, zf(cc), -Drow) : d0 - Drow);
-          const float s1 = pr[cc + 1] * (DROP ? fmaf(d1, zf(cc + 1), -Drow) : d1 - Drow);
-          out[e] = pack2<BF16>(s0, s1);
+          const float2 r = f2split(mul2(f2(pr[cc], pr[cc + 1]), fma2(f2(d0, d1), f2(zf(cc), zf(cc + 1)), nD2)));
+          out[e] = pack2<BF16>(r.x, r.y);
         }
       };
       uint32_t pk[16];

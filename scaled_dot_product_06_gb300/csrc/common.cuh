@@ -41,7 +41,8 @@ struct FwdParams {
 
 // Row statistics the backward kernels share, written by the preprocess kernel:
 // for each (b, h) and each block of 64 query rows (S_q padded to a multiple
-// of 128), 64 floats -LSE * log2(e) followed by 64 floats D = rowsum(dO * O).
+// of 128), 64 floats -LSE * log2(e) followed by 64 floats -D, D = rowsum(dO * O)
+// (negated so dP - D is one fused multiply-add, also with the dropout factor).
 // A tile of 64 or 128 query rows is thus one contiguous run of 512 or 1024
 // bytes, fetched with one bulk copy. Rows past S_q hold -inf and 0.
 __host__ __device__ __forceinline__ size_t stat_index(size_t bh, int S_pad, int q) {
@@ -97,6 +98,30 @@ __device__ __forceinline__ uint4 dropout_draws(uint64_t g, uint32_t seed_lo, uin
 }
 
 // ---------------------------------------------------------------- arithmetic
+// Packed pairs of fp32 (sm_100 family f32x2 arithmetic): one instruction does
+// two lanes' worth of FMA-pipe work, halving the issue slots the softmax and
+// dS loops spend on it (the pipe throughput itself is unchanged).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
