@@ -53,18 +53,30 @@ struct DqCfg {
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int THREADS = NCT + 64;  // + producer warp + MMA warp
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
-  // Q and dO, the operands every tile reuses, live in TMEM when they fit, so
-  // the S and dP products read only K_j / V_j from shared memory.
-  static constexpr bool OPS_IN_TMEM = DQK + DQK / 2 + DV / 2 <= 256;
+  // Two dP buffers where they fit next to the dQ accumulator and the Q / dO
+  // operands (d_qk = 64): dS(j) stays in its dP buffer until dQ(j) has read
+  // it, so with one buffer dP(j+1) queues behind dQ(j) and dQ(j) + dP(j+1) +
+  // the dS step sit on the per-tile critical path; with two, dP(j+1) is
+  // formed while tile j's softmax runs. At d_qk = 128 the second buffer would
+  // cost the TMEM copies of Q and dO; measured on GB300, the S and dP products
+  // then reading both operands from shared memory (and the K ring held longer)
+  // cost more than the shorter chain saves (dQ 2.35 -> 2.94 ms at b1 h32
+  // s16384 causal), so one buffer stays there.
+  static constexpr int DPB = (128 + 2 * 128 + DQK + DQK / 2 + DV / 2 <= 512) ? 2 : 1;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 128 + 128 * DPB;
+  // Q and dO, the operands every tile reuses, live in TMEM when they also fit,
+  // so the S and dP products read only K_j / V_j from shared memory.
+  static constexpr bool OPS_IN_TMEM = T_DQ + DQK + DQK / 2 + DV / 2 <= 512;
   static constexpr uint32_t T_Q = T_DQ + DQK, T_DO = T_Q + DQK / 2;
   static_assert(T_DQ + DQK <= 512, "tensor memory overflow");
+  static_assert(DPB == 1 || STAGES == 2, "two dP buffers issue dP(j+1) before dQ(j)");
   static_assert(SMEM <= 227 * 1024, "shared memory overflow");
   static_assert(CW == 32, "one 32-column TMEM load per compute thread and tile");
 };
 
 enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_VF + 2,
-             QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DS, QB_DONE, QB_DRAIN, QB_OPS, QB_COUNT };
+             QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DS = QB_DP + 2, QB_DONE = QB_DS + 2, QB_DRAIN, QB_OPS,
+             QB_COUNT };
 
 // DROP is a template parameter so the kernel without dropout is compiled
 // alone and stays within 96 registers a thread without spilling.
@@ -101,7 +113,9 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_COUNT; ++i)
-      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS || i == QB_OPS) ? static_cast<uint32_t>(NCT) : 1u);
+      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS || i == QB_DS + 1 || i == QB_OPS)
+                            ? static_cast<uint32_t>(NCT)
+                            : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -165,7 +179,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_f16(128, BN, BF16, false, false);
     constexpr uint32_t kIdDQ = idesc_f16(128, DQK, BF16, false, true);
-    const uint32_t tS = tbase + C::T_S, tDP = tbase + C::T_DP, tDQ = tbase + C::T_DQ;
+    const uint32_t tS = tbase + C::T_S, tDQ = tbase + C::T_DQ;
     // base descriptors, advanced by constant offsets per instruction
     const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024), dO0 = sdesc_sw128(sdO, 16, 1024);
     const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dV0 = sdesc_sw128(sV, 16, 1024);
@@ -181,7 +195,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
           umma_ss_w(tS, desc_adv(dQ0, (kk >> 2) * (BM * 128) + (kk & 3) * 32), bk, kIdS, kk > 0);
       }
     };
-    auto issue_dp = [&](int j) {  // dP = dO V_j^T
+    auto issue_dp = [&](int j) {  // dP = dO V_j^T into buffer j % DPB
+      const uint32_t tDP = tbase + C::T_DP + 128 * (j % C::DPB);
       const uint64_t dv = desc_adv(dV0, (j % ST) * C::V_BYTES);
 #pragma unroll
       for (int kk = 0; kk < DV / 16; ++kk) {
@@ -197,7 +212,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     auto ds_col = [](int kk) -> uint32_t {
       return static_cast<uint32_t>(((kk * 16) / CW) * CW + CW / 2 + ((kk * 16) % CW) / 2);
     };
-    auto issue_dq = [&](int j) {  // dQ += dS K_j
+    auto issue_dq = [&](int j) {  // dQ += dS K_j, dS in dP buffer j % DPB
+      const uint32_t tDP = tbase + C::T_DP + 128 * (j % C::DPB);
       const uint64_t dk = desc_adv(dKm0, (j % ST) * C::K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
@@ -223,34 +239,55 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     }
     for (int j = 0; ok && j < n_kv; ++j) {
       const bool more = j + 1 < n_kv;
-      // With two stages the next S is formed while the compute warps work on
-      // tile j; with one stage K_{j+1} cannot land before dQ(j) frees K_j.
-      if constexpr (ST > 1) {
+      const int b = j % C::DPB;
+      if constexpr (C::DPB == 2) {
+        // S(j+1) and dP(j+1) (other buffer) while the compute warps work on tile j
         if (more) {
           if (!(ok = mbar_wait_w(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
           tc_fence_after();
           issue_s(j + 1);
           umma_commit_w(bar(QB_S));
-        }
-      }
-      if (!(ok = mbar_wait_w(bar(QB_DS), j & 1, ec, kSiteBwdMma))) break;
-      tc_fence_after();
-      issue_dq(j);
-      umma_commit_w(bar(QB_KE + j % ST));
-      if constexpr (ST == 1) {
-        if (more) {
-          if (!(ok = mbar_wait_w(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
+          if (!(ok = wait_kv(QB_VF, j + 1))) break;
           tc_fence_after();
-          issue_s(j + 1);
-          umma_commit_w(bar(QB_S));
+          issue_dp(j + 1);
+          umma_commit_w(bar(QB_DP + (j + 1) % 2));
+          umma_commit_w(bar(QB_VE + (j + 1) % ST));
         }
-      }
-      if (more) {
-        if (!(ok = wait_kv(QB_VF, j + 1))) break;
+        if (!(ok = mbar_wait_w(bar(QB_DS + b), (j / 2) & 1, ec, kSiteBwdMma))) break;
         tc_fence_after();
-        issue_dp(j + 1);
-        umma_commit_w(bar(QB_DP));
-        umma_commit_w(bar(QB_VE + (j + 1) % ST));
+        issue_dq(j);
+        umma_commit_w(bar(QB_KE + j % ST));
+      } else {
+        // one dP buffer: dP(j+1) goes after dQ(j), which reads dS(j) from it.
+        // With two stages the next S is formed while the compute warps work on
+        // tile j; with one stage K_{j+1} cannot land before dQ(j) frees K_j.
+        if constexpr (ST > 1) {
+          if (more) {
+            if (!(ok = mbar_wait_w(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
+            tc_fence_after();
+            issue_s(j + 1);
+            umma_commit_w(bar(QB_S));
+          }
+        }
+        if (!(ok = mbar_wait_w(bar(QB_DS), j & 1, ec, kSiteBwdMma))) break;
+        tc_fence_after();
+        issue_dq(j);
+        umma_commit_w(bar(QB_KE + j % ST));
+        if constexpr (ST == 1) {
+          if (more) {
+            if (!(ok = mbar_wait_w(bar(QB_SFREE), j & 1, ec, kSiteBwdMma) && wait_kv(QB_KF, j + 1))) break;
+            tc_fence_after();
+            issue_s(j + 1);
+            umma_commit_w(bar(QB_S));
+          }
+        }
+        if (more) {
+          if (!(ok = wait_kv(QB_VF, j + 1))) break;
+          tc_fence_after();
+          issue_dp(j + 1);
+          umma_commit_w(bar(QB_DP));
+          umma_commit_w(bar(QB_VE + (j + 1) % ST));
+        }
       }
     }
     if (ok) umma_commit_w(bar(QB_DONE));
@@ -351,11 +388,12 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       }
 #pragma unroll
       for (int c = 0; c < CW; ++c) pr[c] = ex2(pr[c]);
-      if (!(ok = mbar_wait(bar(QB_DP), j & 1, ec, kSiteBwdCompute))) break;
+      const int b = j % C::DPB;  // dP buffer of this tile
+      if (!(ok = mbar_wait(bar(QB_DP + b), (j / C::DPB) & 1, ec, kSiteBwdCompute))) break;
       tc_fence_after();
       // dP in two halves of 16 columns (at most half of dP in registers next
       // to P); dS of all 32 keys goes over the upper half once it is read
-      const uint32_t tcol = tbase + C::T_DP + lane_off + CW * hf;
+      const uint32_t tcol = tbase + C::T_DP + 128 * b + lane_off + CW * hf;
       const uint64_t nD2 = f2(nDrow, nDrow);
       auto ds_half = [&](const uint32_t (&dp)[16], int c0, uint32_t* out) {
 #pragma unroll
@@ -382,7 +420,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       tmem_st16(tcol + 16, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(QB_DS));
+      mbar_arrive(bar(QB_DS + b));
     }
     // ---- epilogue: dQ * scale; the first two groups write half of the columns each
     if (hf < 2 && ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute)) {
