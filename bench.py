@@ -196,6 +196,24 @@ def run_reference(args, w, rank):
     print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Slowest rank's value (all ranks get it); identity for one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, step_flops: float, ms_per_step: float) -> float:
+    """Units all ranks processed / the slowest rank's time: every rank runs
+    the same workload (independent replicas, no data-path collective)."""
+    return world * step_flops / (ms_per_step * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -205,9 +223,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-sample", type=int, default=4096,
-                    help="query positions of the one-head oracle sample (cpu_baseline)")
-    ap.add_argument("--ref-sample", type=int, default=2048,
+    ap.add_argument("--cpu-sample", type=int, default=16384,
+                    help="query positions of the one-head oracle sample (cpu_baseline); the "
+                         "default is a whole head of the long-context workload, ~15 s of CPU")
+    ap.add_argument("--ref-sample", type=int, default=4096,
                     help="query positions of the one-head oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -294,15 +313,11 @@ def main():
         for i, n in enumerate(names):
             per_kernel[n] += e[i].elapsed_time(e[i + 1])
     per_kernel = {n: t / args.steps for n, t in per_kernel.items()}
-    ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(total_ms / args.steps, world, dev)
 
     ff = fwd_flops(w)
     step_flops = 3.5 * ff
-    value = world * step_flops / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, step_flops, ms)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
 
@@ -359,12 +374,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+        e2e = {"value": whole_job_tflops(world, step_flops, e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
@@ -372,8 +383,9 @@ def main():
         secs, flops = oracle_sample(w, args.cpu_sample)
         cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": cpu_threads(),
                "kind": "oracle",
-               "sample": (f"one head, first {min(args.cpu_sample, w['S_q'])} query positions of "
-                          f"the workload, fp64 numpy oracle fwd+bwd ({secs:.1f} s)")}
+               "sample": (f"one head (of {w['B'] * w['H']}), first {min(args.cpu_sample, w['S_q'])} "
+                          f"query positions of the workload, fp64 numpy oracle fwd+bwd "
+                          f"({secs:.1f} s)")}
 
     if rank == 0:
         kt = {n: {"ms": t} for n, t in per_kernel.items()}

@@ -100,16 +100,19 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kLoadWarp = NCT / 32, kMmaWarp = NCT / 32 + 1;
 
-  // ---- query tile of this CTA: heaviest causal tiles first, batch fastest
+  // ---- query tile of this CTA (order: query_tile_order, one head at a time:
+  // measured at b1 h32 s16384 causal, dQ 2.08 ms one head per group, 2.13 ms
+  // eight, 2.29 ms with every head in flight)
   const int n_qt = (p.S_q + BM - 1) / BM;
-  const int n_bh = p.B * p.H;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / n_bh);
-  const int r = static_cast<int>(blockIdx.x % n_bh);
-  const int b = r % p.B, h = r / p.B;
+  const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_qt, 1);
+  const int b = qtile.b, h = qtile.h, qt = qtile.qt;
   const int bh = b * p.H + h;
   const int q0 = qt * BM;
   const int n_kv_all = (p.S_kv + BN - 1) / BN;
   const int n_kv = p.causal ? min(n_kv_all, (q0 + BM - 1) / BN + 1) : n_kv_all;
+  // Iteration j visits key tile n_kv - 1 - j: the CTAs of one head, resident
+  // together, then start on different tiles (their own diagonal) instead of
+  // all requesting tile 0 from L2 at once.
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_COUNT; ++i)
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_KF + s), C::K_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, j * BN, bh);
+          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, (n_kv - 1 - j) * BN, bh);
       }
       if (!mbar_wait(bar(QB_VE + s), ph ^ 1, ec, kSiteBwdLoad)) {
         issued = 2 * j + 1;
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_VF + s), C::V_BYTES);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, j * BN, bh);
+          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, (n_kv - 1 - j) * BN, bh);
       }
       issued = 2 * j + 2;
     }
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     }
     const float zk = p.keep_scale;
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int kc0 = j * BN + CW * hf;  // first key of this thread's columns
+      const int kc0 = (n_kv - 1 - j) * BN + CW * hf;  // first key of this thread's columns
       uint32_t keep = 0;                 // bit c: keep flag of local column c
       if constexpr (DROP) {
 #pragma unroll

@@ -50,6 +50,26 @@ __host__ __device__ __forceinline__ size_t stat_index(size_t bh, int S_pad, int 
 }
 __host__ __device__ __forceinline__ int stat_pad(int S_q) { return (S_q + 127) & ~127; }
 
+// Order of the query tiles of the query-stationary kernels (forward, dQ):
+// heads in groups of G, the largest divisor of H not above gmax, one group
+// after another; within a group the causal tiles with the most key tiles first,
+// across the group's heads; batch fastest (the batches of one head share
+// Bias rows). The CTAs resident together then read the K and V of at most G
+// heads (which stay in L2; with all heads in flight the forward and dQ read
+// K and V 5-7 times from DRAM), while the grid still ends on its lightest
+// tiles (one head after another would end on a head's heaviest tile).
+struct QueryTile {
+  int b, h, qt;
+};
+__device__ __forceinline__ QueryTile query_tile_order(int idx, int B, int H, int n_qt, int gmax) {
+  int G = H < gmax ? H : gmax;
+  while (H % G != 0) --G;
+  const int b = idx % B;
+  const int r = idx / B;
+  const int g = r / (n_qt * G), w = r % (n_qt * G);
+  return QueryTile{b, g * G + w % G, n_qt - 1 - w / G};
+}
+
 struct BwdParams {
   int B, H, S_q, S_kv;
   float scale;             // softmax scale

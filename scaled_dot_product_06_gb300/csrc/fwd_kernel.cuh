@@ -66,16 +66,19 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- tile of this CTA: heaviest causal query tiles first, batch fastest
+  // ---- query tile of this CTA (order: query_tile_order, groups of up to 8
+  // heads: measured at b1 h32 s16384 causal, 1.83 ms, against 1.98 ms one head
+  // at a time, whose grid ends on a head's heaviest tiles)
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
-  const int n_bh = p.B * p.H;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / n_bh);
-  const int r = static_cast<int>(blockIdx.x % n_bh);
-  const int b = r % p.B, h = r / p.B;
+  const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_qt, 8);
+  const int b = qtile.b, h = qtile.h, qt = qtile.qt;
   const int bh = b * p.H + h;
   const int q0 = qt * C::BM;
   const int n_kv_all = (p.S_kv + C::BN - 1) / C::BN;
   const int n_kv = p.causal ? min(n_kv_all, (q0 + C::BM - 1) / C::BN + 1) : n_kv_all;
+  // Iteration j visits key tile n_kv - 1 - j: the CTAs of one head, resident
+  // together, then start on different tiles (their own diagonal) instead of
+  // all requesting tile 0 from L2 at once.
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < FB_COUNT; ++i) mbar_init(bar(i), i == FB_P ? 128u : 1u);
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
           tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64,
-                      j * C::BN, bh);
+                      (n_kv - 1 - j) * C::BN, bh);
       }
       if (!mbar_wait(bar(FB_VE + s), ph ^ 1, ec, kSiteFwdLoad)) {
         issued = 2 * j + 1;
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
           tma_load_3d(sV + s * C::V_BYTES + c * C::BN * 128, &tmV, bar(FB_VF + s), c * 64,
-                      j * C::BN, bh);
+                      (n_kv - 1 - j) * C::BN, bh);
       }
       issued = 2 * j + 2;
     }
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]) * sl2;
       }
-      const int k0 = j * C::BN;
+      const int k0 = (n_kv - 1 - j) * C::BN;  // key tiles from the diagonal down
       if (p.bias != nullptr) {
         if (bias_row != nullptr) {
           if (bias_vec && k0 + C::BN <= p.S_kv) {
