@@ -45,6 +45,10 @@ WORKLOADS = {
                                                  scale=None),
     "b1h32-s16384-d128-causal": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
                                      dtype="bf16", causal=True, bias=False, p=0.0, scale=None),
+    # half the heads and half the sequence of the long-context case: the size the
+    # full ncu section captures in profiles/ are taken at (inputs 134 MB > L2)
+    "b1h16-s8192-d128-causal": dict(B=1, H=16, S_q=8192, S_kv=8192, D_qk=128, D_v=128,
+                                    dtype="bf16", causal=True, bias=False, p=0.0, scale=None),
 }
 DEFAULT_WORKLOAD = "b1h32-s16384-d128-causal"
 DROP_SEED, DROP_OFFSET = 0x1234, 0
