@@ -8,20 +8,33 @@
 // the product with V (keep / (1 - p)) and the softmax statistic returned as in
 // PyTorch cudnn MHA.cpp run_cudnn_SDP_fprop (fp32 [b, h, s_q]).
 //
-// One CTA owns a tile of 128 query rows of one (b, h) and walks the key/value
-// tiles of 128 rows:
-//   warp 4       TMA producer: Q once, then K_j and V_j through a ring.
-//   warp 5       MMA issuer (one lane): S = Q K_j^T into TMEM, then
-//                O += P_j V_j with P_j read from TMEM.
-//   warps 0-3    softmax: thread t owns query row t = TMEM lane t. It reads
-//                S_j, applies scale, bias and mask in the exp2 domain, keeps a
-//                running max m and sum l, writes P_j (io dtype) over the first
-//                half of S_j's columns, and rescales O in TMEM when m has grown
-//                by more than 2^8 since it was last used (otherwise the stale
-//                max is kept; P <= 256 is exact enough in fp32 / bf16).
-// Tensor memory: columns [0,128) hold S_j (P_j aliases [0,64)); columns
-// [128, 128 + D_v) hold the O accumulator. Two CTAs share an SM when shared
-// memory allows, so one CTA's softmax overlaps the other's MMAs.
+// One CTA owns two tiles of 128 query rows (tile t = rows q0 + 128 t ..) of one
+// (b, h), one CTA per SM, and walks the key/value tiles of 128 rows that either
+// query tile sees, from the diagonal down. Each K_j / V_j tile is loaded once
+// for both query tiles.
+//   warpgroup 0, 1   softmax of query tile 0, 1: a thread owns one query row =
+//                    TMEM lane. It reads S_t, applies scale, bias and mask in
+//                    the exp2 domain, keeps a running max m and sum l, writes
+//                    P_t (io dtype) over the first half of S_t's columns, and
+//                    rescales O_t in TMEM when m has grown by more than 2^8
+//                    since it was last used (otherwise the stale max is kept;
+//                    P <= 256 is exact enough in fp32 / bf16).
+//   warpgroup 2      warp 8: TMA producer (both Q tiles once; K_j and V_j
+//                    through a ring). warp 9: MMA issuer; the whole warp runs
+//                    the issue loop and one elected lane issues. Warps 10-11
+//                    only give their registers away.
+// MMA order per key tile j: O_0 += P_0(j) V_j, S_0(j+1), O_1 += P_1(j) V_j,
+// S_1(j+1): while one warpgroup's softmax runs, the tensor core works for the
+// other tile, so each softmax has two MMA groups' time before the tensor core
+// waits for it. S_t(j+1) follows O_t's product in the in-order pipe, so it
+// never overwrites P_t(j) before that product has read it.
+// Tensor memory: S_0 [0,128), S_1 [128,256) (P_t aliases the first 64
+// columns of S_t), O_0 [256, 256 + D_v), O_1 after it.
+// Registers: launched at 168 a thread (384 threads); the producer/MMA
+// warpgroup drops to 72 and the softmax warpgroups rise to 216, enough for a
+// row's 128 scores without spilling: 2 x 128 x 216 + 128 x 72 = 384 x 168.
+// GENERAL (a bias or dropout present) is a template parameter so the plain
+// kernel is compiled without their registers.
 #pragma once
 #include "common.cuh"
 
@@ -29,31 +42,40 @@ namespace sdpa {
 
 template <int DQK, int DV>
 struct FwdCfg {
-  static constexpr int BM = 128, BN = 128;
-  static constexpr int STAGES = (DQK <= 64) ? 2 : (DQK <= 128 ? 1 : 2);
+  static constexpr int BM = 128, BN = 128;  // rows per query tile / key tile
   static constexpr int Q_BYTES = BM * DQK * 2;
   static constexpr int K_BYTES = BN * DQK * 2;
   static constexpr int V_BYTES = BN * DV * 2;
+  // as many K/V stages as fit next to the two Q tiles (at most 3)
+  static constexpr int AVAIL = 227 * 1024 - 2 * Q_BYTES - 256 - 1024;
+  static constexpr int FIT = AVAIL / (K_BYTES + V_BYTES);
+  static constexpr int STAGES = FIT >= 3 ? 3 : FIT;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * V_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
-  static constexpr int MIN_BLOCKS = (2 * SMEM <= 227 * 1024) ? 2 : 1;
-  static constexpr int THREADS = 192;
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_S = 0, T_O = 256;
+  // measured with ptxas at d = 128: the softmax needs ~210 registers, the
+  // MMA issuer ~70; below either the kernel spills
+  static constexpr int REG_LAUNCH = 168, REG_SOFTMAX = 216, REG_OTHER = 72;
+  static_assert(STAGES >= 1 && SMEM <= 227 * 1024, "shared memory");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "unsupported head size");
+  static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_OTHER == THREADS * REG_LAUNCH, "register split");
 };
 
-// Barrier slots.
-enum : int { FB_Q = 0, FB_S, FB_P, FB_O, FB_DRAIN, FB_KF, FB_KE = FB_KF + 2, FB_VF = FB_KE + 2,
-             FB_VE = FB_VF + 2, FB_COUNT = FB_VE + 2 };
+// Barrier slots (the K/V ring has at most 3 stages).
+enum : int { FB_Q = 0, FB_S, FB_P = FB_S + 2, FB_O = FB_P + 2, FB_DRAIN = FB_O + 2, FB_KF,
+             FB_KE = FB_KF + 3, FB_VF = FB_KE + 3, FB_VE = FB_VF + 3, FB_COUNT = FB_VE + 3 };
 
-template <int DQK, int DV, bool BF16>
-__global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
+template <int DQK, int DV, bool BF16, bool GENERAL>
+__global__ void __launch_bounds__(384, 1)
     sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<DQK, DV>;
+  constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sQ = smem_u32(smem + C::OFF_Q);
@@ -66,30 +88,39 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- query tile of this CTA (order: query_tile_order, groups of up to 8
-  // heads: measured at b1 h32 s16384 causal, 1.83 ms, against 1.98 ms one head
-  // at a time, whose grid ends on a head's heaviest tiles)
+  // ---- query tiles of this CTA: query_tile_order over pairs of query tiles,
+  // groups of up to 8 heads (one group's K/V stay in L2, the grid ends on its
+  // lightest pairs)
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
-  const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_qt, 8);
-  const int b = qtile.b, h = qtile.h, qt = qtile.qt;
+  const int n_pairs = (n_qt + 1) / 2;
+  const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_pairs, 8);
+  const int b = qtile.b, h = qtile.h;
   const int bh = b * p.H + h;
-  const int q0 = qt * C::BM;
+  const int q0 = qtile.qt * 2 * C::BM;  // first row of query tile 0
   const int n_kv_all = (p.S_kv + C::BN - 1) / C::BN;
-  const int n_kv = p.causal ? min(n_kv_all, (q0 + C::BM - 1) / C::BN + 1) : n_kv_all;
-  // Iteration j visits key tile n_kv - 1 - j: the CTAs of one head, resident
-  // together, then start on different tiles (their own diagonal) instead of
-  // all requesting tile 0 from L2 at once.
+  // key tiles query tile t sees (0 when the tile lies past S_q)
+  auto tile_kv = [&](int t) -> int {
+    const int qs = q0 + t * C::BM;
+    if (qs >= p.S_q) return 0;
+    return p.causal ? min(n_kv_all, (min(qs + C::BM, p.S_q) - 1) / C::BN + 1) : n_kv_all;
+  };
+  const int n_kv0 = tile_kv(0), n_kv1 = tile_kv(1);
+  const int n_it = max(n_kv0, n_kv1);
+  // Iteration j visits key tile n_it - 1 - j (from the diagonal down); query
+  // tile t takes part in iterations j >= n_it - n_kv_t.
+  const int j0_0 = n_it - n_kv0, j0_1 = n_it - n_kv1;
+  const bool has1 = n_kv1 > 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < FB_COUNT; ++i) mbar_init(bar(i), i == FB_P ? 128u : 1u);
+    for (int i = 0; i < FB_COUNT; ++i) mbar_init(bar(i), (i == FB_P || i == FB_P + 1) ? 128u : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -98,138 +129,182 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const uint32_t tS = tbase, tO = tbase + 128;
   const ErrCtx ec{p.err, abort_flag};
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    int issued = 0;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(FB_Q), C::Q_BYTES);
+  if (warp >= 8) {
+    setmaxnreg_dec<C::REG_OTHER>();
+    if (warp == 8) {
+      // ---------------------------------------------------------- producer
+      int issued = 0;
+      if (lane == 0 && n_it > 0) {
+        mbar_arrive_expect_tx(bar(FB_Q), (has1 ? 2 : 1) * C::Q_BYTES);
 #pragma unroll
-      for (int c = 0; c < DQK / 64; ++c)
-        tma_load_3d(sQ + c * C::BM * 128, &tmQ, bar(FB_Q), c * 64, q0, bh);
-    }
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % C::STAGES;
-      const uint32_t ph = (j / C::STAGES) & 1;
-      if (!mbar_wait(bar(FB_KE + s), ph ^ 1, ec, kSiteFwdLoad)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(FB_KF + s), C::K_BYTES);
+        for (int c = 0; c < DQK / 64; ++c) {
+          tma_load_3d(sQ + c * C::BM * 128, &tmQ, bar(FB_Q), c * 64, q0, bh);
+          if (has1)
+            tma_load_3d(sQ + C::Q_BYTES + c * C::BM * 128, &tmQ, bar(FB_Q), c * 64, q0 + C::BM, bh);
+        }
+      }
+      for (int j = 0; j < n_it; ++j) {
+        const int s = j % ST;
+        const uint32_t ph = (j / ST) & 1;
+        const int kv0 = (n_it - 1 - j) * C::BN;
+        if (!mbar_wait(bar(FB_KE + s), ph ^ 1, ec, kSiteFwdLoad)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(FB_KF + s), C::K_BYTES);
 #pragma unroll
-        for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64,
-                      (n_kv - 1 - j) * C::BN, bh);
-      }
-      if (!mbar_wait(bar(FB_VE + s), ph ^ 1, ec, kSiteFwdLoad)) {
-        issued = 2 * j + 1;
-        break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(FB_VF + s), C::V_BYTES);
+          for (int c = 0; c < DQK / 64; ++c)
+            tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64, kv0, bh);
+        }
+        if (!mbar_wait(bar(FB_VE + s), ph ^ 1, ec, kSiteFwdLoad)) {
+          issued = 2 * j + 1;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(FB_VF + s), C::V_BYTES);
 #pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sV + s * C::V_BYTES + c * C::BN * 128, &tmV, bar(FB_VF + s), c * 64,
-                      (n_kv - 1 - j) * C::BN, bh);
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_3d(sV + s * C::V_BYTES + c * C::BN * 128, &tmV, bar(FB_VF + s), c * 64, kv0, bh);
+        }
+        issued = 2 * j + 2;
       }
-      issued = 2 * j + 2;
-    }
-    __syncwarp();
-    // Drain: every copy issued must land before the CTA can retire. On the
-    // healthy path these phases completed long ago.
-    if (*abort_flag) {
-      mbar_wait(bar(FB_Q), 0, ec, kSiteDrain, false);
-      for (int i = 0; i < issued; ++i) {
-        const int j = i >> 1, s = j % C::STAGES;
-        const uint32_t ph = (j / C::STAGES) & 1;
-        mbar_wait(bar(((i & 1) ? FB_VF : FB_KF) + s), ph, ec, kSiteDrain, false);
+      __syncwarp();
+      // Drain: every copy issued must land before the CTA can retire. On the
+      // healthy path these phases completed long ago.
+      if (*abort_flag && n_it > 0) {
+        mbar_wait(bar(FB_Q), 0, ec, kSiteDrain, false);
+        for (int i = 0; i < issued; ++i) {
+          const int j = i >> 1, s = j % ST;
+          const uint32_t ph = (j / ST) & 1;
+          mbar_wait(bar(((i & 1) ? FB_VF : FB_KF) + s), ph, ec, kSiteDrain, false);
+        }
       }
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
-    constexpr uint32_t kIdO = idesc_f16(128, DV, BF16, false, true);
-    const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
-    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
-    const uint64_t dV0 = sdesc_sw128(sV, C::BN * 128, 1024);
-    // the whole warp runs the issue loop; one elected lane issues (umma_*_w)
-    bool ok = mbar_wait_w(bar(FB_Q), 0, ec, kSiteFwdMma);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int s = j % C::STAGES;
-      const uint32_t ph = (j / C::STAGES) & 1;
-      if (!(ok = mbar_wait_w(bar(FB_KF + s), ph, ec, kSiteFwdMma))) break;
-      tc_fence_after();
-      {
-        const uint64_t dK = desc_adv(dK0, s * C::K_BYTES);
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdS = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t kIdO = idesc_f16(128, DV, BF16, false, true);
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV, C::BN * 128, 1024);
+      uint32_t pph0 = 0, pph1 = 0;  // P phases consumed per query tile
+      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+        const uint64_t dQ = desc_adv(dQ0, t * C::Q_BYTES);
+        const uint64_t dK = desc_adv(dK0, (j % ST) * C::K_BYTES);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          umma_ss_w(tS, desc_adv(dQ0, off), desc_adv(dK, off), kIdS, kk > 0);
+          umma_ss_w(tbase + C::T_S + 128 * t, desc_adv(dQ, off), desc_adv(dK, off), kIdS, kk > 0);
         }
-        umma_commit_w(bar(FB_S));
-        umma_commit_w(bar(FB_KE + s));
-      }
-      if (!(ok = mbar_wait_w(bar(FB_P), j & 1, ec, kSiteFwdMma))) break;
-      if (!(ok = mbar_wait_w(bar(FB_VF + s), ph, ec, kSiteFwdMma))) break;
-      tc_fence_after();
-      {
-        const uint64_t dV = desc_adv(dV0, s * C::V_BYTES);
+        umma_commit_w(bar(FB_S + t));
+      };
+      auto issue_pv = [&](int t, int j, bool first) {  // O_t += P_t V_j
+        const uint64_t dV = desc_adv(dV0, (j % ST) * C::V_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts_w(tO, tS + kk * 8, desc_adv(dV, kk * 2048), kIdO, (j > 0 || kk > 0));
-        umma_commit_w(bar(FB_VE + s));
+          umma_ts_w(tbase + C::T_O + DV * t, tbase + C::T_S + 128 * t + kk * 8, desc_adv(dV, kk * 2048),
+                    kIdO, (!first || kk > 0));
+      };
+      auto wait_k = [&](int j) { return mbar_wait_w(bar(FB_KF + j % ST), (j / ST) & 1, ec, kSiteFwdMma); };
+      auto wait_v = [&](int j) { return mbar_wait_w(bar(FB_VF + j % ST), (j / ST) & 1, ec, kSiteFwdMma); };
+      bool ok = n_it > 0 && mbar_wait_w(bar(FB_Q), 0, ec, kSiteFwdMma) && wait_k(0);
+      if (ok) {
+        tc_fence_after();
+        if (j0_0 == 0) issue_s(0, 0);
+        if (has1 && j0_1 == 0) issue_s(1, 0);
+        umma_commit_w(bar(FB_KE + 0));
       }
+      for (int j = 0; ok && j < n_it; ++j) {
+        const bool more = j + 1 < n_it;
+        if (!(ok = wait_v(j))) break;
+        // query tile 0
+        if (j >= j0_0) {
+          if (!(ok = mbar_wait_w(bar(FB_P + 0), pph0, ec, kSiteFwdMma))) break;
+          pph0 ^= 1u;
+          tc_fence_after();
+          issue_pv(0, j, j == j0_0);
+        }
+        if (more && j + 1 >= j0_0) {
+          if (!(ok = wait_k(j + 1))) break;
+          tc_fence_after();
+          issue_s(0, j + 1);
+        }
+        // query tile 1
+        if (has1 && j >= j0_1) {
+          if (!(ok = mbar_wait_w(bar(FB_P + 1), pph1, ec, kSiteFwdMma))) break;
+          pph1 ^= 1u;
+          tc_fence_after();
+          issue_pv(1, j, j == j0_1);
+        }
+        if (has1 && more && j + 1 >= j0_1) {
+          if (!(ok = wait_k(j + 1))) break;
+          tc_fence_after();
+          issue_s(1, j + 1);
+        }
+        umma_commit_w(bar(FB_VE + j % ST));
+        if (more) umma_commit_w(bar(FB_KE + (j + 1) % ST));
+      }
+      if (ok) {
+        umma_commit_w(bar(FB_O + 0));
+        umma_commit_w(bar(FB_O + 1));
+      }
+      umma_commit_w(bar(FB_DRAIN));
+      mbar_wait(bar(FB_DRAIN), 0, ec, kSiteDrain, false);
     }
-    if (ok) umma_commit_w(bar(FB_O));
-    umma_commit_w(bar(FB_DRAIN));
-    mbar_wait(bar(FB_DRAIN), 0, ec, kSiteDrain, false);
   } else {
+    setmaxnreg_inc<C::REG_SOFTMAX>();
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x;  // 0..127 = TMEM lane = query row within the tile
-    const int row = q0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int t = warp >> 2;  // query tile of this warpgroup
+    const int qt0 = q0 + t * C::BM;
+    const int row = qt0 + (threadIdx.x & 127);
+    const int n_kv = t == 0 ? n_kv0 : n_kv1;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + C::T_S + 128 * t, tO = tbase + C::T_O + DV * t;
     const float sl2 = p.scale_log2;
     const bool row_ok = row < p.S_q;
-    const float* bias_row =
-        (p.bias != nullptr && row_ok) ? p.bias + (static_cast<size_t>(h) * p.S_q + row) * p.S_kv
-                                      : nullptr;
+    const float* bias_row = (GENERAL && p.bias != nullptr && row_ok)
+                                ? p.bias + (static_cast<size_t>(h) * p.S_q + row) * p.S_kv
+                                : nullptr;
     const bool bias_vec = (p.S_kv & 3) == 0;
     const uint64_t lin_row = (static_cast<uint64_t>(bh) * p.S_q + row) * p.S_kv;
+    const uint64_t sl22 = f2(sl2, sl2);
     float m = SDPA_NEG_INF, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!(ok = mbar_wait(bar(FB_S), j & 1, ec, kSiteFwdSoftmax))) break;
+    for (int c = 0; c < n_kv; ++c) {
+      if (!(ok = mbar_wait(bar(FB_S + t), c & 1, ec, kSiteFwdSoftmax))) break;
       tc_fence_after();
+      const int k0 = (n_kv - 1 - c) * C::BN;  // key tiles from the diagonal down
+      // scores in the log2 domain: S * scale * log2e (+ Bias * log2e)
       float x[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t rr[32];
-        tmem_ld32(tS + lane_off + c * 32, rr);
+        tmem_ld32(tS + lane_off + q * 32, rr);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]) * sl2;
-      }
-      const int k0 = (n_kv - 1 - j) * C::BN;  // key tiles from the diagonal down
-      if (p.bias != nullptr) {
-        if (bias_row != nullptr) {
-          if (bias_vec && k0 + C::BN <= p.S_kv) {
-            const float4* b4 = reinterpret_cast<const float4*>(bias_row + k0);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float4 v = __ldg(b4 + i);
-              x[4 * i + 0] = fmaf(v.x, kLog2e, x[4 * i + 0]);
-              x[4 * i + 1] = fmaf(v.y, kLog2e, x[4 * i + 1]);
-              x[4 * i + 2] = fmaf(v.z, kLog2e, x[4 * i + 2]);
-              x[4 * i + 3] = fmaf(v.w, kLog2e, x[4 * i + 3]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 128; ++i)
-              if (k0 + i < p.S_kv) x[i] = fmaf(__ldg(bias_row + k0 + i), kLog2e, x[i]);
-          }
+        for (int i = 0; i < 16; ++i) {
+          const float2 v = f2split(mul2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sl22));
+          x[q * 32 + 2 * i] = v.x;
+          x[q * 32 + 2 * i + 1] = v.y;
         }
       }
-      const bool need_mask = (k0 + C::BN > p.S_kv) || (p.causal && k0 + C::BN - 1 > q0);
+      if (GENERAL && bias_row != nullptr) {
+        if (bias_vec && k0 + C::BN <= p.S_kv) {
+          const float4* b4 = reinterpret_cast<const float4*>(bias_row + k0);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float4 v = __ldg(b4 + i);
+            x[4 * i + 0] = fmaf(v.x, kLog2e, x[4 * i + 0]);
+            x[4 * i + 1] = fmaf(v.y, kLog2e, x[4 * i + 1]);
+            x[4 * i + 2] = fmaf(v.z, kLog2e, x[4 * i + 2]);
+            x[4 * i + 3] = fmaf(v.w, kLog2e, x[4 * i + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (k0 + i < p.S_kv) x[i] = fmaf(__ldg(bias_row + k0 + i), kLog2e, x[i]);
+        }
+      }
+      const bool need_mask = (k0 + C::BN > p.S_kv) || (p.causal && k0 + C::BN - 1 > qt0);
       if (need_mask) {
         const int lim = p.causal ? min(p.S_kv - 1, row) : p.S_kv - 1;  // last visible key
 #pragma unroll
@@ -252,33 +327,38 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
         alpha = ex2(m - mx);  // 0 when m was -inf
         m = mx;
       }
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+      // S_t(c) follows O_t's previous product in the pipe, so O_t is settled
+      if (c > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
-        for (int c = 0; c < DV / 16; ++c) {
+        for (int q = 0; q < DV / 16; ++q) {
           uint32_t rr[16];
-          tmem_ld16(tO + lane_off + c * 16, rr);
+          tmem_ld16(tO + lane_off + q * 16, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st16(tO + lane_off + c * 16, rr);
+          tmem_st16(tO + lane_off + q * 16, rr);
         }
       }
       l *= alpha;
       const float mu = (m == SDPA_NEG_INF) ? 0.f : m;
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      const uint64_t nm2 = f2(-mu, -mu);
+      uint64_t sa = f2(0.f, 0.f), sb = f2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < 128; i += 4) {
-        x[i] = ex2(x[i] - mu);
-        x[i + 1] = ex2(x[i + 1] - mu);
-        x[i + 2] = ex2(x[i + 2] - mu);
-        x[i + 3] = ex2(x[i + 3] - mu);
-        s0 += x[i];
-        s1 += x[i + 1];
-        s2 += x[i + 2];
-        s3 += x[i + 3];
+        const float2 a = f2split(add2(f2(x[i], x[i + 1]), nm2));
+        const float2 bq = f2split(add2(f2(x[i + 2], x[i + 3]), nm2));
+        x[i] = ex2(a.x);
+        x[i + 1] = ex2(a.y);
+        x[i + 2] = ex2(bq.x);
+        x[i + 3] = ex2(bq.y);
+        sa = add2(sa, f2(x[i], x[i + 1]));
+        sb = add2(sb, f2(x[i + 2], x[i + 3]));
       }
-      l += (s0 + s1) + (s2 + s3);
-      if (p.dropout) {
+      {
+        const float2 u = f2split(sa), w = f2split(sb);
+        l += (u.x + u.y) + (w.x + w.y);
+      }
+      if (GENERAL && p.dropout) {
         const uint64_t g0 = (lin_row + k0) >> 2;
 #pragma unroll
         for (int g = 0; g < 32; ++g) {
@@ -290,33 +370,33 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
         }
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(x[c * 32 + 2 * i], x[c * 32 + 2 * i + 1]);
-        tmem_st16(tS + lane_off + c * 16, pk);
+        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(x[q * 32 + 2 * i], x[q * 32 + 2 * i + 1]);
+        tmem_st16(tS + lane_off + q * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(FB_P));
+      mbar_arrive(bar(FB_P + t));
     }
     // ---- epilogue: O / l (times 1/(1-p) under dropout), LSE = m ln2 + ln l
-    if (ok && mbar_wait(bar(FB_O), 0, ec, kSiteFwdSoftmax)) {
+    if (n_kv > 0 && ok && mbar_wait(bar(FB_O + t), 0, ec, kSiteFwdSoftmax)) {
       tc_fence_after();
-      const float inv = (l > 0.f) ? (p.dropout ? p.keep_scale : 1.0f) / l : 0.f;
+      const float inv = (l > 0.f) ? ((GENERAL && p.dropout) ? p.keep_scale : 1.0f) / l : 0.f;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(bh) * p.S_q + (row_ok ? row : 0)) * DV * 2;
 #pragma unroll
-      for (int c = 0; c < DV / 32; ++c) {
+      for (int q = 0; q < DV / 32; ++q) {
         uint32_t rr[32];
-        tmem_ld32(tO + lane_off + c * 32, rr);
+        tmem_ld32(tO + lane_off + q * 32, rr);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack2<BF16>(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+          uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -329,7 +409,7 @@ __global__ void __launch_bounds__(192, FwdCfg<DQK, DV>::MIN_BLOCKS)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
@@ -339,11 +419,22 @@ template <int DQK, int DV, bool BF16>
 cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                          const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
-  auto kern = sdpa_fwd_kernel<DQK, DV, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  const bool general = p.bias != nullptr || p.dropout != 0;
+  auto kern = general ? sdpa_fwd_kernel<DQK, DV, BF16, true> : sdpa_fwd_kernel<DQK, DV, BF16, false>;
+  // The warpgroups' setmaxnreg shares add up to exactly 384 x REG_LAUNCH; had
+  // the compiler given the kernel another launch register count, the softmax
+  // warpgroups' increase could never be granted, so refuse to launch then.
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != C::REG_LAUNCH) {
+    set_last_error("forward kernel compiled with an unexpected register count");
+    return cudaErrorInvalidConfiguration;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
-  const long long grid = static_cast<long long>(n_qt) * p.B * p.H;
+  const long long grid = static_cast<long long>((n_qt + 1) / 2) * p.B * p.H;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, p);
   return cudaGetLastError();
 }

@@ -96,6 +96,19 @@ __device__ __forceinline__ bool mbar_wait_w(uint32_t bar, uint32_t phase, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register budgets: every warp of a warpgroup executes the same
+// call. The increases of some warpgroups must be paid for by decreases of
+// others within the block's launch total (threads x registers at launch).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
