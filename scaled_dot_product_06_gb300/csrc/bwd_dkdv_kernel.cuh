@@ -85,7 +85,7 @@ struct DkdvCfg {
 };
 
 enum : int { AB_KV = 0, AB_QF, AB_DOF = AB_QF + 2, AB_QE = AB_DOF + 2, AB_S = AB_QE + 2, AB_SFREE,
-             AB_P, AB_DP, AB_DS, AB_DKDV, AB_DRAIN, AB_OPS, AB_COUNT };
+             AB_P, AB_DP, AB_DSL, AB_DSH, AB_DKDV, AB_DRAIN, AB_OPS, AB_COUNT };
 
 // Keep bits of key row k for the 32 query rows [row0, row0 + 32) of a tile.
 // One Philox block covers four consecutive keys of one query row, i.e. the
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AB_COUNT; ++i)
-      mbar_init(bar(i), (i == AB_SFREE || i == AB_P || i == AB_DS || i == AB_OPS)
+      mbar_init(bar(i), (i == AB_SFREE || i == AB_P || i == AB_DSL || i == AB_DSH || i == AB_OPS)
                             ? static_cast<uint32_t>(NCT)
                             : 1u);
     *abort_flag = 0u;
@@ -290,13 +290,19 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         for (int kk = 0; kk < BM / 16; ++kk)
           umma_ts_w(tDV, tDP + packed_col(kk), desc_adv(dob, kk * 2048), kIdDV, (i > 0 || kk > 0));
       }
-      if (!(ok = mbar_wait_w(bar(AB_DS), i & 1, ec, kSiteBwdMma))) break;
-      tc_fence_after();
-      {  // dK += dS^T Q_i
+      {  // dK += dS^T Q_i, the query steps of each group's first half of dS^T
+         // as soon as it is written, the second half after
         const uint64_t dqb = desc_adv(dQm0, s * C::Q_BYTES);
+        if (!(ok = mbar_wait_w(bar(AB_DSL), i & 1, ec, kSiteBwdMma))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
+        for (int kk = 0; kk < BM / 16; kk += 2)
           umma_ts_w(tDK, tDP + packed_col(kk) + CW / 2, desc_adv(dqb, kk * 2048), kIdDK, (i > 0 || kk > 0));
+        if (!(ok = mbar_wait_w(bar(AB_DSH), i & 1, ec, kSiteBwdMma))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 1; kk < BM / 16; kk += 2)
+          umma_ts_w(tDK, tDP + packed_col(kk) + CW / 2, desc_adv(dqb, kk * 2048), kIdDK, 1u);
         umma_commit_w(bar(AB_QE + s));  // Q_i and dO_i are no longer read
       }
       if (i + 1 < n_it) {
@@ -458,12 +464,18 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
           uint32_t hi[16];
           tmem_ld16(tcol + 16, hi);
           tmem_wait_ld();
+          // dS^T of the first 16 queries over the upper half just read, so dK
+          // can start on them while the second 16 are formed
+          tmem_st8(tcol + 16, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(AB_DSL));
           ds_half(hi, 16, pk + 8);
         }
-        tmem_st16(tcol + 16, pk);
+        tmem_st8(tcol + 24, pk + 8);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(AB_DS));
+        mbar_arrive(bar(AB_DSH));
       }
     }
     // ---- epilogue: warps 0-3 write dV, warps 4-7 write dK * scale (zeros for

@@ -75,8 +75,8 @@ struct DqCfg {
 };
 
 enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_VF + 2,
-             QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DS = QB_DP + 2, QB_DONE = QB_DS + 2, QB_DRAIN, QB_OPS,
-             QB_COUNT };
+             QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DSL = QB_DP + 2, QB_DSH = QB_DSL + 2,
+             QB_DONE = QB_DSH + 2, QB_DRAIN, QB_OPS, QB_COUNT };
 
 // DROP is a template parameter so the kernel without dropout is compiled
 // alone and stays within 96 registers a thread without spilling.
@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_COUNT; ++i)
-      mbar_init(bar(i), (i == QB_SFREE || i == QB_DS || i == QB_DS + 1 || i == QB_OPS)
+      mbar_init(bar(i), (i == QB_SFREE || i == QB_DSL || i == QB_DSL + 1 || i == QB_DSH ||
+                         i == QB_DSH + 1 || i == QB_OPS)
                             ? static_cast<uint32_t>(NCT)
                             : 1u);
     *abort_flag = 0u;
@@ -215,12 +216,22 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     auto ds_col = [](int kk) -> uint32_t {
       return static_cast<uint32_t>(((kk * 16) / CW) * CW + CW / 2 + ((kk * 16) % CW) / 2);
     };
-    auto issue_dq = [&](int j) {  // dQ += dS K_j, dS in dP buffer j % DPB
+    // dQ += dS K_j, dS in dP buffer j % DPB: the key steps of each group's
+    // first half of dS (even kk) as soon as it is written, then the second
+    auto issue_dq = [&](int j, int half) {
       const uint32_t tDP = tbase + C::T_DP + 128 * (j % C::DPB);
       const uint64_t dk = desc_adv(dKm0, (j % ST) * C::K_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
+      for (int kk = half; kk < BN / 16; kk += 2)
         umma_ts_w(tDQ, tDP + ds_col(kk), desc_adv(dk, kk * 2048), kIdDQ, (j > 0 || kk > 0));
+    };
+    // wait for one half of dS(j), then issue its dQ steps
+    auto ds_then_dq = [&](int j, int half) {
+      const int b = j % C::DPB;
+      if (!mbar_wait_w(bar((half ? QB_DSH : QB_DSL) + b), (j / C::DPB) & 1, ec, kSiteBwdMma)) return false;
+      tc_fence_after();
+      issue_dq(j, half);
+      return true;
     };
     auto wait_kv = [&](int which, int j) {
       return mbar_wait_w(bar(which + j % ST), (j / ST) & 1, ec, kSiteBwdMma);
@@ -242,7 +253,6 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     }
     for (int j = 0; ok && j < n_kv; ++j) {
       const bool more = j + 1 < n_kv;
-      const int b = j % C::DPB;
       if constexpr (C::DPB == 2) {
         // S(j+1) and dP(j+1) (other buffer) while the compute warps work on tile j
         if (more) {
@@ -256,9 +266,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
           umma_commit_w(bar(QB_DP + (j + 1) % 2));
           umma_commit_w(bar(QB_VE + (j + 1) % ST));
         }
-        if (!(ok = mbar_wait_w(bar(QB_DS + b), (j / 2) & 1, ec, kSiteBwdMma))) break;
-        tc_fence_after();
-        issue_dq(j);
+        if (!(ok = ds_then_dq(j, 0) && ds_then_dq(j, 1))) break;
         umma_commit_w(bar(QB_KE + j % ST));
       } else {
         // one dP buffer: dP(j+1) goes after dQ(j), which reads dS(j) from it.
@@ -272,9 +280,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
             umma_commit_w(bar(QB_S));
           }
         }
-        if (!(ok = mbar_wait_w(bar(QB_DS), j & 1, ec, kSiteBwdMma))) break;
-        tc_fence_after();
-        issue_dq(j);
+        if (!(ok = ds_then_dq(j, 0) && ds_then_dq(j, 1))) break;
         umma_commit_w(bar(QB_KE + j % ST));
         if constexpr (ST == 1) {
           if (more) {
@@ -418,12 +424,18 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         uint32_t hi[16];
         tmem_ld16(tcol + 16, hi);
         tmem_wait_ld();
+        // dS of the first 16 keys over the upper half just read, so dQ can
+        // start on them while the second 16 are formed
+        tmem_st8(tcol + 16, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(QB_DSL + b));
         ds_half(hi, 16, pk + 8);
       }
-      tmem_st16(tcol + 16, pk);
+      tmem_st8(tcol + 24, pk + 8);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(QB_DS + b));
+      mbar_arrive(bar(QB_DSH + b));
     }
     // ---- epilogue: dQ * scale; the first two groups write half of the columns each
     if (hf < 2 && ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute)) {
