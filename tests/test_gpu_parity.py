@@ -29,6 +29,9 @@ CASES = [
     Case(2, 1, 257, 129, 192, 128, causal=True),
     Case(1, 2, 200, 72, 64, 64, causal=True, bias=True, dtype="fp16"),
     Case(1, 1, 300, 300, 192, 128, bias=True, p=0.3),
+    # several query-tile pairs per head, the last pair without its second tile,
+    # causal with more keys than queries
+    Case(1, 2, 640, 1000, 128, 128, causal=True),
 ]
 
 
