@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
       for (int i = 0; i < n_it; ++i) {
         const int s = i & 1;
         const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad)) break;
+        if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) break;
         const int q0 = (it0 + i) * BM;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(AB_QF + s), C::Q_BYTES + C::STAT_BYTES);

@@ -152,14 +152,14 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     for (int j = 0; j < n_kv; ++j) {
       const int s = j % ST;
       const uint32_t ph = (j / ST) & 1;
-      if (!mbar_wait(bar(QB_KE + s), ph ^ 1, ec, kSiteBwdLoad)) break;
+      if (!mbar_wait(bar(QB_KE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(QB_KF + s), C::K_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
           tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, (n_kv - 1 - j) * BN, bh);
       }
-      if (!mbar_wait(bar(QB_VE + s), ph ^ 1, ec, kSiteBwdLoad)) {
+      if (!mbar_wait(bar(QB_VE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) {
         issued = 2 * j + 1;
         break;
       }

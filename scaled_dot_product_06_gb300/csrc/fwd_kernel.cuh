@@ -149,14 +149,14 @@ __global__ void __launch_bounds__(384, 1)
         const int s = j % ST;
         const uint32_t ph = (j / ST) & 1;
         const int kv0 = (n_it - 1 - j) * C::BN;
-        if (!mbar_wait(bar(FB_KE + s), ph ^ 1, ec, kSiteFwdLoad)) break;
+        if (!mbar_wait(bar(FB_KE + s), ph ^ 1, ec, kSiteFwdLoad, true, true)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(FB_KF + s), C::K_BYTES);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
             tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64, kv0, bh);
         }
-        if (!mbar_wait(bar(FB_VE + s), ph ^ 1, ec, kSiteFwdLoad)) {
+        if (!mbar_wait(bar(FB_VE + s), ph ^ 1, ec, kSiteFwdLoad, true, true)) {
           issued = 2 * j + 1;
           break;
         }

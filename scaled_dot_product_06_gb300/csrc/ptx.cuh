@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread in hardware for up to `ns` nanoseconds
+// while the phase is incomplete (it resumes as soon as the phase completes),
+// so a warp that mostly waits does not spin on its scheduler's issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t phase, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(phase), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wall-clock limit of one wait. Legitimate waits inside these kernels last
 // microseconds; two seconds only ever trips on a lost arrival.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -70,12 +85,16 @@ struct ErrCtx {
 // CTA) when the limit runs out or another role already aborted.
 // With honor_abort false the wait ignores the abort flag (used to drain copies
 // and MMAs still in flight before the CTA releases its resources).
+// With sleep set, each try may suspend the thread for up to 100 us (used by
+// the producer warps, which spend most of their time waiting; the MMA warp
+// does not sleep: on GB300 its later wake-up cost more than its polling).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, const ErrCtx& e,
-                                          uint32_t site, bool honor_abort = true) {
+                                          uint32_t site, bool honor_abort = true,
+                                          bool sleep = false) {
   if (mbar_try_wait(bar, phase)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, phase)) return true;
+    if (sleep ? mbar_try_wait_sleep(bar, phase, 100000u) : mbar_try_wait(bar, phase)) return true;
     if ((it & 63u) == 0u) {
       if (honor_abort && *e.abort) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs || it > (1u << 30)) {
