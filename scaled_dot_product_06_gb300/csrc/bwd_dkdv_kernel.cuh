@@ -113,11 +113,11 @@ __device__ __forceinline__ void keep_bits_transposed(uint64_t lin_quad, int S_kv
   }
 }
 
-// DROP is a template parameter (not a runtime branch) so the kernel without
-// dropout is compiled alone: at 96 registers a thread (18 warps, five on some
-// schedulers) the dropout body's keep bits would otherwise push the common
-// path into spilling.
-template <int DQK, int DV, bool BF16, bool DROP>
+// DROP and BIAS are template parameters (not runtime branches) so the kernel
+// without them is compiled alone: at 96 registers a thread (18 warps, five on
+// some schedulers) the dropout body's keep bits would otherwise push the
+// common path into spilling, and it carries no bias checks.
+template <int DQK, int DV, bool BF16, bool DROP, bool BIAS>
 __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -361,13 +361,21 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
           if constexpr (DROP) return ((km[c >> 5][c & 3] >> ((c & 31) >> 2)) & 1u) ? zk : 0.f;
           return 1.0f;
         };
+        // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)
+        float pr[CW];
+        if constexpr (BIAS) {
+          // Bias of this key and the thread's queries, loaded before the wait so
+          // its latency overlaps it (columns past S_q or a missing key read 0)
+          const float* bias_col = p.bias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + (kv_ok ? kv : 0);
+          const int lim = kv_ok ? min(CW, p.S_q - qc0) : 0;
+#pragma unroll
+          for (int c = 0; c < CW; ++c) pr[c] = (c < lim) ? __ldg(bias_col + static_cast<size_t>(c) * p.S_kv) : 0.f;
+        }
         if (!(ok = mbar_wait(bar(AB_S), i & 1, ec, kSiteBwdCompute))) break;
         // S^T(i) was issued after Q_i and the statistics landed; the wait on the
         // same barrier makes the statistics visible to this thread too
         if (!(ok = mbar_wait(bar(AB_QF + (i & 1)), (i >> 1) & 1, ec, kSiteBwdCompute))) break;
         tc_fence_after();
-        // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)
-        float pr[CW];
 #pragma unroll
         for (int c = 0; c < CW / 32; ++c) {
           uint32_t a0[32];
@@ -377,10 +385,17 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 n4 = nl2[8 * c + e4];
+            uint64_t t01 = f2(n4.x, n4.y), t23 = f2(n4.z, n4.w);
+            if constexpr (BIAS) {
+              const uint64_t l2e = f2(kLog2e, kLog2e);
+              const int b0 = 32 * c + 4 * e4;
+              t01 = fma2(f2(pr[b0], pr[b0 + 1]), l2e, t01);
+              t23 = fma2(f2(pr[b0 + 2], pr[b0 + 3]), l2e, t23);
+            }
             const float2 x01 = f2split(fma2(f2(__uint_as_float(a0[4 * e4 + 0]), __uint_as_float(a0[4 * e4 + 1])),
-                                            sc2, f2(n4.x, n4.y)));
+                                            sc2, t01));
             const float2 x23 = f2split(fma2(f2(__uint_as_float(a0[4 * e4 + 2]), __uint_as_float(a0[4 * e4 + 3])),
-                                            sc2, f2(n4.z, n4.w)));
+                                            sc2, t23));
             pr[32 * c + 4 * e4 + 0] = x01.x;
             pr[32 * c + 4 * e4 + 1] = x01.y;
             pr[32 * c + 4 * e4 + 2] = x23.x;
@@ -389,13 +404,6 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         }
         tc_fence_before();
         mbar_arrive(bar(AB_SFREE));  // S^T(i) is in registers: S^T(i+1) may overwrite it
-        if (p.bias != nullptr && kv_ok) {
-          const float* bias_col = p.bias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv;
-          const int lim = min(CW, p.S_q - qc0);
-#pragma unroll
-          for (int c = 0; c < CW; ++c)
-            if (c < lim) pr[c] = fmaf(__ldg(bias_col + static_cast<size_t>(c) * p.S_kv), kLog2e, pr[c]);
-        }
         const bool need_mask = (p.causal && qc0 < k0 + C::BN - 1) || (qc0 + CW > p.S_q) || !kv_ok;
         if (need_mask) {
           // visible iff the key exists, the query exists and (causal) key <= query
@@ -416,9 +424,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         // 32 queries goes over it. dV reads P~^T from the first 16 columns of
         // each 32, dK reads dS^T from the second 16.
         const uint32_t tcol = tbase + C::T_DP + lane_off + CW * hf;
-        float* dbias_col = (p.dbias != nullptr && kv_ok)
-                               ? p.dbias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
-                               : nullptr;
+        float* dbias_col = (BIAS && kv_ok) ? p.dbias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + kv
+                                           : nullptr;
         // dS = P * (dP * Z - D) of local columns [c0, c0 + 16) into 8 packed
         // words, two columns per f32x2 instruction (dd holds -D)
         auto ds_half = [&](const uint32_t (&dp)[16], int c0, uint32_t* out) {
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
               ds[2 * h2] = r.x;
               ds[2 * h2 + 1] = r.y;
             }
-            if (dbias_col != nullptr) {
+            if (BIAS && dbias_col != nullptr) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int cc = c0 + 4 * e4 + e;
@@ -529,7 +536,11 @@ template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                               const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
   using C = DkdvCfg<DQK, DV>;
-  auto kern = p.dropout ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true> : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false>;
+  const bool bias = p.bias != nullptr;
+  auto kern = p.dropout ? (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, true>
+                                : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, false>)
+                        : (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, true>
+                                : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;

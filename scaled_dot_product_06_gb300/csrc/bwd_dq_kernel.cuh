@@ -78,9 +78,9 @@ enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_V
              QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DSL = QB_DP + 2, QB_DSH = QB_DSL + 2,
              QB_DONE = QB_DSH + 2, QB_DRAIN, QB_OPS, QB_COUNT };
 
-// DROP is a template parameter so the kernel without dropout is compiled
-// alone and stays within 96 registers a thread without spilling.
-template <int DQK, int DV, bool BF16, bool DROP>
+// DROP and BIAS are template parameters so the kernel without them is
+// compiled alone and stays within 96 registers a thread without spilling.
+template <int DQK, int DV, bool BF16, bool DROP, bool BIAS>
 __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     const float nl2 = p.stats[sidx];
     const float nDrow = p.stats[sidx + 64];  // -D
     const float* bias_row =
-        (p.bias != nullptr && row_ok) ? p.bias + (static_cast<size_t>(h) * p.S_q + qr) * p.S_kv : nullptr;
+        (BIAS && row_ok) ? p.bias + (static_cast<size_t>(h) * p.S_q + qr) * p.S_kv : nullptr;
     const bool bias_vec = (p.S_kv & 3) == 0;
     const uint64_t lin_row = (static_cast<uint64_t>(bh) * p.S_q + qr) * p.S_kv;
     bool ok = true;
@@ -353,10 +353,29 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         if constexpr (DROP) return ((keep >> c) & 1u) ? zk : 0.f;
         return 1.0f;
       };
-      if (!(ok = mbar_wait(bar(QB_S), j & 1, ec, kSiteBwdCompute))) break;
-      tc_fence_after();
       // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)
       float pr[CW];
+      if constexpr (BIAS) {
+        // this row's Bias for the thread's keys, loaded before the wait so its
+        // latency overlaps it (keys past S_kv or a missing row read 0)
+        if (bias_row != nullptr && bias_vec && kc0 + CW <= p.S_kv) {
+          const float4* b4 = reinterpret_cast<const float4*>(bias_row + kc0);
+#pragma unroll
+          for (int i = 0; i < CW / 4; ++i) {
+            const float4 v = __ldg(b4 + i);
+            pr[4 * i + 0] = v.x;
+            pr[4 * i + 1] = v.y;
+            pr[4 * i + 2] = v.z;
+            pr[4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            pr[c] = (bias_row != nullptr && kc0 + c < p.S_kv) ? __ldg(bias_row + kc0 + c) : 0.f;
+        }
+      }
+      if (!(ok = mbar_wait(bar(QB_S), j & 1, ec, kSiteBwdCompute))) break;
+      tc_fence_after();
       {
         uint32_t a0[32];
         tmem_ld32(tbase + C::T_S + lane_off + CW * hf, a0);
@@ -364,30 +383,15 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nl22 = f2(nl2, nl2);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 x = f2split(fma2(f2(__uint_as_float(a0[2 * e]), __uint_as_float(a0[2 * e + 1])), sc2, nl22));
+          uint64_t t = nl22;
+          if constexpr (BIAS) t = fma2(f2(pr[2 * e], pr[2 * e + 1]), f2(kLog2e, kLog2e), nl22);
+          const float2 x = f2split(fma2(f2(__uint_as_float(a0[2 * e]), __uint_as_float(a0[2 * e + 1])), sc2, t));
           pr[2 * e] = x.x;
           pr[2 * e + 1] = x.y;
         }
       }
       tc_fence_before();
       mbar_arrive(bar(QB_SFREE));
-      if (bias_row != nullptr) {
-        if (bias_vec && kc0 + CW <= p.S_kv) {
-          const float4* b4 = reinterpret_cast<const float4*>(bias_row + kc0);
-#pragma unroll
-          for (int i = 0; i < CW / 4; ++i) {
-            const float4 v = __ldg(b4 + i);
-            pr[4 * i + 0] = fmaf(v.x, kLog2e, pr[4 * i + 0]);
-            pr[4 * i + 1] = fmaf(v.y, kLog2e, pr[4 * i + 1]);
-            pr[4 * i + 2] = fmaf(v.z, kLog2e, pr[4 * i + 2]);
-            pr[4 * i + 3] = fmaf(v.w, kLog2e, pr[4 * i + 3]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < CW; ++c)
-            if (kc0 + c < p.S_kv) pr[c] = fmaf(__ldg(bias_row + kc0 + c), kLog2e, pr[c]);
-        }
-      }
       const bool need_mask = (kc0 + CW > p.S_kv) || (p.causal && kc0 + CW - 1 > q0) || !row_ok;
       if (need_mask) {
         const int last = row_ok ? (p.causal ? min(p.S_kv - 1, qr) : p.S_kv - 1) : -1;
@@ -473,7 +477,11 @@ template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
   using C = DqCfg<DQK, DV>;
-  auto kern = p.dropout ? sdpa_bwd_dq_kernel<DQK, DV, BF16, true> : sdpa_bwd_dq_kernel<DQK, DV, BF16, false>;
+  const bool bias = p.bias != nullptr;
+  auto kern = p.dropout ? (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, true, true>
+                                : sdpa_bwd_dq_kernel<DQK, DV, BF16, true, false>)
+                        : (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, false, true>
+                                : sdpa_bwd_dq_kernel<DQK, DV, BF16, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;

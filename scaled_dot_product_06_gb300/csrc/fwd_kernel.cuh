@@ -270,11 +270,29 @@ __global__ void __launch_bounds__(384, 1)
     float m = SDPA_NEG_INF, l = 0.f;
     bool ok = true;
     for (int c = 0; c < n_kv; ++c) {
-      if (!(ok = mbar_wait(bar(FB_S + t), c & 1, ec, kSiteFwdSoftmax))) break;
-      tc_fence_after();
       const int k0 = (n_kv - 1 - c) * C::BN;  // key tiles from the diagonal down
       // scores in the log2 domain: S * scale * log2e (+ Bias * log2e)
       float x[128];
+      if (GENERAL && bias_row != nullptr) {
+        // the row's Bias, loaded before the wait so its latency overlaps it
+        // (keys past S_kv read 0; they are masked below)
+        if (bias_vec && k0 + C::BN <= p.S_kv) {
+          const float4* b4 = reinterpret_cast<const float4*>(bias_row + k0);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float4 v = __ldg(b4 + i);
+            x[4 * i + 0] = v.x;
+            x[4 * i + 1] = v.y;
+            x[4 * i + 2] = v.z;
+            x[4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) x[i] = (k0 + i < p.S_kv) ? __ldg(bias_row + k0 + i) : 0.f;
+        }
+      }
+      if (!(ok = mbar_wait(bar(FB_S + t), c & 1, ec, kSiteFwdSoftmax))) break;
+      tc_fence_after();
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t rr[32];
@@ -282,26 +300,14 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 v = f2split(mul2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sl22));
+          const uint64_t s2 = f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+          float2 v;
+          if (GENERAL && bias_row != nullptr)
+            v = f2split(fma2(s2, sl22, mul2(f2(x[q * 32 + 2 * i], x[q * 32 + 2 * i + 1]), f2(kLog2e, kLog2e))));
+          else
+            v = f2split(mul2(s2, sl22));
           x[q * 32 + 2 * i] = v.x;
           x[q * 32 + 2 * i + 1] = v.y;
-        }
-      }
-      if (GENERAL && bias_row != nullptr) {
-        if (bias_vec && k0 + C::BN <= p.S_kv) {
-          const float4* b4 = reinterpret_cast<const float4*>(bias_row + k0);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float4 v = __ldg(b4 + i);
-            x[4 * i + 0] = fmaf(v.x, kLog2e, x[4 * i + 0]);
-            x[4 * i + 1] = fmaf(v.y, kLog2e, x[4 * i + 1]);
-            x[4 * i + 2] = fmaf(v.z, kLog2e, x[4 * i + 2]);
-            x[4 * i + 3] = fmaf(v.w, kLog2e, x[4 * i + 3]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (k0 + i < p.S_kv) x[i] = fmaf(__ldg(bias_row + k0 + i), kLog2e, x[i]);
         }
       }
       const bool need_mask = (k0 + C::BN > p.S_kv) || (p.causal && k0 + C::BN - 1 > qt0);
