@@ -186,6 +186,23 @@ sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
  */
 sdpa_status_t sdpa_device_error(uint32_t* word, int clear);
 
+/*
+ * Test hook for the bounded-wait path (no counterpart on the pages; it exists
+ * so the hang-safety machinery can be exercised without faulting a GPU).
+ * Applies to sdpa_fwd calls made after it, on any thread, until reset:
+ *   fault 0  normal operation (the default)
+ *   fault 1  the forward kernel's producer warp issues no K/V loads, so the
+ *            MMA issuer's bounded wait runs out: every role leaves its loop,
+ *            drains what is in flight, frees tensor memory and returns; the
+ *            error word gets the MMA site bit, sdpa_device_error then reports
+ *            SDPA_ERR_DEVICE_TIMEOUT, and O / LSE are left unwritten.
+ *   wait_limit_ns  wall-clock limit of each device wait in those forward
+ *            launches; 0 restores the default (2 s).
+ * Returns SDPA_ERR_INVALID_ARG for an unknown fault. Call sdpa_debug_fault(0, 0)
+ * to restore normal operation.
+ */
+sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns);
+
 /* Detail of the calling thread's most recent failure (the step and, for
  * SDPA_ERR_CUDA, the CUDA error string); "" if none. Valid until the thread's
  * next call into the library. */

@@ -131,5 +131,11 @@ def sdpa_device_error(clear: bool = True) -> int:
     return int(w.value)
 
 
+def sdpa_debug_fault(fault: int = 0, wait_limit_ns: int = 0) -> None:
+    """Test hook of the C ABI (see include/sdpa.h): fault 1 makes later forward
+    launches time out in a bounded wait; sdpa_debug_fault() restores normal operation."""
+    _native.check(_native.lib().sdpa_debug_fault(int(fault), int(wait_limit_ns)), "sdpa_debug_fault")
+
+
 def sdpa_status_string(status: int) -> str:
     return _native.status_string(status)

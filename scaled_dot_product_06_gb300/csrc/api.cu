@@ -4,6 +4,7 @@
 // flag, dropout probability with seed and offset, optional bias, fp32 softmax
 // statistics) with plain pointers and a status return instead of exceptions,
 // the way oneDNN's sdpa micro.cpp reports failures through status codes.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -27,6 +28,11 @@ uint32_t* g_err_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 thread_local char g_last_error[256] = "";
+
+// Test hook (sdpa_debug_fault): the fault the next forward launches inject and
+// the wall-clock limit of their device waits (0 = the default two seconds).
+std::atomic<int> g_debug_fault{0};
+std::atomic<uint64_t> g_debug_wait_ns{0};
 
 sdpa_status_t fail(sdpa_status_t s, const char* what, cudaError_t e = cudaSuccess) {
   if (e != cudaSuccess)
@@ -145,6 +151,13 @@ int sdpa_version(void) { return 10000; }
 
 const char* sdpa_last_error(void) { return g_last_error; }
 
+sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns) {
+  if (fault < 0 || fault > 1) return SDPA_ERR_INVALID_ARG;
+  g_debug_fault.store(fault);
+  g_debug_wait_ns.store(wait_limit_ns);
+  return SDPA_OK;
+}
+
 sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
                        float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
                        sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
@@ -181,6 +194,9 @@ sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
   p.offset_hi = static_cast<uint32_t>(offset >> 32);
   p.o = o;
   p.lse = lse;
+  p.fault = static_cast<uint32_t>(g_debug_fault.load());
+  const uint64_t wait_ns = g_debug_wait_ns.load();
+  p.wait_ns = wait_ns != 0 ? wait_ns : kWaitLimitNs;
   if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t e = bf16 ? launch_fwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st)

@@ -37,6 +37,10 @@ struct FwdParams {
   void* o;                 // [B, H, S_q, D_v] io dtype
   float* lse;              // [B, H, S_q] natural-log logsumexp
   uint32_t* err;           // device error word
+  // Test hook (sdpa_debug_fault): 1 = the producer issues no K/V loads, so
+  // the MMA issuer's bounded wait runs out; wait_ns = limit of every wait.
+  uint32_t fault;
+  uint64_t wait_ns;
 };
 
 // Row statistics the backward kernels share, written by the preprocess kernel:

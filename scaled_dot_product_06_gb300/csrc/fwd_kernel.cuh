@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const ErrCtx ec{p.err, abort_flag};
+  const ErrCtx ec{p.err, abort_flag, p.wait_ns};
 
   if (warp >= 8) {
     setmaxnreg_dec<C::REG_OTHER>();
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t ph = (j / ST) & 1;
         const int kv0 = (n_it - 1 - j) * C::BN;
         if (!mbar_wait(bar(FB_KE + s), ph ^ 1, ec, kSiteFwdLoad, true, true)) break;
+        if (p.fault == 1) break;  // test hook: K/V never arrive
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(FB_KF + s), C::K_BYTES);
 #pragma unroll
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       // Drain: every copy issued must land before the CTA can retire. On the
       // healthy path these phases completed long ago.
-      if (*abort_flag && n_it > 0) {
+      if ((*abort_flag || p.fault != 0) && n_it > 0) {
         mbar_wait(bar(FB_Q), 0, ec, kSiteDrain, false);
         for (int i = 0; i < issued; ++i) {
           const int j = i >> 1, s = j % ST;

@@ -79,6 +79,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 struct ErrCtx {
   uint32_t* err_word;         // global; bit per site, 0 when healthy
   volatile uint32_t* abort;   // shared; non-zero once any role gave up
+  uint64_t limit_ns = kWaitLimitNs;  // wall-clock limit of one wait
 };
 
 // Bounded wait on phase `phase` of barrier `bar`. Returns false (and flags the
@@ -97,7 +98,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, const Er
     if (sleep ? mbar_try_wait_sleep(bar, phase, 100000u) : mbar_try_wait(bar, phase)) return true;
     if ((it & 63u) == 0u) {
       if (honor_abort && *e.abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs || it > (1u << 30)) {
+      if (globaltimer_ns() - t0 > e.limit_ns || it > (1u << 30)) {
         atomicOr(e.err_word, site);
         *e.abort = 1u;
         return false;

@@ -109,3 +109,10 @@ def test_dropout_mask_argument_errors(lib):
     assert f(1, 1, 4, 4, 1.5, 0, 0, P, None) == _native.SDPA_ERR_INVALID_ARG
     assert f(1, 1, 4, 4, 0.5, 0, 0, NULL, None) == _native.SDPA_ERR_INVALID_ARG
     assert f(0, 1, 4, 4, 0.5, 0, 0, NULL, None) == _native.SDPA_OK
+
+
+def test_debug_fault_hook_arguments(lib):
+    # host-only: setting and clearing the test hook touches no device
+    assert lib.sdpa_debug_fault(2, 0) == 1          # SDPA_ERR_INVALID_ARG
+    assert lib.sdpa_debug_fault(-1, 0) == 1
+    assert lib.sdpa_debug_fault(0, 0) == 0
