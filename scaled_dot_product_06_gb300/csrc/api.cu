@@ -9,6 +9,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -130,6 +132,30 @@ uint32_t drop_threshold(float p) {
 
 namespace sdpa {
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+cudaError_t prepare_kernel(const void* kern, int smem, int regs) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> ready;  // (kernel, device) pairs prepared
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& r : ready)
+    if (r.first == kern && r.second == dev) return cudaSuccess;
+  if (regs > 0) {
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != regs) {
+      set_last_error("kernel compiled with an unexpected register count");
+      return cudaErrorInvalidConfiguration;
+    }
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ready.emplace_back(kern, dev);
+  return cudaSuccess;
+}
 }  // namespace sdpa
 
 extern "C" {

@@ -541,7 +541,7 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
                                 : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, false>)
                         : (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, true>
                                 : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(n_kt) * p.B * p.H;

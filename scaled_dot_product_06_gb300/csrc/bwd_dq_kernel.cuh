@@ -482,7 +482,7 @@ cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CU
                                 : sdpa_bwd_dq_kernel<DQK, DV, BF16, true, false>)
                         : (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, false, true>
                                 : sdpa_bwd_dq_kernel<DQK, DV, BF16, false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
   const long long grid = static_cast<long long>(n_qt) * p.B * p.H;

@@ -214,6 +214,13 @@ __device__ __forceinline__ void smem_row_to_tmem(const uint8_t* tile, int rows_p
 // Records a failure detail for sdpa_last_error() on the calling thread.
 void set_last_error(const char* msg);
 
+// One-time per (kernel, device) launch preparation: raises the kernel's
+// dynamic shared-memory limit to `smem` and, when regs > 0, checks that the
+// compiled kernel uses exactly `regs` registers a thread. The result is
+// cached, so later launches on the device skip these driver calls (they cost
+// microseconds, which dominate small problems).
+cudaError_t prepare_kernel(const void* kern, int smem, int regs);
+
 // ---------------------------------------------------------------- launchers
 // Defined in the per-dtype kernel translation units; return a CUDA error
 // (cudaErrorInvalidValue for a head-size pair that has no kernel).

@@ -431,14 +431,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
   // The warpgroups' setmaxnreg shares add up to exactly 384 x REG_LAUNCH; had
   // the compiler given the kernel another launch register count, the softmax
   // warpgroups' increase could never be granted, so refuse to launch then.
-  cudaFuncAttributes fa{};
-  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != C::REG_LAUNCH) {
-    set_last_error("forward kernel compiled with an unexpected register count");
-    return cudaErrorInvalidConfiguration;
-  }
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, C::REG_LAUNCH);
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
   const long long grid = static_cast<long long>((n_qt + 1) / 2) * p.B * p.H;
