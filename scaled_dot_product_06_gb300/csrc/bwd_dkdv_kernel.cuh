@@ -345,8 +345,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         const int q0 = (it0 + i) * BM;
         const int qc0 = q0 + CW * hf;  // first query row of this thread's columns
         const float* stat = rowbuf + (i & 1) * (2 * BM) + stat_off;
-        const float4* nl2 = reinterpret_cast<const float4*>(stat);
-        const float4* dd = reinterpret_cast<const float4*>(stat + 64);
+        const uint32_t nl2_s = smem_u32(stat), dd_s = smem_u32(stat + 64);
         uint32_t km[CW / 32][4];
 #pragma unroll
         for (int g = 0; g < CW / 32; ++g) {
@@ -384,7 +383,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
           const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 n4 = nl2[8 * c + e4];
+            const float4 n4 = lds128(nl2_s + 16u * (8 * c + e4));
             uint64_t t01 = f2(n4.x, n4.y), t23 = f2(n4.z, n4.w);
             if constexpr (BIAS) {
               const uint64_t l2e = f2(kLog2e, kLog2e);
@@ -431,7 +430,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         auto ds_half = [&](const uint32_t (&dp)[16], int c0, uint32_t* out) {
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 nd4 = dd[c0 / 4 + e4];
+            const float4 nd4 = lds128(dd_s + 16u * (c0 / 4 + e4));
             float ds[4];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
