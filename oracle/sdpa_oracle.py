@@ -25,6 +25,13 @@ Readings taken where the pages are silent (each is listed in the design doc):
 * D_i = sum_d dO_id * O_id uses the dropout-applied output O, which equals
   sum_j P_ij Z_ij dP_ij; dS = P * (dP * Z - D) with dP = dO V^T.
 * dBias has shape [1, H, S_q, S_kv] and is the sum over the batch of dS.
+* Grouped K/V heads (GQA / MQA, H_kv < H): query head h reads K/V head
+  h // (H / H_kv), so consecutive query heads share one K/V head, as in CK
+  tile fmha_bwd_kernel.hpp (the kernel arguments' nhead_ratio_qk, the K and V
+  pointers taken at i_nhead / nhead_ratio_qk) and oneDNN sdpa micro.cpp
+  (kv_group_size = query heads / KV heads; the query heads of a group add into
+  the shared dK / dV). dK and dV of a K/V head are the sums over its group.
+  The dropout bits and the bias are indexed by the query head.
 """
 from __future__ import annotations
 
@@ -50,6 +57,15 @@ class Problem:
     dropout_p: float = 0.0
     seed: int = 0
     offset: int = 0
+    H_kv: int = 0  # K/V heads; 0 means H (no grouping)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv if self.H_kv else self.H
+
+    def kv_head(self, h: int) -> int:
+        """K/V head read by query head h."""
+        return h // (self.H // self.kv_heads)
 
 
 def _f64(x) -> np.ndarray:
@@ -105,7 +121,8 @@ def forward_head(prob: Problem, b: int, h: int, q, k, v, bias=None, rows=None):
     """
     rows = np.arange(prob.S_q) if rows is None else np.asarray(rows)
     cols = np.arange(prob.S_kv)
-    q_h, k_h, v_h = _f64(q[b, h]), _f64(k[b, h]), _f64(v[b, h])
+    hk = prob.kv_head(h)
+    q_h, k_h, v_h = _f64(q[b, h]), _f64(k[b, hk]), _f64(v[b, hk])
     bias_h = None if bias is None else _f64(bias[0, h])
     p, lse = softmax_rows(scores(prob, q_h, k_h, bias_h, rows, cols))
     z = dropout_scale(prob, b, h, rows, cols)
@@ -124,7 +141,7 @@ def forward(prob: Problem, q, k, v, bias=None):
 
 def backward_head(prob: Problem, b: int, h: int, q, k, v, do, bias=None, rows=None,
                   cols=None, row_chunk=None):
-    """Gradients of the (b, h) slice.
+    """Gradients of the (b, h) slice (h a query head).
 
     Returns (dQ[rows], dK[cols], dV[cols], dS[rows][:, cols]) with rows / cols
     defaulting to all queries / keys. dQ and dS on a query row need only that
@@ -140,7 +157,8 @@ def backward_head(prob: Problem, b: int, h: int, q, k, v, do, bias=None, rows=No
     all_cols = np.arange(prob.S_kv)
     rows = all_rows if rows is None else np.asarray(rows)
     cols = all_cols if cols is None else np.asarray(cols)
-    q_h, k_h, v_h, do_h = _f64(q[b, h]), _f64(k[b, h]), _f64(v[b, h]), _f64(do[b, h])
+    hk = prob.kv_head(h)
+    q_h, k_h, v_h, do_h = _f64(q[b, h]), _f64(k[b, hk]), _f64(v[b, hk]), _f64(do[b, h])
     bias_h = None if bias is None else _f64(bias[0, h])
 
     def grads_of_rows(rr, want_dq):
@@ -169,14 +187,17 @@ def backward_head(prob: Problem, b: int, h: int, q, k, v, do, bias=None, rows=No
 
 
 def backward(prob: Problem, q, k, v, do, bias=None):
-    """dQ, dK, dV [B, H, S, D] and dBias [1, H, S_q, S_kv] (None without bias)."""
+    """dQ [B, H, S_q, D_qk], dK / dV [B, H_kv, S_kv, D] (summed over each K/V
+    head's group of query heads) and dBias [1, H, S_q, S_kv] (None without bias)."""
     dq = np.zeros((prob.B, prob.H, prob.S_q, prob.D_qk))
-    dk = np.zeros((prob.B, prob.H, prob.S_kv, prob.D_qk))
-    dv = np.zeros((prob.B, prob.H, prob.S_kv, prob.D_v))
+    dk = np.zeros((prob.B, prob.kv_heads, prob.S_kv, prob.D_qk))
+    dv = np.zeros((prob.B, prob.kv_heads, prob.S_kv, prob.D_v))
     dbias = None if bias is None else np.zeros((1, prob.H, prob.S_q, prob.S_kv))
     for b in range(prob.B):
         for h in range(prob.H):
-            dq[b, h], dk[b, h], dv[b, h], ds = backward_head(prob, b, h, q, k, v, do, bias)
+            dq[b, h], dk_h, dv_h, ds = backward_head(prob, b, h, q, k, v, do, bias)
+            dk[b, prob.kv_head(h)] += dk_h
+            dv[b, prob.kv_head(h)] += dv_h
             if dbias is not None:
                 dbias[0, h] += ds
     return dq, dk, dv, dbias

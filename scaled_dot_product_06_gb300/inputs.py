@@ -23,6 +23,11 @@ class Shape:
     S_kv: int
     D_qk: int
     D_v: int
+    H_kv: int = 0  # K/V heads (grouped-query attention); 0 means H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv if self.H_kv else self.H
 
 
 def _randn(shape, seed: int, device="cpu") -> torch.Tensor:
@@ -35,13 +40,14 @@ def _randn(shape, seed: int, device="cpu") -> torch.Tensor:
 
 def make_inputs(shape: Shape, dtype: str = "bf16", with_bias: bool = False,
                 seed_base: int = 0, device="cpu") -> dict:
-    """q, k, v, do in the io dtype (BHSD) and bias fp32 [1, H, S_q, S_kv] or None."""
+    """q, do [B, H, S_q, D] and k, v [B, H_kv, S_kv, D] in the io dtype, and bias
+    fp32 [1, H, S_q, S_kv] or None."""
     t = DTYPES[dtype]
     s = shape
     out = {
         "q": _randn((s.B, s.H, s.S_q, s.D_qk), 1 + seed_base, device).to(t),
-        "k": _randn((s.B, s.H, s.S_kv, s.D_qk), 2 + seed_base, device).to(t),
-        "v": _randn((s.B, s.H, s.S_kv, s.D_v), 3 + seed_base, device).to(t),
+        "k": _randn((s.B, s.kv_heads, s.S_kv, s.D_qk), 2 + seed_base, device).to(t),
+        "v": _randn((s.B, s.kv_heads, s.S_kv, s.D_v), 3 + seed_base, device).to(t),
         "do": _randn((s.B, s.H, s.S_q, s.D_v), 4 + seed_base, device).to(t),
         "bias": None,
     }

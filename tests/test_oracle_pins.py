@@ -242,3 +242,62 @@ def test_packed_words_match_mask():
     bits = np.unpackbits(words.view(np.uint8), bitorder="little")[: B * H * S_q * S_kv]
     full = np.stack([philox.keep_mask(B, H, S_q, S_kv, p, 99, 7, 0, h) for h in range(H)])
     np.testing.assert_array_equal(bits.astype(bool), full.reshape(-1))
+
+
+# ------------------------------------------------------------------ grouped K/V heads
+def _gqa_problem(H, H_kv, causal, p=0.0):
+    return Problem(2, H, 9, 13, 8, 6, 0.3, causal, p, 7, 5, H_kv)
+
+
+@pytest.mark.parametrize("H,H_kv,causal,use_bias", [(4, 2, False, False), (6, 2, True, True),
+                                                    (4, 1, True, False)])
+def test_grouped_heads_match_torch_enable_gqa(H, H_kv, causal, use_bias):
+    """PyTorch's CPU scaled_dot_product_attention with enable_gqa (float64) is an
+    independent implementation of the grouped-head mapping: forward, LSE and
+    autograd gradients (dK, dV summed over each group by autograd)."""
+    pr = _gqa_problem(H, H_kv, causal)
+    q, do = rand(pr.B, H, pr.S_q, pr.D_qk), rand(pr.B, H, pr.S_q, pr.D_v)
+    k, v = rand(pr.B, H_kv, pr.S_kv, pr.D_qk), rand(pr.B, H_kv, pr.S_kv, pr.D_v)
+    bias = rand(1, H, pr.S_q, pr.S_kv, scale=0.5) if use_bias else None
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    mask = None
+    if use_bias or causal:
+        m = torch.zeros(pr.S_q, pr.S_kv, dtype=torch.float64)
+        if causal:
+            m = m.masked_fill(torch.ones(pr.S_q, pr.S_kv, dtype=torch.bool).triu(1), float("-inf"))
+        tb = torch.tensor(bias, requires_grad=True) if use_bias else None
+        mask = m + (tb if use_bias else 0)
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask,
+                                                          scale=pr.scale, enable_gqa=True)
+    to.backward(torch.tensor(do))
+    o, lse = forward(pr, q, k, v, bias)
+    np.testing.assert_allclose(o, to.detach().numpy(), rtol=1e-12, atol=1e-13)
+    dq, dk, dv, dbias = backward(pr, q, k, v, do, bias)
+    assert dk.shape == k.shape and dv.shape == v.shape
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-11, atol=1e-12)
+    if use_bias:
+        np.testing.assert_allclose(dbias, tb.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_grouped_heads_equal_repeated_kv_with_dropout():
+    """With dropout (which torch cannot reproduce), grouped heads equal the
+    ungrouped problem on K/V repeated over each group, with dK / dV summed over
+    the group: the dropout bits depend on the query head only."""
+    H, H_kv = 6, 3
+    g = H // H_kv
+    pr = _gqa_problem(H, H_kv, True, p=0.25)
+    full = Problem(pr.B, H, pr.S_q, pr.S_kv, pr.D_qk, pr.D_v, pr.scale, True, 0.25, 7, 5)
+    q, do = rand(pr.B, H, pr.S_q, pr.D_qk), rand(pr.B, H, pr.S_q, pr.D_v)
+    k, v = rand(pr.B, H_kv, pr.S_kv, pr.D_qk), rand(pr.B, H_kv, pr.S_kv, pr.D_v)
+    kr, vr = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    o, lse = forward(pr, q, k, v)
+    o_f, lse_f = forward(full, q, kr, vr)
+    np.testing.assert_array_equal(o, o_f)
+    np.testing.assert_array_equal(lse, lse_f)
+    dq, dk, dv, _ = backward(pr, q, k, v, do)
+    dq_f, dk_f, dv_f, _ = backward(full, q, kr, vr, do)
+    np.testing.assert_array_equal(dq, dq_f)
+    np.testing.assert_allclose(dk, dk_f.reshape(pr.B, H_kv, g, pr.S_kv, pr.D_qk).sum(axis=2), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dv, dv_f.reshape(pr.B, H_kv, g, pr.S_kv, pr.D_v).sum(axis=2), rtol=1e-13, atol=1e-14)
