@@ -160,6 +160,39 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
  *            address (cudaGetSymbolAddress) with that device current; make
  *            that first call before any stream capture begins.
  */
+/*
+ * Grouped K/V heads (GQA; MQA when h_kv = 1): the same three calls with an
+ * h_kv argument. q, o, dout, dq and lse have h query heads; k, v, dk and dv
+ * have h_kv heads, [b, h_kv, s_kv, d]; query head i reads K/V head
+ * i / (h / h_kv), so consecutive query heads share a K/V head (CK tile
+ * fmha_bwd_kernel.hpp: K and V taken at i_nhead / nhead_ratio_qk; oneDNN sdpa
+ * micro.cpp: kv_group_size = query heads / KV heads). dK and dV are the sums
+ * over each group, formed inside the key/value-stationary kernel without
+ * atomics, so they stay bitwise reproducible. Bias, dBias, the dropout bits
+ * and the workspace are per query head, as in the ungrouped calls.
+ * Requires 1 <= h_kv <= h with h_kv dividing h (SDPA_ERR_INVALID_ARG
+ * otherwise); with h_kv = h these are exactly sdpa_fwd / sdpa_bwd /
+ * sdpa_bwd_phases.
+ */
+sdpa_status_t sdpa_fwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                           int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
+                           uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
+                           const void* k, const void* v, const float* bias, void* o, float* lse,
+                           void* stream);
+sdpa_status_t sdpa_bwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                           int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
+                           uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
+                           const void* k, const void* v, const float* bias, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           float* dbias, void* workspace, size_t workspace_bytes, void* stream);
+sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
+                                  int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
+                                  int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
+                                  sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
+                                  const float* bias, const void* o, const void* dout,
+                                  const float* lse, void* dq, void* dk, void* dv, float* dbias,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 sdpa_status_t sdpa_bwd_noalloc(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v, float scale, int is_causal, float dropout_p,
                                uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,

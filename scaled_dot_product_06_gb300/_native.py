@@ -37,6 +37,14 @@ SIGNATURES = {
     "sdpa_bwd_phases": (_int, [_int, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64,
                                _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                _ptr, _ptr, _ptr, _sz, _ptr]),
+    "sdpa_fwd_gqa": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64,
+                            _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
+    "sdpa_bwd_gqa": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64,
+                            _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                            _ptr, _sz, _ptr]),
+    "sdpa_bwd_phases_gqa": (_int, [_int, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32,
+                                   _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                                   _ptr, _ptr, _ptr, _ptr, _sz, _ptr]),
     "sdpa_bwd_noalloc": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64,
                                 _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                 _ptr, _ptr]),

@@ -38,15 +38,18 @@ def _ptr(t):
 
 def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0,
              bias=None, out=None, lse=None, stream=None):
-    """Forward pass. Returns (o [b,h,s_q,d_v], lse fp32 [b,h,s_q])."""
+    """Forward pass. Returns (o [b,h,s_q,d_v], lse fp32 [b,h,s_q]).
+
+    k and v may have fewer heads than q (grouped-query attention): h_kv =
+    k.shape[1] must divide h, and query head i reads K/V head i // (h // h_kv)."""
     b, h, s_q, d_qk = q.shape
-    s_kv, d_v = k.shape[2], v.shape[3]
+    h_kv, s_kv, d_v = k.shape[1], k.shape[2], v.shape[3]
     dt = q.dtype
     if dt not in _DTYPE_CODE:
         raise ValueError("q, k, v must be bf16 or fp16")
     _check_io("q", q, (b, h, s_q, d_qk), dt)
-    _check_io("k", k, (b, h, s_kv, d_qk), dt)
-    _check_io("v", v, (b, h, s_kv, d_v), dt)
+    _check_io("k", k, (b, h_kv, s_kv, d_qk), dt)
+    _check_io("v", v, (b, h_kv, s_kv, d_v), dt)
     if bias is not None:
         _check_io("bias", bias, (1, h, s_q, s_kv), torch.float32)
     scale = 1.0 / math.sqrt(d_qk) if scale is None else float(scale)
@@ -56,11 +59,11 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
         lse = torch.empty((b, h, s_q), dtype=torch.float32, device=q.device)
     _check_io("out", out, (b, h, s_q, d_v), dt)
     _check_io("lse", lse, (b, h, s_q), torch.float32)
-    st = _native.lib().sdpa_fwd(b, h, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
-                                float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
-                                _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse),
-                                ctypes.c_void_p(_stream_ptr(stream)))
-    _native.check(st, "sdpa_fwd")
+    st = _native.lib().sdpa_fwd_gqa(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
+                                    float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
+                                    _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse),
+                                    ctypes.c_void_p(_stream_ptr(stream)))
+    _native.check(st, "sdpa_fwd_gqa")
     return out, lse
 
 
@@ -71,7 +74,8 @@ def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v) -> int:
 def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
              offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None, dbias=None,
              stream=None):
-    """Backward pass. Returns (dq, dk, dv, dbias or None)."""
+    """Backward pass. Returns (dq, dk, dv, dbias or None); dk and dv have k's
+    and v's shapes (with grouped K/V heads, sums over each group)."""
     return sdpa_bwd_phases(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, scale=scale,
                            is_causal=is_causal, dropout_p=dropout_p, seed=seed, offset=offset,
                            bias=bias, workspace=workspace, dq=dq, dk=dk, dv=dv, dbias=dbias,
@@ -83,12 +87,12 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
                     dbias=None, stream=None):
     """The backward phases selected by ``phases`` (SDPA_BWD_* bit mask)."""
     b, h, s_q, d_qk = q.shape
-    s_kv, d_v = k.shape[2], v.shape[3]
+    h_kv, s_kv, d_v = k.shape[1], k.shape[2], v.shape[3]
     dt = q.dtype
     if dt not in _DTYPE_CODE:
         raise ValueError("q, k, v must be bf16 or fp16")
-    for name, t, shp in (("q", q, (b, h, s_q, d_qk)), ("k", k, (b, h, s_kv, d_qk)),
-                         ("v", v, (b, h, s_kv, d_v)), ("o", o, (b, h, s_q, d_v)),
+    for name, t, shp in (("q", q, (b, h, s_q, d_qk)), ("k", k, (b, h_kv, s_kv, d_qk)),
+                         ("v", v, (b, h_kv, s_kv, d_v)), ("o", o, (b, h, s_q, d_v)),
                          ("dout", dout, (b, h, s_q, d_v))):
         _check_io(name, t, shp, dt)
     _check_io("lse", lse, (b, h, s_q), torch.float32)
@@ -103,12 +107,12 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
     need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    st = _native.lib().sdpa_bwd_phases(
-        int(phases), b, h, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)), float(dropout_p),
+    st = _native.lib().sdpa_bwd_phases_gqa(
+        int(phases), b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)), float(dropout_p),
         int(seed), int(offset), _DTYPE_CODE[dt], _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o),
         _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
         workspace.numel(), ctypes.c_void_p(_stream_ptr(stream)))
-    _native.check(st, "sdpa_bwd_phases")
+    _native.check(st, "sdpa_bwd_phases_gqa")
     return dq, dk, dv, dbias
 
 

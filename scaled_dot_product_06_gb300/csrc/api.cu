@@ -124,6 +124,13 @@ sdpa_status_t check_sizes(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64
   return SDPA_OK;
 }
 
+// h_kv K/V heads serve h query heads: 1 <= h_kv <= h and h_kv divides h (any
+// h_kv >= 1 when there are no query heads).
+bool kv_heads_ok(int64_t h, int64_t h_kv) {
+  if (h_kv < 1 || h_kv > (int64_t{1} << 24)) return h == 0 && h_kv == 0;
+  return h == 0 || (h_kv <= h && h % h_kv == 0);
+}
+
 uint32_t drop_threshold(float p) {
   return static_cast<uint32_t>(std::floor(static_cast<double>(p) * 4294967296.0));
 }
@@ -184,12 +191,14 @@ sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns) {
   return SDPA_OK;
 }
 
-sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
-                       float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
-                       sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
-                       const float* bias, void* o, float* lse, void* stream) {
+sdpa_status_t sdpa_fwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                           int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
+                           uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
+                           const void* k, const void* v, const float* bias, void* o, float* lse,
+                           void* stream) {
   bool empty = false;
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
   if (empty) return SDPA_OK;
   if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -200,12 +209,13 @@ sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
   const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
   if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 128, true)) return s;
-  if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
-  if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h_kv, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h_kv, 128, true)) return s;
 
   FwdParams p{};
   p.B = static_cast<int>(b);
   p.H = static_cast<int>(h);
+  p.H_kv = static_cast<int>(h_kv);
   p.S_q = static_cast<int>(s_q);
   p.S_kv = static_cast<int>(s_kv);
   p.scale_log2 = scale * kLog2e;
@@ -239,16 +249,17 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
   return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
 }
 
-sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
-                              int64_t d_qk, int64_t d_v, float scale, int is_causal,
-                              float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
-                              const void* q, const void* k, const void* v, const float* bias,
-                              const void* o, const void* dout, const float* lse, void* dq, void* dk,
-                              void* dv, float* dbias, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
+                                  int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
+                                  int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
+                                  sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
+                                  const float* bias, const void* o, const void* dout,
+                                  const float* lse, void* dq, void* dk, void* dv, float* dbias,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
   if (phases <= 0 || (phases & ~SDPA_BWD_ALL) != 0) return fail(SDPA_ERR_INVALID_ARG, "phases");
   bool empty = false;
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
   if (empty) return SDPA_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
   if ((bias == nullptr) != (dbias == nullptr)) return SDPA_ERR_INVALID_ARG;
@@ -268,6 +279,7 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
   BwdParams p{};
   p.B = static_cast<int>(b);
   p.H = static_cast<int>(h);
+  p.H_kv = static_cast<int>(h_kv);
   p.S_q = static_cast<int>(s_q);
   p.S_kv = static_cast<int>(s_kv);
   p.scale = scale;
@@ -301,8 +313,8 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
     const uint32_t q_rows = d_qk <= 128 ? 128 : 64;
     CUtensorMap mq, mk, mv, mdo;
     if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, q_rows, true)) return s;
-    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h_kv, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h_kv, 128, true)) return s;
     if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, q_rows, true)) return s;
     e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st)
              : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st);
@@ -311,8 +323,8 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
   if (phases & SDPA_BWD_DQ) {
     CUtensorMap mq, mk, mv, mdo;
     if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h_kv, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h_kv, 128, true)) return s;
     if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, 128, true)) return s;
     e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, p, st)
              : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, p, st);
@@ -321,15 +333,47 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
   return SDPA_OK;
 }
 
+sdpa_status_t sdpa_bwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                           int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
+                           uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
+                           const void* k, const void* v, const float* bias, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           float* dbias, void* workspace, size_t workspace_bytes, void* stream) {
+  return sdpa_bwd_phases_gqa(SDPA_BWD_ALL, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, is_causal,
+                             dropout_p, seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk,
+                             dv, dbias, workspace, workspace_bytes, stream);
+}
+
+// The ungrouped entry points: every query head has its own K/V head.
+sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
+                       float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
+                       sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
+                       const float* bias, void* o, float* lse, void* stream) {
+  return sdpa_fwd_gqa(b, h, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed, offset,
+                      dtype, q, k, v, bias, o, lse, stream);
+}
+
+sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
+                              int64_t d_qk, int64_t d_v, float scale, int is_causal,
+                              float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+                              const void* q, const void* k, const void* v, const float* bias,
+                              const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                              void* dv, float* dbias, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  return sdpa_bwd_phases_gqa(phases, b, h, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p,
+                             seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias,
+                             workspace, workspace_bytes, stream);
+}
+
 sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
                        float scale, int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
                        sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
                        const float* bias, const void* o, const void* dout, const float* lse,
                        void* dq, void* dk, void* dv, float* dbias, void* workspace,
                        size_t workspace_bytes, void* stream) {
-  return sdpa_bwd_phases(SDPA_BWD_ALL, b, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed,
-                         offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias, workspace,
-                         workspace_bytes, stream);
+  return sdpa_bwd_phases_gqa(SDPA_BWD_ALL, b, h, h, s_q, s_kv, d_qk, d_v, scale, is_causal,
+                             dropout_p, seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk,
+                             dv, dbias, workspace, workspace_bytes, stream);
 }
 
 sdpa_status_t sdpa_dropout_mask(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, float dropout_p,

@@ -138,18 +138,25 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kLoadWarp = NCT / 32, kMmaWarp = NCT / 32 + 1;
 
-  // ---- key tile of this CTA: head-major (one head's Q / dO stay in L2), then
-  // the key tiles with the most query work first, batch fastest (the batches
-  // of one head share Bias and dBias rows)
+  // ---- key tile of this CTA: K/V-head-major (one head's Q / dO stay in L2),
+  // then the key tiles with the most query work first, batch fastest (the
+  // batches of one head share Bias and dBias rows)
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
   const int b = static_cast<int>(blockIdx.x % p.B);
   const int rest = static_cast<int>(blockIdx.x / p.B);
-  const int kt = rest % n_kt, h = rest / n_kt;
-  const int bh = b * p.H + h;
+  const int kt = rest % n_kt, hk = rest / n_kt;  // hk: K/V head
+  const int bhk = b * p.H_kv + hk;
+  const int grp = p.H / p.H_kv;  // query heads sharing this K/V head
   const int k0 = kt * C::BN;
   const int n_qt = (p.S_q + BM - 1) / BM;
   const int it0 = p.causal ? min(n_qt, k0 / BM) : 0;  // first query tile that sees a key here
-  const int n_it = n_qt - it0;
+  const int n_per = n_qt - it0;                        // query tiles per query head
+  // One loop over (query head of the group, query tile): iteration i visits
+  // query head hk * grp + i / n_per and query tile it0 + i % n_per, so dK and
+  // dV sum over the whole group inside tensor memory.
+  const int n_it = n_per * grp;
+  auto qhead = [&](int i) { return hk * grp + i / n_per; };
+  auto qtile0 = [&](int i) { return (it0 + i % n_per) * BM; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AB_COUNT; ++i)
@@ -183,16 +190,17 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(AB_KV), C::K_BYTES + C::V_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sK + c * C::BN * 128, &tmK, bar(AB_KV), c * 64, k0, bh);
+          tma_load_3d(sK + c * C::BN * 128, &tmK, bar(AB_KV), c * 64, k0, bhk);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sV + c * C::BN * 128, &tmV, bar(AB_KV), c * 64, k0, bh);
+          tma_load_3d(sV + c * C::BN * 128, &tmV, bar(AB_KV), c * 64, k0, bhk);
       }
       for (int i = 0; i < n_it; ++i) {
         const int s = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) break;
-        const int q0 = (it0 + i) * BM;
+        const int q0 = qtile0(i);
+        const int bh = b * p.H + qhead(i);
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(AB_QF + s), C::Q_BYTES + C::STAT_BYTES);
 #pragma unroll
@@ -342,7 +350,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     {
       const float zk = p.keep_scale;
       for (int i = 0; ok && i < n_it; ++i) {
-        const int q0 = (it0 + i) * BM;
+        const int q0 = qtile0(i);
+        const int h = qhead(i);          // query head
+        const int bh = b * p.H + h;
         const int qc0 = q0 + CW * hf;  // first query row of this thread's columns
         const float* stat = rowbuf + (i & 1) * (2 * BM) + stat_off;
         const uint32_t nl2_s = smem_u32(stat), dd_s = smem_u32(stat + 64);
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     const bool ready = have && ok && mbar_wait(bar(AB_DKDV), 0, ec, kSiteBwdCompute);
     if (!have || ready) {
       if (ready) tc_fence_after();
-      const size_t rowi = static_cast<size_t>(bh) * p.S_kv + (kv_ok ? kv : 0);
+      const size_t rowi = static_cast<size_t>(bhk) * p.S_kv + (kv_ok ? kv : 0);
       auto write_rows = [&](auto width_tag, uint32_t tcol, void* base, float mul) {
         constexpr int W = decltype(width_tag)::value;
         uint8_t* dst_row = static_cast<uint8_t*>(base) + rowi * W * 2;
@@ -543,7 +553,7 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
-  const long long grid = static_cast<long long>(n_kt) * p.B * p.H;
+  const long long grid = static_cast<long long>(n_kt) * p.B * p.H_kv;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, p);
   return cudaGetLastError();
 }

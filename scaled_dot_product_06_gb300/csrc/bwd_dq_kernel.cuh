@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_qt, 1);
   const int b = qtile.b, h = qtile.h, qt = qtile.qt;
   const int bh = b * p.H + h;
+  const int bhk = b * p.H_kv + h / (p.H / p.H_kv);  // K/V head of this query head
   const int q0 = qt * BM;
   const int n_kv_all = (p.S_kv + BN - 1) / BN;
   const int n_kv = p.causal ? min(n_kv_all, (q0 + BM - 1) / BN + 1) : n_kv_all;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_KF + s), C::K_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, (n_kv - 1 - j) * BN, bh);
+          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, (n_kv - 1 - j) * BN, bhk);
       }
       if (!mbar_wait(bar(QB_VE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) {
         issued = 2 * j + 1;
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_VF + s), C::V_BYTES);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, (n_kv - 1 - j) * BN, bh);
+          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, (n_kv - 1 - j) * BN, bhk);
       }
       issued = 2 * j + 2;
     }

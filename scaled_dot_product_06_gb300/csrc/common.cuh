@@ -27,6 +27,7 @@ enum : uint32_t {
 
 struct FwdParams {
   int B, H, S_q, S_kv;
+  int H_kv;                // K/V heads; query head h reads K/V head h / (H / H_kv)
   float scale_log2;        // softmax scale * log2(e)
   int causal;              // top-left: key j visible to query i iff j <= i
   const float* bias;       // [1, H, S_q, S_kv] fp32 or null
@@ -76,6 +77,7 @@ __device__ __forceinline__ QueryTile query_tile_order(int idx, int B, int H, int
 
 struct BwdParams {
   int B, H, S_q, S_kv;
+  int H_kv;                // K/V heads; query head h reads K/V head h / (H / H_kv)
   float scale;             // softmax scale
   float scale_log2;        // scale * log2(e)
   int causal;

@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(384, 1)
   const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_pairs, 8);
   const int b = qtile.b, h = qtile.h;
   const int bh = b * p.H + h;
+  const int bhk = b * p.H_kv + h / (p.H / p.H_kv);  // K/V head of this query head
   const int q0 = qtile.qt * 2 * C::BM;  // first row of query tile 0
   const int n_kv_all = (p.S_kv + C::BN - 1) / C::BN;
   // key tiles query tile t sees (0 when the tile lies past S_q)
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(bar(FB_KF + s), C::K_BYTES);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64, kv0, bh);
+            tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64, kv0, bhk);
         }
         if (!mbar_wait(bar(FB_VE + s), ph ^ 1, ec, kSiteFwdLoad, true, true)) {
           issued = 2 * j + 1;
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(bar(FB_VF + s), C::V_BYTES);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sV + s * C::V_BYTES + c * C::BN * 128, &tmV, bar(FB_VF + s), c * 64, kv0, bh);
+            tma_load_3d(sV + s * C::V_BYTES + c * C::BN * 128, &tmV, bar(FB_VF + s), c * 64, kv0, bhk);
         }
         issued = 2 * j + 2;
       }

@@ -34,10 +34,11 @@ class Case:
     scale: float | None = None
     seed: int = 0x1234
     offset: int = 0
+    H_kv: int = 0  # K/V heads (grouped-query attention); 0 means H
 
     @property
     def shape(self):
-        return Shape(self.B, self.H, self.S_q, self.S_kv, self.D_qk, self.D_v)
+        return Shape(self.B, self.H, self.S_q, self.S_kv, self.D_qk, self.D_v, self.H_kv)
 
     @property
     def sc(self):
@@ -45,7 +46,7 @@ class Case:
 
     def problem(self):
         return oracle.Problem(self.B, self.H, self.S_q, self.S_kv, self.D_qk, self.D_v, self.sc,
-                              self.causal, self.p, self.seed, self.offset)
+                              self.causal, self.p, self.seed, self.offset, self.H_kv)
 
 
 def assert_close(name, got, ref, rel=REL_TOL):

@@ -116,3 +116,18 @@ def test_debug_fault_hook_arguments(lib):
     assert lib.sdpa_debug_fault(2, 0) == 1          # SDPA_ERR_INVALID_ARG
     assert lib.sdpa_debug_fault(-1, 0) == 1
     assert lib.sdpa_debug_fault(0, 0) == 0
+
+
+def test_grouped_kv_heads_validated_before_any_device_work(lib):
+    P = ctypes.c_void_p(16)  # never dereferenced: the calls fail validation first
+    def fwd_gqa(h, h_kv):
+        return lib.sdpa_fwd_gqa(1, h, h_kv, 64, 64, 64, 64, 0.125, 0, 0.0, 0, 0, 0, P, P, P, None,
+                                P, P, None)
+    assert fwd_gqa(4, 3) == _native.SDPA_ERR_INVALID_ARG   # 3 does not divide 4
+    assert fwd_gqa(4, 0) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd_gqa(4, 8) == _native.SDPA_ERR_INVALID_ARG   # more K/V heads than query heads
+    assert fwd_gqa(4, -2) == _native.SDPA_ERR_INVALID_ARG
+    ws = ctypes.c_void_p(256)
+    st = lib.sdpa_bwd_phases_gqa(7, 1, 6, 4, 64, 64, 64, 64, 0.125, 0, 0.0, 0, 0, 0, P, P, P, None,
+                                 P, P, P, P, P, P, None, ws, 1 << 20, None)
+    assert st == _native.SDPA_ERR_INVALID_ARG

@@ -32,6 +32,11 @@ CASES = [
     # several query-tile pairs per head, the last pair without its second tile,
     # causal with more keys than queries
     Case(1, 2, 640, 1000, 128, 128, causal=True),
+    # grouped K/V heads (GQA, MQA): dK / dV summed over each group of query heads
+    Case(2, 4, 256, 256, 128, 128, causal=True, H_kv=2),
+    Case(1, 6, 200, 332, 64, 64, bias=True, p=0.1, H_kv=3, dtype="fp16"),
+    Case(1, 4, 384, 256, 128, 128, causal=True, H_kv=1),
+    Case(2, 4, 192, 192, 192, 128, causal=True, bias=True, H_kv=2),
 ]
 
 
@@ -75,3 +80,16 @@ def test_backward_is_bitwise_reproducible():
     second = run_gpu(case, x)
     for name, a, b in zip(("o", "lse", "dq", "dk", "dv", "dbias"), first, second):
         assert torch.equal(a, b), f"{name} differs between two runs"
+
+
+def test_grouped_backward_is_bitwise_reproducible():
+    """With grouped K/V heads, dK and dV of a K/V head are summed over its
+    query heads inside one CTA in a fixed order: identical bits run to run."""
+    from parity_util import run_gpu
+    from scaled_dot_product_06_gb300.inputs import make_inputs
+    case = Case(1, 8, 256, 256, 128, 128, causal=True, H_kv=2)
+    x = make_inputs(case.shape, case.dtype)
+    first = run_gpu(case, x)
+    second = run_gpu(case, x)
+    for a, b in zip(first[2:5], second[2:5]):
+        assert torch.equal(a, b)
