@@ -45,6 +45,11 @@ WORKLOADS = {
                                                  scale=None),
     "b1h32-s16384-d128-causal": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
                                      dtype="bf16", causal=True, bias=False, p=0.0, scale=None),
+    # grouped-query attention at the long-context size: 32 query heads on 4 K/V
+    # heads (groups of 8)
+    "b1h32kv4-s16384-d128-causal": dict(B=1, H=32, H_kv=4, S_q=16384, S_kv=16384, D_qk=128,
+                                        D_v=128, dtype="bf16", causal=True, bias=False, p=0.0,
+                                        scale=None),
     # half the heads and half the sequence of the long-context case: the size the
     # full ncu section captures in profiles/ are taken at (inputs 134 MB > L2)
     "b1h16-s8192-d128-causal": dict(B=1, H=16, S_q=8192, S_kv=8192, D_qk=128, D_v=128,
@@ -262,7 +267,7 @@ def main():
         if world > 1:
             dist.barrier()
 
-    shp = Shape(w["B"], w["H"], w["S_q"], w["S_kv"], w["D_qk"], w["D_v"])
+    shp = Shape(w["B"], w["H"], w["S_q"], w["S_kv"], w["D_qk"], w["D_v"], w.get("H_kv", 0))
     x = make_inputs(shp, w["dtype"], with_bias=w["bias"], seed_base=rank, device=dev)
     q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
     scale = w["scale"] if w["scale"] is not None else 1.0 / math.sqrt(w["D_qk"])
@@ -431,7 +436,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w["dtype"], "data": "synthetic (seeded normal inputs, no dataset)",
-            "config": {"workload": args.workload, "B": w["B"], "H": w["H"], "S_q": w["S_q"],
+            "config": {"workload": args.workload, "B": w["B"], "H": w["H"],
+                       "H_kv": w.get("H_kv", w["H"]), "S_q": w["S_q"],
                        "S_kv": w["S_kv"], "D_qk": w["D_qk"], "D_v": w["D_v"],
                        "causal": w["causal"], "bias": w["bias"], "dropout_p": w["p"],
                        "l2": "inputs larger than L2, no flush",

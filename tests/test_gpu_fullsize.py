@@ -112,3 +112,42 @@ def test_b1h32_s16384_d128_causal_sampled():
     assert_close("dk cols", dk[0, h][c_t], dk_c)
     assert_close("dv cols", dv[0, h][c_t], dv_c)
     key_sum_invariants(case, outs, x)
+
+
+def test_b1h32kv4_s16384_d128_causal_gqa_sampled():
+    """Grouped-query attention at the long-context size (32 query heads on 4 K/V
+    heads): sampled rows of one query head, sampled key columns of one K/V head
+    (the oracle summed over its 8 query heads), and the key-sum invariants."""
+    case = Case(1, 32, 16384, 16384, 128, 128, causal=True, H_kv=4)
+    x = make_inputs(case.shape, case.dtype)
+    o, lse, dq, dk, dv, _ = outs = run_gpu(case, x)
+    assert dk.shape == (1, 4, 16384, 128) and dv.shape == (1, 4, 16384, 128)
+    pr = case.problem()
+    rng = np.random.default_rng(5)
+    h, hk = 21, 2   # query head 21 reads K/V head 2
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(16384 - 64, 16384),
+                                     rng.integers(0, 16384, 64)]))
+    cols = np.unique(np.concatenate([np.arange(0, 32), np.arange(16384 - 32, 16384),
+                                     rng.integers(0, 16384, 32)]))
+    r_t, c_t = torch.as_tensor(rows, device=o.device), torch.as_tensor(cols, device=o.device)
+    o_ref, lse_ref = oracle.forward_head(pr, 0, h, x["q"], x["k"], x["v"], rows=rows)
+    assert_close("o rows", o[0, h][r_t], o_ref)
+    assert_lse(lse[0, h][r_t], lse_ref)
+    dk_ref = np.zeros((len(cols), 128))
+    dv_ref = np.zeros((len(cols), 128))
+    for hq in range(hk * 8, hk * 8 + 8):
+        dq_r, dk_c, dv_c, _ = oracle.backward_head(pr, 0, hq, x["q"], x["k"], x["v"], x["do"],
+                                                   rows=rows if hq == h else rows[:1],
+                                                   cols=cols, row_chunk=4096)
+        if hq == h:
+            assert_close("dq rows", dq[0, h][r_t], dq_r)
+        dk_ref += dk_c
+        dv_ref += dv_c
+    assert_close("dk cols (group sum)", dk[0, hk][c_t], dk_ref)
+    assert_close("dv cols (group sum)", dv[0, hk][c_t], dv_ref)
+    # key sums: dK's vanish; dV's equal the group's query-sum of dO
+    dk64 = dk.double()
+    rel = dk64.sum(dim=2).abs().max().item() / dk64.abs().sum(dim=2).max().item()
+    assert rel < 2e-2, f"key-sum of dK is not ~0 (relative {rel:.3e})"
+    do_sum = x["do"].double().sum(dim=2).reshape(1, 4, 8, 128).sum(dim=2).numpy()
+    assert_close("sum_j dV", dv.double().sum(dim=2).cpu(), do_sum, rel=3e-2)
