@@ -58,6 +58,11 @@ class Problem:
     seed: int = 0
     offset: int = 0
     H_kv: int = 0  # K/V heads; 0 means H (no grouping)
+    # Index space of the dropout bits: (B', S_q', S_kv', b0) makes element
+    # (b, h, i, j) draw the bit of element (b0 + b, h, i, j) of a
+    # [B', H, S_q', S_kv'] problem (a packed sequence draws from the padded
+    # batch); None means this problem's own shape.
+    drop_frame: tuple | None = None
 
     @property
     def kv_heads(self) -> int:
@@ -108,8 +113,9 @@ def dropout_scale(prob: Problem, b: int, h: int, rows: np.ndarray, cols: np.ndar
     """Z = keep / (1 - p) on the (rows, cols) block, or 1.0 without dropout."""
     if prob.dropout_p == 0.0:
         return 1.0
-    keep = philox.keep_mask(prob.B, prob.H, prob.S_q, prob.S_kv, prob.dropout_p, prob.seed,
-                            prob.offset, b, h, rows)[:, cols]
+    fb, fq, fk, b0 = prob.drop_frame or (prob.B, prob.S_q, prob.S_kv, 0)
+    keep = philox.keep_mask(fb, prob.H, fq, fk, prob.dropout_p, prob.seed, prob.offset, b0 + b, h,
+                            rows)[:, cols]
     return keep.astype(np.float64) / (1.0 - prob.dropout_p)
 
 
