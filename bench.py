@@ -50,6 +50,11 @@ WORKLOADS = {
     "b1h32kv4-s16384-d128-causal": dict(B=1, H=32, H_kv=4, S_q=16384, S_kv=16384, D_qk=128,
                                         D_v=128, dtype="bf16", causal=True, bias=False, p=0.0,
                                         scale=None),
+    # packed variable-length sequences (group mode): 16 sequences of 512..8192
+    # tokens (seeded; 74,372 in all), 32 heads, d 128, causal
+    "varlen16-h32-d128-causal": dict(lengths=dict(n=16, lo=512, hi=8192, seed=2024), H=32,
+                                     D_qk=128, D_v=128, dtype="bf16", causal=True, bias=False,
+                                     p=0.0, scale=None),
     # half the heads and half the sequence of the long-context case: the size the
     # full ncu section captures in profiles/ are taken at (inputs 134 MB > L2)
     "b1h16-s8192-d128-causal": dict(B=1, H=16, S_q=8192, S_kv=8192, D_qk=128, D_v=128,
@@ -72,7 +77,21 @@ KERNEL_SOURCES = {
 }
 
 
+def resolve(w: dict) -> dict:
+    """The workload with its sizes filled in: a packed workload gets its
+    sequence lengths ("lens"), B = their number and S_q = S_kv = the longest."""
+    if "lengths" not in w:
+        return dict(w)
+    from scaled_dot_product_06_gb300.inputs import packed_lengths
+    lens = packed_lengths(**w["lengths"])
+    return dict(w, lens=lens, B=len(lens), S_q=max(lens), S_kv=max(lens))
+
+
 def fwd_flops(w: dict) -> float:
+    """Forward FLOPs by the convention; a packed workload sums its sequences."""
+    if w.get("lens"):
+        one = {k: v for k, v in w.items() if k != "lens"}
+        return sum(fwd_flops(dict(one, B=1, S_q=n, S_kv=n)) for n in w["lens"])
     f = 4.0 * w["B"] * w["H"] * w["S_q"] * w["S_kv"] * (w["D_qk"] + w["D_v"]) / 2.0
     return f / 2.0 if w["causal"] else f
 
@@ -162,8 +181,8 @@ def oracle_sample(w: dict, s_sample: int) -> tuple[float, float]:
     oracle.forward(pr, x["q"], x["k"], x["v"], x["bias"])
     oracle.backward(pr, x["q"], x["k"], x["v"], x["do"], x["bias"])
     dt = time.perf_counter() - t0
-    ws = dict(w, B=1, H=1, S_q=s_q, S_kv=s_kv)
-    return dt, 3.5 * fwd_flops(ws)
+    ws = {k: v for k, v in w.items() if k != "lens"}  # one head of one sequence
+    return dt, 3.5 * fwd_flops(dict(ws, B=1, H=1, S_q=s_q, S_kv=s_kv))
 
 
 def cpu_threads() -> int:
@@ -239,7 +258,7 @@ def main():
                     help="query positions of the one-head oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    w = WORKLOADS[args.workload]
+    w = resolve(WORKLOADS[args.workload])
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -251,10 +270,13 @@ def main():
     import torch
     import torch.distributed as dist
 
-    from scaled_dot_product_06_gb300 import (SDPA_BWD_DKDV, SDPA_BWD_DQ, SDPA_BWD_PREPROCESS,
-                                             sdpa_bwd_phases,
-                                             sdpa_bwd_workspace_size, sdpa_device_error, sdpa_fwd)
-    from scaled_dot_product_06_gb300.inputs import Shape, make_inputs
+    from scaled_dot_product_06_gb300 import (SDPA_BWD_ALL, SDPA_BWD_DKDV, SDPA_BWD_DQ,
+                                             SDPA_BWD_PREPROCESS, sdpa_bwd_phases,
+                                             sdpa_bwd_phases_varlen, sdpa_bwd_varlen_workspace_size,
+                                             sdpa_bwd_workspace_size, sdpa_device_error, sdpa_fwd,
+                                             sdpa_fwd_varlen)
+    from scaled_dot_product_06_gb300.inputs import (Shape, make_inputs, make_packed_inputs,
+                                                    seqstarts)
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
@@ -267,30 +289,62 @@ def main():
         if world > 1:
             dist.barrier()
 
-    shp = Shape(w["B"], w["H"], w["S_q"], w["S_kv"], w["D_qk"], w["D_v"], w.get("H_kv", 0))
-    x = make_inputs(shp, w["dtype"], with_bias=w["bias"], seed_base=rank, device=dev)
-    q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
     scale = w["scale"] if w["scale"] is not None else 1.0 / math.sqrt(w["D_qk"])
     kw = dict(scale=scale, is_causal=w["causal"], dropout_p=w["p"], seed=DROP_SEED,
-              offset=DROP_OFFSET, bias=bias)
-    o = torch.empty(shp.B, shp.H, shp.S_q, shp.D_v, dtype=q.dtype, device=dev)
-    lse = torch.empty(shp.B, shp.H, shp.S_q, dtype=torch.float32, device=dev)
+              offset=DROP_OFFSET)
+    packed = "lens" in w
+    if packed:
+        # [H, total, D] tensors; sequence i owns rows seqstart[i] .. seqstart[i+1]-1
+        total = sum(w["lens"])
+        x = make_packed_inputs(w["H"], total, total, w["D_qk"], w["D_v"], w["dtype"],
+                               w.get("H_kv", 0), seed_base=rank, device=dev)
+        x["bias"] = None
+        starts = torch.tensor(seqstarts(w["lens"]), dtype=torch.int32, device=dev)
+        o = torch.empty(w["H"], total, w["D_v"], dtype=x["q"].dtype, device=dev)
+        lse = torch.empty(w["H"], total, dtype=torch.float32, device=dev)
+        ws = torch.empty(sdpa_bwd_varlen_workspace_size(w["B"], w["H"], total), dtype=torch.uint8,
+                         device=dev)
+        mx = w["S_q"]
+
+        def fwd_call(D):
+            sdpa_fwd_varlen(D["q"], D["k"], D["v"], starts, starts, mx, mx, out=D["o"],
+                            lse=D["lse"], **kw)
+
+        def bwd_call(ph, D):
+            sdpa_bwd_phases_varlen(ph, D["q"], D["k"], D["v"], D["o"], D["do"], D["lse"], starts,
+                                   starts, mx, mx, workspace=ws, dq=D["dq"], dk=D["dk"],
+                                   dv=D["dv"], **kw)
+    else:
+        shp = Shape(w["B"], w["H"], w["S_q"], w["S_kv"], w["D_qk"], w["D_v"], w.get("H_kv", 0))
+        x = make_inputs(shp, w["dtype"], with_bias=w["bias"], seed_base=rank, device=dev)
+        o = torch.empty(shp.B, shp.H, shp.S_q, shp.D_v, dtype=x["q"].dtype, device=dev)
+        lse = torch.empty(shp.B, shp.H, shp.S_q, dtype=torch.float32, device=dev)
+        ws = torch.empty(sdpa_bwd_workspace_size(shp.B, shp.H, shp.S_q, shp.S_kv, shp.D_qk,
+                                                 shp.D_v), dtype=torch.uint8, device=dev)
+
+        def fwd_call(D):
+            sdpa_fwd(D["q"], D["k"], D["v"], out=D["o"], lse=D["lse"], bias=D["bias"], **kw)
+
+        def bwd_call(ph, D):
+            sdpa_bwd_phases(ph, D["q"], D["k"], D["v"], D["o"], D["do"], D["lse"], workspace=ws,
+                            dq=D["dq"], dk=D["dk"], dv=D["dv"], bias=D["bias"], dbias=D["dbias"],
+                            **kw)
+    q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dbias = torch.empty_like(bias) if bias is not None else None
-    ws = torch.empty(sdpa_bwd_workspace_size(shp.B, shp.H, shp.S_q, shp.S_kv, shp.D_qk, shp.D_v),
-                     dtype=torch.uint8, device=dev)
+    set0 = {"q": q, "k": k, "v": v, "do": do, "bias": bias, "o": o, "lse": lse, "dq": dq,
+            "dk": dk, "dv": dv, "dbias": dbias}
     stream = torch.cuda.current_stream()
     names = ["fwd", "bwd_pre", "bwd_dkdv", "bwd_dq"]
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        sdpa_fwd(q, k, v, out=o, lse=lse, **kw)
+        fwd_call(set0)
         if ev is not None:
             ev[1].record(stream)
         for i, ph in enumerate((SDPA_BWD_PREPROCESS, SDPA_BWD_DKDV, SDPA_BWD_DQ)):
-            sdpa_bwd_phases(ph, q, k, v, o, do, lse, workspace=ws, dq=dq, dk=dk, dv=dv,
-                            dbias=dbias, **kw)
+            bwd_call(ph, set0)
             if ev is not None:
                 ev[2 + i].record(stream)
 
@@ -355,19 +409,16 @@ def main():
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": hbm, "unit": "GB/s",
                 "frac": None, "traffic": None, "peak_source": f"{peak_kind} HBM copy"}
 
-    # End to end through the public API (sdpa_fwd + sdpa_bwd, the calls a user
-    # makes) with pinned host buffers: every step uploads its inputs and reads
+    # End to end through the public API (sdpa_fwd + sdpa_bwd, or their packed
+    # forms: the calls a user makes) with pinned host buffers: every step uploads its inputs and reads
     # back its results. Two sets of device tensors and two copy streams let the
     # upload of step n+1 and the read-back of step n-1 overlap step n's
     # compute, the way a serving loop would run; each step still moves all its
     # bytes through the host link.
     e2e = None
     if args.e2e_steps > 0:
-        from scaled_dot_product_06_gb300 import sdpa_bwd
         in_names = ["q", "k", "v", "do"] + (["bias"] if bias is not None else [])
         out_names = ["o", "lse", "dq", "dk", "dv"] + (["dbias"] if dbias is not None else [])
-        set0 = {"q": q, "k": k, "v": v, "do": do, "bias": bias, "o": o, "lse": lse, "dq": dq,
-                "dk": dk, "dv": dv, "dbias": dbias}
         set1 = {n: (torch.empty_like(t) if t is not None else None) for n, t in set0.items()}
         sets = [set0, set1]
         hin = {n: set0[n].cpu().pin_memory() for n in in_names}
@@ -394,10 +445,8 @@ def main():
                 ev_in[i].record(s_in)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in[i])
-                kwb = dict(kw, bias=D["bias"])
-                sdpa_fwd(D["q"], D["k"], D["v"], out=D["o"], lse=D["lse"], **kwb)
-                sdpa_bwd(D["q"], D["k"], D["v"], D["o"], D["do"], D["lse"], workspace=ws,
-                         dq=D["dq"], dk=D["dk"], dv=D["dv"], dbias=D["dbias"], **kwb)
+                fwd_call(D)
+                bwd_call(SDPA_BWD_ALL, D)
                 ev_cmp[i].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_cmp[i])
@@ -411,7 +460,8 @@ def main():
         e2e = {"value": whole_job_tflops(world, step_flops, e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": n_e,
-               "method": "sdpa_fwd + sdpa_bwd from pinned host buffers; uploads of step n+1 and "
+               "method": ("sdpa_fwd_varlen + sdpa_bwd_varlen" if packed else "sdpa_fwd + sdpa_bwd") +
+                         " from pinned host buffers; uploads of step n+1 and "
                          "read-backs of step n-1 overlap step n on two copy streams "
                          "(double-buffered device tensors)"}
 
@@ -439,6 +489,8 @@ def main():
             "config": {"workload": args.workload, "B": w["B"], "H": w["H"],
                        "H_kv": w.get("H_kv", w["H"]), "S_q": w["S_q"],
                        "S_kv": w["S_kv"], "D_qk": w["D_qk"], "D_v": w["D_v"],
+                       **({"packed_lengths": w["lens"], "total_tokens": sum(w["lens"])}
+                          if packed else {}),
                        "causal": w["causal"], "bias": w["bias"], "dropout_p": w["p"],
                        "l2": "inputs larger than L2, no flush",
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},

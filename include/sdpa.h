@@ -193,6 +193,64 @@ sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv
                                   const float* lse, void* dq, void* dk, void* dv, float* dbias,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Packed variable-length sequences (CK tile fmha_bwd_kernel.hpp group mode:
+ * seqstart_q_ptr / seqstart_k_ptr give each sequence's first row, and the
+ * batch offsets become query_start / key_start times the row stride).
+ *   Layout   q, o, dout, dq [h, total_q, d]; k, v, dk, dv [h_kv, total_k, d];
+ *            lse [h, total_q] fp32: every head holds all sequences' rows one
+ *            after another (BHSD with the batch folded into the rows).
+ *   Sequences  b of them. seqstart_q / seqstart_k are DEVICE arrays of b + 1
+ *            int32 (4-byte aligned): sequence i owns query rows
+ *            [seqstart_q[i], seqstart_q[i+1]) and key rows [seqstart_k[i],
+ *            seqstart_k[i+1]), non-decreasing, seqstart[b] <= total. They are
+ *            read on the device only; the kernels clamp them into [0, total)
+ *            so that no content makes them access memory out of range (out-of-
+ *            order entries give wrong results, never a fault).
+ *   max_seqlen_q / max_seqlen_k  at least every sequence's length (rows past
+ *            them are neither read nor written); they size the grid and take
+ *            the place of s_q / s_kv in every rule above.
+ *   Masks    each sequence is its own problem: causal is top-left within the
+ *            sequence (local key j visible to local query i iff j <= i); keys
+ *            of other sequences are never visible. A query row whose sequence
+ *            has no key gets O = 0, LSE = -inf and dQ = 0; a key whose
+ *            sequence has no query gets dK = dV = 0.
+ *   Dropout  the keep bit of (sequence i, head hh, local query r, local key c)
+ *            is the batch-mode bit of element (i, hh, r, c) of a
+ *            [b, h, max_seqlen_q, max_seqlen_k] problem (see "Dropout"), so
+ *            max_seqlen_k % 4 == 0 is required when dropout_p > 0.
+ *   Inputs   K/V rows of the neighbouring sequence can enter a tile before
+ *            their scores are masked: inputs must be finite.
+ *   Bias     not supported with packed sequences (no bias argument).
+ *   Workspace  sdpa_bwd_varlen_workspace_size(b, h, total_q) bytes, 256-byte
+ *            aligned (0 for invalid sizes).
+ * h_kv as in the grouped calls. Zero b, h, total_q, total_k, max_seqlen_q or
+ * max_seqlen_k is a no-op returning SDPA_OK.
+ */
+size_t sdpa_bwd_varlen_workspace_size(int64_t b, int64_t h, int64_t total_q);
+sdpa_status_t sdpa_fwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
+                              int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v,
+                              float scale, int is_causal, float dropout_p, uint64_t seed,
+                              uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                              const int32_t* seqstart_k, const void* q, const void* k, const void* v,
+                              void* o, float* lse, void* stream);
+sdpa_status_t sdpa_bwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
+                              int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v,
+                              float scale, int is_causal, float dropout_p, uint64_t seed,
+                              uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                              const int32_t* seqstart_k, const void* q, const void* k, const void* v,
+                              const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                              void* dv, void* workspace, size_t workspace_bytes, void* stream);
+sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+                                     int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
+                                     int64_t d_qk, int64_t d_v, float scale, int is_causal,
+                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                                     const int32_t* seqstart_k, const void* q, const void* k,
+                                     const void* v, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
 sdpa_status_t sdpa_bwd_noalloc(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v, float scale, int is_causal, float dropout_p,
                                uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,

@@ -45,6 +45,15 @@ SIGNATURES = {
     "sdpa_bwd_phases_gqa": (_int, [_int, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32,
                                    _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                    _ptr, _ptr, _ptr, _ptr, _sz, _ptr]),
+    "sdpa_bwd_varlen_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "sdpa_fwd_varlen": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32,
+                               _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
+    "sdpa_bwd_varlen": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32,
+                               _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                               _ptr, _ptr, _ptr, _sz, _ptr]),
+    "sdpa_bwd_phases_varlen": (_int, [_int, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
+                                      _int, _f32, _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
+                                      _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _sz, _ptr]),
     "sdpa_bwd_noalloc": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64,
                                 _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                 _ptr, _ptr]),

@@ -116,6 +116,99 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
     return dq, dk, dv, dbias
 
 
+def _check_seqstart(name: str, t: torch.Tensor) -> int:
+    if not t.is_cuda or t.dtype != torch.int32 or t.dim() != 1 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 1-D int32 CUDA tensor")
+    if t.numel() < 1:
+        raise ValueError(f"{name} needs b + 1 entries")
+    return t.numel() - 1
+
+
+def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *, scale=None,
+                    is_causal=False, dropout_p=0.0, seed=0, offset=0, out=None, lse=None,
+                    stream=None):
+    """Forward pass over packed variable-length sequences. q [h, total_q, d_qk],
+    k [h_kv, total_k, d_qk], v [h_kv, total_k, d_v]; seqstart_q / seqstart_k
+    int32 CUDA tensors of b + 1 row offsets (sequence i owns query rows
+    seqstart_q[i] .. seqstart_q[i+1] - 1 and the matching key rows).
+    Returns (o [h, total_q, d_v], lse fp32 [h, total_q])."""
+    h, total_q, d_qk = q.shape
+    h_kv, total_k, d_v = k.shape[0], k.shape[1], v.shape[2]
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("q, k, v must be bf16 or fp16")
+    b = _check_seqstart("seqstart_q", seqstart_q)
+    if _check_seqstart("seqstart_k", seqstart_k) != b:
+        raise ValueError("seqstart_q and seqstart_k must have the same length")
+    _check_io("q", q, (h, total_q, d_qk), dt)
+    _check_io("k", k, (h_kv, total_k, d_qk), dt)
+    _check_io("v", v, (h_kv, total_k, d_v), dt)
+    scale = 1.0 / math.sqrt(d_qk) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((h, total_q, d_v), dtype=dt, device=q.device)
+    if lse is None:
+        lse = torch.empty((h, total_q), dtype=torch.float32, device=q.device)
+    _check_io("out", out, (h, total_q, d_v), dt)
+    _check_io("lse", lse, (h, total_q), torch.float32)
+    st = _native.lib().sdpa_fwd_varlen(
+        b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale,
+        int(bool(is_causal)), float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
+        _ptr(seqstart_q), _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+        ctypes.c_void_p(_stream_ptr(stream)))
+    _native.check(st, "sdpa_fwd_varlen")
+    return out, lse
+
+
+def sdpa_bwd_varlen_workspace_size(b, h, total_q) -> int:
+    return int(_native.lib().sdpa_bwd_varlen_workspace_size(b, h, total_q))
+
+
+def sdpa_bwd_varlen(q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *,
+                    scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0, workspace=None,
+                    dq=None, dk=None, dv=None, stream=None):
+    """Backward pass over packed sequences (layouts as sdpa_fwd_varlen).
+    Returns (dq, dk, dv) shaped like q, k, v."""
+    return sdpa_bwd_phases_varlen(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, seqstart_q,
+                                  seqstart_k, max_seqlen_q, max_seqlen_k, scale=scale,
+                                  is_causal=is_causal, dropout_p=dropout_p, seed=seed,
+                                  offset=offset, workspace=workspace, dq=dq, dk=dk, dv=dv,
+                                  stream=stream)
+
+
+def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q,
+                           max_seqlen_k, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
+                           offset=0, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """The packed-sequence backward phases selected by ``phases``."""
+    h, total_q, d_qk = q.shape
+    h_kv, total_k, d_v = k.shape[0], k.shape[1], v.shape[2]
+    dt = q.dtype
+    if dt not in _DTYPE_CODE:
+        raise ValueError("q, k, v must be bf16 or fp16")
+    b = _check_seqstart("seqstart_q", seqstart_q)
+    if _check_seqstart("seqstart_k", seqstart_k) != b:
+        raise ValueError("seqstart_q and seqstart_k must have the same length")
+    for name, t, shp in (("q", q, (h, total_q, d_qk)), ("k", k, (h_kv, total_k, d_qk)),
+                         ("v", v, (h_kv, total_k, d_v)), ("o", o, (h, total_q, d_v)),
+                         ("dout", dout, (h, total_q, d_v))):
+        _check_io(name, t, shp, dt)
+    _check_io("lse", lse, (h, total_q), torch.float32)
+    scale = 1.0 / math.sqrt(d_qk) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = sdpa_bwd_varlen_workspace_size(b, h, total_q)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = _native.lib().sdpa_bwd_phases_varlen(
+        int(phases), b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v,
+        scale, int(bool(is_causal)), float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
+        _ptr(seqstart_q), _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+        _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+        ctypes.c_void_p(_stream_ptr(stream)))
+    _native.check(st, "sdpa_bwd_phases_varlen")
+    return dq, dk, dv
+
+
 def sdpa_dropout_mask(b, h, s_q, s_kv, dropout_p, seed, offset, device="cuda", stream=None):
     """Packed keep bits as an int32 tensor of ceil(b*h*s_q*s_kv/32) words."""
     words = (b * h * s_q * s_kv + 31) // 32

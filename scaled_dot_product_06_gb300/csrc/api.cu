@@ -165,6 +165,197 @@ cudaError_t prepare_kernel(const void* kern, int smem, int regs) {
 }
 }  // namespace sdpa
 
+namespace {
+
+// Packed-sequence arguments of the varlen entry points; seqstart_q null means
+// batch mode (rows of (b, h) contiguous, s_q / s_kv of them).
+struct Packing {
+  const int32_t* seqstart_q = nullptr;
+  const int32_t* seqstart_k = nullptr;
+  int64_t total_q = 0, total_k = 0;
+};
+
+// Rows and z extent of the 3-D tensor maps ([z][rows][d]) and the statistics
+// rows per z: batch mode z = (b, h) with s_q / s_kv rows; packed z = head with
+// the packed totals.
+struct Rows {
+  int64_t q, k, zq, zk, stat_pad;
+};
+Rows rows_of(const Packing& pk, int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv) {
+  if (pk.seqstart_q == nullptr) return Rows{s_q, s_kv, b * h, b * h_kv, stat_pad(static_cast<int>(s_q))};
+  return Rows{pk.total_q, pk.total_k, h, h_kv, packed_stat_pad(pk.total_q, b)};
+}
+
+// Checks of the packed-sequence arguments (none in batch mode): totals in
+// range, both seqstart arrays present and 4-byte aligned, no bias (bias and
+// dBias are per padded batch entry on the pages, not defined for packed
+// rows). Sets *empty when either total is zero.
+sdpa_status_t check_packing(const Packing& pk, int64_t b, const float* bias, bool* empty) {
+  if (pk.seqstart_q == nullptr && pk.seqstart_k == nullptr) return SDPA_OK;
+  if (pk.total_q < 0 || pk.total_k < 0) return SDPA_ERR_INVALID_ARG;
+  if (pk.total_q > kMaxSeq || pk.total_k > kMaxSeq || b > (int64_t{1} << 24) ||
+      packed_stat_pad(pk.total_q, b) > (int64_t{1} << 31) - 1)
+    return SDPA_ERR_UNSUPPORTED;
+  if (bias != nullptr) return fail(SDPA_ERR_UNSUPPORTED, "bias with packed sequences");
+  if (pk.total_q == 0 || pk.total_k == 0) *empty = true;
+  if (*empty) return SDPA_OK;
+  if (pk.seqstart_q == nullptr || pk.seqstart_k == nullptr) return SDPA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(pk.seqstart_q) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(pk.seqstart_k) & 3u) != 0)
+    return SDPA_ERR_MISALIGNED;
+  return SDPA_OK;
+}
+
+sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv, int64_t d_qk,
+                       int64_t d_v, float scale, int is_causal, float dropout_p, uint64_t seed,
+                       uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
+                       const void* v, const float* bias, void* o, float* lse, void* stream,
+                       const Packing& pk) {
+  bool empty = false;
+  if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
+  if (sdpa_status_t s = check_packing(pk, b, bias, &empty)) return s;
+  if (empty) return SDPA_OK;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (bias && !aligned16(bias)))
+    return SDPA_ERR_MISALIGNED;
+
+  const bool bf16 = dtype == SDPA_BF16;
+  const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const Rows rw = rows_of(pk, b, h, h_kv, s_q, s_kv);
+  CUtensorMap mq, mk, mv;
+  if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true)) return s;
+  if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true)) return s;
+
+  FwdParams p{};
+  p.B = static_cast<int>(b);
+  p.H = static_cast<int>(h);
+  p.H_kv = static_cast<int>(h_kv);
+  p.S_q = static_cast<int>(s_q);
+  p.S_kv = static_cast<int>(s_kv);
+  p.scale_log2 = scale * kLog2e;
+  p.causal = is_causal ? 1 : 0;
+  p.bias = bias;
+  p.dropout = dropout_p > 0.0f ? 1 : 0;
+  p.drop_threshold = drop_threshold(dropout_p);
+  p.keep_scale = 1.0f / (1.0f - dropout_p);
+  p.seed_lo = static_cast<uint32_t>(seed);
+  p.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.offset_lo = static_cast<uint32_t>(offset);
+  p.offset_hi = static_cast<uint32_t>(offset >> 32);
+  p.o = o;
+  p.lse = lse;
+  p.seqstart_q = pk.seqstart_q;
+  p.seqstart_k = pk.seqstart_k;
+  p.rows_q = static_cast<int>(rw.q);
+  p.rows_k = static_cast<int>(rw.k);
+  p.fault = static_cast<uint32_t>(g_debug_fault.load());
+  const uint64_t wait_ns = g_debug_wait_ns.load();
+  p.wait_ns = wait_ns != 0 ? wait_ns : kWaitLimitNs;
+  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = bf16 ? launch_fwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st)
+                             : launch_fwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st);
+  return cuda_status(e, "forward kernel launch");
+}
+
+
+sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                       int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
+                       uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
+                       const void* k, const void* v, const float* bias, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       float* dbias, void* workspace, size_t workspace_bytes, void* stream,
+                       const Packing& pk) {
+  if (phases <= 0 || (phases & ~SDPA_BWD_ALL) != 0) return fail(SDPA_ERR_INVALID_ARG, "phases");
+  bool empty = false;
+  if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
+  if (sdpa_status_t s = check_packing(pk, b, bias, &empty)) return s;
+  if (empty) return SDPA_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
+  if ((bias == nullptr) != (dbias == nullptr)) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (bias && !aligned16(bias)) || (dbias && !aligned16(dbias)))
+    return SDPA_ERR_MISALIGNED;
+  const size_t need = pk.seqstart_q ? sdpa_bwd_varlen_workspace_size(b, h, pk.total_q)
+                                    : sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v);
+  if (workspace == nullptr || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SDPA_ERR_MISALIGNED;
+
+  const bool bf16 = dtype == SDPA_BF16;
+  const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  float* stats = static_cast<float*>(workspace);
+  const Rows rw = rows_of(pk, b, h, h_kv, s_q, s_kv);
+  const int di = static_cast<int>(d_qk), dvi = static_cast<int>(d_v);
+
+  BwdParams p{};
+  p.B = static_cast<int>(b);
+  p.H = static_cast<int>(h);
+  p.H_kv = static_cast<int>(h_kv);
+  p.S_q = static_cast<int>(s_q);
+  p.S_kv = static_cast<int>(s_kv);
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = is_causal ? 1 : 0;
+  p.bias = bias;
+  p.dbias = dbias;
+  p.dropout = dropout_p > 0.0f ? 1 : 0;
+  p.drop_threshold = drop_threshold(dropout_p);
+  p.keep_scale = 1.0f / (1.0f - dropout_p);
+  p.seed_lo = static_cast<uint32_t>(seed);
+  p.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.offset_lo = static_cast<uint32_t>(offset);
+  p.offset_hi = static_cast<uint32_t>(offset >> 32);
+  p.stats = stats;
+  p.S_pad = static_cast<int>(rw.stat_pad);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.seqstart_q = pk.seqstart_q;
+  p.seqstart_k = pk.seqstart_k;
+  p.rows_q = static_cast<int>(rw.q);
+  p.rows_k = static_cast<int>(rw.k);
+  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e = cudaSuccess;
+  if (phases & SDPA_BWD_PREPROCESS) {
+    const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
+    e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, rw.zq, static_cast<int>(s_q), p.S_pad, p.rows_q,
+                       pk.seqstart_q, static_cast<int>(b), dvi, dbias_elems, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
+  }
+  if (phases & SDPA_BWD_DKDV) {
+    // key/value-stationary kernel: query tiles of 128 rows (64 at d_qk = 192)
+    const uint32_t q_rows = d_qk <= 128 ? 128 : 64;
+    CUtensorMap mq, mk, mv, mdo;
+    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, q_rows, true)) return s;
+    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, q_rows, true)) return s;
+    e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st)
+             : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dK/dV kernel launch", e);
+  }
+  if (phases & SDPA_BWD_DQ) {
+    CUtensorMap mq, mk, mv, mdo;
+    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true)) return s;
+    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, 128, true)) return s;
+    e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, p, st)
+             : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, p, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dQ kernel launch", e);
+  }
+  return SDPA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* sdpa_status_string(sdpa_status_t s) {
@@ -191,55 +382,6 @@ sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns) {
   return SDPA_OK;
 }
 
-sdpa_status_t sdpa_fwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
-                           int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
-                           uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
-                           const void* k, const void* v, const float* bias, void* o, float* lse,
-                           void* stream) {
-  bool empty = false;
-  if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
-  if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
-  if (empty) return SDPA_OK;
-  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      (bias && !aligned16(bias)))
-    return SDPA_ERR_MISALIGNED;
-
-  const bool bf16 = dtype == SDPA_BF16;
-  const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap mq, mk, mv;
-  if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 128, true)) return s;
-  if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h_kv, 128, true)) return s;
-  if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h_kv, 128, true)) return s;
-
-  FwdParams p{};
-  p.B = static_cast<int>(b);
-  p.H = static_cast<int>(h);
-  p.H_kv = static_cast<int>(h_kv);
-  p.S_q = static_cast<int>(s_q);
-  p.S_kv = static_cast<int>(s_kv);
-  p.scale_log2 = scale * kLog2e;
-  p.causal = is_causal ? 1 : 0;
-  p.bias = bias;
-  p.dropout = dropout_p > 0.0f ? 1 : 0;
-  p.drop_threshold = drop_threshold(dropout_p);
-  p.keep_scale = 1.0f / (1.0f - dropout_p);
-  p.seed_lo = static_cast<uint32_t>(seed);
-  p.seed_hi = static_cast<uint32_t>(seed >> 32);
-  p.offset_lo = static_cast<uint32_t>(offset);
-  p.offset_hi = static_cast<uint32_t>(offset >> 32);
-  p.o = o;
-  p.lse = lse;
-  p.fault = static_cast<uint32_t>(g_debug_fault.load());
-  const uint64_t wait_ns = g_debug_wait_ns.load();
-  p.wait_ns = wait_ns != 0 ? wait_ns : kWaitLimitNs;
-  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = bf16 ? launch_fwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st)
-                             : launch_fwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st);
-  return cuda_status(e, "forward kernel launch");
-}
-
 size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v) {
   bool empty = false;
@@ -249,6 +391,15 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
   return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
 }
 
+sdpa_status_t sdpa_fwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                           int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
+                           uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
+                           const void* k, const void* v, const float* bias, void* o, float* lse,
+                           void* stream) {
+  return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed, offset, dtype,
+                  q, k, v, bias, o, lse, stream, Packing{});
+}
+
 sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
                                   int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
                                   int is_causal, float dropout_p, uint64_t seed, uint64_t offset,
@@ -256,81 +407,66 @@ sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv
                                   const float* bias, const void* o, const void* dout,
                                   const float* lse, void* dq, void* dk, void* dv, float* dbias,
                                   void* workspace, size_t workspace_bytes, void* stream) {
-  if (phases <= 0 || (phases & ~SDPA_BWD_ALL) != 0) return fail(SDPA_ERR_INVALID_ARG, "phases");
-  bool empty = false;
-  if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
-  if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
-  if (empty) return SDPA_OK;
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
-  if ((bias == nullptr) != (dbias == nullptr)) return SDPA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      (bias && !aligned16(bias)) || (dbias && !aligned16(dbias)))
-    return SDPA_ERR_MISALIGNED;
-  const size_t need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v);
-  if (workspace == nullptr || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SDPA_ERR_MISALIGNED;
+  return bwd_impl(phases, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed, offset,
+                  dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias, workspace, workspace_bytes,
+                  stream, Packing{});
+}
 
-  const bool bf16 = dtype == SDPA_BF16;
-  const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  float* stats = static_cast<float*>(workspace);
-  const int di = static_cast<int>(d_qk), dvi = static_cast<int>(d_v);
+// Packed sequences: b sequences, the i-th owning packed rows
+// [seqstart_q[i], seqstart_q[i+1]) of the queries and [seqstart_k[i],
+// seqstart_k[i+1]) of the keys of every head; max_seqlen_q / max_seqlen_k take
+// the place of s_q / s_kv.
+size_t sdpa_bwd_varlen_workspace_size(int64_t b, int64_t h, int64_t total_q) {
+  if (b < 0 || h < 0 || total_q < 0 || total_q > kMaxSeq || b > (int64_t{1} << 24)) return 0;
+  const size_t prows = static_cast<size_t>(h) * static_cast<size_t>(packed_stat_pad(total_q, b));
+  return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
+}
 
-  BwdParams p{};
-  p.B = static_cast<int>(b);
-  p.H = static_cast<int>(h);
-  p.H_kv = static_cast<int>(h_kv);
-  p.S_q = static_cast<int>(s_q);
-  p.S_kv = static_cast<int>(s_kv);
-  p.scale = scale;
-  p.scale_log2 = scale * kLog2e;
-  p.causal = is_causal ? 1 : 0;
-  p.bias = bias;
-  p.dbias = dbias;
-  p.dropout = dropout_p > 0.0f ? 1 : 0;
-  p.drop_threshold = drop_threshold(dropout_p);
-  p.keep_scale = 1.0f / (1.0f - dropout_p);
-  p.seed_lo = static_cast<uint32_t>(seed);
-  p.seed_hi = static_cast<uint32_t>(seed >> 32);
-  p.offset_lo = static_cast<uint32_t>(offset);
-  p.offset_hi = static_cast<uint32_t>(offset >> 32);
-  p.stats = stats;
-  p.S_pad = stat_pad(static_cast<int>(s_q));
-  p.dq = dq;
-  p.dk = dk;
-  p.dv = dv;
-  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+sdpa_status_t sdpa_fwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
+                              int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v,
+                              float scale, int is_causal, float dropout_p, uint64_t seed,
+                              uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                              const int32_t* seqstart_k, const void* q, const void* k, const void* v,
+                              void* o, float* lse, void* stream) {
+  const Packing pk{seqstart_q, seqstart_k, total_q, total_k};
+  if (seqstart_q == nullptr || seqstart_k == nullptr) {
+    if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
+    return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
+  }
+  return fwd_impl(b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale, is_causal, dropout_p, seed,
+                  offset, dtype, q, k, v, nullptr, o, lse, stream, pk);
+}
 
-  cudaError_t e = cudaSuccess;
-  if (phases & SDPA_BWD_PREPROCESS) {
-    const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
-    e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, b * h, static_cast<int>(s_q), dvi, dbias_elems, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
+sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+                                     int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
+                                     int64_t d_qk, int64_t d_v, float scale, int is_causal,
+                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                                     const int32_t* seqstart_k, const void* q, const void* k,
+                                     const void* v, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  const Packing pk{seqstart_q, seqstart_k, total_q, total_k};
+  if (seqstart_q == nullptr || seqstart_k == nullptr) {
+    if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
+    return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
-  if (phases & SDPA_BWD_DKDV) {
-    // key/value-stationary kernel: query tiles of 128 rows (64 at d_qk = 192)
-    const uint32_t q_rows = d_qk <= 128 ? 128 : 64;
-    CUtensorMap mq, mk, mv, mdo;
-    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, q_rows, true)) return s;
-    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h_kv, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h_kv, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, q_rows, true)) return s;
-    e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st)
-             : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dK/dV kernel launch", e);
-  }
-  if (phases & SDPA_BWD_DQ) {
-    CUtensorMap mq, mk, mv, mdo;
-    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, s_q, b * h, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, s_kv, b * h_kv, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, s_kv, b * h_kv, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, s_q, b * h, 128, true)) return s;
-    e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, p, st)
-             : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, p, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dQ kernel launch", e);
-  }
-  return SDPA_OK;
+  return bwd_impl(phases, b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale, is_causal,
+                  dropout_p, seed, offset, dtype, q, k, v, nullptr, o, dout, lse, dq, dk, dv, nullptr,
+                  workspace, workspace_bytes, stream, pk);
+}
+
+sdpa_status_t sdpa_bwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
+                              int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v,
+                              float scale, int is_causal, float dropout_p, uint64_t seed,
+                              uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                              const int32_t* seqstart_k, const void* q, const void* k, const void* v,
+                              const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                              void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  return sdpa_bwd_phases_varlen(SDPA_BWD_ALL, b, h, h_kv, total_q, total_k, max_seqlen_q,
+                                max_seqlen_k, d_qk, d_v, scale, is_causal, dropout_p, seed, offset,
+                                dtype, seqstart_q, seqstart_k, q, k, v, o, dout, lse, dq, dk, dv,
+                                workspace, workspace_bytes, stream);
 }
 
 sdpa_status_t sdpa_bwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,

@@ -24,30 +24,50 @@ static int aux_grid(int64_t work_items) {
 }
 
 // One group of DV/8 consecutive threads per row; each thread takes 8 elements.
-// Walks the padded rows (S_pad per (b, h)) so the padding of the statistics is
-// written too: -inf and 0 there, as for a query row that sees no key.
+// Walks the padded rows (s_pad per tensor-map z: (b, h) in batch mode, the head
+// for packed sequences) so the padding of the statistics is written too: -inf
+// and 0 there, as for a query row that sees no key. Packed, statistics row r
+// of a head belongs to the last sequence whose block (packed_stat_row) starts
+// at or before r; rows past that sequence's length are padding.
 template <bool BF16>
 __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __restrict__ o,
                                                               const uint4* __restrict__ dout,
                                                               const float* __restrict__ lse,
                                                               float* __restrict__ stats,
                                                               float4* __restrict__ dbias,
-                                                              int64_t bh_count, int s_q, int s_pad,
-                                                              int d_v, int64_t dbias_elems) {
+                                                              int64_t z_count, int s_q, int s_pad,
+                                                              int rows, const int* __restrict__ seqstart,
+                                                              int n_seq, int d_v, int64_t dbias_elems) {
   const int group = d_v / 8;  // 8 or 16 threads per row (power of two)
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x & 31, sub = lane % group;
   const int64_t rows_per_warp = 32 / group;
   const int64_t warp_id = tid / 32, nwarps = nthreads / 32;
-  const int64_t prow_count = bh_count * s_pad;
+  const int64_t prow_count = z_count * s_pad;
   // wbase is uniform across the warp, so every lane reaches every shuffle
   for (int64_t wbase = warp_id * rows_per_warp; wbase < prow_count; wbase += nwarps * rows_per_warp) {
     const int64_t prow = wbase + lane / group;  // padded row
-    const int64_t bh = prow / s_pad;
-    const int q = static_cast<int>(prow - bh * s_pad);
-    const bool live = prow < prow_count && q < s_q;
-    const int64_t row = bh * s_q + q;  // row of O, dO and LSE
+    const int64_t z = prow / s_pad;
+    const int r = static_cast<int>(prow - z * s_pad);
+    int q = r, len = s_q;
+    int64_t row = z * rows;  // row of O, dO and LSE of local row 0
+    if (seqstart != nullptr && prow < prow_count) {
+      int lo = 0, hi = n_seq - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (packed_stat_row(packed_rows(seqstart, rows, s_q, mid).x, mid) <= r)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const int2 sr = packed_rows(seqstart, rows, s_q, lo);
+      q = r - packed_stat_row(sr.x, lo);
+      len = sr.y;
+      row += sr.x;
+    }
+    const bool live = prow < prow_count && q >= 0 && q < len;
+    row += q;
     float acc = 0.f;
     if (live) {
       const uint4 a = o[row * group + sub];
@@ -63,7 +83,7 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
     for (int off = group / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, group);
     if (prow < prow_count && sub == 0) {
       const float L = live ? lse[row] : SDPA_NEG_INF;
-      const size_t si = stat_index(static_cast<size_t>(bh), s_pad, q);
+      const size_t si = stat_index(static_cast<size_t>(z), s_pad, r);
       stats[si] = (L == SDPA_NEG_INF) ? SDPA_NEG_INF : -L * kLog2e;
       stats[si + 64] = -acc;
     }
@@ -98,16 +118,17 @@ __global__ void __launch_bounds__(kAuxThreads) dropout_mask_kernel(int64_t total
 }
 
 cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
-                           float* dbias, int64_t bh, int s_q, int d_v, int64_t dbias_elems,
+                           float* dbias, int64_t z_count, int s_q, int s_pad, int rows,
+                           const int* seqstart, int n_seq, int d_v, int64_t dbias_elems,
                            cudaStream_t st) {
   const int group = d_v / 8;
-  const int s_pad = stat_pad(s_q);
-  const int64_t work = bh * s_pad * group;
+  const int64_t work = z_count * s_pad * group;
   const int64_t zero_work = dbias_elems / 4;
   const int grid = aux_grid(work > zero_work ? work : zero_work);
   auto kern = bf16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
   kern<<<grid, kAuxThreads, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, stats,
-                                      reinterpret_cast<float4*>(dbias), bh, s_q, s_pad, d_v, dbias_elems);
+                                      reinterpret_cast<float4*>(dbias), z_count, s_q, s_pad, rows, seqstart,
+                                      n_seq, d_v, dbias_elems);
   return cudaGetLastError();
 }
 

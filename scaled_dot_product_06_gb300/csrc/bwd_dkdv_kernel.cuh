@@ -133,6 +133,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + AB_COUNT);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  // dK / dV row of the tile's key 0, set at start-up and read by the epilogue
+  // (kept out of the registers of the compute loop)
+  uint64_t* key_row0 = bars + AB_COUNT + 1;
+  static_assert((AB_COUNT + 2) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -145,10 +149,16 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   const int b = static_cast<int>(blockIdx.x % p.B);
   const int rest = static_cast<int>(blockIdx.x / p.B);
   const int kt = rest % n_kt, hk = rest / n_kt;  // hk: K/V head
-  const int bhk = b * p.H_kv + hk;
+  const SeqSlice sl = seq_slice(p.seqstart_q, p.seqstart_k, p.rows_q, p.rows_k, p.S_q, p.S_kv, p.H,
+                                p.H_kv, b);
+  const int S_q = sl.len_q, S_kv = sl.len_k;  // this sequence's lengths
+  const int zk = sl.zk0 + hk;                 // tensor-map z of the K/V head
   const int grp = p.H / p.H_kv;  // query heads sharing this K/V head
   const int k0 = kt * C::BN;
-  const int n_qt = (p.S_q + BM - 1) / BM;
+  // A key tile past the end of a shorter packed sequence has nothing to do
+  // (uniform over the CTA; never in batch mode).
+  if (k0 >= S_kv) return;
+  const int n_qt = (S_q + BM - 1) / BM;
   const int it0 = p.causal ? min(n_qt, k0 / BM) : 0;  // first query tile that sees a key here
   const int n_per = n_qt - it0;                        // query tiles per query head
   // One loop over (query head of the group, query tile): iteration i visits
@@ -164,6 +174,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
                             ? static_cast<uint32_t>(NCT)
                             : 1u);
     *abort_flag = 0u;
+    *key_row0 = static_cast<uint64_t>(zk) * p.rows_k + sl.row_k + k0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -190,28 +201,28 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(AB_KV), C::K_BYTES + C::V_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sK + c * C::BN * 128, &tmK, bar(AB_KV), c * 64, k0, bhk);
+          tma_load_3d(sK + c * C::BN * 128, &tmK, bar(AB_KV), c * 64, sl.row_k + k0, zk);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sV + c * C::BN * 128, &tmV, bar(AB_KV), c * 64, k0, bhk);
+          tma_load_3d(sV + c * C::BN * 128, &tmV, bar(AB_KV), c * 64, sl.row_k + k0, zk);
       }
       for (int i = 0; i < n_it; ++i) {
         const int s = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) break;
         const int q0 = qtile0(i);
-        const int bh = b * p.H + qhead(i);
+        const int zq = sl.zq0 + qhead(i);  // tensor-map z of the query head
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(AB_QF + s), C::Q_BYTES + C::STAT_BYTES);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(sQ + s * C::Q_BYTES + c * BM * 128, &tmQ, bar(AB_QF + s), c * 64, q0, bh);
-          bulk_load(smem_u32(rowbuf) + s * C::STAT_BYTES, p.stats + stat_index(bh, p.S_pad, q0),
+            tma_load_3d(sQ + s * C::Q_BYTES + c * BM * 128, &tmQ, bar(AB_QF + s), c * 64, sl.row_q + q0, zq);
+          bulk_load(smem_u32(rowbuf) + s * C::STAT_BYTES, p.stats + stat_index(zq, p.S_pad, sl.stat_row + q0),
                     C::STAT_BYTES, bar(AB_QF + s));
           mbar_arrive_expect_tx(bar(AB_DOF + s), C::DO_BYTES);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sdO + s * C::DO_BYTES + c * BM * 128, &tmdO, bar(AB_DOF + s), c * 64, q0, bh);
+            tma_load_3d(sdO + s * C::DO_BYTES + c * BM * 128, &tmdO, bar(AB_DOF + s), c * 64, sl.row_q + q0, zq);
         }
         issued = i + 1;
       }
@@ -330,7 +341,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     const int hf = t >> 7;    // query-column group
     const int kv = k0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const bool kv_ok = kv < p.S_kv;
+    const bool kv_ok = kv < S_kv;
     // This thread's 32 query columns lie in one 64-row block of the statistics
     // slot: 64 values -LSE*log2e (-inf for rows without keys), then 64 -D.
     const int stat_off = ((CW * hf) / 64) * 128 + (CW * hf) % 64;
@@ -413,11 +424,11 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         }
         tc_fence_before();
         mbar_arrive(bar(AB_SFREE));  // S^T(i) is in registers: S^T(i+1) may overwrite it
-        const bool need_mask = (p.causal && qc0 < k0 + C::BN - 1) || (qc0 + CW > p.S_q) || !kv_ok;
+        const bool need_mask = (p.causal && qc0 < k0 + C::BN - 1) || (qc0 + CW > S_q) || !kv_ok;
         if (need_mask) {
           // visible iff the key exists, the query exists and (causal) key <= query
           const int first = p.causal ? kv - qc0 : 0;  // first visible local column
-          const int lim = kv_ok ? min(CW, p.S_q - qc0) : 0;
+          const int lim = kv_ok ? min(CW, S_q - qc0) : 0;
 #pragma unroll
           for (int c = 0; c < CW; ++c)
             if (c < first || c >= lim) pr[c] = SDPA_NEG_INF;
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     const bool ready = have && ok && mbar_wait(bar(AB_DKDV), 0, ec, kSiteBwdCompute);
     if (!have || ready) {
       if (ready) tc_fence_after();
-      const size_t rowi = static_cast<size_t>(bhk) * p.S_kv + (kv_ok ? kv : 0);
+      const size_t rowi = static_cast<size_t>(*key_row0) + (kv_ok ? row : 0);
       auto write_rows = [&](auto width_tag, uint32_t tcol, void* base, float mul) {
         constexpr int W = decltype(width_tag)::value;
         uint8_t* dst_row = static_cast<uint8_t*>(base) + rowi * W * 2;

@@ -106,11 +106,28 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   const int n_qt = (p.S_q + BM - 1) / BM;
   const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_qt, 1);
   const int b = qtile.b, h = qtile.h, qt = qtile.qt;
-  const int bh = b * p.H + h;
-  const int bhk = b * p.H_kv + h / (p.H / p.H_kv);  // K/V head of this query head
+  const int bh = b * p.H + h;  // (batch entry or sequence, head): the dropout index
+  const SeqSlice sl = seq_slice(p.seqstart_q, p.seqstart_k, p.rows_q, p.rows_k, p.S_q, p.S_kv, p.H,
+                                p.H_kv, b);
+  const int S_q = sl.len_q, S_kv = sl.len_k;  // this sequence's lengths
+  const int zq = sl.zq0 + h;                  // tensor-map z of the query head
+  const int zk = sl.zk0 + h / (p.H / p.H_kv);  // and of its K/V head
   const int q0 = qt * BM;
-  const int n_kv_all = (p.S_kv + BN - 1) / BN;
+  const int n_kv_all = (S_kv + BN - 1) / BN;
   const int n_kv = p.causal ? min(n_kv_all, (q0 + BM - 1) / BN + 1) : n_kv_all;
+  // Packed sequences only (uniform over the CTA): a tile past the end of a
+  // shorter sequence has nothing to do, and a sequence without keys has dQ = 0.
+  if (q0 >= S_q) return;
+  if (n_kv == 0) {
+    const int row = q0 + static_cast<int>(threadIdx.x);
+    if (threadIdx.x < BM && row < S_q) {
+      const size_t ri = static_cast<size_t>(zq) * p.rows_q + sl.row_q + row;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dq) + ri * DQK * 2);
+#pragma unroll
+      for (int v = 0; v < DQK / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
   // Iteration j visits key tile n_kv - 1 - j: the CTAs of one head, resident
   // together, then start on different tiles (their own diagonal) instead of
   // all requesting tile 0 from L2 at once.
@@ -146,9 +163,9 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(QB_Q), C::Q_BYTES + C::DO_BYTES);
 #pragma unroll
-      for (int c = 0; c < DQK / 64; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, bar(QB_Q), c * 64, q0, bh);
+      for (int c = 0; c < DQK / 64; ++c) tma_load_3d(sQ + c * BM * 128, &tmQ, bar(QB_Q), c * 64, sl.row_q + q0, zq);
 #pragma unroll
-      for (int c = 0; c < DV / 64; ++c) tma_load_3d(sdO + c * BM * 128, &tmdO, bar(QB_Q), c * 64, q0, bh);
+      for (int c = 0; c < DV / 64; ++c) tma_load_3d(sdO + c * BM * 128, &tmdO, bar(QB_Q), c * 64, sl.row_q + q0, zq);
     }
     for (int j = 0; j < n_kv; ++j) {
       const int s = j % ST;
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_KF + s), C::K_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, (n_kv - 1 - j) * BN, bhk);
+          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, sl.row_k + (n_kv - 1 - j) * BN, zk);
       }
       if (!mbar_wait(bar(QB_VE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) {
         issued = 2 * j + 1;
@@ -168,7 +185,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_VF + s), C::V_BYTES);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, (n_kv - 1 - j) * BN, bhk);
+          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, sl.row_k + (n_kv - 1 - j) * BN, zk);
       }
       issued = 2 * j + 2;
     }
@@ -309,12 +326,12 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     const int row = t & 127;  // query row within the tile = TMEM lane
     const int hf = t >> 7;    // key-column half
     const int qr = q0 + row;
-    const bool row_ok = qr < p.S_q;
+    const bool row_ok = qr < S_q;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const size_t ridx = static_cast<size_t>(bh) * p.S_q + (row_ok ? qr : 0);
+    const size_t ridx = static_cast<size_t>(zq) * p.rows_q + sl.row_q + (row_ok ? qr : 0);
     // -LSE*log2e and D of this row (-inf and 0 past S_q: the tile never
     // reaches beyond the statistics' padding to 128 rows)
-    const size_t sidx = stat_index(static_cast<size_t>(bh), p.S_pad, qr);
+    const size_t sidx = stat_index(static_cast<size_t>(zq), p.S_pad, sl.stat_row + qr);
     const float nl2 = p.stats[sidx];
     const float nDrow = p.stats[sidx + 64];  // -D
     const float* bias_row =
@@ -393,9 +410,9 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(QB_SFREE));
-      const bool need_mask = (kc0 + CW > p.S_kv) || (p.causal && kc0 + CW - 1 > q0) || !row_ok;
+      const bool need_mask = (kc0 + CW > S_kv) || (p.causal && kc0 + CW - 1 > q0) || !row_ok;
       if (need_mask) {
-        const int last = row_ok ? (p.causal ? min(p.S_kv - 1, qr) : p.S_kv - 1) : -1;
+        const int last = row_ok ? (p.causal ? min(S_kv - 1, qr) : S_kv - 1) : -1;
 #pragma unroll
         for (int c = 0; c < CW; ++c)
           if (kc0 + c > last) pr[c] = SDPA_NEG_INF;

@@ -38,6 +38,14 @@ struct FwdParams {
   void* o;                 // [B, H, S_q, D_v] io dtype
   float* lse;              // [B, H, S_q] natural-log logsumexp
   uint32_t* err;           // device error word
+  // Packed sequences (both null in batch mode): sequence b owns rows
+  // [seqstart_q[b], seqstart_q[b+1]) of every query head of Q, O and LSE and
+  // rows [seqstart_k[b], seqstart_k[b+1]) of every K/V head of K and V. B is
+  // then the number of sequences and S_q / S_kv the longest lengths, which
+  // size the grid and stride the dropout index (see SeqSlice).
+  const int* seqstart_q;
+  const int* seqstart_k;
+  int rows_q, rows_k;      // rows per head of the tensors: S_q / S_kv, or the packed totals
   // Test hook (sdpa_debug_fault): 1 = the producer issues no K/V loads, so
   // the MMA issuer's bounded wait runs out; wait_ns = limit of every wait.
   uint32_t fault;
@@ -54,6 +62,45 @@ __host__ __device__ __forceinline__ size_t stat_index(size_t bh, int S_pad, int 
   return (bh * static_cast<size_t>(S_pad) + static_cast<size_t>(q & ~63)) * 2 + static_cast<size_t>(q & 63);
 }
 __host__ __device__ __forceinline__ int stat_pad(int S_q) { return (S_q + 127) & ~127; }
+
+// Packed sequences: the statistics of head z hold one block per sequence,
+// sequence b's at row packed_stat_row(start_b, b) (start_b its first packed
+// query row), padded to a multiple of 128 rows. start rounded up to 64 plus
+// 192 per earlier sequence keeps the blocks disjoint (the next block begins at
+// least len_b + 129 rows later) without a prefix sum, and packed_stat_pad
+// rows per head hold them all for any start_b + len_b <= rows.
+__host__ __device__ __forceinline__ int packed_stat_row(int start, int b) {
+  return ((start + 63) & ~63) + 192 * b;
+}
+__host__ __device__ __forceinline__ int64_t packed_stat_pad(int64_t rows, int64_t n_seq) {
+  return ((rows + 63) & ~int64_t{63}) + 192 * n_seq + 128;
+}
+
+// First row and length of packed sequence b, clamped so that any contents of
+// seqstart stay inside [0, rows) and the length inside [0, max_len].
+__device__ __forceinline__ int2 packed_rows(const int* seqstart, int rows, int max_len, int b) {
+  const int s0 = min(max(__ldg(seqstart + b), 0), rows);
+  const int s1 = min(max(__ldg(seqstart + b + 1), s0), rows);
+  return make_int2(s0, min(s1 - s0, max_len));
+}
+
+// What one (sequence or batch entry) b of a call covers: its lengths, the
+// packed rows of its first query and key, the tensor-map z of its query head
+// 0 and K/V head 0 (z of head h = zq0 + h), and its first statistics row.
+// In batch mode the rows of (b, h) form z = b * H + h; packed, z is the head.
+struct SeqSlice {
+  int len_q, len_k;
+  int row_q, row_k;
+  int zq0, zk0;
+  int stat_row;
+};
+__device__ __forceinline__ SeqSlice seq_slice(const int* seqstart_q, const int* seqstart_k, int rows_q,
+                                              int rows_k, int S_q, int S_kv, int H, int H_kv, int b) {
+  if (seqstart_q == nullptr) return SeqSlice{S_q, S_kv, 0, 0, b * H, b * H_kv, 0};
+  const int2 q = packed_rows(seqstart_q, rows_q, S_q, b);
+  const int2 k = packed_rows(seqstart_k, rows_k, S_kv, b);
+  return SeqSlice{q.y, k.y, q.x, k.x, 0, 0, packed_stat_row(q.x, b)};
+}
 
 // Order of the query tiles of the query-stationary kernels (forward, dQ):
 // heads in groups of G, the largest divisor of H not above gmax, one group
@@ -93,6 +140,9 @@ struct BwdParams {
   void* dk;                // [B, H, S_kv, D_qk]
   void* dv;                // [B, H, S_kv, D_v]
   uint32_t* err;
+  const int* seqstart_q;   // packed sequences, as in FwdParams (null in batch mode)
+  const int* seqstart_k;
+  int rows_q, rows_k;
 };
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -243,7 +293,8 @@ cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CU
                                const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
                                cudaStream_t st);
 cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
-                           float* dbias, int64_t bh, int s_q, int d_v, int64_t dbias_elems,
+                           float* dbias, int64_t z_count, int s_q, int s_pad, int rows,
+                           const int* seqstart, int n_seq, int d_v, int64_t dbias_elems,
                            cudaStream_t st);
 cudaError_t launch_dropout_mask(int64_t total, uint32_t threshold, uint32_t seed_lo,
                                 uint32_t seed_hi, uint32_t off_lo, uint32_t off_hi,

@@ -95,15 +95,28 @@ __global__ void __launch_bounds__(384, 1)
   const int n_pairs = (n_qt + 1) / 2;
   const QueryTile qtile = query_tile_order(static_cast<int>(blockIdx.x), p.B, p.H, n_pairs, 8);
   const int b = qtile.b, h = qtile.h;
-  const int bh = b * p.H + h;
-  const int bhk = b * p.H_kv + h / (p.H / p.H_kv);  // K/V head of this query head
-  const int q0 = qtile.qt * 2 * C::BM;  // first row of query tile 0
-  const int n_kv_all = (p.S_kv + C::BN - 1) / C::BN;
+  const int bh = b * p.H + h;  // (batch entry or sequence, head): the dropout index
+  const SeqSlice sl = seq_slice(p.seqstart_q, p.seqstart_k, p.rows_q, p.rows_k, p.S_q, p.S_kv, p.H,
+                                p.H_kv, b);
+  const int S_q = sl.len_q, S_kv = sl.len_k;  // this sequence's lengths
+  const int zq = sl.zq0 + h;                  // tensor-map z of the query head
+  const int zk = sl.zk0 + h / (p.H / p.H_kv);  // and of its K/V head
+  // Pairs of query tiles: (0,1), (2,3), ... when the sequence has an even
+  // number of tiles; with an odd number, tile 0 goes alone and the pairs are
+  // (1,2), (3,4), ..., so the tile without a partner (which runs without the
+  // other softmax group to overlap it) is the one with the fewest causal key
+  // tiles, not the diagonal-most one that would end the grid.
+  const int n_qt_seq = (S_q + C::BM - 1) / C::BM;
+  const bool odd = (n_qt_seq & 1) != 0;
+  const bool lone = odd && qtile.qt == 0;
+  const int q0 = (odd ? max(2 * qtile.qt - 1, 0) : 2 * qtile.qt) * C::BM;  // first row of tile 0
+  const int n_kv_all = (S_kv + C::BN - 1) / C::BN;
   // key tiles query tile t sees (0 when the tile lies past S_q)
   auto tile_kv = [&](int t) -> int {
+    if (t == 1 && lone) return 0;
     const int qs = q0 + t * C::BM;
-    if (qs >= p.S_q) return 0;
-    return p.causal ? min(n_kv_all, (min(qs + C::BM, p.S_q) - 1) / C::BN + 1) : n_kv_all;
+    if (qs >= S_q) return 0;
+    return p.causal ? min(n_kv_all, (min(qs + C::BM, S_q) - 1) / C::BN + 1) : n_kv_all;
   };
   const int n_kv0 = tile_kv(0), n_kv1 = tile_kv(1);
   const int n_it = max(n_kv0, n_kv1);
@@ -111,6 +124,21 @@ __global__ void __launch_bounds__(384, 1)
   // tile t takes part in iterations j >= n_it - n_kv_t.
   const int j0_0 = n_it - n_kv0, j0_1 = n_it - n_kv1;
   const bool has1 = n_kv1 > 0;
+
+  // Nothing to compute (packed sequences only: a pair past the end of a
+  // shorter sequence, or a sequence without keys, whose rows get O = 0 and
+  // LSE = -inf as any query row that sees no key). Uniform over the CTA.
+  if (n_it == 0) {
+    const int row = q0 + static_cast<int>(threadIdx.x);
+    if (threadIdx.x < (lone ? 1 : 2) * C::BM && row < S_q) {
+      const size_t ri = static_cast<size_t>(zq) * p.rows_q + sl.row_q + row;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + ri * DV * 2);
+#pragma unroll
+      for (int v = 0; v < DV / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+      p.lse[ri] = SDPA_NEG_INF;
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < FB_COUNT; ++i) mbar_init(bar(i), (i == FB_P || i == FB_P + 1) ? 128u : 1u);
@@ -141,22 +169,22 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_expect_tx(bar(FB_Q), (has1 ? 2 : 1) * C::Q_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c) {
-          tma_load_3d(sQ + c * C::BM * 128, &tmQ, bar(FB_Q), c * 64, q0, bh);
+          tma_load_3d(sQ + c * C::BM * 128, &tmQ, bar(FB_Q), c * 64, sl.row_q + q0, zq);
           if (has1)
-            tma_load_3d(sQ + C::Q_BYTES + c * C::BM * 128, &tmQ, bar(FB_Q), c * 64, q0 + C::BM, bh);
+            tma_load_3d(sQ + C::Q_BYTES + c * C::BM * 128, &tmQ, bar(FB_Q), c * 64, sl.row_q + q0 + C::BM, zq);
         }
       }
       for (int j = 0; j < n_it; ++j) {
         const int s = j % ST;
         const uint32_t ph = (j / ST) & 1;
-        const int kv0 = (n_it - 1 - j) * C::BN;
+        const int kv0 = sl.row_k + (n_it - 1 - j) * C::BN;
         if (!mbar_wait(bar(FB_KE + s), ph ^ 1, ec, kSiteFwdLoad, true, true)) break;
         if (p.fault == 1) break;  // test hook: K/V never arrive
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(FB_KF + s), C::K_BYTES);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64, kv0, bhk);
+            tma_load_3d(sK + s * C::K_BYTES + c * C::BN * 128, &tmK, bar(FB_KF + s), c * 64, kv0, zk);
         }
         if (!mbar_wait(bar(FB_VE + s), ph ^ 1, ec, kSiteFwdLoad, true, true)) {
           issued = 2 * j + 1;
@@ -166,7 +194,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(bar(FB_VF + s), C::V_BYTES);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sV + s * C::V_BYTES + c * C::BN * 128, &tmV, bar(FB_VF + s), c * 64, kv0, bhk);
+            tma_load_3d(sV + s * C::V_BYTES + c * C::BN * 128, &tmV, bar(FB_VF + s), c * 64, kv0, zk);
         }
         issued = 2 * j + 2;
       }
@@ -262,7 +290,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + C::T_S + 128 * t, tO = tbase + C::T_O + DV * t;
     const float sl2 = p.scale_log2;
-    const bool row_ok = row < p.S_q;
+    const bool row_ok = row < S_q;
     const float* bias_row = (GENERAL && p.bias != nullptr && row_ok)
                                 ? p.bias + (static_cast<size_t>(h) * p.S_q + row) * p.S_kv
                                 : nullptr;
@@ -312,9 +340,9 @@ __global__ void __launch_bounds__(384, 1)
           x[q * 32 + 2 * i + 1] = v.y;
         }
       }
-      const bool need_mask = (k0 + C::BN > p.S_kv) || (p.causal && k0 + C::BN - 1 > qt0);
+      const bool need_mask = (k0 + C::BN > S_kv) || (p.causal && k0 + C::BN - 1 > qt0);
       if (need_mask) {
-        const int lim = p.causal ? min(p.S_kv - 1, row) : p.S_kv - 1;  // last visible key
+        const int lim = p.causal ? min(S_kv - 1, row) : S_kv - 1;  // last visible key
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (k0 + i > lim) x[i] = SDPA_NEG_INF;
@@ -392,8 +420,8 @@ __global__ void __launch_bounds__(384, 1)
     if (n_kv > 0 && ok && mbar_wait(bar(FB_O + t), 0, ec, kSiteFwdSoftmax)) {
       tc_fence_after();
       const float inv = (l > 0.f) ? ((GENERAL && p.dropout) ? p.keep_scale : 1.0f) / l : 0.f;
-      uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                      (static_cast<size_t>(bh) * p.S_q + (row_ok ? row : 0)) * DV * 2;
+      const size_t ri = static_cast<size_t>(zq) * p.rows_q + sl.row_q + (row_ok ? row : 0);
+      uint8_t* orow = static_cast<uint8_t*>(p.o) + ri * DV * 2;
 #pragma unroll
       for (int q = 0; q < DV / 32; ++q) {
         uint32_t rr[32];
@@ -411,7 +439,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (row_ok)
-        p.lse[static_cast<size_t>(bh) * p.S_q + row] = (l > 0.f) ? fmaf(m, kLn2, __logf(l)) : SDPA_NEG_INF;
+        p.lse[ri] = (l > 0.f) ? fmaf(m, kLn2, __logf(l)) : SDPA_NEG_INF;
     }
   }
 

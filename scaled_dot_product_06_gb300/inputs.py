@@ -54,3 +54,27 @@ def make_inputs(shape: Shape, dtype: str = "bf16", with_bias: bool = False,
     if with_bias:
         out["bias"] = 0.5 * _randn((1, s.H, s.S_q, s.S_kv), 5 + seed_base, device)
     return out
+
+
+def packed_lengths(n: int, lo: int, hi: int, seed: int) -> list[int]:
+    """n sequence lengths drawn uniformly from [lo, hi] by a seeded generator."""
+    g = torch.Generator().manual_seed(seed)
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g)]
+
+
+def seqstarts(lengths) -> list[int]:
+    """Row offsets of packed sequences: 0, then the running sums of the lengths."""
+    out = [0]
+    for n in lengths:
+        out.append(out[-1] + int(n))
+    return out
+
+
+def make_packed_inputs(H: int, total_q: int, total_k: int, D_qk: int, D_v: int,
+                       dtype: str = "bf16", H_kv: int = 0, seed_base: int = 0,
+                       device="cpu") -> dict:
+    """Packed-sequence tensors: q, do [H, total_q, D] and k, v [H_kv, total_k, D]
+    (the batch-mode draws of one batch entry with total rows)."""
+    x = make_inputs(Shape(1, H, total_q, total_k, D_qk, D_v, H_kv), dtype, seed_base=seed_base,
+                    device=device)
+    return {n: x[n][0] for n in ("q", "k", "v", "do")}

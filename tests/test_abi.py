@@ -131,3 +131,45 @@ def test_grouped_kv_heads_validated_before_any_device_work(lib):
     st = lib.sdpa_bwd_phases_gqa(7, 1, 6, 4, 64, 64, 64, 64, 0.125, 0, 0.0, 0, 0, 0, P, P, P, None,
                                  P, P, P, P, P, P, None, ws, 1 << 20, None)
     assert st == _native.SDPA_ERR_INVALID_ARG
+
+
+def test_varlen_workspace_size(lib):
+    # per head: total_q rounded up to 64, 192 rows per sequence and 128 rows of
+    # slack, two floats each, the whole rounded up to 256 bytes
+    def expect(b, h, total_q):
+        rows = ((total_q + 63) // 64) * 64 + 192 * b + 128
+        return (h * rows * 8 + 255) // 256 * 256
+    for b, h, tq in ((1, 1, 1), (3, 4, 1000), (16, 32, 65536), (0, 2, 0)):
+        assert lib.sdpa_bwd_varlen_workspace_size(b, h, tq) == expect(b, h, tq)
+    assert lib.sdpa_bwd_varlen_workspace_size(-1, 2, 10) == 0
+    assert lib.sdpa_bwd_varlen_workspace_size(2, 2, -10) == 0
+
+
+def test_varlen_arguments_validated_before_any_device_work(lib):
+    P = ctypes.c_void_p(16)  # never dereferenced: the calls fail validation first
+    S = ctypes.c_void_p(64)  # a 4-byte-aligned "seqstart"
+
+    def fwd(b=2, h=4, h_kv=4, tq=100, tk=100, mq=64, mk=64, d=64, p=0.0, sq=S, sk=S):
+        return lib.sdpa_fwd_varlen(b, h, h_kv, tq, tk, mq, mk, d, d, 0.125, 1, p, 0, 0, 0, sq, sk,
+                                   P, P, P, P, P, None)
+    assert fwd(sq=None) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(sk=None) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(sq=None, sk=None, tq=0) == _native.SDPA_OK          # empty: a no-op
+    assert fwd(tk=0) == _native.SDPA_OK
+    assert fwd(mq=0) == _native.SDPA_OK
+    assert fwd(sq=ctypes.c_void_p(66)) == _native.SDPA_ERR_MISALIGNED
+    assert fwd(h_kv=3) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(d=96) == _native.SDPA_ERR_UNSUPPORTED
+    assert fwd(p=0.1, mk=66) == _native.SDPA_ERR_UNSUPPORTED        # max_seqlen_k % 4 with dropout
+    assert fwd(tq=-1) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(tq=1 << 40) == _native.SDPA_ERR_UNSUPPORTED
+
+    def bwd(ws_bytes, b=2, h=4, tq=100):
+        return lib.sdpa_bwd_phases_varlen(7, b, h, h, tq, 100, 64, 64, 64, 64, 0.125, 1, 0.0, 0, 0,
+                                          0, S, S, P, P, P, P, P, P, P, P, P, ctypes.c_void_p(256),
+                                          ws_bytes, None)
+    need = lib.sdpa_bwd_varlen_workspace_size(2, 4, 100)
+    assert bwd(need - 1) == _native.SDPA_ERR_WORKSPACE
+    assert lib.sdpa_bwd_phases_varlen(8, 2, 4, 4, 100, 100, 64, 64, 64, 64, 0.125, 1, 0.0, 0, 0, 0,
+                                      S, S, P, P, P, P, P, P, P, P, P, ctypes.c_void_p(256), need,
+                                      None) == _native.SDPA_ERR_INVALID_ARG   # unknown phase bit
