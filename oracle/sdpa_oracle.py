@@ -17,6 +17,12 @@ Readings taken where the pages are silent (each is listed in the design doc):
 * The saved statistic is the natural-log logsumexp of the scaled, biased,
   masked scores, taken before dropout: LSE_i = m_i + ln(sum_j exp(s_ij - m_i)).
 * Causal masking is top-left aligned: key j is visible to query i iff j <= i.
+* Local windows and the bottom-right alignment follow the parameters of CK
+  tile fmha_bwd_kernel.hpp's mask arguments (window_size_left,
+  window_size_right, mask_type top-left or bottom-right): with
+  off = S_kv - S_q for bottom-right and 0 for top-left, key j is visible to
+  query i iff i + off - left <= j <= i + off + right, a negative size leaving
+  that side unbounded. Causal is the window (-1, 0); no mask is (-1, -1).
 * A row with no visible key (possible only through a -inf bias) has P = 0,
   O = 0, LSE = -inf and contributes nothing to any gradient.
 * Dropout multiplies P by Z = keep / (1 - p) before the product with V; the
@@ -58,6 +64,10 @@ class Problem:
     seed: int = 0
     offset: int = 0
     H_kv: int = 0  # K/V heads; 0 means H (no grouping)
+    # Local window (left, right) around the aligned diagonal, a negative size
+    # unbounded; None means (-1, 0) when is_causal, else (-1, -1).
+    window: tuple | None = None
+    bottom_right: bool = False  # diagonal through (S_q - 1, S_kv - 1), not (0, 0)
     # Index space of the dropout bits: (B', S_q', S_kv', b0) makes element
     # (b, h, i, j) draw the bit of element (b0 + b, h, i, j) of a
     # [B', H, S_q', S_kv'] problem (a packed sequence draws from the padded
@@ -79,6 +89,19 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
+def visible(prob: Problem, rows: np.ndarray, cols: np.ndarray) -> np.ndarray:
+    """Boolean [len(rows), len(cols)]: key j visible to query i (module text)."""
+    left, right = prob.window if prob.window is not None else (-1, 0 if prob.is_causal else -1)
+    off = prob.S_kv - prob.S_q if prob.bottom_right else 0
+    d = np.asarray(cols)[None, :] - np.asarray(rows)[:, None] - off  # offset from the diagonal
+    vis = np.ones(d.shape, dtype=bool)
+    if left >= 0:
+        vis &= d >= -left
+    if right >= 0:
+        vis &= d <= right
+    return vis
+
+
 def scores(prob: Problem, q_h: np.ndarray, k_h: np.ndarray, bias_h, rows: np.ndarray,
            cols: np.ndarray) -> np.ndarray:
     """S'' = (Q K^T) * scale + Bias on the (rows, cols) block, -inf where masked.
@@ -88,8 +111,7 @@ def scores(prob: Problem, q_h: np.ndarray, k_h: np.ndarray, bias_h, rows: np.nda
     s = prob.scale * (q_h[rows] @ k_h[cols].T)
     if bias_h is not None:
         s = s + bias_h[np.ix_(rows, cols)]
-    if prob.is_causal:
-        s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
+    s = np.where(visible(prob, rows, cols), s, -np.inf)
     return s
 
 

@@ -18,7 +18,8 @@ Layout (the batch-mode BHSD with the batch folded into the rows): q, do
 Readings where the pages are silent (each is listed in the design doc):
 
 * The causal mask is top-left within each sequence (local key j visible to
-  local query i iff j <= i), as in batch mode.
+  local query i iff j <= i), as in batch mode; windows and the bottom-right
+  alignment likewise use each sequence's own lengths.
 * A query row whose sequence has no key gets O = 0, LSE = -inf and dQ = 0;
   a key whose sequence has no query gets dK = dV = 0 (the batch-mode rule for
   a row that sees no key, and an empty sum).
@@ -53,6 +54,8 @@ class Packed:
     H_kv: int = 0
     max_seqlen_q: int = 0  # 0: the longest sequence
     max_seqlen_k: int = 0
+    window: tuple | None = None  # as in sdpa_oracle.Problem, per sequence
+    bottom_right: bool = False
 
     @property
     def B(self) -> int:
@@ -75,8 +78,8 @@ class Packed:
         lq, lk = self.lens(i)
         mq, mk = self.frame()
         return so.Problem(1, self.H, lq, lk, self.D_qk, self.D_v, self.scale, self.is_causal,
-                          self.dropout_p, self.seed, self.offset, self.H_kv,
-                          drop_frame=(self.B, mq, mk, i))
+                          self.dropout_p, self.seed, self.offset, self.H_kv, self.window,
+                          self.bottom_right, drop_frame=(self.B, mq, mk, i))
 
 
 def _rows(x, a: int, b: int):
