@@ -50,6 +50,10 @@ WORKLOADS = {
     "b1h32kv4-s16384-d128-causal": dict(B=1, H=32, H_kv=4, S_q=16384, S_kv=16384, D_qk=128,
                                         D_v=128, dtype="bf16", causal=True, bias=False, p=0.0,
                                         scale=None),
+    # a sliding window of 4096 keys back (local attention) at the long-context size
+    "b1h32-s16384-d128-window4096": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
+                                         dtype="bf16", causal=True, window=(4096, 0),
+                                         bottom_right=False, bias=False, p=0.0, scale=None),
     # packed variable-length sequences (group mode): 16 sequences of 512..8192
     # tokens (seeded; 74,372 in all), 32 heads, d 128, causal
     "varlen16-h32-d128-causal": dict(lengths=dict(n=16, lo=512, hi=8192, seed=2024), H=32,
@@ -87,11 +91,28 @@ def resolve(w: dict) -> dict:
     return dict(w, lens=lens, B=len(lens), S_q=max(lens), S_kv=max(lens))
 
 
+def visible_pairs(S_q: int, S_kv: int, window, bottom_right: bool) -> int:
+    """Number of (query, key) pairs a local window leaves visible."""
+    import numpy as np
+    left, right = window
+    off = S_kv - S_q if bottom_right else 0
+    i = np.arange(S_q, dtype=np.int64)
+    lo = np.maximum(i + off - left, 0) if left >= 0 else np.zeros_like(i)
+    hi = np.minimum(i + off + right, S_kv - 1) if right >= 0 else np.full_like(i, S_kv - 1)
+    return int(np.maximum(hi - lo + 1, 0).sum())
+
+
 def fwd_flops(w: dict) -> float:
-    """Forward FLOPs by the convention; a packed workload sums its sequences."""
+    """Forward FLOPs by the convention; a packed workload sums its sequences; a
+    windowed one counts its visible pairs, 2 (D_qk + D_v) FLOPs each (the
+    convention's causal half, S^2 / 2 pairs, is the same count for a causal
+    mask)."""
     if w.get("lens"):
         one = {k: v for k, v in w.items() if k != "lens"}
         return sum(fwd_flops(dict(one, B=1, S_q=n, S_kv=n)) for n in w["lens"])
+    if w.get("window") is not None:
+        pairs = visible_pairs(w["S_q"], w["S_kv"], w["window"], w.get("bottom_right", False))
+        return 2.0 * w["B"] * w["H"] * pairs * (w["D_qk"] + w["D_v"])
     f = 4.0 * w["B"] * w["H"] * w["S_q"] * w["S_kv"] * (w["D_qk"] + w["D_v"]) / 2.0
     return f / 2.0 if w["causal"] else f
 
@@ -176,7 +197,8 @@ def oracle_sample(w: dict, s_sample: int) -> tuple[float, float]:
     x = make_inputs(shp, w["dtype"], with_bias=w["bias"])
     scale = w["scale"] if w["scale"] is not None else 1.0 / math.sqrt(w["D_qk"])
     pr = oracle.Problem(1, 1, s_q, s_kv, w["D_qk"], w["D_v"], scale, w["causal"], w["p"],
-                        DROP_SEED, DROP_OFFSET)
+                        DROP_SEED, DROP_OFFSET, window=w.get("window"),
+                        bottom_right=w.get("bottom_right", False))
     t0 = time.perf_counter()
     oracle.forward(pr, x["q"], x["k"], x["v"], x["bias"])
     oracle.backward(pr, x["q"], x["k"], x["v"], x["do"], x["bias"])
@@ -292,6 +314,8 @@ def main():
     scale = w["scale"] if w["scale"] is not None else 1.0 / math.sqrt(w["D_qk"])
     kw = dict(scale=scale, is_causal=w["causal"], dropout_p=w["p"], seed=DROP_SEED,
               offset=DROP_OFFSET)
+    if w.get("window") is not None or w.get("bottom_right"):
+        kw.update(window=w.get("window"), bottom_right=w.get("bottom_right", False))
     packed = "lens" in w
     if packed:
         # [H, total, D] tensors; sequence i owns rows seqstart[i] .. seqstart[i+1]-1
@@ -492,6 +516,8 @@ def main():
                        **({"packed_lengths": w["lens"], "total_tokens": sum(w["lens"])}
                           if packed else {}),
                        "causal": w["causal"], "bias": w["bias"], "dropout_p": w["p"],
+                       **({"window": list(w["window"]), "bottom_right": w.get("bottom_right", False)}
+                          if w.get("window") is not None else {}),
                        "l2": "inputs larger than L2, no flush",
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "pct_of_peak": 100.0 * value / world / peak,

@@ -108,7 +108,9 @@ bool head_sizes_ok(int64_t d_qk, int64_t d_v) {
   return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128);
 }
 
-constexpr int64_t kMaxSeq = (int64_t{1} << 31) - 256;
+// Sequence lengths (and packed totals) below 2^29 keep every sum of a row or
+// key index with a window offset inside an int on the device.
+constexpr int64_t kMaxSeq = (int64_t{1} << 29) - 256;
 
 // Checks shared by fwd and bwd that need no pointer. Sets *empty for a
 // zero-sized problem.
@@ -167,6 +169,26 @@ cudaError_t prepare_kernel(const void* kern, int smem, int regs) {
 
 namespace {
 
+// Visible keys: key j visible to query i iff i + off - left <= j <= i + off + right,
+// off = s_kv - s_q when bottom_right, else 0; a negative size is unbounded.
+struct Mask {
+  int64_t left, right;
+  int bottom_right;
+};
+Mask causal_mask(int is_causal) { return Mask{-1, is_causal ? 0 : -1, 0}; }
+
+// A window size of s_q + s_kv or more admits every key on that side: it is
+// stored as unbounded, which keeps the device arithmetic in range.
+// general = 0 for the plain kernels' cases (top-left, causal or unmasked).
+void set_window(const Mask& mk, int64_t s_q, int64_t s_kv, int* left, int* right, int* br,
+                int* general) {
+  auto norm = [&](int64_t w) { return (w < 0 || w >= s_q + s_kv) ? -1 : static_cast<int>(w); };
+  *left = norm(mk.left);
+  *right = norm(mk.right);
+  *br = mk.bottom_right ? 1 : 0;
+  *general = (*left >= 0 || *right > 0 || *br) ? 1 : 0;
+}
+
 // Packed-sequence arguments of the varlen entry points; seqstart_q null means
 // batch mode (rows of (b, h) contiguous, s_q / s_kv of them).
 struct Packing {
@@ -207,7 +229,7 @@ sdpa_status_t check_packing(const Packing& pk, int64_t b, const float* bias, boo
 }
 
 sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv, int64_t d_qk,
-                       int64_t d_v, float scale, int is_causal, float dropout_p, uint64_t seed,
+                       int64_t d_v, float scale, const Mask& mask, float dropout_p, uint64_t seed,
                        uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                        const void* v, const float* bias, void* o, float* lse, void* stream,
                        const Packing& pk) {
@@ -236,7 +258,7 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
   p.S_q = static_cast<int>(s_q);
   p.S_kv = static_cast<int>(s_kv);
   p.scale_log2 = scale * kLog2e;
-  p.causal = is_causal ? 1 : 0;
+  set_window(mask, s_q, s_kv, &p.win_left, &p.win_right, &p.win_br, &p.win_general);
   p.bias = bias;
   p.dropout = dropout_p > 0.0f ? 1 : 0;
   p.drop_threshold = drop_threshold(dropout_p);
@@ -263,7 +285,7 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
 
 
 sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
-                       int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
+                       int64_t d_qk, int64_t d_v, float scale, const Mask& mask, float dropout_p,
                        uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
                        const void* k, const void* v, const float* bias, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -300,7 +322,7 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   p.S_kv = static_cast<int>(s_kv);
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
-  p.causal = is_causal ? 1 : 0;
+  set_window(mask, s_q, s_kv, &p.win_left, &p.win_right, &p.win_br, &p.win_general);
   p.bias = bias;
   p.dbias = dbias;
   p.dropout = dropout_p > 0.0f ? 1 : 0;
@@ -396,8 +418,8 @@ sdpa_status_t sdpa_fwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int6
                            uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,
                            const void* k, const void* v, const float* bias, void* o, float* lse,
                            void* stream) {
-  return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed, offset, dtype,
-                  q, k, v, bias, o, lse, stream, Packing{});
+  return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, causal_mask(is_causal), dropout_p, seed,
+                  offset, dtype, q, k, v, bias, o, lse, stream, Packing{});
 }
 
 sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
@@ -407,9 +429,9 @@ sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv
                                   const float* bias, const void* o, const void* dout,
                                   const float* lse, void* dq, void* dk, void* dv, float* dbias,
                                   void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_impl(phases, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed, offset,
-                  dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias, workspace, workspace_bytes,
-                  stream, Packing{});
+  return bwd_impl(phases, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, causal_mask(is_causal), dropout_p,
+                  seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias, workspace,
+                  workspace_bytes, stream, Packing{});
 }
 
 // Packed sequences: b sequences, the i-th owning packed rows
@@ -433,8 +455,8 @@ sdpa_status_t sdpa_fwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_
     if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
     return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
-  return fwd_impl(b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale, is_causal, dropout_p, seed,
-                  offset, dtype, q, k, v, nullptr, o, lse, stream, pk);
+  return fwd_impl(b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale, causal_mask(is_causal),
+                  dropout_p, seed, offset, dtype, q, k, v, nullptr, o, lse, stream, pk);
 }
 
 sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
@@ -451,9 +473,9 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
     if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
     return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
-  return bwd_impl(phases, b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale, is_causal,
-                  dropout_p, seed, offset, dtype, q, k, v, nullptr, o, dout, lse, dq, dk, dv, nullptr,
-                  workspace, workspace_bytes, stream, pk);
+  return bwd_impl(phases, b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
+                  causal_mask(is_causal), dropout_p, seed, offset, dtype, q, k, v, nullptr, o, dout,
+                  lse, dq, dk, dv, nullptr, workspace, workspace_bytes, stream, pk);
 }
 
 sdpa_status_t sdpa_bwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
@@ -467,6 +489,96 @@ sdpa_status_t sdpa_bwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_
                                 max_seqlen_k, d_qk, d_v, scale, is_causal, dropout_p, seed, offset,
                                 dtype, seqstart_q, seqstart_k, q, k, v, o, dout, lse, dq, dk, dv,
                                 workspace, workspace_bytes, stream);
+}
+
+// Local windows and the bottom-right alignment (batch and packed forms).
+sdpa_status_t sdpa_fwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                              int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
+                              int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
+                              uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
+                              const void* v, const float* bias, void* o, float* lse, void* stream) {
+  return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, Mask{window_left, window_right, bottom_right},
+                  dropout_p, seed, offset, dtype, q, k, v, bias, o, lse, stream, Packing{});
+}
+
+sdpa_status_t sdpa_bwd_phases_window(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
+                                     int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
+                                     int64_t window_left, int64_t window_right, int bottom_right,
+                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
+                                     const float* bias, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv, float* dbias,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(phases, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale,
+                  Mask{window_left, window_right, bottom_right}, dropout_p, seed, offset, dtype, q, k,
+                  v, bias, o, dout, lse, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
+                  Packing{});
+}
+
+sdpa_status_t sdpa_bwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                              int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
+                              int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
+                              uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
+                              const void* v, const float* bias, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dk, void* dv, float* dbias,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  return sdpa_bwd_phases_window(SDPA_BWD_ALL, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, window_left,
+                                window_right, bottom_right, dropout_p, seed, offset, dtype, q, k, v,
+                                bias, o, dout, lse, dq, dk, dv, dbias, workspace, workspace_bytes,
+                                stream);
+}
+
+sdpa_status_t sdpa_fwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+                                     int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
+                                     int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
+                                     int64_t window_right, int bottom_right, float dropout_p,
+                                     uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+                                     const int32_t* seqstart_q, const int32_t* seqstart_k,
+                                     const void* q, const void* k, const void* v, void* o,
+                                     float* lse, void* stream) {
+  const Packing pk{seqstart_q, seqstart_k, total_q, total_k};
+  if (seqstart_q == nullptr || seqstart_k == nullptr) {
+    if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
+    return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
+  }
+  return fwd_impl(b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
+                  Mask{window_left, window_right, bottom_right}, dropout_p, seed, offset, dtype, q, k,
+                  v, nullptr, o, lse, stream, pk);
+}
+
+sdpa_status_t sdpa_bwd_phases_varlen_window(
+    int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
+    int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v, float scale,
+    int64_t window_left, int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
+    uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q, const int32_t* seqstart_k,
+    const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  const Packing pk{seqstart_q, seqstart_k, total_q, total_k};
+  if (seqstart_q == nullptr || seqstart_k == nullptr) {
+    if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
+    return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
+  }
+  return bwd_impl(phases, b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
+                  Mask{window_left, window_right, bottom_right}, dropout_p, seed, offset, dtype, q, k,
+                  v, nullptr, o, dout, lse, dq, dk, dv, nullptr, workspace, workspace_bytes, stream,
+                  pk);
+}
+
+sdpa_status_t sdpa_bwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+                                     int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
+                                     int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
+                                     int64_t window_right, int bottom_right, float dropout_p,
+                                     uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+                                     const int32_t* seqstart_q, const int32_t* seqstart_k,
+                                     const void* q, const void* k, const void* v, const void* o,
+                                     const void* dout, const float* lse, void* dq, void* dk,
+                                     void* dv, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return sdpa_bwd_phases_varlen_window(SDPA_BWD_ALL, b, h, h_kv, total_q, total_k, max_seqlen_q,
+                                       max_seqlen_k, d_qk, d_v, scale, window_left, window_right,
+                                       bottom_right, dropout_p, seed, offset, dtype, seqstart_q,
+                                       seqstart_k, q, k, v, o, dout, lse, dq, dk, dv, workspace,
+                                       workspace_bytes, stream);
 }
 
 sdpa_status_t sdpa_bwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,

@@ -1,6 +1,5 @@
-// Backward kernel instantiations for bf16 inputs.
+// dK/dV kernel instantiations for bf16 inputs.
 #include "bwd_dkdv_kernel.cuh"
-#include "bwd_dq_kernel.cuh"
 
 namespace sdpa {
 
@@ -13,13 +12,5 @@ cudaError_t launch_bwd_dkdv_bf16(int d_qk, int d_v, const CUtensorMap& q, const 
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_dq_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                             const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
-                             cudaStream_t st) {
-  if (d_qk == 64 && d_v == 64) return launch_bwd_dq_t<64, 64, true>(q, k, v, dout, p, st);
-  if (d_qk == 128 && d_v == 128) return launch_bwd_dq_t<128, 128, true>(q, k, v, dout, p, st);
-  if (d_qk == 192 && d_v == 128) return launch_bwd_dq_t<192, 128, true>(q, k, v, dout, p, st);
-  return cudaErrorInvalidValue;
-}
 
 }  // namespace sdpa

@@ -116,8 +116,10 @@ __device__ __forceinline__ void keep_bits_transposed(uint64_t lin_quad, int S_kv
 // DROP and BIAS are template parameters (not runtime branches) so the kernel
 // without them is compiled alone: at 96 registers a thread (18 warps, five on
 // some schedulers) the dropout body's keep bits would otherwise push the
-// common path into spilling, and it carries no bias checks.
-template <int DQK, int DV, bool BF16, bool DROP, bool BIAS>
+// common path into spilling, and it carries no bias checks. WIN (a local
+// window or the bottom-right alignment) likewise: the plain kernel masks only
+// the top-left causal diagonal.
+template <int DQK, int DV, bool BF16, bool DROP, bool BIAS, bool WIN>
 __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -136,7 +138,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   // dK / dV row of the tile's key 0, set at start-up and read by the epilogue
   // (kept out of the registers of the compute loop)
   uint64_t* key_row0 = bars + AB_COUNT + 1;
-  static_assert((AB_COUNT + 2) * 8 <= 256, "barrier region");
+  Band* band_slot = reinterpret_cast<Band*>(bars + AB_COUNT + 2);  // see lds_band
+  static_assert((AB_COUNT + 3) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -158,9 +161,20 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   // A key tile past the end of a shorter packed sequence has nothing to do
   // (uniform over the CTA; never in batch mode).
   if (k0 >= S_kv) return;
-  const int n_qt = (S_q + BM - 1) / BM;
-  const int it0 = p.causal ? min(n_qt, k0 / BM) : 0;  // first query tile that sees a key here
-  const int n_per = n_qt - it0;                        // query tiles per query head
+  // query tiles [it0, it0 + n_per) holding a row that sees a key of this tile
+  // (WIN: a general window; else top-left, causal when win_right >= 0)
+  const Band bd = WIN ? band_of(p.win_left, p.win_right, p.win_br, S_q, S_kv)
+                      : Band{-kUnbounded, p.win_right >= 0 ? 0 : kUnbounded};
+  int it0, n_per;
+  if constexpr (WIN) {
+    const int qlo = max(k0 - bd.hi, 0), qhi = min(min(k0 + C::BN, S_kv) - 1 - bd.lo, S_q - 1);
+    it0 = qlo / BM;
+    n_per = qlo <= qhi ? qhi / BM - it0 + 1 : 0;
+  } else {
+    const int n_qt = (S_q + BM - 1) / BM;
+    it0 = p.win_right >= 0 ? min(n_qt, k0 / BM) : 0;
+    n_per = n_qt - it0;
+  }
   // One loop over (query head of the group, query tile): iteration i visits
   // query head hk * grp + i / n_per and query tile it0 + i % n_per, so dK and
   // dV sum over the whole group inside tensor memory.
@@ -175,6 +189,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
                             : 1u);
     *abort_flag = 0u;
     *key_row0 = static_cast<uint64_t>(zk) * p.rows_k + sl.row_k + k0;
+    if (WIN) *band_slot = bd;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -424,10 +439,22 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         }
         tc_fence_before();
         mbar_arrive(bar(AB_SFREE));  // S^T(i) is in registers: S^T(i+1) may overwrite it
-        const bool need_mask = (p.causal && qc0 < k0 + C::BN - 1) || (qc0 + CW > S_q) || !kv_ok;
-        if (need_mask) {
+        // the thread's columns need masking where they cross S_q or an edge of
+        // some key's window (a condition uniform over the warp)
+        if constexpr (WIN) {
+          const Band wb = lds_band(band_slot);
+          if ((qc0 < k0 + C::BN - 1 - wb.hi) || (qc0 + CW - 1 > k0 - wb.lo) || (qc0 + CW > S_q) ||
+              !kv_ok) {
+            // visible iff the key exists, the query exists and it lies in the key's window
+            const int first = kv - wb.hi - qc0;  // visible local columns [first, lim)
+            const int lim = kv_ok ? min(CW, min(S_q - 1, kv - wb.lo) + 1 - qc0) : 0;
+#pragma unroll
+            for (int c = 0; c < CW; ++c)
+              if (c < first || c >= lim) pr[c] = SDPA_NEG_INF;
+          }
+        } else if ((p.win_right >= 0 && qc0 < k0 + C::BN - 1) || (qc0 + CW > S_q) || !kv_ok) {
           // visible iff the key exists, the query exists and (causal) key <= query
-          const int first = p.causal ? kv - qc0 : 0;  // first visible local column
+          const int first = p.win_right >= 0 ? kv - qc0 : 0;  // first visible local column
           const int lim = kv_ok ? min(CW, S_q - qc0) : 0;
 #pragma unroll
           for (int c = 0; c < CW; ++c)
@@ -557,10 +584,14 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
                               const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
   using C = DkdvCfg<DQK, DV>;
   const bool bias = p.bias != nullptr;
-  auto kern = p.dropout ? (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, true>
-                                : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, false>)
-                        : (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, true>
-                                : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, false>);
+  auto pick = [&](auto win) {
+    constexpr bool W = decltype(win)::value;
+    return p.dropout ? (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, true, W>
+                             : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, false, W>)
+                     : (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, true, W>
+                             : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, false, W>);
+  };
+  auto kern = p.win_general ? pick(std::true_type{}) : pick(std::false_type{});
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;

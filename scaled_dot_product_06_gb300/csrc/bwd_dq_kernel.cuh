@@ -78,9 +78,10 @@ enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_V
              QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DSL = QB_DP + 2, QB_DSH = QB_DSL + 2,
              QB_DONE = QB_DSH + 2, QB_DRAIN, QB_OPS, QB_COUNT };
 
-// DROP and BIAS are template parameters so the kernel without them is
-// compiled alone and stays within 96 registers a thread without spilling.
-template <int DQK, int DV, bool BF16, bool DROP, bool BIAS>
+// DROP, BIAS and WIN (a local window or the bottom-right alignment) are
+// template parameters so the kernel without them is compiled alone and stays
+// within 96 registers a thread without spilling.
+template <int DQK, int DV, bool BF16, bool DROP, bool BIAS, bool WIN>
 __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -95,6 +96,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + QB_COUNT);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  Band* band_slot = reinterpret_cast<Band*>(bars + QB_COUNT + 1);  // see lds_band
+  static_assert((QB_COUNT + 2) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -113,10 +116,24 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   const int zq = sl.zq0 + h;                  // tensor-map z of the query head
   const int zk = sl.zk0 + h / (p.H / p.H_kv);  // and of its K/V head
   const int q0 = qt * BM;
-  const int n_kv_all = (S_kv + BN - 1) / BN;
-  const int n_kv = p.causal ? min(n_kv_all, (q0 + BM - 1) / BN + 1) : n_kv_all;
-  // Packed sequences only (uniform over the CTA): a tile past the end of a
-  // shorter sequence has nothing to do, and a sequence without keys has dQ = 0.
+  // key tiles [khi - n_kv + 1, khi] holding a key some row of the tile sees
+  // (WIN: a general window; else top-left, causal when win_right >= 0)
+  const bool causal = p.win_right >= 0;
+  const Band bd = WIN ? band_of(p.win_left, p.win_right, p.win_br, S_q, S_kv)
+                      : Band{-kUnbounded, causal ? 0 : kUnbounded};
+  int khi, n_kv;
+  if constexpr (WIN) {
+    const int klo_key = max(q0 + bd.lo, 0), khi_key = min(min(q0 + BM, S_q) - 1 + bd.hi, S_kv - 1);
+    khi = khi_key / BN;
+    n_kv = (q0 < S_q && klo_key <= khi_key) ? khi - klo_key / BN + 1 : 0;
+  } else {
+    const int n_kv_all = (S_kv + BN - 1) / BN;
+    n_kv = causal ? min(n_kv_all, (q0 + BM - 1) / BN + 1) : n_kv_all;
+    khi = n_kv - 1;
+  }
+  // Uniform over the CTA: a tile past the end of a shorter packed sequence has
+  // nothing to do, and rows that see no key (a sequence without keys, or the
+  // window) have dQ = 0.
   if (q0 >= S_q) return;
   if (n_kv == 0) {
     const int row = q0 + static_cast<int>(threadIdx.x);
@@ -139,6 +156,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
                             ? static_cast<uint32_t>(NCT)
                             : 1u);
     *abort_flag = 0u;
+    if (WIN) *band_slot = bd;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -175,7 +193,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_KF + s), C::K_BYTES);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, sl.row_k + (n_kv - 1 - j) * BN, zk);
+          tma_load_3d(sK + s * C::K_BYTES + c * BN * 128, &tmK, bar(QB_KF + s), c * 64, sl.row_k + (khi - j) * BN, zk);
       }
       if (!mbar_wait(bar(QB_VE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) {
         issued = 2 * j + 1;
@@ -185,7 +203,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         mbar_arrive_expect_tx(bar(QB_VF + s), C::V_BYTES);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, sl.row_k + (n_kv - 1 - j) * BN, zk);
+          tma_load_3d(sV + s * C::V_BYTES + c * BN * 128, &tmV, bar(QB_VF + s), c * 64, sl.row_k + (khi - j) * BN, zk);
       }
       issued = 2 * j + 2;
     }
@@ -353,7 +371,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     }
     const float zk = p.keep_scale;
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int kc0 = (n_kv - 1 - j) * BN + CW * hf;  // first key of this thread's columns
+      const int kc0 = (khi - j) * BN + CW * hf;  // first key of this thread's columns
       uint32_t keep = 0;                 // bit c: keep flag of local column c
       if constexpr (DROP) {
 #pragma unroll
@@ -410,12 +428,27 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(QB_SFREE));
-      const bool need_mask = (kc0 + CW > S_kv) || (p.causal && kc0 + CW - 1 > q0) || !row_ok;
-      if (need_mask) {
-        const int last = row_ok ? (p.causal ? min(S_kv - 1, qr) : S_kv - 1) : -1;
+      if constexpr (WIN) {
+        // the thread's columns need masking where they cross S_kv or an edge of
+        // some row's window (a condition uniform over the warp)
+        const Band wb = lds_band(band_slot);
+        const bool need_mask = (kc0 + CW > S_kv) || (kc0 + CW - 1 > q0 + wb.hi) ||
+                               (kc0 < q0 + BM - 1 + wb.lo) || !row_ok;
+        if (need_mask) {
+          const int first = qr + wb.lo;  // the row's visible keys, none past S_q
+          const int last = row_ok ? min(S_kv - 1, qr + wb.hi) : -1;
 #pragma unroll
-        for (int c = 0; c < CW; ++c)
-          if (kc0 + c > last) pr[c] = SDPA_NEG_INF;
+          for (int c = 0; c < CW; ++c)
+            if (kc0 + c < first || kc0 + c > last) pr[c] = SDPA_NEG_INF;
+        }
+      } else {
+        const bool need_mask = (kc0 + CW > S_kv) || (p.win_right >= 0 && kc0 + CW - 1 > q0) || !row_ok;
+        if (need_mask) {
+          const int last = row_ok ? (p.win_right >= 0 ? min(S_kv - 1, qr) : S_kv - 1) : -1;
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            if (kc0 + c > last) pr[c] = SDPA_NEG_INF;
+        }
       }
 #pragma unroll
       for (int c = 0; c < CW; ++c) pr[c] = ex2(pr[c]);
@@ -496,10 +529,14 @@ cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CU
                             const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
   using C = DqCfg<DQK, DV>;
   const bool bias = p.bias != nullptr;
-  auto kern = p.dropout ? (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, true, true>
-                                : sdpa_bwd_dq_kernel<DQK, DV, BF16, true, false>)
-                        : (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, false, true>
-                                : sdpa_bwd_dq_kernel<DQK, DV, BF16, false, false>);
+  auto pick = [&](auto win) {
+    constexpr bool W = decltype(win)::value;
+    return p.dropout ? (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, true, true, W>
+                             : sdpa_bwd_dq_kernel<DQK, DV, BF16, true, false, W>)
+                     : (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, false, true, W>
+                             : sdpa_bwd_dq_kernel<DQK, DV, BF16, false, false, W>);
+  };
+  auto kern = p.win_general ? pick(std::true_type{}) : pick(std::false_type{});
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;

@@ -29,7 +29,13 @@ struct FwdParams {
   int B, H, S_q, S_kv;
   int H_kv;                // K/V heads; query head h reads K/V head h / (H / H_kv)
   float scale_log2;        // softmax scale * log2(e)
-  int causal;              // top-left: key j visible to query i iff j <= i
+  // Visible keys (CK's window_size_left / window_size_right and top-left /
+  // bottom-right mask type): key j is visible to query i iff
+  // i + off - win_left <= j <= i + off + win_right with off = S_kv - S_q (the
+  // sequence's lengths) when win_br, else 0; a negative size leaves that side
+  // unbounded. Causal is (-1, 0, 0); no mask (-1, -1, 0). See Band.
+  int win_left, win_right, win_br;
+  int win_general;         // 0: top-left, causal (win_right = 0) or unmasked (-1)
   const float* bias;       // [1, H, S_q, S_kv] fp32 or null
   int dropout;             // 0 / 1
   uint32_t drop_threshold; // drop iff draw < threshold
@@ -62,6 +68,27 @@ __host__ __device__ __forceinline__ size_t stat_index(size_t bh, int S_pad, int 
   return (bh * static_cast<size_t>(S_pad) + static_cast<size_t>(q & ~63)) * 2 + static_cast<size_t>(q & 63);
 }
 __host__ __device__ __forceinline__ int stat_pad(int S_q) { return (S_q + 127) & ~127; }
+
+// The visible keys of query row i are [i + lo, i + hi] (clamp to [0, S_kv)
+// where used); an unbounded side is +-2^30. The host keeps sequence lengths
+// below 2^29 and window sizes below S_q + S_kv (larger ones are unbounded),
+// so every sum of a row or key index with lo or hi fits in an int.
+constexpr int kUnbounded = 1 << 30;
+struct Band {
+  int lo, hi;
+};
+__device__ __forceinline__ Band band_of(int win_left, int win_right, int win_br, int S_q, int S_kv) {
+  const int off = win_br ? S_kv - S_q : 0;
+  return Band{win_left < 0 ? -kUnbounded : off - win_left, win_right < 0 ? kUnbounded : off + win_right};
+}
+
+// The band kept in shared memory and re-read where a loop needs it, so that
+// it does not hold two registers through the loop (volatile: read each time).
+__device__ __forceinline__ Band lds_band(const void* p) {
+  int lo, hi;
+  asm volatile("ld.shared.v2.s32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(smem_u32(p)));
+  return Band{lo, hi};
+}
 
 // Packed sequences: the statistics of head z hold one block per sequence,
 // sequence b's at row packed_stat_row(start_b, b) (start_b its first packed
@@ -127,7 +154,8 @@ struct BwdParams {
   int H_kv;                // K/V heads; query head h reads K/V head h / (H / H_kv)
   float scale;             // softmax scale
   float scale_log2;        // scale * log2(e)
-  int causal;
+  int win_left, win_right, win_br;  // visible keys, as in FwdParams
+  int win_general;
   const float* bias;       // [1, H, S_q, S_kv] or null
   float* dbias;            // [1, H, S_q, S_kv] or null (accumulated with atomics)
   int dropout;

@@ -33,8 +33,9 @@
 // Registers: launched at 168 a thread (384 threads); the producer/MMA
 // warpgroup drops to 72 and the softmax warpgroups rise to 216, enough for a
 // row's 128 scores without spilling: 2 x 128 x 216 + 128 x 72 = 384 x 168.
-// GENERAL (a bias or dropout present) is a template parameter so the plain
-// kernel is compiled without their registers.
+// GENERAL (a bias or dropout present) and WIN (a local window or the
+// bottom-right alignment) are template parameters so the plain kernel is
+// compiled without their registers.
 #pragma once
 #include "common.cuh"
 
@@ -70,7 +71,7 @@ struct FwdCfg {
 enum : int { FB_Q = 0, FB_S, FB_P = FB_S + 2, FB_O = FB_P + 2, FB_DRAIN = FB_O + 2, FB_KF,
              FB_KE = FB_KF + 3, FB_VF = FB_KE + 3, FB_VE = FB_VF + 3, FB_COUNT = FB_VE + 3 };
 
-template <int DQK, int DV, bool BF16, bool GENERAL>
+template <int DQK, int DV, bool BF16, bool GENERAL, bool WIN>
 __global__ void __launch_bounds__(384, 1)
     sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -84,6 +85,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + FB_COUNT);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  Band* band_slot = reinterpret_cast<Band*>(bars + FB_COUNT + 1);  // see lds_band
+  static_assert((FB_COUNT + 2) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -110,20 +113,32 @@ __global__ void __launch_bounds__(384, 1)
   const bool odd = (n_qt_seq & 1) != 0;
   const bool lone = odd && qtile.qt == 0;
   const int q0 = (odd ? max(2 * qtile.qt - 1, 0) : 2 * qtile.qt) * C::BM;  // first row of tile 0
-  const int n_kv_all = (S_kv + C::BN - 1) / C::BN;
-  // key tiles query tile t sees (0 when the tile lies past S_q)
-  auto tile_kv = [&](int t) -> int {
-    if (t == 1 && lone) return 0;
+  // (WIN: any window; else top-left, causal when win_right >= 0)
+  const Band bd = WIN ? band_of(p.win_left, p.win_right, p.win_br, S_q, S_kv)
+                          : Band{-kUnbounded, p.win_right >= 0 ? 0 : kUnbounded};
+  // key tiles [klo_t, khi_t] query tile t sees: those holding a visible key of
+  // one of its rows (none when the tile lies past S_q or no row sees a key)
+  int klo0 = 0, khi0 = -1, klo1 = 0, khi1 = -1;
+  auto tile_keys = [&](int t, int& klo, int& khi) {
     const int qs = q0 + t * C::BM;
-    if (qs >= S_q) return 0;
-    return p.causal ? min(n_kv_all, (min(qs + C::BM, S_q) - 1) / C::BN + 1) : n_kv_all;
+    if ((t == 1 && lone) || qs >= S_q) return;
+    const int lo = max(qs + bd.lo, 0), hi = min(min(qs + C::BM, S_q) - 1 + bd.hi, S_kv - 1);
+    if (lo <= hi) {
+      klo = lo / C::BN;
+      khi = hi / C::BN;
+    }
   };
-  const int n_kv0 = tile_kv(0), n_kv1 = tile_kv(1);
-  const int n_it = max(n_kv0, n_kv1);
-  // Iteration j visits key tile n_it - 1 - j (from the diagonal down); query
-  // tile t takes part in iterations j >= n_it - n_kv_t.
-  const int j0_0 = n_it - n_kv0, j0_1 = n_it - n_kv1;
-  const bool has1 = n_kv1 > 0;
+  tile_keys(0, klo0, khi0);
+  tile_keys(1, klo1, khi1);
+  const int n_kv0 = khi0 - klo0 + 1, n_kv1 = khi1 - klo1 + 1;
+  const bool has0 = n_kv0 > 0, has1 = n_kv1 > 0;
+  // Iteration j visits key tile khi - j (from the diagonal down); query tile
+  // t takes part in iterations [j0_t, j1_t]. The rows of tile 1 follow those
+  // of tile 0, so its key range starts and ends no earlier.
+  const int khi = max(khi0, khi1);
+  const int n_it = (has0 || has1) ? khi - (has0 ? klo0 : klo1) + 1 : 0;
+  const int j0_0 = has0 ? khi - khi0 : n_it, j1_0 = has0 ? khi - klo0 : -1;
+  const int j0_1 = has1 ? khi - khi1 : n_it, j1_1 = has1 ? khi - klo1 : -1;
 
   // Nothing to compute (packed sequences only: a pair past the end of a
   // shorter sequence, or a sequence without keys, whose rows get O = 0 and
@@ -143,6 +158,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < FB_COUNT; ++i) mbar_init(bar(i), (i == FB_P || i == FB_P + 1) ? 128u : 1u);
     *abort_flag = 0u;
+    if (WIN) *band_slot = bd;
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -177,7 +193,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; j < n_it; ++j) {
         const int s = j % ST;
         const uint32_t ph = (j / ST) & 1;
-        const int kv0 = sl.row_k + (n_it - 1 - j) * C::BN;
+        const int kv0 = sl.row_k + (khi - j) * C::BN;
         if (!mbar_wait(bar(FB_KE + s), ph ^ 1, ec, kSiteFwdLoad, true, true)) break;
         if (p.fault == 1) break;  // test hook: K/V never arrive
         if (lane == 0) {
@@ -236,36 +252,38 @@ __global__ void __launch_bounds__(384, 1)
       };
       auto wait_k = [&](int j) { return mbar_wait_w(bar(FB_KF + j % ST), (j / ST) & 1, ec, kSiteFwdMma); };
       auto wait_v = [&](int j) { return mbar_wait_w(bar(FB_VF + j % ST), (j / ST) & 1, ec, kSiteFwdMma); };
+      auto in0 = [&](int j) { return j >= j0_0 && j <= j1_0; };  // tile 0 uses key tile khi - j
+      auto in1 = [&](int j) { return j >= j0_1 && j <= j1_1; };
       bool ok = n_it > 0 && mbar_wait_w(bar(FB_Q), 0, ec, kSiteFwdMma) && wait_k(0);
       if (ok) {
         tc_fence_after();
-        if (j0_0 == 0) issue_s(0, 0);
-        if (has1 && j0_1 == 0) issue_s(1, 0);
+        if (in0(0)) issue_s(0, 0);
+        if (in1(0)) issue_s(1, 0);
         umma_commit_w(bar(FB_KE + 0));
       }
       for (int j = 0; ok && j < n_it; ++j) {
         const bool more = j + 1 < n_it;
         if (!(ok = wait_v(j))) break;
         // query tile 0
-        if (j >= j0_0) {
+        if (in0(j)) {
           if (!(ok = mbar_wait_w(bar(FB_P + 0), pph0, ec, kSiteFwdMma))) break;
           pph0 ^= 1u;
           tc_fence_after();
           issue_pv(0, j, j == j0_0);
         }
-        if (more && j + 1 >= j0_0) {
+        if (more && in0(j + 1)) {
           if (!(ok = wait_k(j + 1))) break;
           tc_fence_after();
           issue_s(0, j + 1);
         }
         // query tile 1
-        if (has1 && j >= j0_1) {
+        if (in1(j)) {
           if (!(ok = mbar_wait_w(bar(FB_P + 1), pph1, ec, kSiteFwdMma))) break;
           pph1 ^= 1u;
           tc_fence_after();
           issue_pv(1, j, j == j0_1);
         }
-        if (has1 && more && j + 1 >= j0_1) {
+        if (more && in1(j + 1)) {
           if (!(ok = wait_k(j + 1))) break;
           tc_fence_after();
           issue_s(1, j + 1);
@@ -287,6 +305,7 @@ __global__ void __launch_bounds__(384, 1)
     const int qt0 = q0 + t * C::BM;
     const int row = qt0 + (threadIdx.x & 127);
     const int n_kv = t == 0 ? n_kv0 : n_kv1;
+    const int khi_t = WIN ? (t == 0 ? khi0 : khi1) : n_kv - 1;  // the plain masks start at key 0
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + C::T_S + 128 * t, tO = tbase + C::T_O + DV * t;
     const float sl2 = p.scale_log2;
@@ -300,7 +319,7 @@ __global__ void __launch_bounds__(384, 1)
     float m = SDPA_NEG_INF, l = 0.f;
     bool ok = true;
     for (int c = 0; c < n_kv; ++c) {
-      const int k0 = (n_kv - 1 - c) * C::BN;  // key tiles from the diagonal down
+      const int k0 = (khi_t - c) * C::BN;  // key tiles from the diagonal down
       // scores in the log2 domain: S * scale * log2e (+ Bias * log2e)
       float x[128];
       if (GENERAL && bias_row != nullptr) {
@@ -340,9 +359,17 @@ __global__ void __launch_bounds__(384, 1)
           x[q * 32 + 2 * i + 1] = v.y;
         }
       }
-      const bool need_mask = (k0 + C::BN > S_kv) || (p.causal && k0 + C::BN - 1 > qt0);
-      if (need_mask) {
-        const int lim = p.causal ? min(S_kv - 1, row) : S_kv - 1;  // last visible key
+      if constexpr (WIN) {
+        // a tile needs masking where it crosses S_kv or an edge of some row's window
+        const Band wb = lds_band(band_slot);
+        if ((k0 + C::BN > S_kv) || (k0 + C::BN - 1 > qt0 + wb.hi) || (k0 < qt0 + C::BM - 1 + wb.lo)) {
+          const int first = row + wb.lo, last = min(S_kv - 1, row + wb.hi);  // visible keys
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (k0 + i < first || k0 + i > last) x[i] = SDPA_NEG_INF;
+        }
+      } else if ((k0 + C::BN > S_kv) || (p.win_right >= 0 && k0 + C::BN - 1 > qt0)) {
+        const int lim = p.win_right >= 0 ? min(S_kv - 1, row) : S_kv - 1;  // last visible key
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (k0 + i > lim) x[i] = SDPA_NEG_INF;
@@ -440,6 +467,14 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (row_ok)
         p.lse[ri] = (l > 0.f) ? fmaf(m, kLn2, __logf(l)) : SDPA_NEG_INF;
+    } else if (n_kv == 0 && row_ok && !(t == 1 && lone)) {
+      // no row of this tile sees a key (the other tile's rows do): O = 0, LSE = -inf
+      // (a lone tile 0's partner rows belong to the next pair)
+      const size_t ri = static_cast<size_t>(zq) * p.rows_q + sl.row_q + row;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.o) + ri * DV * 2);
+#pragma unroll
+      for (int v = 0; v < DV / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+      p.lse[ri] = SDPA_NEG_INF;
     }
   }
 
@@ -456,7 +491,10 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
                          const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
   const bool general = p.bias != nullptr || p.dropout != 0;
-  auto kern = general ? sdpa_fwd_kernel<DQK, DV, BF16, true> : sdpa_fwd_kernel<DQK, DV, BF16, false>;
+  auto kern = general ? (p.win_general ? sdpa_fwd_kernel<DQK, DV, BF16, true, true>
+                                       : sdpa_fwd_kernel<DQK, DV, BF16, true, false>)
+                      : (p.win_general ? sdpa_fwd_kernel<DQK, DV, BF16, false, true>
+                                       : sdpa_fwd_kernel<DQK, DV, BF16, false, false>);
   // The warpgroups' setmaxnreg shares add up to exactly 384 x REG_LAUNCH; had
   // the compiler given the kernel another launch register count, the softmax
   // warpgroups' increase could never be granted, so refuse to launch then.
