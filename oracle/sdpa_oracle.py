@@ -23,6 +23,14 @@ Readings taken where the pages are silent (each is listed in the design doc):
   off = S_kv - S_q for bottom-right and 0 for top-left, key j is visible to
   query i iff i + off - left <= j <= i + off + right, a negative size leaving
   that side unbounded. Causal is the window (-1, 0); no mask is (-1, -1).
+* ALiBi: CK tile fmha_bwd_kernel.hpp reads one slope per (batch, head)
+  (alibi_slope_ptr at i_batch * alibi_slope_stride + i_nhead), takes it into
+  the log2 domain beside the scale, and aligns the position encoding
+  bottom-right when there is no mask, else as the mask is aligned; the form
+  of the encoding is not on the page. Reading: the linear distance penalty of
+  ALiBi, -slope * |j - i - off| added to the scaled score (not multiplied by
+  the scale), off = 0 under a top-left mask and S_kv - S_q otherwise; the
+  slopes are constants (no gradient).
 * A row with no visible key (possible only through a -inf bias) has P = 0,
   O = 0, LSE = -inf and contributes nothing to any gradient.
 * Dropout multiplies P by Z = keep / (1 - p) before the product with V; the
@@ -73,6 +81,14 @@ class Problem:
     # [B', H, S_q', S_kv'] problem (a packed sequence draws from the padded
     # batch); None means this problem's own shape.
     drop_frame: tuple | None = None
+    # ALiBi slopes, [B][H] (nested sequences) or None
+    alibi_slopes: tuple | None = None
+
+    def alibi_offset(self) -> int:
+        """Diagonal of the ALiBi distance: top-left under a top-left mask."""
+        left, right = self.window if self.window is not None else (-1, 0 if self.is_causal else -1)
+        masked = left >= 0 or right >= 0
+        return 0 if (masked and not self.bottom_right) else self.S_kv - self.S_q
 
     @property
     def kv_heads(self) -> int:
@@ -103,7 +119,7 @@ def visible(prob: Problem, rows: np.ndarray, cols: np.ndarray) -> np.ndarray:
 
 
 def scores(prob: Problem, q_h: np.ndarray, k_h: np.ndarray, bias_h, rows: np.ndarray,
-           cols: np.ndarray) -> np.ndarray:
+           cols: np.ndarray, slope: float = 0.0) -> np.ndarray:
     """S'' = (Q K^T) * scale + Bias on the (rows, cols) block, -inf where masked.
 
     CK tile fmha_bwd_kernel.hpp header: S = Q K^T, S' = S * Scale, S'' = S' + Bias.
@@ -111,6 +127,9 @@ def scores(prob: Problem, q_h: np.ndarray, k_h: np.ndarray, bias_h, rows: np.nda
     s = prob.scale * (q_h[rows] @ k_h[cols].T)
     if bias_h is not None:
         s = s + bias_h[np.ix_(rows, cols)]
+    if slope != 0.0:  # ALiBi (module text)
+        dist = np.asarray(cols)[None, :] - np.asarray(rows)[:, None] - prob.alibi_offset()
+        s = s - slope * np.abs(dist)
     s = np.where(visible(prob, rows, cols), s, -np.inf)
     return s
 
@@ -129,6 +148,10 @@ def softmax_rows(s: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     p = np.where(alive[:, None], e / np.where(alive, l, 1.0)[:, None], 0.0)
     lse = np.where(alive, m0 + np.log(np.where(alive, l, 1.0)), -np.inf)
     return p, lse
+
+
+def alibi_slope(prob: Problem, b: int, h: int) -> float:
+    return 0.0 if prob.alibi_slopes is None else float(prob.alibi_slopes[b][h])
 
 
 def dropout_scale(prob: Problem, b: int, h: int, rows: np.ndarray, cols: np.ndarray):
@@ -152,7 +175,7 @@ def forward_head(prob: Problem, b: int, h: int, q, k, v, bias=None, rows=None):
     hk = prob.kv_head(h)
     q_h, k_h, v_h = _f64(q[b, h]), _f64(k[b, hk]), _f64(v[b, hk])
     bias_h = None if bias is None else _f64(bias[0, h])
-    p, lse = softmax_rows(scores(prob, q_h, k_h, bias_h, rows, cols))
+    p, lse = softmax_rows(scores(prob, q_h, k_h, bias_h, rows, cols, alibi_slope(prob, b, h)))
     z = dropout_scale(prob, b, h, rows, cols)
     return (p * z) @ v_h, lse
 
@@ -190,7 +213,7 @@ def backward_head(prob: Problem, b: int, h: int, q, k, v, do, bias=None, rows=No
     bias_h = None if bias is None else _f64(bias[0, h])
 
     def grads_of_rows(rr, want_dq):
-        p, _ = softmax_rows(scores(prob, q_h, k_h, bias_h, rr, all_cols))
+        p, _ = softmax_rows(scores(prob, q_h, k_h, bias_h, rr, all_cols, alibi_slope(prob, b, h)))
         z = dropout_scale(prob, b, h, rr, all_cols)
         pz = p * z
         o = pz @ v_h

@@ -56,6 +56,7 @@ class Packed:
     max_seqlen_k: int = 0
     window: tuple | None = None  # as in sdpa_oracle.Problem, per sequence
     bottom_right: bool = False
+    alibi_slopes: tuple | None = None  # [B][H], sequence i taking row i
 
     @property
     def B(self) -> int:
@@ -79,7 +80,8 @@ class Packed:
         mq, mk = self.frame()
         return so.Problem(1, self.H, lq, lk, self.D_qk, self.D_v, self.scale, self.is_causal,
                           self.dropout_p, self.seed, self.offset, self.H_kv, self.window,
-                          self.bottom_right, drop_frame=(self.B, mq, mk, i))
+                          self.bottom_right, drop_frame=(self.B, mq, mk, i),
+                          alibi_slopes=None if self.alibi_slopes is None else (self.alibi_slopes[i],))
 
 
 def _rows(x, a: int, b: int):
