@@ -54,6 +54,11 @@ WORKLOADS = {
     "b1h32-s16384-d128-window4096": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
                                          dtype="bf16", causal=True, window=(4096, 0),
                                          bottom_right=False, bias=False, p=0.0, scale=None),
+    # ALiBi (geometric slopes 2^(-8 (h + 1) / H), one per head) on the causal
+    # long-context case
+    "b1h32-s16384-d128-causal-alibi": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
+                                           dtype="bf16", causal=True, alibi=True, bias=False,
+                                           p=0.0, scale=None),
     # packed variable-length sequences (group mode): 16 sequences of 512..8192
     # tokens (seeded; 74,372 in all), 32 heads, d 128, causal
     "varlen16-h32-d128-causal": dict(lengths=dict(n=16, lo=512, hi=8192, seed=2024), H=32,
@@ -198,7 +203,8 @@ def oracle_sample(w: dict, s_sample: int) -> tuple[float, float]:
     scale = w["scale"] if w["scale"] is not None else 1.0 / math.sqrt(w["D_qk"])
     pr = oracle.Problem(1, 1, s_q, s_kv, w["D_qk"], w["D_v"], scale, w["causal"], w["p"],
                         DROP_SEED, DROP_OFFSET, window=w.get("window"),
-                        bottom_right=w.get("bottom_right", False))
+                        bottom_right=w.get("bottom_right", False),
+                        alibi_slopes=((2.0 ** (-8.0 / w["H"]),),) if w.get("alibi") else None)
     t0 = time.perf_counter()
     oracle.forward(pr, x["q"], x["k"], x["v"], x["bias"])
     oracle.backward(pr, x["q"], x["k"], x["v"], x["do"], x["bias"])
@@ -316,6 +322,9 @@ def main():
               offset=DROP_OFFSET)
     if w.get("window") is not None or w.get("bottom_right"):
         kw.update(window=w.get("window"), bottom_right=w.get("bottom_right", False))
+    if w.get("alibi"):
+        kw["alibi_slopes"] = torch.tensor([2.0 ** (-8.0 * (hh + 1) / w["H"]) for hh in range(w["H"])],
+                                          dtype=torch.float32, device=dev)
     packed = "lens" in w
     if packed:
         # [H, total, D] tensors; sequence i owns rows seqstart[i] .. seqstart[i+1]-1
@@ -518,6 +527,7 @@ def main():
                        "causal": w["causal"], "bias": w["bias"], "dropout_p": w["p"],
                        **({"window": list(w["window"]), "bottom_right": w.get("bottom_right", False)}
                           if w.get("window") is not None else {}),
+                       **({"alibi": "slopes 2^(-8(h+1)/H)"} if w.get("alibi") else {}),
                        "l2": "inputs larger than L2, no flush",
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "pct_of_peak": 100.0 * value / world / peak,

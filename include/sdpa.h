@@ -252,17 +252,25 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Local windows and the bottom-right alignment (CK tile fmha_bwd_kernel.hpp
- * mask arguments window_size_left, window_size_right and mask_type
- * MASK_FROM_TOP_LEFT / bottom-right; oneDNN sdpa micro.cpp's top_left and
- * bottom_right attention masks). The grouped and packed calls with
- * is_causal replaced by three arguments:
+ * Local windows, the bottom-right alignment and ALiBi (CK tile
+ * fmha_bwd_kernel.hpp mask arguments window_size_left, window_size_right and
+ * mask_type, and its ALiBi slopes alibi_slope_ptr / alibi_slope_stride;
+ * oneDNN sdpa micro.cpp's top_left and bottom_right attention masks). The
+ * grouped and packed calls with is_causal replaced by:
  *   window_left, window_right  key j is visible to query i iff
  *            i + off - window_left <= j <= i + off + window_right; a negative
  *            size leaves that side unbounded (so does one of s_q + s_kv or
  *            more).
  *   bottom_right  0: off = 0 (diagonal through (0, 0)); 1: off = s_kv - s_q
  *            (diagonal through (s_q - 1, s_kv - 1)), per sequence when packed.
+ *   alibi_slopes  null, or a DEVICE fp32 array: the score of (i, j) in batch
+ *            entry (or sequence) bb and query head hh gets
+ *            -alibi_slopes[bb * alibi_stride + hh] * |j - i - off_a| added
+ *            after the scale (the slopes are constants, with no gradient);
+ *            off_a = 0 when a window size is given (>= 0) and bottom_right is
+ *            0, else s_kv - s_q. 4-byte aligned (SDPA_ERR_MISALIGNED).
+ *   alibi_stride  0 (one slope per head for every batch entry) or >= h
+ *            (SDPA_ERR_INVALID_ARG otherwise).
  * Causal is (-1, 0, 0), bottom-right causal (-1, 0, 1), a sliding window of
  * w keys back (w, 0, 0), no mask (-1, -1, 0). A query row that sees no key
  * gets O = 0, LSE = -inf and dQ = 0; a key no query sees gets dK = dV = 0.
@@ -271,12 +279,14 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
  */
 sdpa_status_t sdpa_fwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                              int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
+                              int64_t window_right, int bottom_right, const float* alibi_slopes,
+                              int64_t alibi_stride, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, void* o, float* lse, void* stream);
 sdpa_status_t sdpa_bwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                              int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
+                              int64_t window_right, int bottom_right, const float* alibi_slopes,
+                              int64_t alibi_stride, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, float* dbias,
@@ -284,6 +294,7 @@ sdpa_status_t sdpa_bwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, i
 sdpa_status_t sdpa_bwd_phases_window(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
                                      int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
                                      int64_t window_left, int64_t window_right, int bottom_right,
+                                     const float* alibi_slopes, int64_t alibi_stride,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
                                      const float* bias, const void* o, const void* dout,
@@ -292,28 +303,31 @@ sdpa_status_t sdpa_bwd_phases_window(int phases, int64_t b, int64_t h, int64_t h
 sdpa_status_t sdpa_fwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                                     int64_t window_right, int bottom_right, float dropout_p,
-                                     uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
-                                     const int32_t* seqstart_q, const int32_t* seqstart_k,
-                                     const void* q, const void* k, const void* v, void* o,
-                                     float* lse, void* stream);
+                                     int64_t window_right, int bottom_right,
+                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                                     const int32_t* seqstart_k, const void* q, const void* k,
+                                     const void* v, void* o, float* lse, void* stream);
 sdpa_status_t sdpa_bwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                                     int64_t window_right, int bottom_right, float dropout_p,
-                                     uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
-                                     const int32_t* seqstart_q, const int32_t* seqstart_k,
-                                     const void* q, const void* k, const void* v, const void* o,
-                                     const void* dout, const float* lse, void* dq, void* dk,
-                                     void* dv, void* workspace, size_t workspace_bytes,
-                                     void* stream);
+                                     int64_t window_right, int bottom_right,
+                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                                     const int32_t* seqstart_k, const void* q, const void* k,
+                                     const void* v, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, void* stream);
 sdpa_status_t sdpa_bwd_phases_varlen_window(
     int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
     int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v, float scale,
-    int64_t window_left, int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
-    uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q, const int32_t* seqstart_k,
-    const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
+    int64_t window_left, int64_t window_right, int bottom_right, const float* alibi_slopes,
+    int64_t alibi_stride, float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+    const int32_t* seqstart_q, const int32_t* seqstart_k, const void* q, const void* k,
+    const void* v, const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
+    void* workspace, size_t workspace_bytes, void* stream);
 
 sdpa_status_t sdpa_bwd_noalloc(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v, float scale, int is_causal, float dropout_p,

@@ -36,24 +36,40 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _window(is_causal, window, bottom_right):
-    """(left, right, bottom_right) of the visible-key band, or None for the
-    plain causal / unmasked calls."""
-    if window is None and not bottom_right:
+def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h):
+    """(left, right, bottom_right, slopes pointer, slope stride) for the window
+    entry points, or None for the plain causal / unmasked calls. alibi_slopes:
+    fp32 CUDA [h] (every batch entry) or [n_batch, h]."""
+    if window is None and not bottom_right and alibi_slopes is None:
         return None
     left, right = window if window is not None else (-1, 0 if is_causal else -1)
-    return int(left), int(right), int(bool(bottom_right))
+    stride = 0
+    if alibi_slopes is not None:
+        a = alibi_slopes
+        if not a.is_cuda or a.dtype != torch.float32 or not a.is_contiguous():
+            raise ValueError("alibi_slopes must be a contiguous fp32 CUDA tensor")
+        if tuple(a.shape) == (h,):
+            stride = 0
+        elif tuple(a.shape) == (n_batch, h):
+            stride = h
+        else:
+            raise ValueError(f"alibi_slopes has shape {tuple(a.shape)}, expected ({h},) or "
+                             f"({n_batch}, {h})")
+    return int(left), int(right), int(bool(bottom_right)), _ptr(alibi_slopes), stride
 
 
 def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0,
-             bias=None, out=None, lse=None, stream=None, window=None, bottom_right=False):
+             bias=None, out=None, lse=None, stream=None, window=None, bottom_right=False,
+             alibi_slopes=None):
     """Forward pass. Returns (o [b,h,s_q,d_v], lse fp32 [b,h,s_q]).
 
     k and v may have fewer heads than q (grouped-query attention): h_kv =
     k.shape[1] must divide h, and query head i reads K/V head i // (h // h_kv).
     window=(left, right) keeps key j visible to query i iff
     i + off - left <= j <= i + off + right (a negative size unbounded), with
-    off = s_kv - s_q when bottom_right, else 0; is_causal is window (-1, 0)."""
+    off = s_kv - s_q when bottom_right, else 0; is_causal is window (-1, 0).
+    alibi_slopes (fp32 CUDA [h] or [b, h]) adds -slope * |j - i - off_a| to the
+    scaled scores, off_a = 0 under a top-left window, else s_kv - s_q."""
     b, h, s_q, d_qk = q.shape
     h_kv, s_kv, d_v = k.shape[1], k.shape[2], v.shape[3]
     dt = q.dtype
@@ -71,7 +87,7 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
         lse = torch.empty((b, h, s_q), dtype=torch.float32, device=q.device)
     _check_io("out", out, (b, h, s_q, d_v), dt)
     _check_io("lse", lse, (b, h, s_q), torch.float32)
-    w = _window(is_causal, window, bottom_right)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
     if w is None:
         st = _native.lib().sdpa_fwd_gqa(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
                                         float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
@@ -93,18 +109,19 @@ def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v) -> int:
 
 def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
              offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None, dbias=None,
-             stream=None, window=None, bottom_right=False):
+             stream=None, window=None, bottom_right=False, alibi_slopes=None):
     """Backward pass. Returns (dq, dk, dv, dbias or None); dk and dv have k's
     and v's shapes (with grouped K/V heads, sums over each group)."""
     return sdpa_bwd_phases(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, scale=scale,
                            is_causal=is_causal, dropout_p=dropout_p, seed=seed, offset=offset,
                            bias=bias, workspace=workspace, dq=dq, dk=dk, dv=dv, dbias=dbias,
-                           stream=stream, window=window, bottom_right=bottom_right)
+                           stream=stream, window=window, bottom_right=bottom_right,
+                           alibi_slopes=alibi_slopes)
 
 
 def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0,
                     seed=0, offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None,
-                    dbias=None, stream=None, window=None, bottom_right=False):
+                    dbias=None, stream=None, window=None, bottom_right=False, alibi_slopes=None):
     """The backward phases selected by ``phases`` (SDPA_BWD_* bit mask)."""
     b, h, s_q, d_qk = q.shape
     h_kv, s_kv, d_v = k.shape[1], k.shape[2], v.shape[3]
@@ -127,7 +144,7 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
     need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    w = _window(is_causal, window, bottom_right)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
     if w is None:
         st = _native.lib().sdpa_bwd_phases_gqa(
             int(phases), b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
@@ -155,7 +172,7 @@ def _check_seqstart(name: str, t: torch.Tensor) -> int:
 
 def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *, scale=None,
                     is_causal=False, dropout_p=0.0, seed=0, offset=0, out=None, lse=None,
-                    stream=None, window=None, bottom_right=False):
+                    stream=None, window=None, bottom_right=False, alibi_slopes=None):
     """Forward pass over packed variable-length sequences. q [h, total_q, d_qk],
     k [h_kv, total_k, d_qk], v [h_kv, total_k, d_v]; seqstart_q / seqstart_k
     int32 CUDA tensors of b + 1 row offsets (sequence i owns query rows
@@ -179,7 +196,7 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
         lse = torch.empty((h, total_q), dtype=torch.float32, device=q.device)
     _check_io("out", out, (h, total_q, d_v), dt)
     _check_io("lse", lse, (h, total_q), torch.float32)
-    w = _window(is_causal, window, bottom_right)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
     if w is None:
         st = _native.lib().sdpa_fwd_varlen(
             b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale,
@@ -203,20 +220,22 @@ def sdpa_bwd_varlen_workspace_size(b, h, total_q) -> int:
 
 def sdpa_bwd_varlen(q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *,
                     scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0, workspace=None,
-                    dq=None, dk=None, dv=None, stream=None, window=None, bottom_right=False):
+                    dq=None, dk=None, dv=None, stream=None, window=None, bottom_right=False,
+                    alibi_slopes=None):
     """Backward pass over packed sequences (layouts as sdpa_fwd_varlen).
     Returns (dq, dk, dv) shaped like q, k, v."""
     return sdpa_bwd_phases_varlen(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, seqstart_q,
                                   seqstart_k, max_seqlen_q, max_seqlen_k, scale=scale,
                                   is_causal=is_causal, dropout_p=dropout_p, seed=seed,
                                   offset=offset, workspace=workspace, dq=dq, dk=dk, dv=dv,
-                                  stream=stream, window=window, bottom_right=bottom_right)
+                                  stream=stream, window=window, bottom_right=bottom_right,
+                                  alibi_slopes=alibi_slopes)
 
 
 def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q,
                            max_seqlen_k, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
                            offset=0, workspace=None, dq=None, dk=None, dv=None, stream=None,
-                           window=None, bottom_right=False):
+                           window=None, bottom_right=False, alibi_slopes=None):
     """The packed-sequence backward phases selected by ``phases``."""
     h, total_q, d_qk = q.shape
     h_kv, total_k, d_v = k.shape[0], k.shape[1], v.shape[2]
@@ -238,7 +257,7 @@ def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k
     need = sdpa_bwd_varlen_workspace_size(b, h, total_q)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    w = _window(is_causal, window, bottom_right)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
     if w is None:
         st = _native.lib().sdpa_bwd_phases_varlen(
             int(phases), b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk,

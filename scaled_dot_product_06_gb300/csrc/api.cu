@@ -174,19 +174,38 @@ namespace {
 struct Mask {
   int64_t left, right;
   int bottom_right;
+  const float* alibi = nullptr;  // ALiBi slopes (device), slope of (b, h) at b * alibi_stride + h
+  int64_t alibi_stride = 0;
 };
 Mask causal_mask(int is_causal) { return Mask{-1, is_causal ? 0 : -1, 0}; }
 
 // A window size of s_q + s_kv or more admits every key on that side: it is
 // stored as unbounded, which keeps the device arithmetic in range.
 // general = 0 for the plain kernels' cases (top-left, causal or unmasked).
-void set_window(const Mask& mk, int64_t s_q, int64_t s_kv, int* left, int* right, int* br,
-                int* general) {
+// ALiBi is aligned top-left under a top-left mask (any window size given),
+// bottom-right otherwise.
+template <typename P>
+void set_window(const Mask& mk, int64_t s_q, int64_t s_kv, P* p) {
   auto norm = [&](int64_t w) { return (w < 0 || w >= s_q + s_kv) ? -1 : static_cast<int>(w); };
-  *left = norm(mk.left);
-  *right = norm(mk.right);
-  *br = mk.bottom_right ? 1 : 0;
-  *general = (*left >= 0 || *right > 0 || *br) ? 1 : 0;
+  p->win_left = norm(mk.left);
+  p->win_right = norm(mk.right);
+  p->win_br = mk.bottom_right ? 1 : 0;
+  p->win_general = (p->win_left >= 0 || p->win_right > 0 || p->win_br) ? 1 : 0;
+  p->alibi = mk.alibi;
+  p->alibi_stride = static_cast<int>(mk.alibi_stride);
+  const bool masked = mk.left >= 0 || mk.right >= 0;
+  p->alibi_br = (masked && !mk.bottom_right) ? 0 : 1;
+}
+
+// ALiBi slopes: 4-byte aligned; the stride between batch rows 0 (one row for
+// all) or at least h, and small enough for an int index.
+sdpa_status_t check_alibi(const Mask& mk, int64_t b, int64_t h) {
+  if (mk.alibi == nullptr) return SDPA_OK;
+  if ((reinterpret_cast<uintptr_t>(mk.alibi) & 3u) != 0) return SDPA_ERR_MISALIGNED;
+  if (mk.alibi_stride < 0 || (mk.alibi_stride > 0 && mk.alibi_stride < h) ||
+      (b - 1) * mk.alibi_stride + h > (int64_t{1} << 30))
+    return fail(SDPA_ERR_INVALID_ARG, "alibi_stride");
+  return SDPA_OK;
 }
 
 // Packed-sequence arguments of the varlen entry points; seqstart_q null means
@@ -237,6 +256,7 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
   if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
   if (sdpa_status_t s = check_packing(pk, b, bias, &empty)) return s;
+  if (sdpa_status_t s = check_alibi(mask, b, h)) return s;
   if (empty) return SDPA_OK;
   if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -258,7 +278,7 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
   p.S_q = static_cast<int>(s_q);
   p.S_kv = static_cast<int>(s_kv);
   p.scale_log2 = scale * kLog2e;
-  set_window(mask, s_q, s_kv, &p.win_left, &p.win_right, &p.win_br, &p.win_general);
+  set_window(mask, s_q, s_kv, &p);
   p.bias = bias;
   p.dropout = dropout_p > 0.0f ? 1 : 0;
   p.drop_threshold = drop_threshold(dropout_p);
@@ -296,6 +316,7 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
   if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
   if (sdpa_status_t s = check_packing(pk, b, bias, &empty)) return s;
+  if (sdpa_status_t s = check_alibi(mask, b, h)) return s;
   if (empty) return SDPA_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
   if ((bias == nullptr) != (dbias == nullptr)) return SDPA_ERR_INVALID_ARG;
@@ -322,7 +343,7 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   p.S_kv = static_cast<int>(s_kv);
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
-  set_window(mask, s_q, s_kv, &p.win_left, &p.win_right, &p.win_br, &p.win_general);
+  set_window(mask, s_q, s_kv, &p);
   p.bias = bias;
   p.dbias = dbias;
   p.dropout = dropout_p > 0.0f ? 1 : 0;
@@ -494,91 +515,98 @@ sdpa_status_t sdpa_bwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_
 // Local windows and the bottom-right alignment (batch and packed forms).
 sdpa_status_t sdpa_fwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                              int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
+                              int64_t window_right, int bottom_right, const float* alibi_slopes,
+                              int64_t alibi_stride, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, void* o, float* lse, void* stream) {
-  return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, Mask{window_left, window_right, bottom_right},
+  return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale,
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
                   dropout_p, seed, offset, dtype, q, k, v, bias, o, lse, stream, Packing{});
 }
 
 sdpa_status_t sdpa_bwd_phases_window(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
                                      int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
                                      int64_t window_left, int64_t window_right, int bottom_right,
+                                     const float* alibi_slopes, int64_t alibi_stride,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
                                      const float* bias, const void* o, const void* dout,
                                      const float* lse, void* dq, void* dk, void* dv, float* dbias,
                                      void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(phases, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right}, dropout_p, seed, offset, dtype, q, k,
-                  v, bias, o, dout, lse, dq, dk, dv, dbias, workspace, workspace_bytes, stream,
-                  Packing{});
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
+                  dropout_p, seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias,
+                  workspace, workspace_bytes, stream, Packing{});
 }
 
 sdpa_status_t sdpa_bwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                              int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
+                              int64_t window_right, int bottom_right, const float* alibi_slopes,
+                              int64_t alibi_stride, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, float* dbias,
                               void* workspace, size_t workspace_bytes, void* stream) {
   return sdpa_bwd_phases_window(SDPA_BWD_ALL, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, window_left,
-                                window_right, bottom_right, dropout_p, seed, offset, dtype, q, k, v,
-                                bias, o, dout, lse, dq, dk, dv, dbias, workspace, workspace_bytes,
-                                stream);
+                                window_right, bottom_right, alibi_slopes, alibi_stride, dropout_p,
+                                seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias,
+                                workspace, workspace_bytes, stream);
 }
 
 sdpa_status_t sdpa_fwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                                     int64_t window_right, int bottom_right, float dropout_p,
-                                     uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
-                                     const int32_t* seqstart_q, const int32_t* seqstart_k,
-                                     const void* q, const void* k, const void* v, void* o,
-                                     float* lse, void* stream) {
+                                     int64_t window_right, int bottom_right,
+                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                                     const int32_t* seqstart_k, const void* q, const void* k,
+                                     const void* v, void* o, float* lse, void* stream) {
   const Packing pk{seqstart_q, seqstart_k, total_q, total_k};
   if (seqstart_q == nullptr || seqstart_k == nullptr) {
     if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
     return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
   return fwd_impl(b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right}, dropout_p, seed, offset, dtype, q, k,
-                  v, nullptr, o, lse, stream, pk);
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
+                  dropout_p, seed, offset, dtype, q, k, v, nullptr, o, lse, stream, pk);
 }
 
 sdpa_status_t sdpa_bwd_phases_varlen_window(
     int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
     int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v, float scale,
-    int64_t window_left, int64_t window_right, int bottom_right, float dropout_p, uint64_t seed,
-    uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q, const int32_t* seqstart_k,
-    const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+    int64_t window_left, int64_t window_right, int bottom_right, const float* alibi_slopes,
+    int64_t alibi_stride, float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+    const int32_t* seqstart_q, const int32_t* seqstart_k, const void* q, const void* k,
+    const void* v, const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
+    void* workspace, size_t workspace_bytes, void* stream) {
   const Packing pk{seqstart_q, seqstart_k, total_q, total_k};
   if (seqstart_q == nullptr || seqstart_k == nullptr) {
     if (b == 0 || h == 0 || total_q == 0 || total_k == 0) return SDPA_OK;
     return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
   return bwd_impl(phases, b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right}, dropout_p, seed, offset, dtype, q, k,
-                  v, nullptr, o, dout, lse, dq, dk, dv, nullptr, workspace, workspace_bytes, stream,
-                  pk);
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
+                  dropout_p, seed, offset, dtype, q, k, v, nullptr, o, dout, lse, dq, dk, dv,
+                  nullptr, workspace, workspace_bytes, stream, pk);
 }
 
 sdpa_status_t sdpa_bwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
-                                     int64_t window_right, int bottom_right, float dropout_p,
-                                     uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
-                                     const int32_t* seqstart_q, const int32_t* seqstart_k,
-                                     const void* q, const void* k, const void* v, const void* o,
-                                     const void* dout, const float* lse, void* dq, void* dk,
-                                     void* dv, void* workspace, size_t workspace_bytes,
-                                     void* stream) {
+                                     int64_t window_right, int bottom_right,
+                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                                     const int32_t* seqstart_k, const void* q, const void* k,
+                                     const void* v, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
   return sdpa_bwd_phases_varlen_window(SDPA_BWD_ALL, b, h, h_kv, total_q, total_k, max_seqlen_q,
                                        max_seqlen_k, d_qk, d_v, scale, window_left, window_right,
-                                       bottom_right, dropout_p, seed, offset, dtype, seqstart_q,
-                                       seqstart_k, q, k, v, o, dout, lse, dq, dk, dv, workspace,
-                                       workspace_bytes, stream);
+                                       bottom_right, alibi_slopes, alibi_stride, dropout_p, seed,
+                                       offset, dtype, seqstart_q, seqstart_k, q, k, v, o, dout, lse,
+                                       dq, dk, dv, workspace, workspace_bytes, stream);
 }
 
 sdpa_status_t sdpa_bwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,

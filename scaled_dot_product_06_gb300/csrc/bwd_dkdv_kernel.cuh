@@ -442,6 +442,12 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         // the thread's columns need masking where they cross S_q or an edge of
         // some key's window (a condition uniform over the warp)
         if constexpr (WIN) {
+          if (p.alibi != nullptr) {  // ALiBi: -slope |j - i - off|, in the log2 domain
+            const float ns = -__ldg(p.alibi + b * p.alibi_stride + h) * kLog2e;
+            const float base = static_cast<float>(kv - qc0 - (p.alibi_br ? S_kv - S_q : 0));
+#pragma unroll
+            for (int c = 0; c < CW; ++c) pr[c] = fmaf(ns, fabsf(base - static_cast<float>(c)), pr[c]);
+          }
           const Band wb = lds_band(band_slot);
           if ((qc0 < k0 + C::BN - 1 - wb.hi) || (qc0 + CW - 1 > k0 - wb.lo) || (qc0 + CW > S_q) ||
               !kv_ok) {
@@ -591,7 +597,7 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
                      : (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, true, W>
                              : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, false, W>);
   };
-  auto kern = p.win_general ? pick(std::true_type{}) : pick(std::false_type{});
+  auto kern = (p.win_general || p.alibi != nullptr) ? pick(std::true_type{}) : pick(std::false_type{});
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;

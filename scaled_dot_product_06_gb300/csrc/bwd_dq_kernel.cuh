@@ -429,6 +429,12 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(QB_SFREE));
       if constexpr (WIN) {
+        if (p.alibi != nullptr) {  // ALiBi: -slope |j - i - off|, in the log2 domain
+          const float ns = -__ldg(p.alibi + b * p.alibi_stride + h) * kLog2e;
+          const float base = static_cast<float>(kc0 - qr - (p.alibi_br ? S_kv - S_q : 0));
+#pragma unroll
+          for (int c = 0; c < CW; ++c) pr[c] = fmaf(ns, fabsf(base + static_cast<float>(c)), pr[c]);
+        }
         // the thread's columns need masking where they cross S_kv or an edge of
         // some row's window (a condition uniform over the warp)
         const Band wb = lds_band(band_slot);
@@ -536,7 +542,7 @@ cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CU
                      : (bias ? sdpa_bwd_dq_kernel<DQK, DV, BF16, false, true, W>
                              : sdpa_bwd_dq_kernel<DQK, DV, BF16, false, false, W>);
   };
-  auto kern = p.win_general ? pick(std::true_type{}) : pick(std::false_type{});
+  auto kern = (p.win_general || p.alibi != nullptr) ? pick(std::true_type{}) : pick(std::false_type{});
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;

@@ -36,6 +36,11 @@ struct FwdParams {
   // unbounded. Causal is (-1, 0, 0); no mask (-1, -1, 0). See Band.
   int win_left, win_right, win_br;
   int win_general;         // 0: top-left, causal (win_right = 0) or unmasked (-1)
+  // ALiBi (null: none): score of (i, j) gets -alibi[b * alibi_stride + h] *
+  // |j - i - off|, off = S_kv - S_q when alibi_br, else 0 (a top-left mask).
+  // Handled by the kernels compiled for general windows.
+  const float* alibi;
+  int alibi_stride, alibi_br;
   const float* bias;       // [1, H, S_q, S_kv] fp32 or null
   int dropout;             // 0 / 1
   uint32_t drop_threshold; // drop iff draw < threshold
@@ -156,6 +161,8 @@ struct BwdParams {
   float scale_log2;        // scale * log2(e)
   int win_left, win_right, win_br;  // visible keys, as in FwdParams
   int win_general;
+  const float* alibi;      // ALiBi slopes, as in FwdParams
+  int alibi_stride, alibi_br;
   const float* bias;       // [1, H, S_q, S_kv] or null
   float* dbias;            // [1, H, S_q, S_kv] or null (accumulated with atomics)
   int dropout;

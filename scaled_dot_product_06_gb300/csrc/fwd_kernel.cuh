@@ -360,6 +360,14 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if constexpr (WIN) {
+        if (p.alibi != nullptr) {  // ALiBi: -slope |j - i - off|, in the log2 domain
+          const float ns = -__ldg(p.alibi + b * p.alibi_stride + h) * kLog2e;
+          const float base = static_cast<float>(k0 - row - (p.alibi_br ? S_kv - S_q : 0));
+#pragma unroll
+          for (int i = 0; i < 128; ++i) x[i] = fmaf(ns, fabsf(base + static_cast<float>(i)), x[i]);
+        }
+      }
+      if constexpr (WIN) {
         // a tile needs masking where it crosses S_kv or an edge of some row's window
         const Band wb = lds_band(band_slot);
         if ((k0 + C::BN > S_kv) || (k0 + C::BN - 1 > qt0 + wb.hi) || (k0 < qt0 + C::BM - 1 + wb.lo)) {
@@ -491,10 +499,11 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
                          const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
   const bool general = p.bias != nullptr || p.dropout != 0;
-  auto kern = general ? (p.win_general ? sdpa_fwd_kernel<DQK, DV, BF16, true, true>
-                                       : sdpa_fwd_kernel<DQK, DV, BF16, true, false>)
-                      : (p.win_general ? sdpa_fwd_kernel<DQK, DV, BF16, false, true>
-                                       : sdpa_fwd_kernel<DQK, DV, BF16, false, false>);
+  const bool win = p.win_general || p.alibi != nullptr;
+  auto kern = general ? (win ? sdpa_fwd_kernel<DQK, DV, BF16, true, true>
+                             : sdpa_fwd_kernel<DQK, DV, BF16, true, false>)
+                      : (win ? sdpa_fwd_kernel<DQK, DV, BF16, false, true>
+                             : sdpa_fwd_kernel<DQK, DV, BF16, false, false>);
   // The warpgroups' setmaxnreg shares add up to exactly 384 x REG_LAUNCH; had
   // the compiler given the kernel another launch register count, the softmax
   // warpgroups' increase could never be granted, so refuse to launch then.

@@ -173,3 +173,15 @@ def test_varlen_arguments_validated_before_any_device_work(lib):
     assert lib.sdpa_bwd_phases_varlen(8, 2, 4, 4, 100, 100, 64, 64, 64, 64, 0.125, 1, 0.0, 0, 0, 0,
                                       S, S, P, P, P, P, P, P, P, P, P, ctypes.c_void_p(256), need,
                                       None) == _native.SDPA_ERR_INVALID_ARG   # unknown phase bit
+
+
+def test_alibi_arguments_validated_before_any_device_work(lib):
+    P = ctypes.c_void_p(16)
+
+    def fwd(slopes, stride, b=2, h=4):
+        return lib.sdpa_fwd_window(b, h, h, 64, 64, 64, 64, 0.125, -1, 0, 0, slopes, stride, 0.0, 0, 0,
+                                   0, P, P, P, None, P, P, None)
+    assert fwd(ctypes.c_void_p(18), 0) == _native.SDPA_ERR_MISALIGNED
+    assert fwd(ctypes.c_void_p(64), -1) == _native.SDPA_ERR_INVALID_ARG
+    assert fwd(ctypes.c_void_p(64), 3) == _native.SDPA_ERR_INVALID_ARG   # 0 < stride < h
+    assert fwd(ctypes.c_void_p(64), 1 << 40) == _native.SDPA_ERR_INVALID_ARG

@@ -130,3 +130,67 @@ def test_diagonal_window_is_exact():
     ref_lse = (q.double() * k.double()).sum(-1) / np.sqrt(D)
     assert (lse.double() - ref_lse).abs().max().item() < 1e-3
     assert dq.abs().max().item() < 1e-3 and dk.abs().max().item() < 1e-3
+
+
+def alibi_slopes(H):
+    """The geometric ALiBi slopes 2^(-8 (h + 1) / H)."""
+    return [2.0 ** (-8.0 * (h + 1) / H) for h in range(H)]
+
+
+# (B, H, H_kv, S_q, S_kv, D, dtype, window, bottom_right, p, per_batch)
+ALIBI_CASES = [
+    (1, 4, 2, 300, 520, 64, "bf16", None, False, 0.0, False),      # unmasked: bottom-right
+    (2, 4, 4, 384, 384, 128, "fp16", (-1, 0), False, 0.0, True),   # causal, slopes per batch
+    (1, 2, 2, 333, 700, 128, "bf16", (200, 0), True, 0.1, False),  # window, bottom-right, dropout
+]
+
+
+@pytest.mark.parametrize("c", ALIBI_CASES, ids=lambda c: f"b{c[0]}h{c[1]}-{c[3]}x{c[4]}-d{c[5]}-"
+                         f"w{c[7]}{'-br' if c[8] else ''}{'-p' if c[9] else ''}")
+def test_alibi_matches_oracle(c):
+    B, H, H_kv, S_q, S_kv, D, dt, win, br, p, per_batch = c
+    x = make_inputs(Shape(B, H, S_q, S_kv, D, D, H_kv), dt)
+    sl = np.array([[s * (1.0 + 0.5 * b) for s in alibi_slopes(H)] for b in range(B)]
+                  if per_batch else [alibi_slopes(H)] * B, dtype=np.float32)
+    slopes_t = torch.tensor(sl if per_batch else sl[0], device="cuda")
+    scale = 1.0 / np.sqrt(D)
+    pr = oracle.Problem(B, H, S_q, S_kv, D, D, scale, False, p, SEED, OFFSET, H_kv, win, br,
+                        alibi_slopes=tuple(tuple(float(v) for v in row) for row in sl))
+    q, k, v, do = (x[n].to("cuda") for n in ("q", "k", "v", "do"))
+    kw = dict(scale=scale, dropout_p=p, seed=SEED, offset=OFFSET, window=win, bottom_right=br,
+              alibi_slopes=slopes_t)
+    o, lse = sdpa_fwd(q, k, v, **kw)
+    dq, dk, dv, _ = sdpa_bwd(q, k, v, o, do, lse, **kw)
+    torch.cuda.synchronize()
+    assert sdpa_device_error() == 0
+    o_ref, lse_ref = oracle.forward(pr, x["q"], x["k"], x["v"])
+    assert_close("o", o, o_ref)
+    assert_lse(lse, lse_ref)
+    dq_r, dk_r, dv_r, _ = oracle.backward(pr, x["q"], x["k"], x["v"], x["do"])
+    assert_close("dq", dq, dq_r)
+    assert_close("dk", dk, dk_r)
+    assert_close("dv", dv, dv_r)
+
+
+def test_packed_alibi_causal_matches_oracle():
+    lq = lk = (130, 257, 64)
+    H, D = 4, 128
+    sl = np.array([[s * (i + 1) for s in alibi_slopes(H)] for i in range(3)], dtype=np.float32)
+    scale = 1.0 / np.sqrt(D)
+    pk = ovl.Packed(tuple(seqstarts(lq)), tuple(seqstarts(lk)), H, D, D, scale, True,
+                    alibi_slopes=tuple(tuple(float(v) for v in row) for row in sl))
+    x = make_packed_inputs(H, sum(lq), sum(lk), D, D, "bf16")
+    q, k, v, do = (x[n].to("cuda") for n in ("q", "k", "v", "do"))
+    st = torch.tensor(seqstarts(lq), dtype=torch.int32, device="cuda")
+    kw = dict(scale=scale, is_causal=True, alibi_slopes=torch.tensor(sl, device="cuda"))
+    o, lse = sdpa_fwd_varlen(q, k, v, st, st, max(lq), max(lk), **kw)
+    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, st, st, max(lq), max(lk), **kw)
+    torch.cuda.synchronize()
+    assert sdpa_device_error() == 0
+    o_ref, lse_ref = ovl.forward(pk, x["q"], x["k"], x["v"])
+    assert_close("o", o, o_ref)
+    assert_lse(lse, lse_ref)
+    dq_r, dk_r, dv_r = ovl.backward(pk, x["q"], x["k"], x["v"], x["do"])
+    assert_close("dq", dq, dq_r)
+    assert_close("dk", dk, dk_r)
+    assert_close("dv", dv, dv_r)
