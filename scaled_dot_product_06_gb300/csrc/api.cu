@@ -208,6 +208,38 @@ sdpa_status_t check_alibi(const Mask& mk, int64_t b, int64_t h) {
   return SDPA_OK;
 }
 
+// A high-priority side stream and two events per (host thread, device), made
+// on first use and kept: the full backward runs the dK/dV kernel there,
+// concurrently with the dQ kernel on the caller's stream (both need only the
+// preprocess output), so that dQ's CTAs fill the SMs dK/dV's last wave leaves
+// idle (dK/dV's CTAs are preferred while any is pending). Per thread, so that
+// concurrent callers never share an event. Returns false if they cannot be
+// made; the kernels then run one after the other on the caller's stream.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+bool side_stream(SideStream* out) {
+  thread_local SideStream cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  SideStream& c = cache[dev];
+  if (c.stream == nullptr) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
+    SideStream n;
+    if (cudaStreamCreateWithPriority(&n.stream, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaStreamDestroy(n.stream);
+      return false;
+    }
+    c = n;
+  }
+  *out = c;
+  return true;
+}
+
 // Packed-sequence arguments of the varlen entry points; seqstart_q null means
 // batch mode (rows of (b, h) contiguous, s_q / s_kv of them).
 struct Packing {
@@ -372,28 +404,56 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
                        pk.seqstart_q, static_cast<int>(b), dvi, dbias_elems, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
   }
+  // Both main kernels requested: dK/dV on the side stream, forked after the
+  // preprocess and joined back before the call returns (see SideStream).
+  SideStream side;
+  const bool fork = (phases & SDPA_BWD_DKDV) && (phases & SDPA_BWD_DQ) && side_stream(&side) &&
+                    cudaEventRecord(side.fork, st) == cudaSuccess &&
+                    cudaStreamWaitEvent(side.stream, side.fork, 0) == cudaSuccess;
+  const cudaStream_t st_dkdv = fork ? side.stream : st;
+  auto join = [&]() {
+    if (fork) {
+      cudaEventRecord(side.join, side.stream);
+      cudaStreamWaitEvent(st, side.join, 0);
+    }
+  };
   if (phases & SDPA_BWD_DKDV) {
     // key/value-stationary kernel: query tiles of 128 rows (64 at d_qk = 192)
     const uint32_t q_rows = d_qk <= 128 ? 128 : 64;
     CUtensorMap mq, mk, mv, mdo;
-    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, q_rows, true)) return s;
-    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, q_rows, true)) return s;
-    e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st)
-             : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dK/dV kernel launch", e);
+    sdpa_status_t ms = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, q_rows, true);
+    if (!ms) ms = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true);
+    if (!ms) ms = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true);
+    if (!ms) ms = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, q_rows, true);
+    if (ms) {
+      join();
+      return ms;
+    }
+    e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
+             : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
+    if (e != cudaSuccess) {
+      join();
+      return fail(SDPA_ERR_CUDA, "backward dK/dV kernel launch", e);
+    }
   }
   if (phases & SDPA_BWD_DQ) {
     CUtensorMap mq, mk, mv, mdo;
-    if (sdpa_status_t s = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true)) return s;
-    if (sdpa_status_t s = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, 128, true)) return s;
+    sdpa_status_t ms = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, 128, true);
+    if (!ms) ms = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true);
+    if (!ms) ms = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true);
+    if (!ms) ms = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, 128, true);
+    if (ms) {
+      join();
+      return ms;
+    }
     e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, p, st)
              : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, p, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dQ kernel launch", e);
+    if (e != cudaSuccess) {
+      join();
+      return fail(SDPA_ERR_CUDA, "backward dQ kernel launch", e);
+    }
   }
+  join();
   return SDPA_OK;
 }
 
