@@ -50,6 +50,10 @@ WORKLOADS = {
     "b1h32kv4-s16384-d128-causal": dict(B=1, H=32, H_kv=4, S_q=16384, S_kv=16384, D_qk=128,
                                         D_v=128, dtype="bf16", causal=True, bias=False, p=0.0,
                                         scale=None),
+    # multi-query attention (one K/V head) at the long-context size
+    "b1h32kv1-s16384-d128-causal": dict(B=1, H=32, H_kv=1, S_q=16384, S_kv=16384, D_qk=128,
+                                        D_v=128, dtype="bf16", causal=True, bias=False, p=0.0,
+                                        scale=None),
     # a sliding window of 4096 keys back (local attention) at the long-context size
     "b1h32-s16384-d128-window4096": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
                                          dtype="bf16", causal=True, window=(4096, 0),
@@ -353,7 +357,8 @@ def main():
         o = torch.empty(shp.B, shp.H, shp.S_q, shp.D_v, dtype=x["q"].dtype, device=dev)
         lse = torch.empty(shp.B, shp.H, shp.S_q, dtype=torch.float32, device=dev)
         ws = torch.empty(sdpa_bwd_workspace_size(shp.B, shp.H, shp.S_q, shp.S_kv, shp.D_qk,
-                                                 shp.D_v), dtype=torch.uint8, device=dev)
+                                                 shp.D_v, shp.kv_heads), dtype=torch.uint8,
+                         device=dev)
 
         def fwd_call(D):
             sdpa_fwd(D["q"], D["k"], D["v"], out=D["o"], lse=D["lse"], bias=D["bias"], **kw)

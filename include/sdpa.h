@@ -174,6 +174,18 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
  * otherwise); with h_kv = h these are exactly sdpa_fwd / sdpa_bwd /
  * sdpa_bwd_phases.
  */
+/*
+ * Workspace for the grouped backward: sdpa_bwd_workspace_size's bytes plus,
+ * when the group is large for the number of key tiles (e.g. MQA at a small
+ * batch), room for splitting each group's query heads over several CTAs per
+ * key tile (fp32 partial dK / dV rows and one counter per key tile; the last
+ * CTA of a tile adds the partials in a fixed order, so results stay bitwise
+ * reproducible). sdpa_bwd_gqa / sdpa_bwd_phases_gqa split only when given
+ * at least this many bytes and run one CTA per key tile with the smaller
+ * workspace. 0 for invalid sizes.
+ */
+size_t sdpa_bwd_workspace_size_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                                   int64_t d_qk, int64_t d_v);
 sdpa_status_t sdpa_fwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                            int64_t d_qk, int64_t d_v, float scale, int is_causal, float dropout_p,
                            uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,

@@ -31,6 +31,7 @@ SIGNATURES = {
     "sdpa_fwd": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64, _int,
                         _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
     "sdpa_bwd_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64]),
+    "sdpa_bwd_workspace_size_gqa": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64, _i64]),
     "sdpa_bwd": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64, _int,
                         _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                         _sz, _ptr]),

@@ -103,8 +103,12 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
     return out, lse
 
 
-def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v) -> int:
-    return int(_native.lib().sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v))
+def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv=None) -> int:
+    """Backward workspace bytes; with h_kv (grouped K/V heads) the room for
+    splitting large groups over several CTAs per key tile is included."""
+    if h_kv is None or h_kv == h:
+        return int(_native.lib().sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v))
+    return int(_native.lib().sdpa_bwd_workspace_size_gqa(b, h, h_kv, s_q, s_kv, d_qk, d_v))
 
 
 def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
@@ -141,7 +145,7 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
     dv = torch.empty_like(v) if dv is None else dv
     if bias is not None and dbias is None:
         dbias = torch.empty_like(bias)
-    need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v)
+    need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)

@@ -240,6 +240,34 @@ bool side_stream(SideStream* out) {
   return true;
 }
 
+// Grouped K/V heads whose key tiles make few CTAs split each group's query
+// heads over several CTAs per key tile (BwdParams::kv_split): the largest
+// divisor of the group size not above ceil(8 * 152 / CTAs), about eight CTAs
+// per SM of a GB300; 1 without groups. Batch mode only.
+int64_t dkdv_splits(int64_t b, int64_t h, int64_t h_kv, int64_t s_kv) {
+  if (h_kv <= 0 || h <= h_kv || b <= 0 || s_kv <= 0) return 1;
+  const int64_t grp = h / h_kv;
+  const int64_t ctas = ((s_kv + 127) / 128) * b * h_kv;
+  const int64_t want = (8 * 152 + ctas - 1) / ctas;
+  int64_t best = 1;
+  for (int64_t d = 1; d <= grp; ++d)
+    if (grp % d == 0 && d <= want) best = d;
+  return best;
+}
+
+// Workspace of a split dK/dV past the row statistics: one counter per key
+// tile (rounded up to 256 bytes), then the fp32 partial rows.
+size_t split_counter_bytes(int64_t b, int64_t h_kv, int64_t s_kv) {
+  const size_t tiles = static_cast<size_t>((s_kv + 127) / 128) * b * h_kv;
+  return (tiles * sizeof(int) + 255) & ~size_t(255);
+}
+size_t split_bytes(int64_t b, int64_t h, int64_t h_kv, int64_t s_kv, int64_t d_qk, int64_t d_v) {
+  const int64_t ns = dkdv_splits(b, h, h_kv, s_kv);
+  if (ns <= 1) return 0;
+  const size_t tiles = static_cast<size_t>((s_kv + 127) / 128) * b * h_kv;
+  return split_counter_bytes(b, h_kv, s_kv) + tiles * ns * 128 * (d_qk + d_v) * sizeof(float);
+}
+
 // Packed-sequence arguments of the varlen entry points; seqstart_q null means
 // batch mode (rows of (b, h) contiguous, s_q / s_kv of them).
 struct Packing {
@@ -360,6 +388,10 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
                                     : sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v);
   if (workspace == nullptr || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SDPA_ERR_MISALIGNED;
+  // A split dK/dV when the group is large for the grid and the workspace has
+  // the room sdpa_bwd_workspace_size_gqa asks for; else one CTA per key tile.
+  int64_t kv_split = pk.seqstart_q ? 1 : dkdv_splits(b, h, h_kv, s_kv);
+  if (kv_split > 1 && workspace_bytes < need + split_bytes(b, h, h_kv, s_kv, d_qk, d_v)) kv_split = 1;
 
   const bool bf16 = dtype == SDPA_BF16;
   const CUtensorMapDataType tt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -394,6 +426,13 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   p.seqstart_k = pk.seqstart_k;
   p.rows_q = static_cast<int>(rw.q);
   p.rows_k = static_cast<int>(rw.k);
+  p.kv_split = static_cast<int>(kv_split);
+  const int n_counters = kv_split > 1 ? static_cast<int>(((s_kv + 127) / 128) * b * h_kv) : 0;
+  if (kv_split > 1) {
+    uint8_t* extra = static_cast<uint8_t*>(workspace) + need;
+    p.dkdv_count = reinterpret_cast<int*>(extra);
+    p.dkdv_part = reinterpret_cast<float*>(extra + split_counter_bytes(b, h_kv, s_kv));
+  }
   if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -401,7 +440,8 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   if (phases & SDPA_BWD_PREPROCESS) {
     const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
     e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, rw.zq, static_cast<int>(s_q), p.S_pad, p.rows_q,
-                       pk.seqstart_q, static_cast<int>(b), dvi, dbias_elems, st);
+                       pk.seqstart_q, static_cast<int>(b), dvi, dbias_elems, p.dkdv_count, n_counters,
+                       st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
   }
   // Both main kernels requested: dK/dV on the side stream, forked after the
@@ -483,6 +523,13 @@ sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns) {
   g_debug_fault.store(fault);
   g_debug_wait_ns.store(wait_limit_ns);
   return SDPA_OK;
+}
+
+size_t sdpa_bwd_workspace_size_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                                   int64_t d_qk, int64_t d_v) {
+  const size_t base = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v);
+  if (base == 0 || !kv_heads_ok(h, h_kv)) return 0;
+  return base + split_bytes(b, h, h_kv, s_kv, d_qk, d_v);
 }
 
 size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,

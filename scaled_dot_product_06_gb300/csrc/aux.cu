@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
                                                               float4* __restrict__ dbias,
                                                               int64_t z_count, int s_q, int s_pad,
                                                               int rows, const int* __restrict__ seqstart,
-                                                              int n_seq, int d_v, int64_t dbias_elems) {
+                                                              int n_seq, int d_v, int64_t dbias_elems,
+                                                              int* __restrict__ counters, int n_counters) {
   const int group = d_v / 8;  // 8 or 16 threads per row (power of two)
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
   const int64_t dbias_vec = dbias_elems / 4;
   for (int64_t i = tid; i < dbias_vec; i += nthreads) dbias[i] = z;
   if (tid < (dbias_elems & 3)) reinterpret_cast<float*>(dbias)[dbias_vec * 4 + tid] = 0.f;
+  for (int64_t i = tid; i < n_counters; i += nthreads) counters[i] = 0;  // split dK/dV tiles
 }
 
 // Word w holds the keep bits of elements 32w .. 32w+31 (bit e = element 32w+e).
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(kAuxThreads) dropout_mask_kernel(int64_t total
 cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
                            float* dbias, int64_t z_count, int s_q, int s_pad, int rows,
                            const int* seqstart, int n_seq, int d_v, int64_t dbias_elems,
-                           cudaStream_t st) {
+                           int* counters, int n_counters, cudaStream_t st) {
   const int group = d_v / 8;
   const int64_t work = z_count * s_pad * group;
   const int64_t zero_work = dbias_elems / 4;
@@ -128,7 +130,7 @@ cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const flo
   auto kern = bf16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
   kern<<<grid, kAuxThreads, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, stats,
                                       reinterpret_cast<float4*>(dbias), z_count, s_q, s_pad, rows, seqstart,
-                                      n_seq, d_v, dbias_elems);
+                                      n_seq, d_v, dbias_elems, counters, n_counters);
   return cudaGetLastError();
 }
 

@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   // (kept out of the registers of the compute loop)
   uint64_t* key_row0 = bars + AB_COUNT + 1;
   Band* band_slot = reinterpret_cast<Band*>(bars + AB_COUNT + 2);  // see lds_band
-  static_assert((AB_COUNT + 3) * 8 <= 256, "barrier region");
+  volatile int* last_split = reinterpret_cast<volatile int*>(bars + AB_COUNT + 3);
+  static_assert((AB_COUNT + 4) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -148,15 +149,19 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   // ---- key tile of this CTA: K/V-head-major (one head's Q / dO stay in L2),
   // then the key tiles with the most query work first, batch fastest (the
   // batches of one head share Bias and dBias rows)
+  // (with kv_split > 1, the splits of one key tile next to each other)
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
+  const int nsp = p.kv_split;
   const int b = static_cast<int>(blockIdx.x % p.B);
   const int rest = static_cast<int>(blockIdx.x / p.B);
-  const int kt = rest % n_kt, hk = rest / n_kt;  // hk: K/V head
+  const int sp = rest % nsp;  // split: query heads [sp * gs, sp * gs + gs) of the group
+  const int kt = (rest / nsp) % n_kt, hk = (rest / nsp) / n_kt;  // hk: K/V head
   const SeqSlice sl = seq_slice(p.seqstart_q, p.seqstart_k, p.rows_q, p.rows_k, p.S_q, p.S_kv, p.H,
                                 p.H_kv, b);
   const int S_q = sl.len_q, S_kv = sl.len_k;  // this sequence's lengths
   const int zk = sl.zk0 + hk;                 // tensor-map z of the K/V head
   const int grp = p.H / p.H_kv;  // query heads sharing this K/V head
+  const int gs = grp / nsp;      // of them, those this CTA sums over
   const int k0 = kt * C::BN;
   // A key tile past the end of a shorter packed sequence has nothing to do
   // (uniform over the CTA; never in batch mode).
@@ -175,11 +180,14 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     it0 = p.win_right >= 0 ? min(n_qt, k0 / BM) : 0;
     n_per = n_qt - it0;
   }
-  // One loop over (query head of the group, query tile): iteration i visits
-  // query head hk * grp + i / n_per and query tile it0 + i % n_per, so dK and
-  // dV sum over the whole group inside tensor memory.
-  const int n_it = n_per * grp;
-  auto qhead = [&](int i) { return hk * grp + i / n_per; };
+  // A key tile no query sees: its first split writes the zeros alone.
+  if (nsp > 1 && n_per == 0 && sp != 0) return;
+  // One loop over (query head of the split, query tile): iteration i visits
+  // query head hk * grp + sp * gs + i / n_per and query tile it0 + i % n_per,
+  // so dK and dV sum over the split's heads (the whole group when
+  // kv_split = 1) inside tensor memory.
+  const int n_it = n_per * gs;
+  auto qhead = [&](int i) { return hk * grp + sp * gs + i / n_per; };
   auto qtile0 = [&](int i) { return (it0 + i % n_per) * BM; };
 
   if (threadIdx.x == 0) {
@@ -542,7 +550,63 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     // a key tile that no query sees)
     const bool have = n_it > 0;
     const bool ready = have && ok && mbar_wait(bar(AB_DKDV), 0, ec, kSiteBwdCompute);
-    if (!have || ready) {
+    if (nsp > 1 && have) {
+      // Split key tile: this CTA's fp32 sums as partial rows [dK | dV], then
+      // the last split to count itself in adds all partials in split order.
+      constexpr int RW = DQK + DV;
+      const int tile = (hk * n_kt + kt) * p.B + b;
+      float* part0 = p.dkdv_part + static_cast<size_t>(tile) * nsp * (C::BN * RW);
+      if (ready) tc_fence_after();
+      // tcgen05.ld is warp-collective: the loads run on the warp-uniform
+      // condition (ready, hf), only the stores on the per-lane kv_ok
+      if (ready && hf < 2) {
+        float* dst = part0 + (static_cast<size_t>(sp) * C::BN + row) * RW + (hf == 0 ? DQK : 0);
+        const uint32_t tcol = hf == 0 ? C::T_DV : C::T_DK;
+        const int W = hf == 0 ? DV : DQK;
+        for (int c = 0; c < W / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tbase + tcol + lane_off + c * 32, a);
+          tmem_wait_ld();
+          if (kv_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              d4[e] = make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                  __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
+          }
+        }
+      }
+      __threadfence();
+      named_bar_sync(1, NCT);
+      if (threadIdx.x == 0)
+        *last_split = ready ? (atomicAdd(p.dkdv_count + tile, 1) == nsp - 1) : 0;
+      named_bar_sync(1, NCT);
+      if (*last_split) {
+        __threadfence();
+        if (kv_ok && hf < 2) {
+          const size_t rowi = static_cast<size_t>(*key_row0) + row;
+          const int W = hf == 0 ? DV : DQK;
+          const float mul = hf == 0 ? 1.0f : p.scale;
+          const float* src = part0 + static_cast<size_t>(row) * RW + (hf == 0 ? DQK : 0);
+          uint8_t* dst_row = static_cast<uint8_t*>(hf == 0 ? p.dv : p.dk) + rowi * W * 2;
+          for (int c = 0; c < W / 8; ++c) {
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            for (int s2 = 0; s2 < nsp; ++s2) {  // split order: the same sum whoever is last
+              const float4* s4 = reinterpret_cast<const float4*>(src + static_cast<size_t>(s2) * C::BN * RW + c * 8);
+              const float4 u = __ldcg(s4), w = __ldcg(s4 + 1);
+              acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
+              acc[4] += w.x; acc[5] += w.y; acc[6] += w.z; acc[7] += w.w;
+            }
+            reinterpret_cast<uint4*>(dst_row)[c] =
+                make_uint4(pack2<BF16>(acc[0] * mul, acc[1] * mul), pack2<BF16>(acc[2] * mul, acc[3] * mul),
+                           pack2<BF16>(acc[4] * mul, acc[5] * mul), pack2<BF16>(acc[6] * mul, acc[7] * mul));
+          }
+        }
+        if (threadIdx.x == 0) p.dkdv_count[tile] = 0;  // ready for the next call
+      }
+    } else if (!have || ready) {
       if (ready) tc_fence_after();
       const size_t rowi = static_cast<size_t>(*key_row0) + (kv_ok ? row : 0);
       auto write_rows = [&](auto width_tag, uint32_t tcol, void* base, float mul) {
@@ -601,7 +665,7 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
-  const long long grid = static_cast<long long>(n_kt) * p.B * p.H_kv;
+  const long long grid = static_cast<long long>(n_kt) * p.B * p.H_kv * p.kv_split;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, p);
   return cudaGetLastError();
 }

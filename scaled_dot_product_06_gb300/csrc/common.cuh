@@ -163,6 +163,14 @@ struct BwdParams {
   int win_general;
   const float* alibi;      // ALiBi slopes, as in FwdParams
   int alibi_stride, alibi_br;
+  // Grouped K/V heads with a small grid: kv_split CTAs share a key tile, each
+  // summing dK / dV over grp / kv_split query heads into fp32 partial rows
+  // (dkdv_part, [tile][split][BN][d_qk + d_v]); the last of them to count
+  // itself in (dkdv_count[tile]) adds the partials in split order and writes
+  // dK / dV, so the result does not depend on which CTA finished last.
+  int kv_split;
+  float* dkdv_part;
+  int* dkdv_count;
   const float* bias;       // [1, H, S_q, S_kv] or null
   float* dbias;            // [1, H, S_q, S_kv] or null (accumulated with atomics)
   int dropout;
@@ -330,7 +338,7 @@ cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CU
 cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
                            float* dbias, int64_t z_count, int s_q, int s_pad, int rows,
                            const int* seqstart, int n_seq, int d_v, int64_t dbias_elems,
-                           cudaStream_t st);
+                           int* counters, int n_counters, cudaStream_t st);
 cudaError_t launch_dropout_mask(int64_t total, uint32_t threshold, uint32_t seed_lo,
                                 uint32_t seed_hi, uint32_t off_lo, uint32_t off_hi,
                                 uint32_t* bits, cudaStream_t st);

@@ -185,3 +185,24 @@ def test_alibi_arguments_validated_before_any_device_work(lib):
     assert fwd(ctypes.c_void_p(64), -1) == _native.SDPA_ERR_INVALID_ARG
     assert fwd(ctypes.c_void_p(64), 3) == _native.SDPA_ERR_INVALID_ARG   # 0 < stride < h
     assert fwd(ctypes.c_void_p(64), 1 << 40) == _native.SDPA_ERR_INVALID_ARG
+
+
+def test_grouped_workspace_size(lib):
+    """sdpa_bwd_workspace_size_gqa: the ungrouped bytes, plus for a large group
+    on few key tiles one counter per tile (rounded to 256 bytes) and fp32
+    partial rows for each split (the largest divisor of the group not above
+    ceil(8 * 152 / tiles))."""
+    base = lib.sdpa_bwd_workspace_size(1, 32, 16384, 16384, 128, 128)
+    assert lib.sdpa_bwd_workspace_size_gqa(1, 32, 32, 16384, 16384, 128, 128) == base
+    # MQA: 128 key tiles -> want ceil(1216 / 128) = 10 -> split 8
+    tiles, split = 128, 8
+    extra = 512 + tiles * split * 128 * 256 * 4
+    assert lib.sdpa_bwd_workspace_size_gqa(1, 32, 1, 16384, 16384, 128, 128) == base + extra
+    # GQA 8 groups of 4 K/V heads: 512 tiles -> want 3 -> split 2
+    tiles, split = 512, 2
+    extra = 2048 + tiles * split * 128 * 256 * 4
+    assert lib.sdpa_bwd_workspace_size_gqa(1, 32, 4, 16384, 16384, 128, 128) == base + extra
+    # many tiles: no split
+    assert lib.sdpa_bwd_workspace_size_gqa(8, 32, 8, 8192, 8192, 128, 128) == \
+        lib.sdpa_bwd_workspace_size(8, 32, 8192, 8192, 128, 128)
+    assert lib.sdpa_bwd_workspace_size_gqa(1, 32, 3, 128, 128, 128, 128) == 0  # 3 does not divide 32

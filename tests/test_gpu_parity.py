@@ -84,7 +84,9 @@ def test_backward_is_bitwise_reproducible():
 
 def test_grouped_backward_is_bitwise_reproducible():
     """With grouped K/V heads, dK and dV of a K/V head are summed over its
-    query heads inside one CTA in a fixed order: identical bits run to run."""
+    query heads in a fixed order (inside one CTA, or over the CTAs of a split
+    key tile in split order whichever finishes last): identical bits run to
+    run."""
     from parity_util import run_gpu
     from scaled_dot_product_06_gb300.inputs import make_inputs
     case = Case(1, 8, 256, 256, 128, 128, causal=True, H_kv=2)
@@ -93,3 +95,24 @@ def test_grouped_backward_is_bitwise_reproducible():
     second = run_gpu(case, x)
     for a, b in zip(first[2:5], second[2:5]):
         assert torch.equal(a, b)
+
+
+def test_grouped_backward_without_split_room():
+    """Given only the ungrouped workspace size, a grouped backward runs one CTA
+    per key tile (no split) and still matches the oracle."""
+    import oracle
+    from parity_util import assert_close
+    from scaled_dot_product_06_gb300 import sdpa_bwd, sdpa_bwd_workspace_size, sdpa_fwd
+    from scaled_dot_product_06_gb300.inputs import make_inputs
+    case = Case(1, 4, 384, 256, 128, 128, causal=True, H_kv=1)
+    x = make_inputs(case.shape, case.dtype)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    small = sdpa_bwd_workspace_size(1, 4, 384, 256, 128, 128)
+    assert small < sdpa_bwd_workspace_size(1, 4, 384, 256, 128, 128, h_kv=1)
+    ws = torch.empty(small, dtype=torch.uint8, device="cuda")
+    o, lse = sdpa_fwd(q, k, v, is_causal=True)
+    dq, dk, dv, _ = sdpa_bwd(q, k, v, o, do, lse, is_causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    _, dk_r, dv_r, _ = oracle.backward(case.problem(), x["q"], x["k"], x["v"], x["do"])
+    assert_close("dk", dk, dk_r)
+    assert_close("dv", dv, dv_r)
