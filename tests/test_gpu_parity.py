@@ -116,3 +116,27 @@ def test_grouped_backward_without_split_room():
     _, dk_r, dv_r, _ = oracle.backward(case.problem(), x["q"], x["k"], x["v"], x["do"])
     assert_close("dk", dk, dk_r)
     assert_close("dv", dv, dv_r)
+
+
+@pytest.mark.parametrize("h_kv", [8, 2])
+def test_concurrent_backward_equals_phases_bitwise(h_kv):
+    """sdpa_bwd runs dK/dV on a side stream next to dQ; the same kernels run
+    one after the other through sdpa_bwd_phases give the same bits."""
+    from scaled_dot_product_06_gb300 import (SDPA_BWD_DKDV, SDPA_BWD_DQ, SDPA_BWD_PREPROCESS,
+                                             sdpa_bwd, sdpa_bwd_phases, sdpa_bwd_workspace_size,
+                                             sdpa_fwd)
+    from scaled_dot_product_06_gb300.inputs import make_inputs
+    case = Case(2, 8, 640, 640, 128, 128, causal=True, H_kv=h_kv)
+    x = make_inputs(case.shape, case.dtype, device="cuda")
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o, lse = sdpa_fwd(q, k, v, is_causal=True)
+    a = sdpa_bwd(q, k, v, o, do, lse, is_causal=True)
+    ws = torch.empty(sdpa_bwd_workspace_size(2, 8, 640, 640, 128, 128, h_kv=h_kv),
+                     dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for ph in (SDPA_BWD_PREPROCESS, SDPA_BWD_DKDV, SDPA_BWD_DQ):
+        sdpa_bwd_phases(ph, q, k, v, o, do, lse, is_causal=True, dq=dq, dk=dk, dv=dv,
+                        workspace=ws)
+    torch.cuda.synchronize()
+    for x1, x2 in zip(a[:3], (dq, dk, dv)):
+        assert torch.equal(x1, x2)
