@@ -43,6 +43,11 @@ WORKLOADS = {
     "b8h16-s1024x2048-d64-fp16-dropout0.1": dict(B=8, H=16, S_q=1024, S_kv=2048, D_qk=64, D_v=64,
                                                  dtype="fp16", causal=False, bias=False, p=0.1,
                                                  scale=None),
+    # the dropout case with its keep bits drawn once per step (sdpa_dropout_mask,
+    # timed with the forward) and read by the three kernels
+    "b8h16-s1024x2048-d64-fp16-dropout0.1-bits": dict(B=8, H=16, S_q=1024, S_kv=2048, D_qk=64,
+                                                      D_v=64, dtype="fp16", causal=False,
+                                                      bias=False, p=0.1, scale=None, bits=True),
     "b1h32-s16384-d128-causal": dict(B=1, H=32, S_q=16384, S_kv=16384, D_qk=128, D_v=128,
                                      dtype="bf16", causal=True, bias=False, p=0.0, scale=None),
     # grouped-query attention at the long-context size: 32 query heads on 4 K/V
@@ -304,6 +309,7 @@ def main():
 
     from scaled_dot_product_06_gb300 import (SDPA_BWD_ALL, SDPA_BWD_DKDV, SDPA_BWD_DQ,
                                              SDPA_BWD_PREPROCESS, sdpa_bwd_phases,
+                                             sdpa_dropout_mask,
                                              sdpa_bwd_phases_varlen, sdpa_bwd_varlen_workspace_size,
                                              sdpa_bwd_workspace_size, sdpa_device_error, sdpa_fwd,
                                              sdpa_fwd_varlen)
@@ -326,6 +332,10 @@ def main():
               offset=DROP_OFFSET)
     if w.get("window") is not None or w.get("bottom_right"):
         kw.update(window=w.get("window"), bottom_right=w.get("bottom_right", False))
+    mask_words = 0
+    if w.get("bits"):
+        mask_words = (w["B"] * w["H"] * w["S_q"] * w["S_kv"] + 31) // 32
+        kw["dropout_mask"] = torch.empty(mask_words, dtype=torch.int32, device=dev)
     if w.get("alibi"):
         kw["alibi_slopes"] = torch.tensor([2.0 ** (-8.0 * (hh + 1) / w["H"]) for hh in range(w["H"])],
                                           dtype=torch.float32, device=dev)
@@ -384,6 +394,9 @@ def main():
         # dK/dV start, dK/dV end (the last two on the side stream)
         if ev is not None:
             ev[0].record(stream)
+        if mask_words:  # the keep bits of this step, drawn once for all three kernels
+            sdpa_dropout_mask(w["B"], w["H"], w["S_q"], w["S_kv"], w["p"], DROP_SEED, DROP_OFFSET,
+                              out=kw["dropout_mask"])
         fwd_call(set0)
         if ev is not None:
             ev[1].record(stream)
@@ -504,6 +517,9 @@ def main():
                 ev_in[i].record(s_in)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in[i])
+                if mask_words:
+                    sdpa_dropout_mask(w["B"], w["H"], w["S_q"], w["S_kv"], w["p"], DROP_SEED,
+                                      DROP_OFFSET, out=kw["dropout_mask"], stream=s_cmp)
                 fwd_call(D)
                 bwd_call(SDPA_BWD_ALL, D)
                 ev_cmp[i].record(s_cmp)
@@ -564,7 +580,7 @@ def main():
             "bwd_tflops": 2.5 * ff / (bwd_ms * 1e-3) / 1e12,
             "kernels": kt,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": (5 if mask_words else 4) * args.steps,
         }
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -264,7 +264,8 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Local windows, the bottom-right alignment and ALiBi (CK tile
+ * Local windows, the bottom-right alignment, ALiBi and dropout bits drawn
+ * beforehand (CK tile
  * fmha_bwd_kernel.hpp mask arguments window_size_left, window_size_right and
  * mask_type, and its ALiBi slopes alibi_slope_ptr / alibi_slope_stride;
  * oneDNN sdpa micro.cpp's top_left and bottom_right attention masks). The
@@ -283,60 +284,65 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
  *            0, else s_kv - s_q. 4-byte aligned (SDPA_ERR_MISALIGNED).
  *   alibi_stride  0 (one slope per head for every batch entry) or >= h
  *            (SDPA_ERR_INVALID_ARG otherwise).
+ *   keep_bits  null, or the dropout keep bits of the whole problem drawn
+ *            beforehand by sdpa_dropout_mask with the same b, h, s_q, s_kv (the
+ *            max lengths when packed), p, seed and offset (DEVICE, 4-byte
+ *            aligned): the kernels then read them instead of drawing Philox
+ *            numbers, with identical results. Ignored when dropout_p is 0.
  * Causal is (-1, 0, 0), bottom-right causal (-1, 0, 1), a sliding window of
  * w keys back (w, 0, 0), no mask (-1, -1, 0). A query row that sees no key
  * gets O = 0, LSE = -inf and dQ = 0; a key no query sees gets dK = dV = 0.
  * Key tiles outside every window of a tile's rows are skipped, so a window of
  * w keys costs about (w + 128) / s_kv of the unmasked work.
  */
-sdpa_status_t sdpa_fwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+sdpa_status_t sdpa_fwd_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                               int64_t window_right, int bottom_right, const float* alibi_slopes,
-                              int64_t alibi_stride, float dropout_p, uint64_t seed,
+                              int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, void* o, float* lse, void* stream);
-sdpa_status_t sdpa_bwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+sdpa_status_t sdpa_bwd_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                               int64_t window_right, int bottom_right, const float* alibi_slopes,
-                              int64_t alibi_stride, float dropout_p, uint64_t seed,
+                              int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, float* dbias,
                               void* workspace, size_t workspace_bytes, void* stream);
-sdpa_status_t sdpa_bwd_phases_window(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
+sdpa_status_t sdpa_bwd_phases_ex(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
                                      int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
                                      int64_t window_left, int64_t window_right, int bottom_right,
-                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
                                      const float* bias, const void* o, const void* dout,
                                      const float* lse, void* dq, void* dk, void* dv, float* dbias,
                                      void* workspace, size_t workspace_bytes, void* stream);
-sdpa_status_t sdpa_fwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+sdpa_status_t sdpa_fwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                                      int64_t window_right, int bottom_right,
-                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const int32_t* seqstart_q,
                                      const int32_t* seqstart_k, const void* q, const void* k,
                                      const void* v, void* o, float* lse, void* stream);
-sdpa_status_t sdpa_bwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+sdpa_status_t sdpa_bwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                                      int64_t window_right, int bottom_right,
-                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const int32_t* seqstart_q,
                                      const int32_t* seqstart_k, const void* q, const void* k,
                                      const void* v, const void* o, const void* dout,
                                      const float* lse, void* dq, void* dk, void* dv,
                                      void* workspace, size_t workspace_bytes, void* stream);
-sdpa_status_t sdpa_bwd_phases_varlen_window(
+sdpa_status_t sdpa_bwd_phases_varlen_ex(
     int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
     int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v, float scale,
     int64_t window_left, int64_t window_right, int bottom_right, const float* alibi_slopes,
-    int64_t alibi_stride, float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+    int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
     const int32_t* seqstart_q, const int32_t* seqstart_k, const void* q, const void* k,
     const void* v, const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
     void* workspace, size_t workspace_bytes, void* stream);

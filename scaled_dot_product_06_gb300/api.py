@@ -36,12 +36,16 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h):
-    """(left, right, bottom_right, slopes pointer, slope stride) for the window
-    entry points, or None for the plain causal / unmasked calls. alibi_slopes:
-    fp32 CUDA [h] (every batch entry) or [n_batch, h]."""
-    if window is None and not bottom_right and alibi_slopes is None:
+def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h, dropout_mask=None):
+    """(left, right, bottom_right, slopes pointer, slope stride, keep-bits
+    pointer) for the *_ex entry points, or None for the plain causal / unmasked
+    calls. alibi_slopes: fp32 CUDA [h] (every batch entry) or [n_batch, h];
+    dropout_mask: the int32 words of sdpa_dropout_mask for the same problem."""
+    if window is None and not bottom_right and alibi_slopes is None and dropout_mask is None:
         return None
+    if dropout_mask is not None and (not dropout_mask.is_cuda or dropout_mask.dtype != torch.int32
+                                     or not dropout_mask.is_contiguous()):
+        raise ValueError("dropout_mask must be the contiguous int32 CUDA words of sdpa_dropout_mask")
     left, right = window if window is not None else (-1, 0 if is_causal else -1)
     stride = 0
     if alibi_slopes is not None:
@@ -55,12 +59,12 @@ def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h):
         else:
             raise ValueError(f"alibi_slopes has shape {tuple(a.shape)}, expected ({h},) or "
                              f"({n_batch}, {h})")
-    return int(left), int(right), int(bool(bottom_right)), _ptr(alibi_slopes), stride
+    return int(left), int(right), int(bool(bottom_right)), _ptr(alibi_slopes), stride, _ptr(dropout_mask)
 
 
 def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0,
              bias=None, out=None, lse=None, stream=None, window=None, bottom_right=False,
-             alibi_slopes=None):
+             alibi_slopes=None, dropout_mask=None):
     """Forward pass. Returns (o [b,h,s_q,d_v], lse fp32 [b,h,s_q]).
 
     k and v may have fewer heads than q (grouped-query attention): h_kv =
@@ -87,7 +91,7 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
         lse = torch.empty((b, h, s_q), dtype=torch.float32, device=q.device)
     _check_io("out", out, (b, h, s_q, d_v), dt)
     _check_io("lse", lse, (b, h, s_q), torch.float32)
-    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)
     if w is None:
         st = _native.lib().sdpa_fwd_gqa(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
                                         float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
@@ -95,11 +99,11 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
                                         ctypes.c_void_p(_stream_ptr(stream)))
         _native.check(st, "sdpa_fwd_gqa")
     else:
-        st = _native.lib().sdpa_fwd_window(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, *w,
+        st = _native.lib().sdpa_fwd_ex(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, *w,
                                            float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
                                            _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out),
                                            _ptr(lse), ctypes.c_void_p(_stream_ptr(stream)))
-        _native.check(st, "sdpa_fwd_window")
+        _native.check(st, "sdpa_fwd_ex")
     return out, lse
 
 
@@ -113,19 +117,21 @@ def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv=None) -> int:
 
 def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
              offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None, dbias=None,
-             stream=None, window=None, bottom_right=False, alibi_slopes=None):
+             stream=None, window=None, bottom_right=False, alibi_slopes=None,
+             dropout_mask=None):
     """Backward pass. Returns (dq, dk, dv, dbias or None); dk and dv have k's
     and v's shapes (with grouped K/V heads, sums over each group)."""
     return sdpa_bwd_phases(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, scale=scale,
                            is_causal=is_causal, dropout_p=dropout_p, seed=seed, offset=offset,
                            bias=bias, workspace=workspace, dq=dq, dk=dk, dv=dv, dbias=dbias,
                            stream=stream, window=window, bottom_right=bottom_right,
-                           alibi_slopes=alibi_slopes)
+                           alibi_slopes=alibi_slopes, dropout_mask=dropout_mask)
 
 
 def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0,
                     seed=0, offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None,
-                    dbias=None, stream=None, window=None, bottom_right=False, alibi_slopes=None):
+                    dbias=None, stream=None, window=None, bottom_right=False, alibi_slopes=None,
+             dropout_mask=None):
     """The backward phases selected by ``phases`` (SDPA_BWD_* bit mask)."""
     b, h, s_q, d_qk = q.shape
     h_kv, s_kv, d_v = k.shape[1], k.shape[2], v.shape[3]
@@ -148,7 +154,7 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
     need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)
     if w is None:
         st = _native.lib().sdpa_bwd_phases_gqa(
             int(phases), b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
@@ -157,12 +163,12 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
             _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream_ptr(stream)))
         _native.check(st, "sdpa_bwd_phases_gqa")
     else:
-        st = _native.lib().sdpa_bwd_phases_window(
+        st = _native.lib().sdpa_bwd_phases_ex(
             int(phases), b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, *w, float(dropout_p), int(seed),
             int(offset), _DTYPE_CODE[dt], _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o),
             _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
             workspace.numel(), ctypes.c_void_p(_stream_ptr(stream)))
-        _native.check(st, "sdpa_bwd_phases_window")
+        _native.check(st, "sdpa_bwd_phases_ex")
     return dq, dk, dv, dbias
 
 
@@ -176,7 +182,8 @@ def _check_seqstart(name: str, t: torch.Tensor) -> int:
 
 def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *, scale=None,
                     is_causal=False, dropout_p=0.0, seed=0, offset=0, out=None, lse=None,
-                    stream=None, window=None, bottom_right=False, alibi_slopes=None):
+                    stream=None, window=None, bottom_right=False, alibi_slopes=None,
+             dropout_mask=None):
     """Forward pass over packed variable-length sequences. q [h, total_q, d_qk],
     k [h_kv, total_k, d_qk], v [h_kv, total_k, d_v]; seqstart_q / seqstart_k
     int32 CUDA tensors of b + 1 row offsets (sequence i owns query rows
@@ -200,7 +207,7 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
         lse = torch.empty((h, total_q), dtype=torch.float32, device=q.device)
     _check_io("out", out, (h, total_q, d_v), dt)
     _check_io("lse", lse, (h, total_q), torch.float32)
-    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)
     if w is None:
         st = _native.lib().sdpa_fwd_varlen(
             b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale,
@@ -209,12 +216,12 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
             ctypes.c_void_p(_stream_ptr(stream)))
         _native.check(st, "sdpa_fwd_varlen")
     else:
-        st = _native.lib().sdpa_fwd_varlen_window(
+        st = _native.lib().sdpa_fwd_varlen_ex(
             b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale, *w,
             float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt], _ptr(seqstart_q),
             _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
             ctypes.c_void_p(_stream_ptr(stream)))
-        _native.check(st, "sdpa_fwd_varlen_window")
+        _native.check(st, "sdpa_fwd_varlen_ex")
     return out, lse
 
 
@@ -225,7 +232,7 @@ def sdpa_bwd_varlen_workspace_size(b, h, total_q) -> int:
 def sdpa_bwd_varlen(q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *,
                     scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0, workspace=None,
                     dq=None, dk=None, dv=None, stream=None, window=None, bottom_right=False,
-                    alibi_slopes=None):
+                    alibi_slopes=None, dropout_mask=None):
     """Backward pass over packed sequences (layouts as sdpa_fwd_varlen).
     Returns (dq, dk, dv) shaped like q, k, v."""
     return sdpa_bwd_phases_varlen(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, seqstart_q,
@@ -233,13 +240,14 @@ def sdpa_bwd_varlen(q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q,
                                   is_causal=is_causal, dropout_p=dropout_p, seed=seed,
                                   offset=offset, workspace=workspace, dq=dq, dk=dk, dv=dv,
                                   stream=stream, window=window, bottom_right=bottom_right,
-                                  alibi_slopes=alibi_slopes)
+                                  alibi_slopes=alibi_slopes, dropout_mask=dropout_mask)
 
 
 def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q,
                            max_seqlen_k, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
                            offset=0, workspace=None, dq=None, dk=None, dv=None, stream=None,
-                           window=None, bottom_right=False, alibi_slopes=None):
+                           window=None, bottom_right=False, alibi_slopes=None,
+                           dropout_mask=None):
     """The packed-sequence backward phases selected by ``phases``."""
     h, total_q, d_qk = q.shape
     h_kv, total_k, d_v = k.shape[0], k.shape[1], v.shape[2]
@@ -261,7 +269,7 @@ def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k
     need = sdpa_bwd_varlen_workspace_size(b, h, total_q)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)
     if w is None:
         st = _native.lib().sdpa_bwd_phases_varlen(
             int(phases), b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk,
@@ -271,20 +279,25 @@ def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k
             ctypes.c_void_p(_stream_ptr(stream)))
         _native.check(st, "sdpa_bwd_phases_varlen")
     else:
-        st = _native.lib().sdpa_bwd_phases_varlen_window(
+        st = _native.lib().sdpa_bwd_phases_varlen_ex(
             int(phases), b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk,
             d_v, scale, *w, float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
             _ptr(seqstart_q), _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
             _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
             ctypes.c_void_p(_stream_ptr(stream)))
-        _native.check(st, "sdpa_bwd_phases_varlen_window")
+        _native.check(st, "sdpa_bwd_phases_varlen_ex")
     return dq, dk, dv
 
 
-def sdpa_dropout_mask(b, h, s_q, s_kv, dropout_p, seed, offset, device="cuda", stream=None):
-    """Packed keep bits as an int32 tensor of ceil(b*h*s_q*s_kv/32) words."""
+def sdpa_dropout_mask(b, h, s_q, s_kv, dropout_p, seed, offset, device="cuda", stream=None,
+                      out=None):
+    """Packed keep bits as an int32 tensor of ceil(b*h*s_q*s_kv/32) words (into
+    ``out`` when given). Passed back as ``dropout_mask``, the attention calls
+    read these bits instead of drawing them."""
     words = (b * h * s_q * s_kv + 31) // 32
-    bits = torch.empty(max(words, 1), dtype=torch.int32, device=device)
+    bits = torch.empty(max(words, 1), dtype=torch.int32, device=device) if out is None else out
+    if out is not None and (out.dtype != torch.int32 or out.numel() < words or not out.is_cuda):
+        raise ValueError(f"out must be an int32 CUDA tensor of at least {words} words")
     st = _native.lib().sdpa_dropout_mask(b, h, s_q, s_kv, float(dropout_p), int(seed), int(offset),
                                          _ptr(bits), ctypes.c_void_p(_stream_ptr(stream)))
     _native.check(st, "sdpa_dropout_mask")

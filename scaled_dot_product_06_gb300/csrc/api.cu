@@ -176,6 +176,7 @@ struct Mask {
   int bottom_right;
   const float* alibi = nullptr;  // ALiBi slopes (device), slope of (b, h) at b * alibi_stride + h
   int64_t alibi_stride = 0;
+  const uint32_t* keep_bits = nullptr;  // dropout keep bits drawn beforehand (device)
 };
 Mask causal_mask(int is_causal) { return Mask{-1, is_causal ? 0 : -1, 0}; }
 
@@ -200,6 +201,7 @@ void set_window(const Mask& mk, int64_t s_q, int64_t s_kv, P* p) {
 // ALiBi slopes: 4-byte aligned; the stride between batch rows 0 (one row for
 // all) or at least h, and small enough for an int index.
 sdpa_status_t check_alibi(const Mask& mk, int64_t b, int64_t h) {
+  if ((reinterpret_cast<uintptr_t>(mk.keep_bits) & 3u) != 0) return SDPA_ERR_MISALIGNED;
   if (mk.alibi == nullptr) return SDPA_OK;
   if ((reinterpret_cast<uintptr_t>(mk.alibi) & 3u) != 0) return SDPA_ERR_MISALIGNED;
   if (mk.alibi_stride < 0 || (mk.alibi_stride > 0 && mk.alibi_stride < h) ||
@@ -339,6 +341,10 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
   p.S_kv = static_cast<int>(s_kv);
   p.scale_log2 = scale * kLog2e;
   set_window(mask, s_q, s_kv, &p);
+  if (dropout_p > 0.0f && mask.keep_bits != nullptr) {  // bits drawn beforehand, [b, h, s_q, s_kv] frame
+    p.keep_bits = mask.keep_bits;
+    p.keep_words = (b * h * s_q * s_kv + 31) / 32;
+  }
   p.bias = bias;
   p.dropout = dropout_p > 0.0f ? 1 : 0;
   p.drop_threshold = drop_threshold(dropout_p);
@@ -408,6 +414,10 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   set_window(mask, s_q, s_kv, &p);
+  if (dropout_p > 0.0f && mask.keep_bits != nullptr) {  // bits drawn beforehand, [b, h, s_q, s_kv] frame
+    p.keep_bits = mask.keep_bits;
+    p.keep_words = (b * h * s_q * s_kv + 31) / 32;
+  }
   p.bias = bias;
   p.dbias = dbias;
   p.dropout = dropout_p > 0.0f ? 1 : 0;
@@ -620,51 +630,51 @@ sdpa_status_t sdpa_bwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_
 }
 
 // Local windows and the bottom-right alignment (batch and packed forms).
-sdpa_status_t sdpa_fwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+sdpa_status_t sdpa_fwd_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                               int64_t window_right, int bottom_right, const float* alibi_slopes,
-                              int64_t alibi_stride, float dropout_p, uint64_t seed,
+                              int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, void* o, float* lse, void* stream) {
   return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits},
                   dropout_p, seed, offset, dtype, q, k, v, bias, o, lse, stream, Packing{});
 }
 
-sdpa_status_t sdpa_bwd_phases_window(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
+sdpa_status_t sdpa_bwd_phases_ex(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s_q,
                                      int64_t s_kv, int64_t d_qk, int64_t d_v, float scale,
                                      int64_t window_left, int64_t window_right, int bottom_right,
-                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const void* q, const void* k, const void* v,
                                      const float* bias, const void* o, const void* dout,
                                      const float* lse, void* dq, void* dk, void* dv, float* dbias,
                                      void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(phases, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits},
                   dropout_p, seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias,
                   workspace, workspace_bytes, stream, Packing{});
 }
 
-sdpa_status_t sdpa_bwd_window(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+sdpa_status_t sdpa_bwd_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                               int64_t window_right, int bottom_right, const float* alibi_slopes,
-                              int64_t alibi_stride, float dropout_p, uint64_t seed,
+                              int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, float* dbias,
                               void* workspace, size_t workspace_bytes, void* stream) {
-  return sdpa_bwd_phases_window(SDPA_BWD_ALL, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, window_left,
-                                window_right, bottom_right, alibi_slopes, alibi_stride, dropout_p,
+  return sdpa_bwd_phases_ex(SDPA_BWD_ALL, b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, window_left,
+                                window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits, dropout_p,
                                 seed, offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias,
                                 workspace, workspace_bytes, stream);
 }
 
-sdpa_status_t sdpa_fwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+sdpa_status_t sdpa_fwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                                      int64_t window_right, int bottom_right,
-                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const int32_t* seqstart_q,
                                      const int32_t* seqstart_k, const void* q, const void* k,
@@ -675,15 +685,15 @@ sdpa_status_t sdpa_fwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t
     return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
   return fwd_impl(b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits},
                   dropout_p, seed, offset, dtype, q, k, v, nullptr, o, lse, stream, pk);
 }
 
-sdpa_status_t sdpa_bwd_phases_varlen_window(
+sdpa_status_t sdpa_bwd_phases_varlen_ex(
     int phases, int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
     int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v, float scale,
     int64_t window_left, int64_t window_right, int bottom_right, const float* alibi_slopes,
-    int64_t alibi_stride, float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
+    int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed, uint64_t offset, sdpa_dtype_t dtype,
     const int32_t* seqstart_q, const int32_t* seqstart_k, const void* q, const void* k,
     const void* v, const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
     void* workspace, size_t workspace_bytes, void* stream) {
@@ -693,25 +703,25 @@ sdpa_status_t sdpa_bwd_phases_varlen_window(
     return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
   return bwd_impl(phases, b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride},
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits},
                   dropout_p, seed, offset, dtype, q, k, v, nullptr, o, dout, lse, dq, dk, dv,
                   nullptr, workspace, workspace_bytes, stream, pk);
 }
 
-sdpa_status_t sdpa_bwd_varlen_window(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
+sdpa_status_t sdpa_bwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,
                                      int64_t total_k, int64_t max_seqlen_q, int64_t max_seqlen_k,
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                                      int64_t window_right, int bottom_right,
-                                     const float* alibi_slopes, int64_t alibi_stride,
+                                     const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
                                      float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const int32_t* seqstart_q,
                                      const int32_t* seqstart_k, const void* q, const void* k,
                                      const void* v, const void* o, const void* dout,
                                      const float* lse, void* dq, void* dk, void* dv,
                                      void* workspace, size_t workspace_bytes, void* stream) {
-  return sdpa_bwd_phases_varlen_window(SDPA_BWD_ALL, b, h, h_kv, total_q, total_k, max_seqlen_q,
+  return sdpa_bwd_phases_varlen_ex(SDPA_BWD_ALL, b, h, h_kv, total_q, total_k, max_seqlen_q,
                                        max_seqlen_k, d_qk, d_v, scale, window_left, window_right,
-                                       bottom_right, alibi_slopes, alibi_stride, dropout_p, seed,
+                                       bottom_right, alibi_slopes, alibi_stride, keep_bits, dropout_p, seed,
                                        offset, dtype, seqstart_q, seqstart_k, q, k, v, o, dout, lse,
                                        dq, dk, dv, workspace, workspace_bytes, stream);
 }

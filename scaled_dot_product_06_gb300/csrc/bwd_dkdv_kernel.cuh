@@ -53,6 +53,7 @@ namespace sdpa {
 
 template <int DQK, int DV>
 struct DkdvCfg {
+  static constexpr int DQK_ = DQK, DV_ = DV;
   static constexpr int BN = 128;                      // key rows per CTA
   static constexpr int BM = (DQK <= 128) ? 128 : 64;  // query rows per tile
   static constexpr int NQ = BM / 32;                  // compute warpgroups (32 query columns each)
@@ -113,13 +114,75 @@ __device__ __forceinline__ void keep_bits_transposed(uint64_t lin_quad, int S_kv
   }
 }
 
+// Epilogue of a split key tile (BwdParams::kv_split > 1), run by all NCT
+// compute threads: this CTA's fp32 dK / dV sums go to its partial rows
+// [dK | dV]; after a fence, one atomic per key tile counts the CTA in, and the
+// CTA that completes the count adds every split's partial rows in split order
+// (the same sum whichever finishes last), scales dK, rounds, writes dK / dV
+// and resets the counter. tl = TMEM base plus the warp's lane offset.
+template <typename C, bool BF16>
+__device__ __noinline__ void split_epilogue(float* dkdv_part, int* dkdv_count, int nsp, int tile,
+                                            int sp, bool ready, bool kv_ok, int row, int hf,
+                                            uint32_t tl, uint64_t rowi, float scale, void* dv,
+                                            void* dk, volatile int* last_split) {
+  constexpr int DQK = C::DQK_, DV = C::DV_, RW = DQK + DV;
+  float* part0 = dkdv_part + static_cast<size_t>(tile) * nsp * (C::BN * RW);
+  // tcgen05.ld is warp-collective: the loads run on the warp-uniform
+  // condition (ready, hf), only the stores on the per-lane kv_ok
+  if (ready && hf < 2) {
+    float* dst = part0 + (static_cast<size_t>(sp) * C::BN + row) * RW + (hf == 0 ? DQK : 0);
+    const uint32_t tcol = hf == 0 ? C::T_DV : C::T_DK;
+    const int W = hf == 0 ? DV : DQK;
+    for (int c = 0; c < W / 32; ++c) {
+      uint32_t a[32];
+      tmem_ld32(tl + tcol + c * 32, a);
+      tmem_wait_ld();
+      if (kv_ok) {
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          d4[e] = make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                              __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
+      }
+    }
+  }
+  __threadfence();
+  named_bar_sync(1, C::NCT);
+  if (threadIdx.x == 0) *last_split = ready ? (atomicAdd(dkdv_count + tile, 1) == nsp - 1) : 0;
+  named_bar_sync(1, C::NCT);
+  if (!*last_split) return;
+  __threadfence();
+  if (kv_ok && hf < 2) {
+    const int W = hf == 0 ? DV : DQK;
+    const float mul = hf == 0 ? 1.0f : scale;
+    const float* src = part0 + static_cast<size_t>(row) * RW + (hf == 0 ? DQK : 0);
+    uint8_t* dst_row = static_cast<uint8_t*>(hf == 0 ? dv : dk) + rowi * W * 2;
+    for (int c = 0; c < W / 8; ++c) {
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int s2 = 0; s2 < nsp; ++s2) {  // split order: the same sum whoever is last
+        const float4* s4 = reinterpret_cast<const float4*>(src + static_cast<size_t>(s2) * C::BN * RW + c * 8);
+        const float4 u = __ldcg(s4), w = __ldcg(s4 + 1);
+        acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
+        acc[4] += w.x; acc[5] += w.y; acc[6] += w.z; acc[7] += w.w;
+      }
+      reinterpret_cast<uint4*>(dst_row)[c] =
+          make_uint4(pack2<BF16>(acc[0] * mul, acc[1] * mul), pack2<BF16>(acc[2] * mul, acc[3] * mul),
+                     pack2<BF16>(acc[4] * mul, acc[5] * mul), pack2<BF16>(acc[6] * mul, acc[7] * mul));
+    }
+  }
+  if (threadIdx.x == 0) dkdv_count[tile] = 0;  // ready for the next call
+}
+
 // DROP and BIAS are template parameters (not runtime branches) so the kernel
 // without them is compiled alone: at 96 registers a thread (18 warps, five on
 // some schedulers) the dropout body's keep bits would otherwise push the
 // common path into spilling, and it carries no bias checks. WIN (a local
 // window or the bottom-right alignment) likewise: the plain kernel masks only
-// the top-left causal diagonal.
-template <int DQK, int DV, bool BF16, bool DROP, bool BIAS, bool WIN>
+// the top-left causal diagonal. SPLIT (kv_split > 1) likewise: its epilogue
+// keeps the key tile's indices and the partial-row code out of the others.
+template <int DQK, int DV, bool BF16, bool DROP, bool BIAS, bool WIN, bool SPLIT>
 __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -140,7 +203,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   uint64_t* key_row0 = bars + AB_COUNT + 1;
   Band* band_slot = reinterpret_cast<Band*>(bars + AB_COUNT + 2);  // see lds_band
   volatile int* last_split = reinterpret_cast<volatile int*>(bars + AB_COUNT + 3);
-  static_assert((AB_COUNT + 4) * 8 <= 256, "barrier region");
+  // key tile index and split of this CTA for a split epilogue, set at start-up
+  // (kept out of the registers of the compute loop)
+  int* split_tile = reinterpret_cast<int*>(bars + AB_COUNT + 4);
+  static_assert((AB_COUNT + 5) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,7 +217,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   // batches of one head share Bias and dBias rows)
   // (with kv_split > 1, the splits of one key tile next to each other)
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
-  const int nsp = p.kv_split;
+  const int nsp = SPLIT ? p.kv_split : 1;
   const int b = static_cast<int>(blockIdx.x % p.B);
   const int rest = static_cast<int>(blockIdx.x / p.B);
   const int sp = rest % nsp;  // split: query heads [sp * gs, sp * gs + gs) of the group
@@ -181,7 +247,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     n_per = n_qt - it0;
   }
   // A key tile no query sees: its first split writes the zeros alone.
-  if (nsp > 1 && n_per == 0 && sp != 0) return;
+  if (SPLIT && n_per == 0 && sp != 0) return;
   // One loop over (query head of the split, query tile): iteration i visits
   // query head hk * grp + sp * gs + i / n_per and query tile it0 + i % n_per,
   // so dK and dV sum over the split's heads (the whole group when
@@ -197,6 +263,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
                             : 1u);
     *abort_flag = 0u;
     *key_row0 = static_cast<uint64_t>(zk) * p.rows_k + sl.row_k + k0;
+    if (SPLIT) {
+      split_tile[0] = (hk * n_kt + kt) * p.B + b;
+      split_tile[1] = sp;
+    }
     if (WIN) *band_slot = bd;
     fence_mbar_init();
   }
@@ -394,7 +464,20 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 #pragma unroll
         for (int g = 0; g < CW / 32; ++g) {
           km[g][0] = km[g][1] = km[g][2] = km[g][3] = 0xFFu;
-          if constexpr (DROP)
+          if (DROP && p.keep_bits != nullptr) {
+            // keep bits drawn beforehand: one word per query row (the warp's
+            // lanes, consecutive keys, share it), in keep_bits_transposed's
+            // layout (bit r of km[src] = query row 4r + src)
+            km[g][0] = km[g][1] = km[g][2] = km[g][3] = 0u;
+            const uint64_t L0 = (static_cast<uint64_t>(bh) * p.S_q + qc0 + 32 * g) * p.S_kv + kv;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const uint64_t L = L0 + static_cast<uint64_t>(c) * p.S_kv;
+              const int64_t w = static_cast<int64_t>(L >> 5);
+              const uint32_t bit = w < p.keep_words ? (__ldg(p.keep_bits + w) >> (L & 31)) & 1u : 0u;
+              km[g][c & 3] |= bit << (c >> 2);
+            }
+          } else if constexpr (DROP)
             keep_bits_transposed(
                 (static_cast<uint64_t>(bh) * p.S_q + qc0 + 32 * g) * p.S_kv + k0 + (row & ~3),
                 p.S_kv, lane, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi,
@@ -550,62 +633,11 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     // a key tile that no query sees)
     const bool have = n_it > 0;
     const bool ready = have && ok && mbar_wait(bar(AB_DKDV), 0, ec, kSiteBwdCompute);
-    if (nsp > 1 && have) {
-      // Split key tile: this CTA's fp32 sums as partial rows [dK | dV], then
-      // the last split to count itself in adds all partials in split order.
-      constexpr int RW = DQK + DV;
-      const int tile = (hk * n_kt + kt) * p.B + b;
-      float* part0 = p.dkdv_part + static_cast<size_t>(tile) * nsp * (C::BN * RW);
+    if (SPLIT && have) {
       if (ready) tc_fence_after();
-      // tcgen05.ld is warp-collective: the loads run on the warp-uniform
-      // condition (ready, hf), only the stores on the per-lane kv_ok
-      if (ready && hf < 2) {
-        float* dst = part0 + (static_cast<size_t>(sp) * C::BN + row) * RW + (hf == 0 ? DQK : 0);
-        const uint32_t tcol = hf == 0 ? C::T_DV : C::T_DK;
-        const int W = hf == 0 ? DV : DQK;
-        for (int c = 0; c < W / 32; ++c) {
-          uint32_t a[32];
-          tmem_ld32(tbase + tcol + lane_off + c * 32, a);
-          tmem_wait_ld();
-          if (kv_ok) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              d4[e] = make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                  __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
-          }
-        }
-      }
-      __threadfence();
-      named_bar_sync(1, NCT);
-      if (threadIdx.x == 0)
-        *last_split = ready ? (atomicAdd(p.dkdv_count + tile, 1) == nsp - 1) : 0;
-      named_bar_sync(1, NCT);
-      if (*last_split) {
-        __threadfence();
-        if (kv_ok && hf < 2) {
-          const size_t rowi = static_cast<size_t>(*key_row0) + row;
-          const int W = hf == 0 ? DV : DQK;
-          const float mul = hf == 0 ? 1.0f : p.scale;
-          const float* src = part0 + static_cast<size_t>(row) * RW + (hf == 0 ? DQK : 0);
-          uint8_t* dst_row = static_cast<uint8_t*>(hf == 0 ? p.dv : p.dk) + rowi * W * 2;
-          for (int c = 0; c < W / 8; ++c) {
-            float acc[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-            for (int s2 = 0; s2 < nsp; ++s2) {  // split order: the same sum whoever is last
-              const float4* s4 = reinterpret_cast<const float4*>(src + static_cast<size_t>(s2) * C::BN * RW + c * 8);
-              const float4 u = __ldcg(s4), w = __ldcg(s4 + 1);
-              acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
-              acc[4] += w.x; acc[5] += w.y; acc[6] += w.z; acc[7] += w.w;
-            }
-            reinterpret_cast<uint4*>(dst_row)[c] =
-                make_uint4(pack2<BF16>(acc[0] * mul, acc[1] * mul), pack2<BF16>(acc[2] * mul, acc[3] * mul),
-                           pack2<BF16>(acc[4] * mul, acc[5] * mul), pack2<BF16>(acc[6] * mul, acc[7] * mul));
-          }
-        }
-        if (threadIdx.x == 0) p.dkdv_count[tile] = 0;  // ready for the next call
-      }
+      split_epilogue<C, BF16>(p.dkdv_part, p.dkdv_count, nsp, split_tile[0], split_tile[1], ready,
+                              kv_ok, row, hf, tbase + lane_off, *key_row0 + row, p.scale, p.dv,
+                              p.dk, last_split);
     } else if (!have || ready) {
       if (ready) tc_fence_after();
       const size_t rowi = static_cast<size_t>(*key_row0) + (kv_ok ? row : 0);
@@ -654,14 +686,18 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
                               const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
   using C = DkdvCfg<DQK, DV>;
   const bool bias = p.bias != nullptr;
-  auto pick = [&](auto win) {
-    constexpr bool W = decltype(win)::value;
-    return p.dropout ? (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, true, W>
-                             : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, false, W>)
-                     : (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, true, W>
-                             : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, false, W>);
+  auto pick = [&](auto win, auto split) {
+    constexpr bool W = decltype(win)::value, SP = decltype(split)::value;
+    return p.dropout ? (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, true, W, SP>
+                             : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, true, false, W, SP>)
+                     : (bias ? sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, true, W, SP>
+                             : sdpa_bwd_dkdv_kernel<DQK, DV, BF16, false, false, W, SP>);
   };
-  auto kern = (p.win_general || p.alibi != nullptr) ? pick(std::true_type{}) : pick(std::false_type{});
+  const bool win = p.win_general || p.alibi != nullptr;
+  auto kern = p.kv_split > 1 ? (win ? pick(std::true_type{}, std::true_type{})
+                                    : pick(std::false_type{}, std::true_type{}))
+                             : (win ? pick(std::true_type{}, std::false_type{})
+                                    : pick(std::false_type{}, std::false_type{}));
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM, 0);
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;

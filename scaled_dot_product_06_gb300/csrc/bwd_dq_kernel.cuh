@@ -373,7 +373,9 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     for (int j = 0; ok && j < n_kv; ++j) {
       const int kc0 = (khi - j) * BN + CW * hf;  // first key of this thread's columns
       uint32_t keep = 0;                 // bit c: keep flag of local column c
-      if constexpr (DROP) {
+      if (DROP && p.keep_bits != nullptr) {  // keep bits drawn beforehand
+        keep = keep_word(p.keep_bits, p.keep_words, lin_row + kc0);
+      } else if constexpr (DROP) {
 #pragma unroll
         for (int g = 0; g < CW / 4; ++g) {
           const uint4 d = dropout_draws((lin_row + kc0) / 4 + g, p.seed_lo, p.seed_hi,

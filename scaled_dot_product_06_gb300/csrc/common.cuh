@@ -36,6 +36,11 @@ struct FwdParams {
   // unbounded. Causal is (-1, 0, 0); no mask (-1, -1, 0). See Band.
   int win_left, win_right, win_br;
   int win_general;         // 0: top-left, causal (win_right = 0) or unmasked (-1)
+  // Dropout keep bits drawn beforehand (sdpa_dropout_mask's packing: bit
+  // L % 32 of word L / 32, L the linear element index of the dropout rule) or
+  // null to draw them here; keep_words is the array's length in words.
+  const uint32_t* keep_bits;
+  int64_t keep_words;
   // ALiBi (null: none): score of (i, j) gets -alibi[b * alibi_stride + h] *
   // |j - i - off|, off = S_kv - S_q when alibi_br, else 0 (a top-left mask).
   // Handled by the kernels compiled for general windows.
@@ -186,6 +191,8 @@ struct BwdParams {
   const int* seqstart_q;   // packed sequences, as in FwdParams (null in batch mode)
   const int* seqstart_k;
   int rows_q, rows_k;
+  const uint32_t* keep_bits;  // dropout keep bits drawn beforehand, as in FwdParams
+  int64_t keep_words;
 };
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -206,6 +213,17 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
   }
   return c;
+}
+
+// Keep flags of elements L0 .. L0 + 31 from packed keep bits (bit L % 32 of
+// word L / 32): two words joined by a funnel shift; words past the array
+// (elements past the problem, which callers mask anyway) read as 0.
+__device__ __forceinline__ uint32_t keep_word(const uint32_t* bits, int64_t n_words, uint64_t L0) {
+  const int64_t w = static_cast<int64_t>(L0 >> 5);
+  const uint32_t sh = static_cast<uint32_t>(L0 & 31);
+  const uint32_t lo = w < n_words ? __ldg(bits + w) : 0u;
+  const uint32_t hi = (sh != 0 && w + 1 < n_words) ? __ldg(bits + w + 1) : 0u;
+  return __funnelshift_r(lo, hi, sh);
 }
 
 // The four draws of linear-index group g (elements 4g .. 4g+3).

@@ -429,7 +429,15 @@ __global__ void __launch_bounds__(384, 1)
         const float2 u = f2split(sa), w = f2split(sb);
         l += (u.x + u.y) + (w.x + w.y);
       }
-      if (GENERAL && p.dropout) {
+      if (GENERAL && p.dropout && p.keep_bits != nullptr) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {  // keep bits drawn beforehand
+          const uint32_t kw = keep_word(p.keep_bits, p.keep_words, lin_row + k0 + 32 * w);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (!((kw >> i) & 1u)) x[32 * w + i] = 0.f;
+        }
+      } else if (GENERAL && p.dropout) {
         const uint64_t g0 = (lin_row + k0) >> 2;
 #pragma unroll
         for (int g = 0; g < 32; ++g) {

@@ -140,3 +140,28 @@ def test_concurrent_backward_equals_phases_bitwise(h_kv):
     torch.cuda.synchronize()
     for x1, x2 in zip(a[:3], (dq, dk, dv)):
         assert torch.equal(x1, x2)
+
+
+@pytest.mark.parametrize("case", [
+    Case(2, 4, 384, 512, 64, 64, dtype="fp16", p=0.1),
+    Case(1, 4, 300, 332, 128, 128, causal=True, p=0.2, H_kv=2),
+    Case(2, 2, 256, 256, 192, 128, causal=True, bias=True, p=0.15),
+], ids=["d64-fp16", "d128-causal-gqa-ragged", "d192-bias"])
+def test_dropout_bits_drawn_beforehand_give_the_same_bits(case):
+    """With the keep bits of sdpa_dropout_mask passed in, every kernel reads them
+    instead of drawing Philox numbers: O, LSE, dQ, dK, dV, dBias identical."""
+    from scaled_dot_product_06_gb300 import sdpa_bwd, sdpa_dropout_mask, sdpa_fwd
+    from scaled_dot_product_06_gb300.inputs import make_inputs
+    x = make_inputs(case.shape, case.dtype, with_bias=case.bias, device="cuda")
+    q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
+    kw = dict(scale=case.sc, is_causal=case.causal, dropout_p=case.p, seed=case.seed,
+              offset=case.offset, bias=bias)
+    o1, l1 = sdpa_fwd(q, k, v, **kw)
+    g1 = sdpa_bwd(q, k, v, o1, do, l1, **kw)
+    mask = sdpa_dropout_mask(case.B, case.H, case.S_q, case.S_kv, case.p, case.seed, case.offset)
+    o2, l2 = sdpa_fwd(q, k, v, dropout_mask=mask, **kw)
+    g2 = sdpa_bwd(q, k, v, o2, do, l2, dropout_mask=mask, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for a, b in zip(g1, g2):
+        assert (a is None and b is None) or torch.equal(a, b)

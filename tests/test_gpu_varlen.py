@@ -155,3 +155,25 @@ def test_packed_h32_d128_causal_16_sequences_sampled():
         assert rel < 2e-2, f"sequence {i}: key-sum of dK is not ~0 (relative {rel:.3e})"
         assert_close(f"sum_j dV seq {i}", dv[:, a:b].double().sum(dim=1).cpu(),
                      x["do"][:, a:b].double().sum(dim=1).numpy(), rel=3e-2)
+
+
+def test_packed_dropout_bits_drawn_beforehand_give_the_same_bits():
+    """Packed: the mask of the padded [b, h, max_q, max_k] frame, passed in,
+    gives the bits of the drawing path."""
+    from scaled_dot_product_06_gb300 import sdpa_dropout_mask
+    c = VCase(2, (100, 60), (92, 140), 128, 128, p=0.2, max_q=512, max_k=512)
+    x = make_packed_inputs(c.H, sum(c.lq), sum(c.lk), c.D_qk, c.D_v, c.dtype)
+    a = run_varlen(c, x)
+    dev = "cuda"
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    sq = torch.tensor(seqstarts(c.lq), dtype=torch.int32, device=dev)
+    sk = torch.tensor(seqstarts(c.lk), dtype=torch.int32, device=dev)
+    mq, mk = c.maxes
+    mask = sdpa_dropout_mask(len(c.lq), c.H, mq, mk, c.p, c.seed, c.offset)
+    kw = dict(scale=c.sc, is_causal=c.causal, dropout_p=c.p, seed=c.seed, offset=c.offset,
+              dropout_mask=mask)
+    o, lse = sdpa_fwd_varlen(q, k, v, sq, sk, mq, mk, **kw)
+    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, sq, sk, mq, mk, **kw)
+    torch.cuda.synchronize()
+    for x1, x2 in zip(a, (o, lse, dq, dk, dv)):
+        assert torch.equal(x1, x2)
