@@ -261,6 +261,35 @@ def run_reference(args, w, rank):
     print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------------- host placement
+def bind_near_gpu(index: int):
+    """Run this process on the CPUs the GPU's PCI device reports as local, so
+    that the pinned host buffers of the end-to-end measurement (placed on
+    first touch) sit on the GPU's own memory node rather than across a socket
+    link. Returns the CPU list used, or None when the system does not say."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(index)
+        path = (f"/sys/bus/pci/devices/{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:"
+                f"{pr.pci_device_id:02x}.0/local_cpulist")
+        with open(path) as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        allowed = cpus & os.sched_getaffinity(0)
+        if not allowed:
+            return None
+        os.sched_setaffinity(0, allowed)
+        return spec
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
 # ---------------------------------------------------------------- ranks
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """Slowest rank's value (all ranks get it); identity for one rank."""
@@ -320,6 +349,7 @@ def main():
         raise SystemExit("bench.py needs a CUDA device")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    host_cpus = bind_near_gpu(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
@@ -535,6 +565,7 @@ def main():
         e2e = {"value": whole_job_tflops(world, step_flops, e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": n_e,
+               "host_cpus": host_cpus,
                "method": ("sdpa_fwd_varlen + sdpa_bwd_varlen" if packed else "sdpa_fwd + sdpa_bwd") +
                          " from pinned host buffers; uploads of step n+1 and "
                          "read-backs of step n-1 overlap step n on two copy streams "

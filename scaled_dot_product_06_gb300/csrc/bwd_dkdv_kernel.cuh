@@ -464,20 +464,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 #pragma unroll
         for (int g = 0; g < CW / 32; ++g) {
           km[g][0] = km[g][1] = km[g][2] = km[g][3] = 0xFFu;
-          if (DROP && p.keep_bits != nullptr) {
-            // keep bits drawn beforehand: one word per query row (the warp's
-            // lanes, consecutive keys, share it), in keep_bits_transposed's
-            // layout (bit r of km[src] = query row 4r + src)
-            km[g][0] = km[g][1] = km[g][2] = km[g][3] = 0u;
-            const uint64_t L0 = (static_cast<uint64_t>(bh) * p.S_q + qc0 + 32 * g) * p.S_kv + kv;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const uint64_t L = L0 + static_cast<uint64_t>(c) * p.S_kv;
-              const int64_t w = static_cast<int64_t>(L >> 5);
-              const uint32_t bit = w < p.keep_words ? (__ldg(p.keep_bits + w) >> (L & 31)) & 1u : 0u;
-              km[g][c & 3] |= bit << (c >> 2);
-            }
-          } else if constexpr (DROP)
+          // (keep bits drawn beforehand are not read here: this kernel needs
+          // them down a column, one word per query row, which measured slower
+          // than drawing them; both give the same bits)
+          if constexpr (DROP)
             keep_bits_transposed(
                 (static_cast<uint64_t>(bh) * p.S_q + qc0 + 32 * g) * p.S_kv + k0 + (row & ~3),
                 p.S_kv, lane, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi,
