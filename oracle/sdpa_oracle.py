@@ -228,6 +228,8 @@ def backward_head(prob: Problem, b: int, h: int, q, k, v, do, bias=None, rows=No
 
     dk = np.zeros((len(cols), prob.D_qk))
     dv = np.zeros((len(cols), prob.D_v))
+    if len(cols) == 0:  # no key column asked for: the sums over every row are empty
+        return dq, dk, dv, ds_block
     step = prob.S_q if row_chunk is None else int(row_chunk)
     for r0 in range(0, prob.S_q, step):
         rr = all_rows[r0:r0 + step]

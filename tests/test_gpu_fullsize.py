@@ -151,3 +151,31 @@ def test_b1h32kv4_s16384_d128_causal_gqa_sampled():
     assert rel < 2e-2, f"key-sum of dK is not ~0 (relative {rel:.3e})"
     do_sum = x["do"].double().sum(dim=2).reshape(1, 4, 8, 128).sum(dim=2).numpy()
     assert_close("sum_j dV", dv.double().sum(dim=2).cpu(), do_sum, rel=3e-2)
+
+
+def test_dropout_element_index_past_2_pow_32():
+    """b1 h8 s32768 d64 with dropout: the last head's linear element indices
+    pass 2^32 (the Philox counter's high word is in use). Sampled query rows
+    of that head (O, LSE, dQ over all keys) against the oracle, and the last
+    keep-bit words the GPU draws against the oracle's Philox."""
+    case = Case(1, 8, 32768, 32768, 64, 64, causal=True, p=0.1)
+    x = make_inputs(case.shape, case.dtype)
+    o, lse, dq, dk, dv, _ = run_gpu(case, x)
+    pr = case.problem()
+    h = 7
+    rows = np.array([0, 1, 4097, 20000, 32766, 32767])
+    assert (h * 32768 + int(rows[0])) * 32768 > (1 << 32)
+    r_t = torch.as_tensor(rows, device=o.device)
+    o_ref, lse_ref = oracle.forward_head(pr, 0, h, x["q"], x["k"], x["v"], rows=rows)
+    assert_close("o rows", o[0, h][r_t], o_ref)
+    assert_lse(lse[0, h][r_t], lse_ref)
+    dq_r, _, _, _ = oracle.backward_head(pr, 0, h, x["q"], x["k"], x["v"], x["do"], rows=rows,
+                                         cols=np.array([], dtype=np.int64))
+    assert_close("dq rows", dq[0, h][r_t], dq_r)
+    total = 8 * 32768 * 32768
+    words = sdpa_dropout_mask(1, 8, 32768, 32768, case.p, case.seed, case.offset)
+    last = words[-64:].cpu().numpy().view(np.uint32)
+    lin = np.arange(total - 64 * 32, total, dtype=np.uint64)
+    keep = philox.random_words(lin, case.seed, case.offset) >= np.uint32(philox.drop_threshold(case.p))
+    ref = (keep.reshape(-1, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(axis=1)
+    assert np.array_equal(last, ref.astype(np.uint32))
