@@ -264,6 +264,36 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return r;
 }
 
+// Three-input max / min (sm_100 family): one instruction takes two more
+// scores into a running maximum.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Largest (MIN: smallest) of x[0, N), N a multiple of 8, in four chains.
+template <bool MIN, int N>
+__device__ __forceinline__ float extreme_of(const float* x) {
+  static_assert(N % 8 == 0, "extreme_of");
+  auto f3 = [](float a, float b, float c) { return MIN ? fmin3(a, b, c) : fmax3(a, b, c); };
+  float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
+#pragma unroll
+  for (int i = 4; i < N - 4; i += 8) {
+    a0 = f3(a0, x[i], x[i + 4]);
+    a1 = f3(a1, x[i + 1], x[i + 5]);
+    a2 = f3(a2, x[i + 2], x[i + 6]);
+    a3 = f3(a3, x[i + 3], x[i + 7]);
+  }
+  a0 = f3(a0, a1, x[N - 4]);
+  a2 = f3(a2, a3, x[N - 3]);
+  return f3(a0, a2, f3(x[N - 2], x[N - 1], x[N - 1]));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -35,7 +35,9 @@
 // row's 128 scores without spilling: 2 x 128 x 216 + 128 x 72 = 384 x 168.
 // GENERAL (a bias or dropout present) and WIN (a local window or the
 // bottom-right alignment) are template parameters so the plain kernel is
-// compiled without their registers.
+// compiled without their registers. RAW (no bias, dropout or ALiBi, a nonzero
+// scale) keeps the scores unscaled until the exponential, which takes the
+// scale and the row max in one FMA per score.
 #pragma once
 #include "common.cuh"
 
@@ -71,7 +73,7 @@ struct FwdCfg {
 enum : int { FB_Q = 0, FB_S, FB_P = FB_S + 2, FB_O = FB_P + 2, FB_DRAIN = FB_O + 2, FB_KF,
              FB_KE = FB_KF + 3, FB_VF = FB_KE + 3, FB_VE = FB_VF + 3, FB_COUNT = FB_VE + 3 };
 
-template <int DQK, int DV, bool BF16, bool GENERAL, bool WIN>
+template <int DQK, int DV, bool BF16, bool GENERAL, bool WIN, bool RAW>
 __global__ void __launch_bounds__(384, 1)
     sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -316,6 +318,13 @@ __global__ void __launch_bounds__(384, 1)
     const bool bias_vec = (p.S_kv & 3) == 0;
     const uint64_t lin_row = (static_cast<uint64_t>(bh) * p.S_q + row) * p.S_kv;
     const uint64_t sl22 = f2(sl2, sl2);
+    // RAW (no bias, dropout or ALiBi, a nonzero scale): the scores stay raw
+    // until the exponential. A masked key takes the raw value that scales to
+    // -inf, the row max is the largest raw score (the smallest under a
+    // negative scale) times scale * log2e, which equals the largest scaled
+    // score since rounding is monotonic, and P = 2^fma(S, scale * log2e, -m).
+    static_assert(!(RAW && GENERAL), "raw scores have no additive terms");
+    const float neg = (RAW && sl2 < 0.f) ? -SDPA_NEG_INF : SDPA_NEG_INF;  // masked score
     float m = SDPA_NEG_INF, l = 0.f;
     bool ok = true;
     for (int c = 0; c < n_kv; ++c) {
@@ -353,13 +362,15 @@ __global__ void __launch_bounds__(384, 1)
           float2 v;
           if (GENERAL && bias_row != nullptr)
             v = f2split(fma2(s2, sl22, mul2(f2(x[q * 32 + 2 * i], x[q * 32 + 2 * i + 1]), f2(kLog2e, kLog2e))));
-          else
+          else if (!RAW)
             v = f2split(mul2(s2, sl22));
+          else
+            v = f2split(s2);
           x[q * 32 + 2 * i] = v.x;
           x[q * 32 + 2 * i + 1] = v.y;
         }
       }
-      if constexpr (WIN) {
+      if constexpr (WIN && !RAW) {
         if (p.alibi != nullptr) {  // ALiBi: -slope |j - i - off|, in the log2 domain
           const float ns = -__ldg(p.alibi + b * p.alibi_stride + h) * kLog2e;
           const float base = static_cast<float>(k0 - row - (p.alibi_br ? S_kv - S_q : 0));
@@ -374,23 +385,21 @@ __global__ void __launch_bounds__(384, 1)
           const int first = row + wb.lo, last = min(S_kv - 1, row + wb.hi);  // visible keys
 #pragma unroll
           for (int i = 0; i < 128; ++i)
-            if (k0 + i < first || k0 + i > last) x[i] = SDPA_NEG_INF;
+            if (k0 + i < first || k0 + i > last) x[i] = neg;
         }
       } else if ((k0 + C::BN > S_kv) || (p.win_right >= 0 && k0 + C::BN - 1 > qt0)) {
         const int lim = p.win_right >= 0 ? min(S_kv - 1, row) : S_kv - 1;  // last visible key
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (k0 + i > lim) x[i] = SDPA_NEG_INF;
+          if (k0 + i > lim) x[i] = neg;
       }
-      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
-#pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx0 = fmaxf(mx0, x[i]);
-        mx1 = fmaxf(mx1, x[i + 1]);
-        mx2 = fmaxf(mx2, x[i + 2]);
-        mx3 = fmaxf(mx3, x[i + 3]);
+      float mx;
+      if (!RAW || sl2 > 0.f) {
+        mx = extreme_of<false, 128>(x);
+        if (RAW) mx *= sl2;
+      } else {
+        mx = extreme_of<true, 128>(x) * sl2;
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       // Rescale only when the max grew by more than 8 (a factor 256).
       const bool grow = mx > m + 8.0f;
       float alpha = 1.0f;
@@ -416,8 +425,9 @@ __global__ void __launch_bounds__(384, 1)
       uint64_t sa = f2(0.f, 0.f), sb = f2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < 128; i += 4) {
-        const float2 a = f2split(add2(f2(x[i], x[i + 1]), nm2));
-        const float2 bq = f2split(add2(f2(x[i + 2], x[i + 3]), nm2));
+        const float2 a = f2split(RAW ? fma2(f2(x[i], x[i + 1]), sl22, nm2) : add2(f2(x[i], x[i + 1]), nm2));
+        const float2 bq =
+            f2split(RAW ? fma2(f2(x[i + 2], x[i + 3]), sl22, nm2) : add2(f2(x[i + 2], x[i + 3]), nm2));
         x[i] = ex2(a.x);
         x[i + 1] = ex2(a.y);
         x[i + 2] = ex2(bq.x);
@@ -507,11 +517,15 @@ cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUten
                          const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
   const bool general = p.bias != nullptr || p.dropout != 0;
-  const bool win = p.win_general || p.alibi != nullptr;
-  auto kern = general ? (win ? sdpa_fwd_kernel<DQK, DV, BF16, true, true>
-                             : sdpa_fwd_kernel<DQK, DV, BF16, true, false>)
-                      : (win ? sdpa_fwd_kernel<DQK, DV, BF16, false, true>
-                             : sdpa_fwd_kernel<DQK, DV, BF16, false, false>);
+  // raw scores (RAW) unless ALiBi or a zero scale; those take the windowed
+  // kernel, which also runs the plain masks
+  const bool raw = !general && p.alibi == nullptr && p.scale_log2 != 0.f;
+  const bool win = p.win_general || p.alibi != nullptr || (!general && !raw);
+  auto kern = general ? (win ? sdpa_fwd_kernel<DQK, DV, BF16, true, true, false>
+                             : sdpa_fwd_kernel<DQK, DV, BF16, true, false, false>)
+                      : !raw ? sdpa_fwd_kernel<DQK, DV, BF16, false, true, false>
+                             : (win ? sdpa_fwd_kernel<DQK, DV, BF16, false, true, true>
+                                    : sdpa_fwd_kernel<DQK, DV, BF16, false, false, true>);
   // The warpgroups' setmaxnreg shares add up to exactly 384 x REG_LAUNCH; had
   // the compiler given the kernel another launch register count, the softmax
   // warpgroups' increase could never be granted, so refuse to launch then.

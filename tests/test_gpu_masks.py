@@ -65,6 +65,30 @@ def test_window_matches_oracle(c):
         assert_close("dbias", dbias, db_r)
 
 
+@pytest.mark.parametrize("scale", [-0.1, 0.0])
+def test_window_with_negative_or_zero_scale(scale):
+    """A window under a negative scale (raw scores, row max from their
+    minimum, masked keys at +inf before scaling) and under a zero scale (the
+    kernel that scales first)."""
+    B, H, S_q, S_kv, D = 1, 2, 384, 520, 128
+    win, br = (100, 20), True
+    x = make_inputs(Shape(B, H, S_q, S_kv, D, D), "bf16")
+    pr = oracle.Problem(B, H, S_q, S_kv, D, D, scale, False, window=win, bottom_right=br)
+    q, k, v, do = (x[n].to("cuda") for n in ("q", "k", "v", "do"))
+    kw = dict(scale=scale, window=win, bottom_right=br)
+    o, lse = sdpa_fwd(q, k, v, **kw)
+    dq, dk, dv, _ = sdpa_bwd(q, k, v, o, do, lse, **kw)
+    torch.cuda.synchronize()
+    assert sdpa_device_error() == 0
+    o_ref, lse_ref = oracle.forward(pr, x["q"], x["k"], x["v"])
+    assert_close("o", o, o_ref)
+    assert_lse(lse, lse_ref)
+    dq_r, dk_r, dv_r, _ = oracle.backward(pr, x["q"], x["k"], x["v"], x["do"])
+    assert_close("dq", dq, dq_r)
+    assert_close("dk", dk, dk_r)
+    assert_close("dv", dv, dv_r)
+
+
 def test_packed_window_bottom_right_matches_oracle():
     lq, lk = (100, 300, 7, 256), (200, 150, 64, 256)
     H, H_kv, D = 4, 2, 128

@@ -37,6 +37,12 @@ CASES = [
     Case(1, 6, 200, 332, 64, 64, bias=True, p=0.1, H_kv=3, dtype="fp16"),
     Case(1, 4, 384, 256, 128, 128, causal=True, H_kv=1),
     Case(2, 4, 192, 192, 192, 128, causal=True, bias=True, H_kv=2),
+    # the sign of the scale: the plain kernels take the row max from the raw
+    # scores (the smallest under a negative scale); a zero scale runs the
+    # kernel that scales first (uniform weights over the visible keys)
+    Case(1, 2, 300, 300, 128, 128, causal=True, scale=-0.09),
+    Case(1, 1, 200, 260, 64, 64, scale=-0.125, dtype="fp16"),
+    Case(1, 2, 256, 300, 128, 128, causal=True, scale=0.0),
 ]
 
 
