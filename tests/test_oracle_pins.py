@@ -82,6 +82,27 @@ def test_zero_queries_average_visible_values(causal):
         np.testing.assert_allclose(o[0, 0, i], v[0, 0, :n].mean(axis=0), rtol=1e-13, atol=1e-15)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale_averages_visible_values(causal):
+    """scale = 0 with nonzero queries: every visible key weighs 1/n, so
+    O_i is the mean of the visible V rows, LSE_i = ln n, dQ = dK = 0 (both
+    carry the factor scale) and dV_j sums dO_i / n_i over the rows i that
+    see key j."""
+    pr = problem(S_q=6, S_kv=9, causal=causal, scale=0.0)
+    q, k, v, do, _ = tensors(pr)
+    o, lse = forward(pr, q, k, v)
+    dq, dk, dv, _ = backward(pr, q, k, v, do)
+    n = [min(i + 1, 9) if causal else 9 for i in range(6)]
+    for i in range(6):
+        assert lse[0, 0, i] == pytest.approx(math.log(n[i]), rel=1e-14)
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, :n[i]].mean(axis=0), rtol=1e-13, atol=1e-15)
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    want = np.zeros((9, pr.D_v))
+    for i in range(6):
+        want[:n[i]] += do[0, 0, i] / n[i]
+    np.testing.assert_allclose(dv[0, 0], want, rtol=1e-13, atol=1e-15)
+
+
 def test_fully_masked_row_is_zero():
     pr = problem(S_q=4, S_kv=5)
     q, k, v, do, bias = tensors(pr, bias=True)
@@ -180,6 +201,24 @@ def test_matches_torch_float64_attention_and_autograd(causal, use_bias):
     np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-11, atol=1e-12)
     if use_bias:
         np.testing.assert_allclose(dbias, tb.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_negative_scale_matches_torch_float64(causal):
+    """A negative scale (the softmax then favours the smallest products):
+    PyTorch's float64 attention with the same scale, and autograd."""
+    pr = problem(B=1, H=2, S_q=7, S_kv=10, D_qk=5, D_v=4, scale=-0.4, causal=causal)
+    q, k, v, do, _ = tensors(pr)
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                          scale=pr.scale)
+    to.backward(torch.tensor(do))
+    o, _ = forward(pr, q, k, v)
+    dq, dk, dv, _ = backward(pr, q, k, v, do)
+    np.testing.assert_allclose(o, to.detach().numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-11, atol=1e-12)
 
 
 # ------------------------------------------------------------------ sampled slices
