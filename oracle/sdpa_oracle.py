@@ -12,7 +12,7 @@ shape [b, h, s_q], BHSD tensors, optional bias, dropout by seed and offset).
 Every matrix is materialised; there is no tiling and no online softmax. Matrix
 products are numpy ``@`` in float64.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * The saved statistic is the natural-log logsumexp of the scaled, biased,
   masked scores, taken before dropout: LSE_i = m_i + ln(sum_j exp(s_ij - m_i)).

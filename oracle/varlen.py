@@ -15,7 +15,7 @@ rows to the batch-mode oracle (``sdpa_oracle``) as a problem with B = 1.
 Layout (the batch-mode BHSD with the batch folded into the rows): q, do
 [H, total_q, D], k, v [H_kv, total_k, D], lse [H, total_q].
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * The causal mask is top-left within each sequence (local key j visible to
   local query i iff j <= i), as in batch mode; windows and the bottom-right
