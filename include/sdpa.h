@@ -22,6 +22,8 @@
  *   Types       Q, K, V, O, dO, dQ, dK, dV are bf16 or fp16 (dtype argument);
  *               accumulation and softmax are fp32.
  *   Head sizes  (d_qk, d_v) in {(64,64), (128,128), (192,128)}.
+ *   Scale       Any float whose product with log2(e) is finite, of either
+ *               sign or zero; a NaN or infinite one is SDPA_ERR_INVALID_ARG.
  *   Causal      Top-left: key j is visible to query i iff j <= i.
  *   LSE         Natural-log logsumexp of the scaled, biased, masked scores
  *               before dropout; -inf for a row that sees no key (its O row

@@ -112,6 +112,10 @@ bool head_sizes_ok(int64_t d_qk, int64_t d_v) {
 // key index with a window offset inside an int on the device.
 constexpr int64_t kMaxSeq = (int64_t{1} << 29) - 256;
 
+// A scale whose product with log2(e) is finite (the kernels work in the
+// exp2 domain); any sign, zero included.
+bool scale_ok(float scale) { return std::isfinite(scale) && std::isfinite(scale * kLog2e); }
+
 // Checks shared by fwd and bwd that need no pointer. Sets *empty for a
 // zero-sized problem.
 sdpa_status_t check_sizes(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk, int64_t d_v,
@@ -316,6 +320,7 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
                        const Packing& pk) {
   bool empty = false;
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (!scale_ok(scale)) return fail(SDPA_ERR_INVALID_ARG, "scale must be finite");
   if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
   if (sdpa_status_t s = check_packing(pk, b, bias, &empty)) return s;
   if (sdpa_status_t s = check_alibi(mask, b, h)) return s;
@@ -380,6 +385,7 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   if (phases <= 0 || (phases & ~SDPA_BWD_ALL) != 0) return fail(SDPA_ERR_INVALID_ARG, "phases");
   bool empty = false;
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
+  if (!scale_ok(scale)) return fail(SDPA_ERR_INVALID_ARG, "scale must be finite");
   if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
   if (sdpa_status_t s = check_packing(pk, b, bias, &empty)) return s;
   if (sdpa_status_t s = check_alibi(mask, b, h)) return s;

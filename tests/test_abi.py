@@ -53,8 +53,8 @@ MIS = ctypes.c_void_p((1 << 20) + 8)
 
 
 def fwd(lib, b=1, h=1, sq=128, skv=128, dqk=64, dv=64, p=0.0, dtype=0, q=P, k=P, v=P, bias=NULL,
-        o=P, lse=P):
-    return lib.sdpa_fwd(b, h, sq, skv, dqk, dv, 0.125, 0, p, 0, 0, dtype, q, k, v, bias, o, lse,
+        o=P, lse=P, scale=0.125):
+    return lib.sdpa_fwd(b, h, sq, skv, dqk, dv, scale, 0, p, 0, 0, dtype, q, k, v, bias, o, lse,
                         None)
 
 
@@ -67,6 +67,8 @@ def test_fwd_argument_errors(lib):
     assert fwd(lib, p=-0.1) == _native.SDPA_ERR_INVALID_ARG
     assert fwd(lib, p=float("nan")) == _native.SDPA_ERR_INVALID_ARG
     assert fwd(lib, p=0.1, skv=130) == _native.SDPA_ERR_UNSUPPORTED
+    for bad in (float("nan"), float("inf"), -float("inf"), 3.0e38):  # scale * log2(e) not finite
+        assert fwd(lib, scale=bad) == _native.SDPA_ERR_INVALID_ARG
     assert fwd(lib, q=NULL) == _native.SDPA_ERR_INVALID_ARG
     assert fwd(lib, lse=NULL) == _native.SDPA_ERR_INVALID_ARG
     assert fwd(lib, k=MIS) == _native.SDPA_ERR_MISALIGNED
@@ -77,10 +79,10 @@ def test_fwd_argument_errors(lib):
 
 
 def bwd(lib, b=1, h=1, sq=128, skv=128, dqk=64, dv=64, p=0.0, bias=NULL, dbias=NULL, ws=P,
-        ws_bytes=None, dout=P, q=P):
+        ws_bytes=None, dout=P, q=P, scale=0.125):
     if ws_bytes is None:
         ws_bytes = lib.sdpa_bwd_workspace_size(b, h, sq, skv, dqk, dv)
-    return lib.sdpa_bwd(b, h, sq, skv, dqk, dv, 0.125, 1, p, 0, 0, 0, q, P, P, bias, P, dout, P,
+    return lib.sdpa_bwd(b, h, sq, skv, dqk, dv, scale, 1, p, 0, 0, 0, q, P, P, bias, P, dout, P,
                         P, P, P, dbias, ws, ws_bytes, None)
 
 
@@ -101,6 +103,8 @@ def test_bwd_argument_errors(lib):
     assert bwd(lib, ws=ctypes.c_void_p((1 << 20) + 16)) == _native.SDPA_ERR_MISALIGNED
     assert bwd(lib, q=MIS) == _native.SDPA_ERR_MISALIGNED
     assert bwd(lib, dqk=192, dv=192) == _native.SDPA_ERR_UNSUPPORTED
+    assert bwd(lib, scale=float("nan")) == _native.SDPA_ERR_INVALID_ARG
+    assert bwd(lib, scale=-float("inf")) == _native.SDPA_ERR_INVALID_ARG
     assert bwd(lib, skv=0, q=NULL) == _native.SDPA_OK
 
 
