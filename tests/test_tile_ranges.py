@@ -168,3 +168,31 @@ def test_causal_ranges_skip_tiles_above_the_diagonal():
         assert vis[q0:q0 + BM, kt * BN:kt * BN + BN].any()
     for q0, b, kt in dkdv_tiles(S, S, -U, 0, 128, plain_causal=True):
         assert vis[q0:q0 + b, kt * BN:kt * BN + BN].any()
+
+
+def test_packed_statistics_blocks_are_disjoint_and_inside_the_pad():
+    """Packed sequences keep their softmax statistics (and D) in one block per
+    sequence: sequence b's block starts at round_up(start_b, 64) + 192 b
+    (common.cuh packed_stat_row) and spans its query rows rounded up to whole
+    128-row tiles. The blocks must not overlap and must fit in
+    packed_stat_pad(rows, n) = round_up(rows, 64) + 192 n + 128 rows, the size
+    the backward workspace query reserves per head, for any lengths."""
+    def stat_row(start, b):
+        return (start + 63) // 64 * 64 + 192 * b
+
+    def pad(rows, n):
+        return (rows + 63) // 64 * 64 + 192 * n + 128
+
+    rng = np.random.default_rng(5)
+    cases = [[1], [128], [129, 1, 0, 255], [0, 0, 0], [64] * 9, [63, 65, 127, 129]]
+    cases += [list(rng.integers(0, 700, int(rng.integers(1, 40)))) for _ in range(300)]
+    for lens in cases:
+        starts = np.concatenate([[0], np.cumsum(lens)])
+        rows = int(starts[-1])
+        end_prev = 0
+        for b, n in enumerate(lens):
+            first = stat_row(int(starts[b]), b)
+            size = (int(n) + BM - 1) // BM * BM
+            assert first >= end_prev, (lens, b)
+            end_prev = first + size
+            assert end_prev <= pad(rows, len(lens)), (lens, b)
