@@ -323,6 +323,9 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=4096,
                     help="query positions of the one-head oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the deterministic backward (query-stationary dQ kernel beside the "
+                         "dK/dV kernel) instead of the default fused one")
     args = ap.parse_args()
     w = resolve(WORKLOADS[args.workload])
 
@@ -397,8 +400,9 @@ def main():
         o = torch.empty(shp.B, shp.H, shp.S_q, shp.D_v, dtype=x["q"].dtype, device=dev)
         lse = torch.empty(shp.B, shp.H, shp.S_q, dtype=torch.float32, device=dev)
         ws = torch.empty(sdpa_bwd_workspace_size(shp.B, shp.H, shp.S_q, shp.S_kv, shp.D_qk,
-                                                 shp.D_v, shp.kv_heads), dtype=torch.uint8,
-                         device=dev)
+                                                 shp.D_v, shp.kv_heads,
+                                                 deterministic=args.deterministic),
+                         dtype=torch.uint8, device=dev)
 
         def fwd_call(D):
             sdpa_fwd(D["q"], D["k"], D["v"], out=D["o"], lse=D["lse"], bias=D["bias"], **kw)
@@ -406,7 +410,13 @@ def main():
         def bwd_call(ph, D, stream=None):
             sdpa_bwd_phases(ph, D["q"], D["k"], D["v"], D["o"], D["do"], D["lse"], workspace=ws,
                             dq=D["dq"], dk=D["dk"], dv=D["dv"], bias=D["bias"], dbias=D["dbias"],
-                            stream=stream, **kw)
+                            stream=stream, deterministic=args.deterministic, **kw)
+    # The default backward at d_qk <= 128 in batch mode is the fused one: the
+    # preprocess, one key/value-stationary kernel that also accumulates dQ,
+    # and the dQ convert pass, one after the other. Otherwise (d_qk = 192,
+    # packed sequences, --deterministic) the dK/dV and dQ kernels run
+    # concurrently after the preprocess.
+    fused = not args.deterministic and w["D_qk"] <= 128 and not packed
     q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dbias = torch.empty_like(bias) if bias is not None else None
@@ -421,7 +431,8 @@ def main():
 
     def step(ev=None):
         # ev: fwd start, fwd end = pre start, pre end = dQ start, dQ end,
-        # dK/dV start, dK/dV end (the last two on the side stream)
+        # dK/dV start, dK/dV end (the last two on the side stream; fused:
+        # all on one stream, dK/dV start = pre end, dK/dV end = dQ start)
         if ev is not None:
             ev[0].record(stream)
         if mask_words:  # the keep bits of this step, drawn once for all three kernels
@@ -431,6 +442,17 @@ def main():
         if ev is not None:
             ev[1].record(stream)
         bwd_call(SDPA_BWD_PREPROCESS, set0)
+        if fused:
+            if ev is not None:
+                ev[2].record(stream)
+                ev[4].record(stream)
+            bwd_call(SDPA_BWD_DKDV, set0)
+            if ev is not None:
+                ev[5].record(stream)
+            bwd_call(SDPA_BWD_DQ, set0)
+            if ev is not None:
+                ev[3].record(stream)
+            return
         fork = torch.cuda.Event()
         fork.record(stream)
         if ev is not None:
@@ -472,7 +494,8 @@ def main():
         raise SystemExit("a kernel wait ran out during the timed steps")
     total_ms = t_start.elapsed_time(t_end)
     per_kernel = {n: 0.0 for n in names}
-    spans = {"fwd": (0, 1), "bwd_pre": (1, 2), "bwd_dkdv": (4, 5), "bwd_dq": (2, 3)}
+    spans = {"fwd": (0, 1), "bwd_pre": (1, 2), "bwd_dkdv": (4, 5),
+             "bwd_dq": (5, 3) if fused else (2, 3)}
     for e in evs:
         for n, (a, b) in spans.items():
             per_kernel[n] += e[a].elapsed_time(e[b])
@@ -485,14 +508,17 @@ def main():
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
 
-    # dominant kernel and its roofline (dQ's span holds the concurrent dK/dV,
-    # so the choice is among the kernels timed alone)
-    dom = max((n for n in per_kernel if n != "bwd_dq"), key=per_kernel.get)
+    # dominant kernel and its roofline (deterministic: dQ's span holds the
+    # concurrent dK/dV, so the choice is among the kernels timed alone)
+    dom = max((n for n in per_kernel if fused or n != "bwd_dq"), key=per_kernel.get)
     # algorithmic FLOPs per launch: the dK/dV kernel forms S^T, dP^T, dV, dK
-    # (2x the forward); the dQ kernel's algorithmic share is the dQ product
-    # alone (its recomputed S and dP are not counted)
+    # (2x the forward), the fused one dQ as well; the deterministic dQ
+    # kernel's algorithmic share is the dQ product alone (its recomputed S and
+    # dP are not counted); the convert pass is memory traffic only
     dq_share = 2.0 * w["D_qk"] / (w["D_qk"] + w["D_v"]) * 0.5 * ff
-    kernel_flops = {"fwd": ff, "bwd_dkdv": 2.0 * ff, "bwd_dq": dq_share}
+    kernel_flops = {"fwd": ff, "bwd_dkdv": 2.0 * ff + (dq_share if fused else 0.0)}
+    if not fused:
+        kernel_flops["bwd_dq"] = dq_share
     roof = None
     if dom in kernel_flops:
         achieved = kernel_flops[dom] / (per_kernel[dom] * 1e-3) / 1e12
@@ -583,11 +609,17 @@ def main():
     if rank == 0:
         kt = {n: {"ms": t} for n, t in per_kernel.items()}
         kt["fwd"]["tflops"] = ff / (per_kernel["fwd"] * 1e-3) / 1e12
-        kt["bwd_dkdv"]["tflops"] = 2.0 * ff / (per_kernel["bwd_dkdv"] * 1e-3) / 1e12
-        kt["bwd_dq"]["tflops_algorithmic"] = dq_share / (per_kernel["bwd_dq"] * 1e-3) / 1e12
-        kt["bwd_dq"]["tflops_executed"] = (dq_share + ff) / (per_kernel["bwd_dq"] * 1e-3) / 1e12
-        kt["bwd_dq"]["note"] = ("span from the end of the preprocess to the end of dQ, which runs "
-                                "concurrently with dK/dV (side stream) and fills its last wave")
+        kt["bwd_dkdv"]["tflops"] = kernel_flops["bwd_dkdv"] / (per_kernel["bwd_dkdv"] * 1e-3) / 1e12
+        if fused:
+            kt["bwd_dkdv"]["note"] = ("fused key/value-stationary kernel: S^T, dP^T, dV, dK and dQ "
+                                      "(fp32 reductions into the workspace accumulator)")
+            kt["bwd_dq"]["note"] = "dQ = scale * dQacc convert pass"
+        else:
+            kt["bwd_dq"]["tflops_algorithmic"] = dq_share / (per_kernel["bwd_dq"] * 1e-3) / 1e12
+            kt["bwd_dq"]["tflops_executed"] = (dq_share + ff) / (per_kernel["bwd_dq"] * 1e-3) / 1e12
+            kt["bwd_dq"]["note"] = ("span from the end of the preprocess to the end of dQ, which "
+                                    "runs concurrently with dK/dV (side stream) and fills its "
+                                    "last wave")
         # dK/dV and dQ overlap: the backward is the step without the forward
         bwd_ms = ms - per_kernel["fwd"]
         out = {
@@ -604,6 +636,7 @@ def main():
                        **({"window": list(w["window"]), "bottom_right": w.get("bottom_right", False)}
                           if w.get("window") is not None else {}),
                        **({"alibi": "slopes 2^(-8(h+1)/H)"} if w.get("alibi") else {}),
+                       "backward": "fused (dQ by fp32 reductions)" if fused else "deterministic",
                        "l2": "inputs larger than L2, no flush",
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "pct_of_peak": 100.0 * value / world / peak,

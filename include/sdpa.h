@@ -85,14 +85,27 @@ sdpa_status_t sdpa_fwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
                        const void* v, const float* bias, void* o, float* lse, void* stream);
 
 /*
- * Bytes of device workspace sdpa_bwd needs: two fp32 row statistics per query
- * row, D = rowsum(dO * O) (oneDNN's sdpa micro.cpp books the same buffer in
- * its scratchpad) and -LSE * log2(e), with s_q padded up to a multiple of 128
- * for each (b, h): 8 * b * h * ceil(s_q / 128) * 128 bytes, rounded up to 256.
- * Returns 0 for invalid sizes.
+ * Bytes of device workspace sdpa_bwd needs. Every backward keeps two fp32 row
+ * statistics per query row, D = rowsum(dO * O) (oneDNN's sdpa micro.cpp books
+ * the same buffer in its scratchpad) and -LSE * log2(e), with s_q padded up
+ * to a multiple of 128 for each (b, h): 8 * b * h * ceil(s_q / 128) * 128
+ * bytes, rounded up to 256. The default backward at d_qk <= 128 also keeps
+ * its fp32 dQ accumulator there (CK tile fmha_bwd_kernel.hpp's dq_acc,
+ * oneDNN's f32 dQ scratchpad): 4 * b * h * ceil(s_q / 128) * 128 * d_qk bytes
+ * more. Returns 0 for invalid sizes.
  */
 size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v);
+
+/*
+ * The workspace of any batch-mode backward: h_kv K/V heads (h_kv = h when
+ * they are not grouped; see the grouped calls), and deterministic != 0 for
+ * the deterministic backward (SDPA_BWD_DETERMINISTIC), which needs only the
+ * row statistics. With grouped heads the room for splitting large groups is
+ * included (see sdpa_bwd_workspace_size_gqa). 0 for invalid sizes.
+ */
+size_t sdpa_bwd_workspace_size_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                                  int64_t d_qk, int64_t d_v, int deterministic);
 
 /*
  * Backward pass (the dV .. dQ lines of the CK header equations; argument set
@@ -105,10 +118,18 @@ size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
  *   workspace caller-owned device memory of at least
  *             sdpa_bwd_workspace_size(...) bytes, 256-byte aligned; its
  *             contents on entry are ignored and on exit are unspecified.
- * Runs three kernels on `stream`: preprocess (row statistics; zero dBias), the
- * key/value-stationary kernel (dK, dV, dBias) and the query-stationary kernel
- * (dQ). dQ, dK and dV are bitwise reproducible; dBias sums the batch with
- * fp32 atomics, reproducible for b <= 2.
+ * Runs three kernels on `stream`. At d_qk <= 128 (the default backward):
+ * preprocess (row statistics; zero dBias and the dQ accumulator), one
+ * key/value-stationary kernel that forms every product of each (query tile,
+ * key tile) pair once (dK, dV, dBias, and dQ added into the fp32 accumulator
+ * with fp32 reductions, as CK tile's FmhaBwdDQDKDVKernel and oneDNN's backward
+ * kernel do), and a convert pass dQ = scale * dQacc. dK and dV are bitwise
+ * reproducible; dQ's fp32 sums depend on the order the reductions arrive in
+ * (results of two calls may differ in the last bits), as does dBias for
+ * b > 2. At d_qk = 192, and with SDPA_BWD_DETERMINISTIC, the deterministic
+ * backward instead: preprocess, the key/value-stationary kernel (dK, dV,
+ * dBias) and a query-stationary kernel that sums dQ over the key tiles inside
+ * one CTA (recomputing S and dP), so dQ, dK and dV are bitwise reproducible.
  */
 sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                        int64_t d_v, float scale, int is_causal, float dropout_p, uint64_t seed,
@@ -117,23 +138,28 @@ sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
                        const float* lse, void* dq, void* dk, void* dv, float* dbias,
                        void* workspace, size_t workspace_bytes, void* stream);
 
-/* Phases of the backward pass, in the order they must run. */
+/* Phases of the backward pass, in the order they must run, and the flag that
+ * selects the deterministic backward. */
 typedef enum {
-  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O) and -LSE*log2e; zero dBias */
-  SDPA_BWD_DKDV = 2,       /* key/value-stationary kernel: dK, dV, dBias */
-  SDPA_BWD_DQ = 4,         /* query-stationary kernel: dQ */
-  SDPA_BWD_ALL = 7
+  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O) and -LSE*log2e; zero dBias (and dQacc) */
+  SDPA_BWD_DKDV = 2,       /* key/value-stationary kernel: dK, dV, dBias (and dQacc) */
+  SDPA_BWD_DQ = 4,         /* dQ: convert dQacc, or the query-stationary kernel */
+  SDPA_BWD_ALL = 7,
+  SDPA_BWD_DETERMINISTIC = 8 /* flag: the deterministic backward (no dQ accumulator) */
 } sdpa_bwd_phase_t;
 
 /*
  * sdpa_bwd restricted to the phases set in `phases` (a non-empty subset of
- * SDPA_BWD_ALL), with identical arguments and validation. Issuing the three
- * phases in order, with the same arguments, on one stream is exactly
- * sdpa_bwd; they are separate so a caller can time them one by one (the CK
- * page also splits its backward into three kernels). The dK/dV and dQ phases
- * both read the row statistics the preprocess phase leaves in `workspace`,
- * and the dK/dV phase adds into `dbias`, so the preprocess phase must run
- * first.
+ * SDPA_BWD_ALL, optionally with SDPA_BWD_DETERMINISTIC), with identical
+ * arguments and validation. Issuing the three phases in order, with the same
+ * arguments and flag, on one stream is exactly sdpa_bwd (or its
+ * deterministic form); they are separate so a caller can time them one by
+ * one (the CK page also splits its backward into three kernels:
+ * FmhaBwdOGradDotOKernel, FmhaBwdDQDKDVKernel, FmhaBwdConvertQGradKernel).
+ * The later phases read the row statistics (and the zeroed dQ accumulator)
+ * the preprocess phase leaves in `workspace`, and the dK/dV phase adds into
+ * `dbias`, so the preprocess phase must run first. With the flag the
+ * workspace need only hold sdpa_bwd_workspace_size_ex(..., 1) bytes.
  */
 sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int is_causal,
@@ -143,25 +169,6 @@ sdpa_status_t sdpa_bwd_phases(int phases, int64_t b, int64_t h, int64_t s_q, int
                               void* dv, float* dbias, void* workspace, size_t workspace_bytes,
                               void* stream);
 
-/*
- * sdpa_bwd for callers that cannot allocate device memory when they run the
- * backward pass (a host framework that owns all GPU memory through its own
- * pool, or a latency-critical loop that cannot afford cudaMalloc's implicit
- * synchronisation). There is no counterpart on the pages; it exists for such
- * callers. Same arguments and results as sdpa_bwd minus the workspace: the
- * scratch lives in a 16 MiB static device array inside the library, which
- * every GPU that loads the library holds until the process exits. The call
- * allocates nothing.
- *   Limit    problems with sdpa_bwd_workspace_size(...) > 16 MiB are rejected
- *            with SDPA_ERR_WORKSPACE (detail in sdpa_last_error).
- *   Sharing  all calls on a device use the same array and leave their data in
- *            it; each call re-zeroes what must start at zero, but calls whose
- *            kernels overlap on the GPU (e.g. on two streams) race: serialise
- *            them.
- *   Set-up   the first call on each device looks up the array's device
- *            address (cudaGetSymbolAddress) with that device current; make
- *            that first call before any stream capture begins.
- */
 /*
  * Grouped K/V heads (GQA; MQA when h_kv = 1): the same three calls with an
  * h_kv argument. q, o, dout, dq and lse have h query heads; k, v, dk and dv
@@ -349,6 +356,27 @@ sdpa_status_t sdpa_bwd_phases_varlen_ex(
     const void* v, const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
     void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The backward pass for callers that cannot allocate device memory when they
+ * run it (a host framework that owns all GPU memory through its own pool, or
+ * a latency-critical loop that cannot afford cudaMalloc's implicit
+ * synchronisation). There is no counterpart on the pages; it exists for such
+ * callers. Same arguments as sdpa_bwd minus the workspace, and the results of
+ * the deterministic backward (sdpa_bwd_phases with SDPA_BWD_ALL |
+ * SDPA_BWD_DETERMINISTIC): its scratch, the per-row statistics, lives in a
+ * 16 MiB static device array inside the library, which every GPU that loads
+ * the library holds until the process exits. The call allocates nothing.
+ *   Limit    problems whose sdpa_bwd_workspace_size_ex(b, h, h, s_q, s_kv,
+ *            d_qk, d_v, 1) exceeds 16 MiB are rejected with
+ *            SDPA_ERR_WORKSPACE before any device work (detail in
+ *            sdpa_last_error).
+ *   Sharing  all calls on a device use the same array and leave their data in
+ *            it; each call rewrites what it reads, but calls whose kernels
+ *            overlap on the GPU (e.g. on two streams) race: serialise them.
+ *   Set-up   the first call on each device looks up the array's device
+ *            address (cudaGetSymbolAddress) with that device current; make
+ *            that first call before any stream capture begins.
+ */
 sdpa_status_t sdpa_bwd_noalloc(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v, float scale, int is_causal, float dropout_p,
                                uint64_t seed, uint64_t offset, sdpa_dtype_t dtype, const void* q,

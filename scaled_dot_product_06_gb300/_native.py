@@ -21,6 +21,7 @@ SDPA_BWD_PREPROCESS = 1
 SDPA_BWD_DKDV = 2
 SDPA_BWD_DQ = 4
 SDPA_BWD_ALL = 7
+SDPA_BWD_DETERMINISTIC = 8
 SDPA_BF16 = 0
 SDPA_FP16 = 1
 
@@ -31,6 +32,7 @@ SIGNATURES = {
     "sdpa_fwd": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64, _int,
                         _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
     "sdpa_bwd_workspace_size": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64]),
+    "sdpa_bwd_workspace_size_ex": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _int]),
     "sdpa_bwd_workspace_size_gqa": (_sz, [_i64, _i64, _i64, _i64, _i64, _i64, _i64]),
     "sdpa_bwd": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _f32, _int, _f32, _u64, _u64, _int,
                         _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,

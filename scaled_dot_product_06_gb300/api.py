@@ -107,32 +107,41 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
     return out, lse
 
 
-def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv=None) -> int:
-    """Backward workspace bytes; with h_kv (grouped K/V heads) the room for
-    splitting large groups over several CTAs per key tile is included."""
-    if h_kv is None or h_kv == h:
-        return int(_native.lib().sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v))
-    return int(_native.lib().sdpa_bwd_workspace_size_gqa(b, h, h_kv, s_q, s_kv, d_qk, d_v))
+def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv=None, deterministic=False) -> int:
+    """Backward workspace bytes: the row statistics, plus the fp32 dQ
+    accumulator of the default backward at d_qk <= 128 (not with
+    deterministic=True); with h_kv (grouped K/V heads) the room for splitting
+    large groups over several CTAs per key tile is included."""
+    return int(_native.lib().sdpa_bwd_workspace_size_ex(b, h, h if h_kv is None else h_kv, s_q, s_kv,
+                                                        d_qk, d_v, int(bool(deterministic))))
 
 
 def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
              offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None, dbias=None,
              stream=None, window=None, bottom_right=False, alibi_slopes=None,
-             dropout_mask=None):
+             dropout_mask=None, deterministic=False):
     """Backward pass. Returns (dq, dk, dv, dbias or None); dk and dv have k's
-    and v's shapes (with grouped K/V heads, sums over each group)."""
+    and v's shapes (with grouped K/V heads, sums over each group).
+    deterministic=True runs the deterministic backward (dQ from the
+    query-stationary kernel, bitwise reproducible) instead of accumulating dQ
+    with fp32 reductions."""
     return sdpa_bwd_phases(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, scale=scale,
                            is_causal=is_causal, dropout_p=dropout_p, seed=seed, offset=offset,
                            bias=bias, workspace=workspace, dq=dq, dk=dk, dv=dv, dbias=dbias,
                            stream=stream, window=window, bottom_right=bottom_right,
-                           alibi_slopes=alibi_slopes, dropout_mask=dropout_mask)
+                           alibi_slopes=alibi_slopes, dropout_mask=dropout_mask,
+                           deterministic=deterministic)
 
 
 def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0,
                     seed=0, offset=0, bias=None, workspace=None, dq=None, dk=None, dv=None,
                     dbias=None, stream=None, window=None, bottom_right=False, alibi_slopes=None,
-             dropout_mask=None):
-    """The backward phases selected by ``phases`` (SDPA_BWD_* bit mask)."""
+                    dropout_mask=None, deterministic=False):
+    """The backward phases selected by ``phases`` (SDPA_BWD_* bit mask; the
+    SDPA_BWD_DETERMINISTIC bit, or deterministic=True, selects the
+    deterministic backward)."""
+    deterministic = bool(deterministic) or bool(int(phases) & _native.SDPA_BWD_DETERMINISTIC)
+    phases = int(phases) | (_native.SDPA_BWD_DETERMINISTIC if deterministic else 0)
     b, h, s_q, d_qk = q.shape
     h_kv, s_kv, d_v = k.shape[1], k.shape[2], v.shape[3]
     dt = q.dtype
@@ -151,7 +160,7 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
     dv = torch.empty_like(v) if dv is None else dv
     if bias is not None and dbias is None:
         dbias = torch.empty_like(bias)
-    need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv)
+    need = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv, deterministic)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)

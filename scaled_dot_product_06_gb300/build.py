@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdpa.so")
 SOURCES = ["api.cu", "aux.cu", "noalloc.cu", "fwd_bf16.cu", "fwd_fp16.cu", "bwd_dkdv_bf16.cu",
-           "bwd_dkdv_fp16.cu", "bwd_dq_bf16.cu", "bwd_dq_fp16.cu"]
+           "bwd_dkdv_fp16.cu", "bwd_dq_bf16.cu", "bwd_dq_fp16.cu", "bwd_fused_bf16.cu",
+           "bwd_fused_fp16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -124,6 +124,8 @@ sdpa_status_t check_sizes(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64
   if (!(dropout_p >= 0.0f && dropout_p < 1.0f)) return SDPA_ERR_INVALID_ARG;
   if (dtype != SDPA_BF16 && dtype != SDPA_FP16) return SDPA_ERR_UNSUPPORTED;
   if (!head_sizes_ok(d_qk, d_v)) return SDPA_ERR_UNSUPPORTED;
+  // b and h bounded one by one before their product, which could overflow
+  if (b > (int64_t{1} << 24) || h > (int64_t{1} << 24)) return SDPA_ERR_UNSUPPORTED;
   if (s_q > kMaxSeq || s_kv > kMaxSeq || b * h > (int64_t{1} << 24)) return SDPA_ERR_UNSUPPORTED;
   if (dropout_p > 0.0f && (s_kv % 4) != 0) return SDPA_ERR_UNSUPPORTED;
   *empty = (b == 0 || h == 0 || s_q == 0 || s_kv == 0);
@@ -313,6 +315,29 @@ sdpa_status_t check_packing(const Packing& pk, int64_t b, const float* bias, boo
   return SDPA_OK;
 }
 
+// Bytes of the row statistics (-LSE log2e and D per query row, rows padded
+// to 128 per (b, h)), rounded up to 256: the whole workspace of the
+// deterministic backward.
+size_t stats_bytes(int64_t b, int64_t h, int64_t s_q) {
+  const size_t prows = static_cast<size_t>(b) * h * static_cast<size_t>(sdpa::stat_pad(static_cast<int>(s_q)));
+  return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
+}
+
+// Bytes of the fused backward's fp32 dQ accumulator: d_qk floats per query
+// row, rows padded to 128 per (b, h) (a multiple of 256 bytes).
+size_t dq_acc_bytes(int64_t b, int64_t h, int64_t s_q, int64_t d_qk) {
+  return static_cast<size_t>(b) * h * static_cast<size_t>((s_q + 127) / 128) * 128 * d_qk * sizeof(float);
+}
+
+// The fused backward (one key/value-stationary kernel that also accumulates
+// dQ) serves batch mode with d_qk <= 128 unless the caller asks for the
+// deterministic backward; tensor memory has no room for its dQ tile beside
+// dK at d_qk = 192, and the packed entry points size their workspace without
+// d_qk.
+bool use_fused(int phases, int64_t d_qk, const Packing& pk) {
+  return (phases & SDPA_BWD_DETERMINISTIC) == 0 && d_qk <= 128 && pk.seqstart_q == nullptr;
+}
+
 sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv, int64_t d_qk,
                        int64_t d_v, float scale, const Mask& mask, float dropout_p, uint64_t seed,
                        uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
@@ -382,7 +407,9 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
                        float* dbias, void* workspace, size_t workspace_bytes, void* stream,
                        const Packing& pk) {
-  if (phases <= 0 || (phases & ~SDPA_BWD_ALL) != 0) return fail(SDPA_ERR_INVALID_ARG, "phases");
+  if ((phases & SDPA_BWD_ALL) == 0 || (phases & ~(SDPA_BWD_ALL | SDPA_BWD_DETERMINISTIC)) != 0)
+    return fail(SDPA_ERR_INVALID_ARG, "phases");
+  const bool fused = use_fused(phases, d_qk, pk);
   bool empty = false;
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
   if (!scale_ok(scale)) return fail(SDPA_ERR_INVALID_ARG, "scale must be finite");
@@ -396,8 +423,10 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (bias && !aligned16(bias)) || (dbias && !aligned16(dbias)))
     return SDPA_ERR_MISALIGNED;
-  const size_t need = pk.seqstart_q ? sdpa_bwd_varlen_workspace_size(b, h, pk.total_q)
-                                    : sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v);
+  const size_t stat_bytes = pk.seqstart_q ? sdpa_bwd_varlen_workspace_size(b, h, pk.total_q)
+                                          : stats_bytes(b, h, s_q);
+  // the fused backward's fp32 dQ accumulator follows the statistics
+  const size_t need = stat_bytes + (fused ? dq_acc_bytes(b, h, s_q, d_qk) : 0);
   if (workspace == nullptr || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SDPA_ERR_MISALIGNED;
   // A split dK/dV when the group is large for the grid and the workspace has
@@ -443,6 +472,11 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   p.rows_q = static_cast<int>(rw.q);
   p.rows_k = static_cast<int>(rw.k);
   p.kv_split = static_cast<int>(kv_split);
+  if (fused) {
+    p.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + stat_bytes);
+    p.dq_tiles = static_cast<int>((rw.q + 127) / 128);
+  }
+  const int64_t dq_acc_elems = fused ? rw.zq * p.dq_tiles * 128 * d_qk : 0;
   const int n_counters = kv_split > 1 ? static_cast<int>(((s_kv + 127) / 128) * b * h_kv) : 0;
   if (kv_split > 1) {
     uint8_t* extra = static_cast<uint8_t*>(workspace) + need;
@@ -457,13 +491,16 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
     const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
     e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, rw.zq, static_cast<int>(s_q), p.S_pad, p.rows_q,
                        pk.seqstart_q, static_cast<int>(b), dvi, dbias_elems, p.dkdv_count, n_counters,
-                       st);
+                       p.dq_acc, dq_acc_elems, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward preprocess launch", e);
   }
   // Both main kernels requested: dK/dV on the side stream, forked after the
-  // preprocess and joined back before the call returns (see SideStream).
+  // preprocess and joined back before the call returns (see SideStream). The
+  // fused backward's convert pass reads what its main kernel accumulates, so
+  // both stay on `stream`.
   SideStream side;
-  const bool fork = (phases & SDPA_BWD_DKDV) && (phases & SDPA_BWD_DQ) && side_stream(&side) &&
+  const bool fork = !fused && (phases & SDPA_BWD_DKDV) && (phases & SDPA_BWD_DQ) &&
+                    side_stream(&side) &&
                     cudaEventRecord(side.fork, st) == cudaSuccess &&
                     cudaStreamWaitEvent(side.stream, side.fork, 0) == cudaSuccess;
   const cudaStream_t st_dkdv = fork ? side.stream : st;
@@ -485,14 +522,21 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
       join();
       return ms;
     }
-    e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
-             : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
+    if (fused)
+      e = bf16 ? launch_bwd_fused_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
+               : launch_bwd_fused_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
+    else
+      e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
+               : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
     if (e != cudaSuccess) {
       join();
       return fail(SDPA_ERR_CUDA, "backward dK/dV kernel launch", e);
     }
   }
-  if (phases & SDPA_BWD_DQ) {
+  if ((phases & SDPA_BWD_DQ) && fused) {  // dQ = scale * dQacc in the io dtype
+    e = launch_dq_convert(bf16, p.dq_acc, dq, rw.zq, static_cast<int>(rw.q), p.dq_tiles, di, scale, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dQ convert launch", e);
+  } else if (phases & SDPA_BWD_DQ) {
     CUtensorMap mq, mk, mv, mdo;
     sdpa_status_t ms = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, 128, true);
     if (!ms) ms = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true);
@@ -530,7 +574,7 @@ const char* sdpa_status_string(sdpa_status_t s) {
   return "unknown sdpa status";
 }
 
-int sdpa_version(void) { return 10000; }
+int sdpa_version(void) { return 10100; }
 
 const char* sdpa_last_error(void) { return g_last_error; }
 
@@ -541,20 +585,25 @@ sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns) {
   return SDPA_OK;
 }
 
+size_t sdpa_bwd_workspace_size_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
+                                  int64_t d_qk, int64_t d_v, int deterministic) {
+  bool empty = false;
+  if (check_sizes(b, h, s_q, s_kv, d_qk, d_v, 0.0f, SDPA_BF16, &empty) != SDPA_OK) return 0;
+  if (!kv_heads_ok(h, h_kv)) return 0;
+  const int phases = SDPA_BWD_ALL | (deterministic ? SDPA_BWD_DETERMINISTIC : 0);
+  const size_t base = stats_bytes(b, h, s_q) +
+                      (use_fused(phases, d_qk, Packing{}) ? dq_acc_bytes(b, h, s_q, d_qk) : 0);
+  return base + split_bytes(b, h, h_kv, s_kv, d_qk, d_v);
+}
+
 size_t sdpa_bwd_workspace_size_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                                    int64_t d_qk, int64_t d_v) {
-  const size_t base = sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v);
-  if (base == 0 || !kv_heads_ok(h, h_kv)) return 0;
-  return base + split_bytes(b, h, h_kv, s_kv, d_qk, d_v);
+  return sdpa_bwd_workspace_size_ex(b, h, h_kv, s_q, s_kv, d_qk, d_v, 0);
 }
 
 size_t sdpa_bwd_workspace_size(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t d_qk,
                                int64_t d_v) {
-  bool empty = false;
-  if (check_sizes(b, h, s_q, s_kv, d_qk, d_v, 0.0f, SDPA_BF16, &empty) != SDPA_OK) return 0;
-  // two floats (-LSE*log2e, D) per query row, rows padded to 128 per (b, h)
-  const size_t prows = static_cast<size_t>(b) * h * static_cast<size_t>(sdpa::stat_pad(static_cast<int>(s_q)));
-  return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
+  return sdpa_bwd_workspace_size_ex(b, h, h, s_q, s_kv, d_qk, d_v, 0);
 }
 
 sdpa_status_t sdpa_fwd_gqa(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,

@@ -5,7 +5,10 @@
 //   -LSE * log2(e), in the tiled row-statistics layout of stat_index, and zeroing
 //   of dBias, which the key/value-stationary kernel accumulates into (oneDNN
 //   sdpa micro.cpp, execute_backward: preprocess and fill of the f32
-//   intermediates).
+//   intermediates), and of the fused backward's fp32 dQ accumulator.
+// * dq_convert: dQ = scale * dQacc rounded to the io dtype, the fused
+//   backward's last step (CK tile fmha_bwd_kernel.hpp FmhaBwdConvertQGradKernel;
+//   oneDNN sdpa micro.cpp's postprocess cast of the f32 dQ).
 // * dropout_mask: the packed keep bits of the whole problem, drawn by the same
 //   device Philox function the fused kernels use (oneDNN's dropout mask output
 //   and CK's stored random values serve the same purpose).
@@ -38,7 +41,9 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
                                                               int64_t z_count, int s_q, int s_pad,
                                                               int rows, const int* __restrict__ seqstart,
                                                               int n_seq, int d_v, int64_t dbias_elems,
-                                                              int* __restrict__ counters, int n_counters) {
+                                                              int* __restrict__ counters, int n_counters,
+                                                              float4* __restrict__ dq_acc,
+                                                              int64_t dq_acc_vec) {
   const int group = d_v / 8;  // 8 or 16 threads per row (power of two)
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -94,6 +99,38 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
   for (int64_t i = tid; i < dbias_vec; i += nthreads) dbias[i] = z;
   if (tid < (dbias_elems & 3)) reinterpret_cast<float*>(dbias)[dbias_vec * 4 + tid] = 0.f;
   for (int64_t i = tid; i < n_counters; i += nthreads) counters[i] = 0;  // split dK/dV tiles
+  for (int64_t i = tid; i < dq_acc_vec; i += nthreads) dq_acc[i] = z;    // fused dQ accumulator
+}
+
+// dQ = scale * dQacc in the io dtype: one thread per (z, row, 8 columns); the
+// threads of a warp take 32 consecutive rows of one 8-column block, so each of
+// their two 16-byte accumulator reads is one 512-byte run of the tiled layout
+// (dq_acc_index: per z and 128-row tile, per group of 4 columns, 128 rows of
+// 16 bytes).
+template <bool BF16>
+__global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const float4* __restrict__ acc,
+                                                                 uint4* __restrict__ dq, int64_t z_count,
+                                                                 int rows, int dq_tiles, int d,
+                                                                 float scale) {
+  const int c8n = d / 8;  // 8-column blocks per row
+  const int64_t per_z = static_cast<int64_t>(dq_tiles) * 128 * c8n;
+  const int64_t total = z_count * per_z;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += nthreads) {
+    const int64_t z = t / per_z;
+    const int64_t r0 = t - z * per_z;
+    const int tile = static_cast<int>(r0 / (128 * c8n));
+    const int r1 = static_cast<int>(r0 - static_cast<int64_t>(tile) * 128 * c8n);
+    const int c8 = r1 / 128, rr = r1 % 128;
+    const int row = tile * 128 + rr;
+    if (row >= rows) continue;
+    // groups 2 c8 and 2 c8 + 1 of the row, 128 rows apart in float4 units
+    const int64_t g0 = ((z * dq_tiles + tile) * (d / 4) + 2 * c8) * 128 + rr;
+    const float4 a = acc[g0], b = acc[g0 + 128];
+    dq[(z * rows + row) * c8n + c8] =
+        make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
+                   pack2<BF16>(b.x * scale, b.y * scale), pack2<BF16>(b.z * scale, b.w * scale));
+  }
 }
 
 // Word w holds the keep bits of elements 32w .. 32w+31 (bit e = element 32w+e).
@@ -122,15 +159,27 @@ __global__ void __launch_bounds__(kAuxThreads) dropout_mask_kernel(int64_t total
 cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
                            float* dbias, int64_t z_count, int s_q, int s_pad, int rows,
                            const int* seqstart, int n_seq, int d_v, int64_t dbias_elems,
-                           int* counters, int n_counters, cudaStream_t st) {
+                           int* counters, int n_counters, float* dq_acc, int64_t dq_acc_elems,
+                           cudaStream_t st) {
   const int group = d_v / 8;
   const int64_t work = z_count * s_pad * group;
-  const int64_t zero_work = dbias_elems / 4;
+  const int64_t zero_work = (dbias_elems + dq_acc_elems) / 4;
   const int grid = aux_grid(work > zero_work ? work : zero_work);
   auto kern = bf16 ? bwd_pre_kernel<true> : bwd_pre_kernel<false>;
   kern<<<grid, kAuxThreads, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, stats,
                                       reinterpret_cast<float4*>(dbias), z_count, s_q, s_pad, rows, seqstart,
-                                      n_seq, d_v, dbias_elems, counters, n_counters);
+                                      n_seq, d_v, dbias_elems, counters, n_counters,
+                                      reinterpret_cast<float4*>(dq_acc), dq_acc_elems / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(bool bf16, const float* dq_acc, void* dq, int64_t z_count, int rows,
+                              int dq_tiles, int d_qk, float scale, cudaStream_t st) {
+  const int64_t work = z_count * dq_tiles * 128 * (d_qk / 8);
+  auto kern = bf16 ? dq_convert_kernel<true> : dq_convert_kernel<false>;
+  kern<<<aux_grid(work), kAuxThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
+                                               static_cast<uint4*>(dq), z_count, rows, dq_tiles,
+                                               d_qk, scale);
   return cudaGetLastError();
 }
 

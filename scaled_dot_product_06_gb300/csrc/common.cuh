@@ -23,6 +23,7 @@ enum : uint32_t {
   kSiteBwdMma = 1u << 5,
   kSiteBwdCompute = 1u << 6,
   kSiteDrain = 1u << 8,
+  kSiteSmemAlign = 1u << 9,  // dynamic shared memory not 1024-byte aligned
 };
 
 struct FwdParams {
@@ -193,6 +194,10 @@ struct BwdParams {
   int rows_q, rows_k;
   const uint32_t* keep_bits;  // dropout keep bits drawn beforehand, as in FwdParams
   int64_t keep_words;
+  // fp32 dQ accumulator of the fused backward (bwd_fused_kernel.cuh,
+  // dq_acc_index): dq_tiles 128-row tiles per tensor-map z; null otherwise.
+  float* dq_acc;
+  int dq_tiles;
 };
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -383,10 +388,19 @@ cudaError_t launch_bwd_dq_bf16(int d_qk, int d_v, const CUtensorMap& q, const CU
 cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
                                const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
                                cudaStream_t st);
+cudaError_t launch_bwd_fused_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                                  const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                                  cudaStream_t st);
+cudaError_t launch_bwd_fused_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
+                                  const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                                  cudaStream_t st);
 cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
                            float* dbias, int64_t z_count, int s_q, int s_pad, int rows,
                            const int* seqstart, int n_seq, int d_v, int64_t dbias_elems,
-                           int* counters, int n_counters, cudaStream_t st);
+                           int* counters, int n_counters, float* dq_acc, int64_t dq_acc_elems,
+                           cudaStream_t st);
+cudaError_t launch_dq_convert(bool bf16, const float* dq_acc, void* dq, int64_t z_count, int rows,
+                              int dq_tiles, int d_qk, float scale, cudaStream_t st);
 cudaError_t launch_dropout_mask(int64_t total, uint32_t threshold, uint32_t seed_lo,
                                 uint32_t seed_hi, uint32_t off_lo, uint32_t off_hi,
                                 uint32_t* bits, cudaStream_t st);

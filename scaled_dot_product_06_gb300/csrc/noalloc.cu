@@ -9,11 +9,14 @@
 // kernels share) in a fixed,
 // file-scope device array that exists for as long as the library is loaded,
 // on every GPU that loads it. It calls no cudaMalloc, cudaFree or other
-// allocating routine.
+// allocating routine. It runs the deterministic backward
+// (SDPA_BWD_DETERMINISTIC), whose scratch is only those statistics, so its
+// results are bitwise those of sdpa_bwd_phases with that flag.
 //
 // Limits and sharing:
 // * The array holds kNoAllocScratchBytes (16 MiB). A problem whose scratch
-//   (sdpa_bwd_workspace_size) is larger is rejected with SDPA_ERR_WORKSPACE.
+//   (sdpa_bwd_workspace_size_ex with deterministic = 1) is larger is
+//   rejected with SDPA_ERR_WORKSPACE.
 // * Every call on a device uses the same array and leaves its contents behind;
 //   the preprocess kernel of each call overwrites the statistics before the other kernels
 //   read it, so nothing carries over.
@@ -42,8 +45,12 @@ void* g_scratch_ptr[kMaxDevices] = {};
 // Device address of g_bwd_scratch on the current device (looked up once).
 sdpa_status_t scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     sdpa::set_last_error("sdpa_bwd_noalloc: cudaGetDevice failed");
+    return SDPA_ERR_CUDA;
+  }
+  if (dev >= kMaxDevices) {
+    sdpa::set_last_error("sdpa_bwd_noalloc: device index exceeds the 64-device scratch cache");
     return SDPA_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
@@ -73,11 +80,12 @@ sdpa_status_t sdpa_bwd_noalloc(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
   // checks sizes, pointers and alignment first and, given no workspace,
   // answers SDPA_ERR_WORKSPACE only when all of them are fine (an empty
   // problem returns SDPA_OK there and launches nothing).
-  const sdpa_status_t pre = sdpa_bwd(b, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed,
-                                     offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias,
-                                     nullptr, 0, stream);
+  constexpr int kPhases = SDPA_BWD_ALL | SDPA_BWD_DETERMINISTIC;
+  const sdpa_status_t pre =
+      sdpa_bwd_phases(kPhases, b, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed, offset,
+                      dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias, nullptr, 0, stream);
   if (pre != SDPA_ERR_WORKSPACE) return pre;
-  if (sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v) > kNoAllocScratchBytes) {
+  if (sdpa_bwd_workspace_size_ex(b, h, h, s_q, s_kv, d_qk, d_v, 1) > kNoAllocScratchBytes) {
     sdpa::set_last_error(
         "sdpa_bwd_noalloc: the problem needs more backward scratch than the 16 MiB static array "
         "holds; use sdpa_bwd with a caller-allocated workspace");
@@ -85,8 +93,9 @@ sdpa_status_t sdpa_bwd_noalloc(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, 
   }
   void* scratch = nullptr;
   if (sdpa_status_t s = scratch_address(&scratch)) return s;
-  return sdpa_bwd(b, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed, offset, dtype, q, k,
-                  v, bias, o, dout, lse, dq, dk, dv, dbias, scratch, kNoAllocScratchBytes, stream);
+  return sdpa_bwd_phases(kPhases, b, h, s_q, s_kv, d_qk, d_v, scale, is_causal, dropout_p, seed,
+                         offset, dtype, q, k, v, bias, o, dout, lse, dq, dk, dv, dbias, scratch,
+                         kNoAllocScratchBytes, stream);
 }
 
 }  // extern "C"

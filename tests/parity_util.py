@@ -68,30 +68,39 @@ def assert_lse(got, ref):
     assert err <= LSE_TOL, f"lse: max|err| {err:.3e} > {LSE_TOL}"
 
 
-def run_gpu(case: Case, x: dict, dev="cuda"):
+def fused_applies(case: Case) -> bool:
+    """The default backward accumulates dQ in the key/value-stationary kernel
+    at d_qk <= 128; at d_qk = 192 it is the deterministic backward."""
+    return case.D_qk <= 128
+
+
+def run_gpu(case: Case, x: dict, dev="cuda", deterministic=False):
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     bias = None if x["bias"] is None else x["bias"].to(dev)
     kw = dict(scale=case.sc, is_causal=case.causal, dropout_p=case.p, seed=case.seed,
               offset=case.offset, bias=bias)
     o, lse = sdpa_fwd(q, k, v, **kw)
-    dq, dk, dv, dbias = sdpa_bwd(q, k, v, o, do, lse, **kw)
+    dq, dk, dv, dbias = sdpa_bwd(q, k, v, o, do, lse, deterministic=deterministic, **kw)
     torch.cuda.synchronize()
     assert sdpa_device_error() == 0, "a kernel wait ran out"
     return o, lse, dq, dk, dv, dbias
 
 
 def check_full(case: Case):
-    """Element-by-element comparison of every output on the whole problem."""
+    """Element-by-element comparison of every output on the whole problem, for
+    the default backward and (where it differs) the deterministic one."""
     x = make_inputs(case.shape, case.dtype, with_bias=case.bias)
-    o, lse, dq, dk, dv, dbias = run_gpu(case, x)
     pr = case.problem()
     o_ref, lse_ref = oracle.forward(pr, x["q"], x["k"], x["v"], x["bias"])
-    assert_close("o", o, o_ref)
-    assert_lse(lse, lse_ref)
     dq_ref, dk_ref, dv_ref, db_ref = oracle.backward(pr, x["q"], x["k"], x["v"], x["do"],
                                                      x["bias"])
-    assert_close("dq", dq, dq_ref)
-    assert_close("dk", dk, dk_ref)
-    assert_close("dv", dv, dv_ref)
-    if case.bias:
-        assert_close("dbias", dbias, db_ref)
+    for deterministic in ((False, True) if fused_applies(case) else (False,)):
+        o, lse, dq, dk, dv, dbias = run_gpu(case, x, deterministic=deterministic)
+        tag = " (deterministic)" if deterministic else ""
+        assert_close("o", o, o_ref)
+        assert_lse(lse, lse_ref)
+        assert_close("dq" + tag, dq, dq_ref)
+        assert_close("dk" + tag, dk, dk_ref)
+        assert_close("dv" + tag, dv, dv_ref)
+        if case.bias:
+            assert_close("dbias" + tag, dbias, db_ref)

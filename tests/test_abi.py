@@ -87,11 +87,49 @@ def bwd(lib, b=1, h=1, sq=128, skv=128, dqk=64, dv=64, p=0.0, bias=NULL, dbias=N
 
 
 def test_workspace_size(lib):
-    b, h, sq, dqk = 2, 3, 100, 128
+    b, h, sq = 2, 3, 100
     s_pad = (sq + 127) // 128 * 128  # query rows padded to whole 128-row tiles
-    want = ((b * h * s_pad * 2 * 4 + 255) // 256) * 256  # -LSE*log2e and D, fp32 per row
-    assert lib.sdpa_bwd_workspace_size(b, h, sq, 50, dqk, 128) == want
+    stats = ((b * h * s_pad * 2 * 4 + 255) // 256) * 256  # -LSE*log2e and D, fp32 per row
+    for dqk, dv in ((64, 64), (128, 128)):
+        dq_acc = b * h * s_pad * dqk * 4  # the default backward's fp32 dQ accumulator
+        assert lib.sdpa_bwd_workspace_size(b, h, sq, 50, dqk, dv) == stats + dq_acc
+        assert lib.sdpa_bwd_workspace_size_ex(b, h, h, sq, 50, dqk, dv, 0) == stats + dq_acc
+        assert lib.sdpa_bwd_workspace_size_ex(b, h, h, sq, 50, dqk, dv, 1) == stats
+    # d_qk = 192 always runs the deterministic backward: statistics only
+    assert lib.sdpa_bwd_workspace_size(b, h, sq, 50, 192, 128) == stats
+    assert lib.sdpa_bwd_workspace_size_ex(b, h, h, sq, 50, 192, 128, 0) == stats
     assert lib.sdpa_bwd_workspace_size(1, 1, 8, 8, 80, 80) == 0
+    assert lib.sdpa_bwd_workspace_size_ex(1, 4, 3, 8, 8, 64, 64, 0) == 0  # 3 does not divide 4
+    # b and h are bounded one by one before their product is formed
+    assert lib.sdpa_bwd_workspace_size(1 << 40, 1 << 40, 8, 8, 64, 64) == 0
+
+
+def test_backward_phase_flags_validated(lib):
+    for phases in (0, 8, 16, 7 | 16):  # no phase, the flag alone, unknown bits
+        st = lib.sdpa_bwd_phases(phases, 1, 1, 128, 128, 64, 64, 0.125, 1, 0.0, 0, 0, 0, P, P, P,
+                                 None, P, P, P, P, P, P, None, P, 1 << 20, None)
+        assert st == _native.SDPA_ERR_INVALID_ARG
+
+
+def test_deterministic_backward_needs_only_the_statistics(lib):
+    # the default backward wants the dQ accumulator too; the deterministic
+    # one is satisfied by the statistics alone (both rejected before any launch)
+    stats = lib.sdpa_bwd_workspace_size_ex(1, 1, 1, 128, 128, 64, 64, 1)
+    assert bwd(lib, ws_bytes=stats) == _native.SDPA_ERR_WORKSPACE
+    st = lib.sdpa_bwd_phases(7 | 8, 1, 1, 128, 128, 64, 64, 0.125, 1, 0.0, 0, 0, 0, P, P, P, None,
+                             P, P, P, P, P, P, None, P, stats - 256, None)
+    assert st == _native.SDPA_ERR_WORKSPACE
+
+
+def test_noalloc_rejects_problems_larger_than_its_scratch(lib):
+    # Host-only: the size check runs before any CUDA call, so the pointers are
+    # never dereferenced. 64 * 64 * 2048 query rows need 64 * 64 * 2048 * 8
+    # bytes (~67 MB) of statistics, more than the 16 MiB static scratch.
+    B, H, S, D = 64, 64, 2048, 128
+    st = lib.sdpa_bwd_noalloc(B, H, S, S, D, D, 0.1, 1, 0.0, 0, 0, _native.SDPA_BF16, P, P, P, None,
+                              P, P, P, P, P, P, None, None)
+    assert st == _native.SDPA_ERR_WORKSPACE
+    assert "16 MiB" in lib.sdpa_last_error().decode()
 
 
 def test_bwd_argument_errors(lib):

@@ -51,18 +51,19 @@ def test_window_matches_oracle(c):
     kw = dict(scale=scale, dropout_p=p, seed=SEED, offset=OFFSET, bias=bias, window=win,
               bottom_right=br)
     o, lse = sdpa_fwd(q, k, v, **kw)
-    dq, dk, dv, dbias = sdpa_bwd(q, k, v, o, do, lse, **kw)
-    torch.cuda.synchronize()
-    assert sdpa_device_error() == 0
     o_ref, lse_ref = oracle.forward(pr, x["q"], x["k"], x["v"], x["bias"])
     assert_close("o", o, o_ref)
     assert_lse(lse, lse_ref)
     dq_r, dk_r, dv_r, db_r = oracle.backward(pr, x["q"], x["k"], x["v"], x["do"], x["bias"])
-    assert_close("dq", dq, dq_r)
-    assert_close("dk", dk, dk_r)
-    assert_close("dv", dv, dv_r)
-    if with_bias:
-        assert_close("dbias", dbias, db_r)
+    for det in (False, True):  # the default (fused) and the deterministic backward
+        dq, dk, dv, dbias = sdpa_bwd(q, k, v, o, do, lse, deterministic=det, **kw)
+        torch.cuda.synchronize()
+        assert sdpa_device_error() == 0
+        assert_close(f"dq det={det}", dq, dq_r)
+        assert_close(f"dk det={det}", dk, dk_r)
+        assert_close(f"dv det={det}", dv, dv_r)
+        if with_bias:
+            assert_close(f"dbias det={det}", dbias, db_r)
 
 
 @pytest.mark.parametrize("scale", [-0.1, 0.0])
@@ -125,15 +126,19 @@ def test_window_path_equals_plain_path_bitwise(causal):
     x = make_inputs(Shape(B, H, S, S, D, D), "bf16", device="cuda")
     q, k, v, do = x["q"], x["k"], x["v"], x["do"]
     o_a, lse_a = sdpa_fwd(q, k, v, is_causal=causal)
-    g_a = sdpa_bwd(q, k, v, o_a, do, lse_a, is_causal=causal)
     wins = [(-1, 0), (S - 1, 0)] if causal else [(5000, 5000), (S - 1, S - 1)]
-    for win in wins:
-        o_b, lse_b = sdpa_fwd(q, k, v, window=win, bottom_right=False)
-        g_b = sdpa_bwd(q, k, v, o_b, do, lse_b, window=win, bottom_right=False)
-        torch.cuda.synchronize()
-        assert torch.equal(o_a, o_b) and torch.equal(lse_a, lse_b), win
-        for a, b in zip(g_a[:3], g_b[:3]):
-            assert torch.equal(a, b), win
+    # every gradient of the deterministic backward; dK and dV of the default
+    # one (its dQ sums fp32 reductions in arrival order)
+    for det in (True, False):
+        g_a = sdpa_bwd(q, k, v, o_a, do, lse_a, is_causal=causal, deterministic=det)
+        for win in wins:
+            o_b, lse_b = sdpa_fwd(q, k, v, window=win, bottom_right=False)
+            g_b = sdpa_bwd(q, k, v, o_b, do, lse_b, window=win, bottom_right=False,
+                           deterministic=det)
+            torch.cuda.synchronize()
+            assert torch.equal(o_a, o_b) and torch.equal(lse_a, lse_b), win
+            for a, b in zip(g_a[0 if det else 1:3], g_b[0 if det else 1:3]):
+                assert torch.equal(a, b), (win, det)
 
 
 def test_diagonal_window_is_exact():

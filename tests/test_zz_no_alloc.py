@@ -4,9 +4,12 @@ Some callers cannot allocate device memory when they run the backward pass
 (a framework that owns all GPU memory through its own pool, or a
 latency-critical loop that cannot pay for cudaMalloc's implicit
 synchronisation). sdpa_bwd_noalloc serves them with a fixed 16 MiB scratch
-array inside the library instead of a caller workspace. These tests call it
-through the C ABI and compare it with sdpa_bwd on the same inputs, twice in a
-row (the second call reuses the scratch the first one left behind).
+array inside the library instead of a caller workspace, running the
+deterministic backward. These tests call it through the C ABI and compare it
+with the deterministic sdpa_bwd on the same inputs, bit for bit, twice in a
+row (the second call reuses the scratch the first one left behind, so stale
+contents that changed even the last bit would show). The size limit is
+checked on the host and tested in test_abi.py.
 
 The file is named so that pytest collects it last.
 """
@@ -15,7 +18,6 @@ import ctypes
 import pytest
 import torch
 
-from parity_util import assert_close
 from scaled_dot_product_06_gb300 import _native, sdpa_bwd, sdpa_device_error, sdpa_fwd
 from scaled_dot_product_06_gb300.inputs import Shape, make_inputs
 
@@ -49,7 +51,7 @@ def test_noalloc_matches_workspace_backward_twice(shape, dtype, causal, with_bia
     kw = dict(scale=scale, is_causal=causal, dropout_p=p, seed=seed, offset=offset,
               bias=x["bias"])
     o, lse = sdpa_fwd(x["q"], x["k"], x["v"], **kw)
-    ref = sdpa_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, **kw)
+    ref = sdpa_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, deterministic=True, **kw)
     torch.cuda.synchronize()
     assert sdpa_device_error() == 0
     for _ in range(2):
@@ -61,14 +63,5 @@ def test_noalloc_matches_workspace_backward_twice(shape, dtype, causal, with_bia
         assert sdpa_device_error() == 0
         for name, got, want in zip(("dq", "dk", "dv", "dbias"), outs, ref):
             if want is not None:
-                assert_close(name, got, want.double().cpu().numpy())
+                assert torch.equal(got, want), f"{name} differs from the deterministic sdpa_bwd"
 
-
-def test_noalloc_rejects_problems_larger_than_its_scratch():
-    aligned = ctypes.c_void_p(1 << 20)  # never dereferenced: rejected before any launch
-    B, H, S, D = 64, 64, 2048, 128      # 8.4M query rows: ~34 MB of scratch
-    st = _native.lib().sdpa_bwd_noalloc(B, H, S, S, D, D, 0.1, 1, 0.0, 0, 0, _native.SDPA_BF16,
-                                        aligned, aligned, aligned, None, aligned, aligned,
-                                        aligned, aligned, aligned, aligned, None, None)
-    assert st == _native.SDPA_ERR_WORKSPACE
-    assert "16 MiB" in _native.lib().sdpa_last_error().decode()
