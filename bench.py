@@ -43,6 +43,9 @@ WORKLOADS = {
     "b8h16-s1024x2048-d64-fp16-dropout0.1": dict(B=8, H=16, S_q=1024, S_kv=2048, D_qk=64, D_v=64,
                                                  dtype="fp16", causal=False, bias=False, p=0.1,
                                                  scale=None),
+    # the dropout case's shape without dropout: what the Philox draws cost
+    "b8h16-s1024x2048-d64-fp16": dict(B=8, H=16, S_q=1024, S_kv=2048, D_qk=64, D_v=64,
+                                      dtype="fp16", causal=False, bias=False, p=0.0, scale=None),
     # the dropout case with its keep bits drawn once per step (sdpa_dropout_mask,
     # timed with the forward) and read by the three kernels
     "b8h16-s1024x2048-d64-fp16-dropout0.1-bits": dict(B=8, H=16, S_q=1024, S_kv=2048, D_qk=64,
@@ -92,7 +95,70 @@ KERNEL_SOURCES = {
     "fwd": ["scaled_dot_product_06_gb300/csrc/fwd_kernel.cuh",
             "scaled_dot_product_06_gb300/csrc/common.cuh",
             "scaled_dot_product_06_gb300/csrc/ptx.cuh"],
+    "bwd_fused": ["scaled_dot_product_06_gb300/csrc/bwd_fused_kernel.cuh",
+                  "scaled_dot_product_06_gb300/csrc/bwd_dkdv_kernel.cuh",
+                  "scaled_dot_product_06_gb300/csrc/common.cuh",
+                  "scaled_dot_product_06_gb300/csrc/ptx.cuh"],
+    "bwd_pre": ["scaled_dot_product_06_gb300/csrc/aux.cu",
+                "scaled_dot_product_06_gb300/csrc/common.cuh"],
+    "dq_convert": ["scaled_dot_product_06_gb300/csrc/aux.cu",
+                   "scaled_dot_product_06_gb300/csrc/common.cuh"],
 }
+
+
+def visible_pairs_per_head(w: dict) -> int:
+    """(query, key) pairs a head's mask leaves visible (summed over the
+    sequences of a packed workload)."""
+    if w.get("lens"):
+        return sum(n * (n + 1) // 2 if w["causal"] else n * n for n in w["lens"])
+    if w.get("window") is not None:
+        return visible_pairs(w["S_q"], w["S_kv"], w["window"], w.get("bottom_right", False))
+    if w["causal"]:  # top-left: row i sees min(i + 1, S_kv) keys
+        return sum(min(i + 1, w["S_kv"]) for i in range(w["S_q"]))
+    return w["S_q"] * w["S_kv"]
+
+
+def kernel_bytes(w: dict, fused: bool) -> dict:
+    """Algorithmic DRAM bytes per launch of each kernel: every operand read
+    once and every result written once; the bias read and dBias written once
+    per head over the visible pairs (shared by the batch); the row statistics
+    8 bytes per query row. The fused kernel's dQ reductions stay in L2; its dQ
+    is written by the convert pass, which reads the fp32 accumulator."""
+    e = 2
+    B = 1 if w.get("lens") else w["B"]
+    H, Hkv, Dk, Dv = w["H"], w.get("H_kv", w["H"]), w["D_qk"], w["D_v"]
+    rq = H * sum(w["lens"]) if w.get("lens") else B * H * w["S_q"]
+    rk = Hkv * sum(w["lens"]) if w.get("lens") else B * Hkv * w["S_kv"]
+    q, o, lse, st = rq * Dk * e, rq * Dv * e, rq * 4, rq * 8
+    kv = rk * (Dk + Dv) * e
+    bias = H * visible_pairs_per_head(w) * 4 if w["bias"] else 0  # read over the visible pairs
+    dbias = H * w["S_q"] * w["S_kv"] * 4 if w["bias"] else 0       # written in full (0 where masked)
+    acc = B * H * ((w["S_q"] + 127) // 128) * 128 * Dk * 4  # fp32, rows padded to 128 per (b, h)
+    out = {"fwd": q + kv + o + lse + bias, "bwd_pre": 2 * o + lse + st}
+    main = q + o + kv + st + kv + bias + dbias  # Q, dO, K, V, stats, Bias in; dK, dV, dBias out
+    if fused:
+        out["bwd_fused"] = main
+        out["dq_convert"] = acc + q
+    else:
+        out["bwd_dkdv"] = main
+        out["bwd_dq"] = q + o + kv + st + q + bias
+    return out
+
+
+def workload_bound(w: dict, fwd_gflop: float) -> str:
+    """The roofline that bounds the workload (the hot-path table's bound
+    column): HBM with an fp32 bias (its 4-byte-per-pair Bias and dBias
+    dominate the bytes), the integer ALU with dropout (Philox4x32-10, ten
+    rounds per four elements, drawn in the forward and again in the
+    backward), HBM (latency) for a problem too small to fill the GPU, the
+    tensor cores otherwise."""
+    if w["bias"]:
+        return "hbm"
+    if w["p"] > 0:
+        return "alu"
+    if fwd_gflop < 1.0:
+        return "hbm"
+    return "tensor"
 
 
 def resolve(w: dict) -> dict:
@@ -419,6 +485,24 @@ def main():
     fused = not args.deterministic and w["D_qk"] <= 128 and not packed
     q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def philox_peak_gblocks(wl):
+        """Philox4x32-10 blocks per second (G) of sdpa_dropout_mask over the
+        workload's [B, H, S_q, S_kv] elements: the path's ALU roofline."""
+        nb = 1 if wl.get("lens") else wl["B"]
+        words = (nb * wl["H"] * wl["S_q"] * wl["S_kv"] + 31) // 32
+        buf = torch.empty(words, dtype=torch.int32, device=dev)
+        best = None
+        for _ in range(6):
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(torch.cuda.current_stream())
+            sdpa_dropout_mask(nb, wl["H"], wl["S_q"], wl["S_kv"], wl["p"], DROP_SEED, DROP_OFFSET,
+                              out=buf)
+            b2.record(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            t = a.elapsed_time(b2)
+            best = t if best is None else min(best, t)
+        return nb * wl["H"] * wl["S_q"] * wl["S_kv"] / 4.0 / (best * 1e-3) / 1e9
     dbias = torch.empty_like(bias) if bias is not None else None
     set0 = {"q": q, "k": k, "v": v, "do": do, "bias": bias, "o": o, "lse": lse, "dq": dq,
             "dk": dk, "dv": dv, "dbias": dbias}
@@ -507,35 +591,67 @@ def main():
     value = whole_job_tflops(world, step_flops, ms)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    # display names: the fused backward's main kernel and its convert pass
+    if fused:
+        per_kernel = {{"bwd_dkdv": "bwd_fused", "bwd_dq": "dq_convert"}.get(n, n): t
+                      for n, t in per_kernel.items()}
 
-    # dominant kernel and its roofline (deterministic: dQ's span holds the
-    # concurrent dK/dV, so the choice is among the kernels timed alone)
-    dom = max((n for n in per_kernel if fused or n != "bwd_dq"), key=per_kernel.get)
     # algorithmic FLOPs per launch: the dK/dV kernel forms S^T, dP^T, dV, dK
     # (2x the forward), the fused one dQ as well; the deterministic dQ
     # kernel's algorithmic share is the dQ product alone (its recomputed S and
-    # dP are not counted); the convert pass is memory traffic only
+    # dP are not counted); the preprocess and convert passes are memory
+    # traffic only
     dq_share = 2.0 * w["D_qk"] / (w["D_qk"] + w["D_v"]) * 0.5 * ff
-    kernel_flops = {"fwd": ff, "bwd_dkdv": 2.0 * ff + (dq_share if fused else 0.0)}
-    if not fused:
-        kernel_flops["bwd_dq"] = dq_share
-    roof = None
-    if dom in kernel_flops:
-        achieved = kernel_flops[dom] / (per_kernel[dom] * 1e-3) / 1e12
-        traffic = None
-        tpath = os.path.join(ROOT, "profiles", "traffic.json")
-        if os.path.exists(tpath):
-            with open(tpath) as f:
-                tr = json.load(f).get(args.workload, {}).get(dom)
-            if tr and tr.get("source_sha") == source_sha(dom):
-                traffic = tr.get("bytes_per_launch")
+    if fused:
+        kernel_flops = {"fwd": ff, "bwd_fused": 2.0 * ff + dq_share}
+    else:
+        kernel_flops = {"fwd": ff, "bwd_dkdv": 2.0 * ff, "bwd_dq": dq_share}
+    kbytes = kernel_bytes(w, fused)
+    # Philox4x32-10 blocks (four elements each) a kernel draws per launch:
+    # every visible element once in the forward and once in the main
+    # backward kernel(s); the deterministic dQ kernel draws them again
+    drawn = 0.0
+    if w["p"] > 0 and not w.get("bits"):
+        drawn = (1 if w.get("lens") else w["B"]) * w["H"] * visible_pairs_per_head(w) / 4.0
+    kernel_blocks = {n: drawn for n in ("fwd", "bwd_fused", "bwd_dkdv", "bwd_dq") if n in per_kernel}
+
+    # the roofline of the workload's bound, for its dominant kernel (the
+    # deterministic dQ span holds the concurrent dK/dV, so there the choice is
+    # among the kernels timed alone)
+    bound = workload_bound(w, ff / 1e9)
+    dom = max((n for n in per_kernel if fused or n != "bwd_dq"), key=per_kernel.get)
+    sec = per_kernel[dom] * 1e-3
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath) and dom in KERNEL_SOURCES:
+        with open(tpath) as f:
+            tr = json.load(f).get(args.workload, {}).get(dom)
+        if tr and tr.get("source_sha") == source_sha(dom):
+            traffic = tr.get("bytes_per_launch")
+    if bound == "tensor" and dom in kernel_flops:
+        achieved = kernel_flops[dom] / sec / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} bf16 dense (burst)"}
+    elif bound == "alu" and kernel_blocks.get(dom):
+        # peak: the same Philox4x32-10 arithmetic alone at full occupancy,
+        # sdpa_dropout_mask over this workload's elements (timed here)
+        alu_peak = philox_peak_gblocks(w)
+        achieved = kernel_blocks[dom] / sec / 1e9
+        roof = {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": alu_peak,
+                "unit": "G Philox4x32-10 blocks/s", "frac": achieved / alu_peak,
+                "traffic": traffic,
+                "peak_source": "measured: sdpa_dropout_mask (the same Philox draws, nothing else) "
+                               "over this workload's elements, best of 5"}
     else:
-        hbm = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": hbm, "unit": "GB/s",
-                "frac": None, "traffic": None, "peak_source": f"{peak_kind} HBM copy"}
+        achieved = kbytes[dom] / sec / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic,
+                "peak_source": f"{peak_kind} HBM copy",
+                "bytes_per_launch": kbytes[dom]}
+    if bound != "tensor":
+        roof["tensor_frac"] = (kernel_flops.get(dom, 0.0) / sec / 1e12) / peak
 
     # End to end through the public API (sdpa_fwd + sdpa_bwd, or their packed
     # forms: the calls a user makes) with pinned host buffers: every step uploads its inputs and reads
@@ -608,18 +724,25 @@ def main():
 
     if rank == 0:
         kt = {n: {"ms": t} for n, t in per_kernel.items()}
-        kt["fwd"]["tflops"] = ff / (per_kernel["fwd"] * 1e-3) / 1e12
-        kt["bwd_dkdv"]["tflops"] = kernel_flops["bwd_dkdv"] / (per_kernel["bwd_dkdv"] * 1e-3) / 1e12
+        for n, t in per_kernel.items():
+            if n in kernel_flops and not (n == "bwd_dq"):
+                kt[n]["tflops"] = kernel_flops[n] / (t * 1e-3) / 1e12
+            if n in kbytes:
+                gbs = kbytes[n] / (t * 1e-3) / 1e9
+                kt[n]["gbs"] = gbs
+                kt[n]["hbm_frac"] = gbs / hbm
+            if kernel_blocks.get(n):
+                kt[n]["philox_gblocks_per_s"] = kernel_blocks[n] / (t * 1e-3) / 1e9
         if fused:
-            kt["bwd_dkdv"]["note"] = ("fused key/value-stationary kernel: S^T, dP^T, dV, dK and dQ "
-                                      "(fp32 reductions into the workspace accumulator)")
-            kt["bwd_dq"]["note"] = "dQ = scale * dQacc convert pass"
+            kt["bwd_fused"]["note"] = ("fused key/value-stationary kernel: S^T, dP^T, dV, dK and dQ "
+                                       "(fp32 reductions into the workspace accumulator)")
+            kt["dq_convert"]["note"] = "dQ = scale * dQacc convert pass"
         else:
             kt["bwd_dq"]["tflops_algorithmic"] = dq_share / (per_kernel["bwd_dq"] * 1e-3) / 1e12
             kt["bwd_dq"]["tflops_executed"] = (dq_share + ff) / (per_kernel["bwd_dq"] * 1e-3) / 1e12
             kt["bwd_dq"]["note"] = ("span from the end of the preprocess to the end of dQ, which "
                                     "runs concurrently with dK/dV (side stream) and fills its "
-                                    "last wave")
+                                    "last wave; gbs counts its own bytes over that span")
         # dK/dV and dQ overlap: the backward is the step without the forward
         bwd_ms = ms - per_kernel["fwd"]
         out = {
@@ -644,6 +767,7 @@ def main():
             "bwd_tflops": 2.5 * ff / (bwd_ms * 1e-3) / 1e12,
             "kernels": kt,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            **({"latency_us_per_step": ms * 1e3} if ff < 1e9 else {}),
             "gpu_launches": (5 if mask_words else 4) * args.steps,
         }
         print(json.dumps(out), flush=True)
