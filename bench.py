@@ -145,16 +145,15 @@ def kernel_bytes(w: dict, fused: bool) -> dict:
     return out
 
 
-def workload_bound(w: dict, fwd_gflop: float) -> str:
-    """The roofline that bounds the workload (the hot-path table's bound
-    column): HBM with an fp32 bias (its 4-byte-per-pair Bias and dBias
-    dominate the bytes), the integer ALU with dropout (Philox4x32-10, ten
-    rounds per four elements, drawn in the forward and again in the
-    backward), HBM (latency) for a problem too small to fill the GPU, the
-    tensor cores otherwise."""
+def workload_bound(w: dict, fwd_gflop: float, draws: bool) -> str:
+    """The roofline that bounds the dominant kernel (the hot-path table's
+    bound column): HBM with an fp32 bias (its 4-byte-per-pair Bias and dBias
+    dominate the bytes), the integer ALU for a kernel that draws dropout
+    numbers (Philox4x32-10, ten rounds per four elements), HBM (latency) for a
+    problem too small to fill the GPU, the tensor cores otherwise."""
     if w["bias"]:
         return "hbm"
-    if w["p"] > 0:
+    if draws:
         return "alu"
     if fwd_gflop < 1.0:
         return "hbm"
@@ -389,6 +388,9 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=4096,
                     help="query positions of the one-head oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-record", action="store_true",
+                    help="with dropout, let the backward draw its own keep bits instead of reading "
+                         "the record the forward leaves")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic backward (query-stationary dQ kernel beside the "
                          "dK/dV kernel) instead of the default fused one")
@@ -435,6 +437,13 @@ def main():
     if w.get("bits"):
         mask_words = (w["B"] * w["H"] * w["S_q"] * w["S_kv"] + 31) // 32
         kw["dropout_mask"] = torch.empty(mask_words, dtype=torch.int32, device=dev)
+    # With dropout (batch mode, s_kv % 32 == 0) the forward records the keep
+    # bits it draws and the backward reads them: Philox runs once per step.
+    record_words = 0
+    if (w["p"] > 0 and not w.get("bits") and "lens" not in w and w["S_kv"] % 32 == 0
+            and not args.no_record):
+        record_words = (w["B"] * w["H"] * w["S_q"] * w["S_kv"] + 31) // 32
+        keep_record = torch.empty(record_words, dtype=torch.int32, device=dev)
     if w.get("alibi"):
         kw["alibi_slopes"] = torch.tensor([2.0 ** (-8.0 * (hh + 1) / w["H"]) for hh in range(w["H"])],
                                           dtype=torch.float32, device=dev)
@@ -470,13 +479,17 @@ def main():
                                                  deterministic=args.deterministic),
                          dtype=torch.uint8, device=dev)
 
+        rec_fwd = {"dropout_mask_out": keep_record} if record_words else {}
+        rec_bwd = {"dropout_mask": keep_record} if record_words else {}
+
         def fwd_call(D):
-            sdpa_fwd(D["q"], D["k"], D["v"], out=D["o"], lse=D["lse"], bias=D["bias"], **kw)
+            sdpa_fwd(D["q"], D["k"], D["v"], out=D["o"], lse=D["lse"], bias=D["bias"], **kw,
+                     **rec_fwd)
 
         def bwd_call(ph, D, stream=None):
             sdpa_bwd_phases(ph, D["q"], D["k"], D["v"], D["o"], D["do"], D["lse"], workspace=ws,
                             dq=D["dq"], dk=D["dk"], dv=D["dv"], bias=D["bias"], dbias=D["dbias"],
-                            stream=stream, deterministic=args.deterministic, **kw)
+                            stream=stream, deterministic=args.deterministic, **kw, **rec_bwd)
     # The default backward at d_qk <= 128 in batch mode is the fused one: the
     # preprocess, one key/value-stationary kernel that also accumulates dQ,
     # and the dQ convert pass, one after the other. Otherwise (d_qk = 192,
@@ -609,18 +622,20 @@ def main():
         kernel_flops = {"fwd": ff, "bwd_dkdv": 2.0 * ff, "bwd_dq": dq_share}
     kbytes = kernel_bytes(w, fused)
     # Philox4x32-10 blocks (four elements each) a kernel draws per launch:
-    # every visible element once in the forward and once in the main
-    # backward kernel(s); the deterministic dQ kernel draws them again
+    # every visible element once in the forward and, unless the forward
+    # recorded its keep bits for it, once in the main backward kernel(s)
+    # (the deterministic dQ kernel draws them again)
     drawn = 0.0
     if w["p"] > 0 and not w.get("bits"):
         drawn = (1 if w.get("lens") else w["B"]) * w["H"] * visible_pairs_per_head(w) / 4.0
-    kernel_blocks = {n: drawn for n in ("fwd", "bwd_fused", "bwd_dkdv", "bwd_dq") if n in per_kernel}
+    drawers = ("fwd",) if record_words else ("fwd", "bwd_fused", "bwd_dkdv", "bwd_dq")
+    kernel_blocks = {n: drawn for n in drawers if n in per_kernel}
 
     # the roofline of the workload's bound, for its dominant kernel (the
     # deterministic dQ span holds the concurrent dK/dV, so there the choice is
     # among the kernels timed alone)
-    bound = workload_bound(w, ff / 1e9)
     dom = max((n for n in per_kernel if fused or n != "bwd_dq"), key=per_kernel.get)
+    bound = workload_bound(w, ff / 1e9, bool(kernel_blocks.get(dom)))
     sec = per_kernel[dom] * 1e-3
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
@@ -760,6 +775,8 @@ def main():
                           if w.get("window") is not None else {}),
                        **({"alibi": "slopes 2^(-8(h+1)/H)"} if w.get("alibi") else {}),
                        "backward": "fused (dQ by fp32 reductions)" if fused else "deterministic",
+                       **({"dropout_bits": "drawn once by the forward, recorded, read by the "
+                                           "backward"} if record_words else {}),
                        "l2": "inputs larger than L2, no flush",
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "pct_of_peak": 100.0 * value / world / peak,

@@ -296,8 +296,19 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
  *   keep_bits  null, or the dropout keep bits of the whole problem drawn
  *            beforehand by sdpa_dropout_mask with the same b, h, s_q, s_kv (the
  *            max lengths when packed), p, seed and offset (DEVICE, 4-byte
- *            aligned): the kernels then read them instead of drawing Philox
- *            numbers, with identical results. Ignored when dropout_p is 0.
+ *            aligned), or recorded by a forward call (keep_bits_out): the
+ *            kernels then read them instead of drawing Philox numbers, with
+ *            identical results. Ignored when dropout_p is 0.
+ *   keep_bits_out  (forward calls) null, or DEVICE memory of
+ *            ceil(b*h*s_q*s_kv / 32) words (4-byte aligned) where the forward
+ *            records the keep bits it draws, in sdpa_dropout_mask's packing,
+ *            so that the backward can take them as keep_bits instead of
+ *            drawing them again (CK tile's kIsStoreRandval keeps its random
+ *            values for the same reason). Only the words of (query row, key
+ *            tile) pairs the forward visits are written; a backward with the
+ *            same mask reads no other. Requires s_kv % 32 == 0
+ *            (SDPA_ERR_UNSUPPORTED) and keep_bits null (SDPA_ERR_INVALID_ARG);
+ *            ignored when dropout_p is 0.
  * Causal is (-1, 0, 0), bottom-right causal (-1, 0, 1), a sliding window of
  * w keys back (w, 0, 0), no mask (-1, -1, 0). A query row that sees no key
  * gets O = 0, LSE = -inf and dQ = 0; a key no query sees gets dK = dV = 0.
@@ -307,7 +318,8 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
 sdpa_status_t sdpa_fwd_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                               int64_t window_right, int bottom_right, const float* alibi_slopes,
-                              int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed,
+                              int64_t alibi_stride, const uint32_t* keep_bits, uint32_t* keep_bits_out,
+                              float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, void* o, float* lse, void* stream);
 sdpa_status_t sdpa_bwd_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
@@ -332,8 +344,8 @@ sdpa_status_t sdpa_fwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t tot
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                                      int64_t window_right, int bottom_right,
                                      const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
-                                     float dropout_p, uint64_t seed, uint64_t offset,
-                                     sdpa_dtype_t dtype, const int32_t* seqstart_q,
+                                     uint32_t* keep_bits_out, float dropout_p, uint64_t seed,
+                                     uint64_t offset, sdpa_dtype_t dtype, const int32_t* seqstart_q,
                                      const int32_t* seqstart_k, const void* q, const void* k,
                                      const void* v, void* o, float* lse, void* stream);
 sdpa_status_t sdpa_bwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t total_q,

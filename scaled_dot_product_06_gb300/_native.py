@@ -57,7 +57,7 @@ SIGNATURES = {
     "sdpa_bwd_phases_varlen": (_int, [_int, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32,
                                       _int, _f32, _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                       _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _sz, _ptr]),
-    "sdpa_fwd_ex": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _i64, _i64, _int, _ptr, _i64, _ptr, _f32, _u64,
+    "sdpa_fwd_ex": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _i64, _i64, _int, _ptr, _i64, _ptr, _ptr, _f32, _u64,
                                _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
     "sdpa_bwd_ex": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _i64, _i64, _int, _ptr, _i64, _ptr, _f32, _u64,
                                _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _sz,
@@ -66,7 +66,7 @@ SIGNATURES = {
                                       _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                       _sz, _ptr]),
     "sdpa_fwd_varlen_ex": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _i64, _i64, _int, _ptr, _i64, _ptr,
-                                      _f32, _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
+                                      _ptr, _f32, _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr]),
     "sdpa_bwd_varlen_ex": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _f32, _i64, _i64, _int, _ptr, _i64, _ptr,
                                       _f32, _u64, _u64, _int, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr, _ptr,
                                       _ptr, _sz, _ptr]),

@@ -36,12 +36,15 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h, dropout_mask=None):
+def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h, dropout_mask=None,
+            force=False):
     """(left, right, bottom_right, slopes pointer, slope stride, keep-bits
     pointer) for the *_ex entry points, or None for the plain causal / unmasked
-    calls. alibi_slopes: fp32 CUDA [h] (every batch entry) or [n_batch, h];
-    dropout_mask: the int32 words of sdpa_dropout_mask for the same problem."""
-    if window is None and not bottom_right and alibi_slopes is None and dropout_mask is None:
+    calls (unless force). alibi_slopes: fp32 CUDA [h] (every batch entry) or
+    [n_batch, h]; dropout_mask: the int32 words of sdpa_dropout_mask (or of a
+    forward's dropout_mask_out) for the same problem."""
+    if (window is None and not bottom_right and alibi_slopes is None and dropout_mask is None
+            and not force):
         return None
     if dropout_mask is not None and (not dropout_mask.is_cuda or dropout_mask.dtype != torch.int32
                                      or not dropout_mask.is_contiguous()):
@@ -62,9 +65,19 @@ def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h, dropout_m
     return int(left), int(right), int(bool(bottom_right)), _ptr(alibi_slopes), stride, _ptr(dropout_mask)
 
 
+def _mask_out(t, words):
+    """A forward's keep-bit record buffer: contiguous int32 CUDA words."""
+    if t is None:
+        return None
+    if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < words:
+        raise ValueError(f"dropout_mask_out must be a contiguous int32 CUDA tensor of at least "
+                         f"{words} words")
+    return _ptr(t)
+
+
 def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0,
              bias=None, out=None, lse=None, stream=None, window=None, bottom_right=False,
-             alibi_slopes=None, dropout_mask=None):
+             alibi_slopes=None, dropout_mask=None, dropout_mask_out=None):
     """Forward pass. Returns (o [b,h,s_q,d_v], lse fp32 [b,h,s_q]).
 
     k and v may have fewer heads than q (grouped-query attention): h_kv =
@@ -73,7 +86,10 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
     i + off - left <= j <= i + off + right (a negative size unbounded), with
     off = s_kv - s_q when bottom_right, else 0; is_causal is window (-1, 0).
     alibi_slopes (fp32 CUDA [h] or [b, h]) adds -slope * |j - i - off_a| to the
-    scaled scores, off_a = 0 under a top-left window, else s_kv - s_q."""
+    scaled scores, off_a = 0 under a top-left window, else s_kv - s_q.
+    dropout_mask_out (int32 CUDA, ceil(b*h*s_q*s_kv/32) words): the forward
+    records the dropout keep bits it draws there, for sdpa_bwd's
+    dropout_mask (needs s_kv % 32 == 0)."""
     b, h, s_q, d_qk = q.shape
     h_kv, s_kv, d_v = k.shape[1], k.shape[2], v.shape[3]
     dt = q.dtype
@@ -91,7 +107,8 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
         lse = torch.empty((b, h, s_q), dtype=torch.float32, device=q.device)
     _check_io("out", out, (b, h, s_q, d_v), dt)
     _check_io("lse", lse, (b, h, s_q), torch.float32)
-    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask,
+                force=dropout_mask_out is not None)
     if w is None:
         st = _native.lib().sdpa_fwd_gqa(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
                                         float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
@@ -99,7 +116,8 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
                                         ctypes.c_void_p(_stream_ptr(stream)))
         _native.check(st, "sdpa_fwd_gqa")
     else:
-        st = _native.lib().sdpa_fwd_ex(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, *w,
+        rec = _mask_out(dropout_mask_out, (b * h * s_q * s_kv + 31) // 32)
+        st = _native.lib().sdpa_fwd_ex(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, *w, rec,
                                            float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
                                            _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out),
                                            _ptr(lse), ctypes.c_void_p(_stream_ptr(stream)))
@@ -192,7 +210,7 @@ def _check_seqstart(name: str, t: torch.Tensor) -> int:
 def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *, scale=None,
                     is_causal=False, dropout_p=0.0, seed=0, offset=0, out=None, lse=None,
                     stream=None, window=None, bottom_right=False, alibi_slopes=None,
-             dropout_mask=None):
+                    dropout_mask=None, dropout_mask_out=None):
     """Forward pass over packed variable-length sequences. q [h, total_q, d_qk],
     k [h_kv, total_k, d_qk], v [h_kv, total_k, d_v]; seqstart_q / seqstart_k
     int32 CUDA tensors of b + 1 row offsets (sequence i owns query rows
@@ -216,7 +234,8 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
         lse = torch.empty((h, total_q), dtype=torch.float32, device=q.device)
     _check_io("out", out, (h, total_q, d_v), dt)
     _check_io("lse", lse, (h, total_q), torch.float32)
-    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)
+    w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask,
+                force=dropout_mask_out is not None)
     if w is None:
         st = _native.lib().sdpa_fwd_varlen(
             b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale,
@@ -225,9 +244,10 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
             ctypes.c_void_p(_stream_ptr(stream)))
         _native.check(st, "sdpa_fwd_varlen")
     else:
+        rec = _mask_out(dropout_mask_out, (b * h * int(max_seqlen_q) * int(max_seqlen_k) + 31) // 32)
         st = _native.lib().sdpa_fwd_varlen_ex(
             b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale, *w,
-            float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt], _ptr(seqstart_q),
+            rec, float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt], _ptr(seqstart_q),
             _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
             ctypes.c_void_p(_stream_ptr(stream)))
         _native.check(st, "sdpa_fwd_varlen_ex")

@@ -183,6 +183,7 @@ struct Mask {
   const float* alibi = nullptr;  // ALiBi slopes (device), slope of (b, h) at b * alibi_stride + h
   int64_t alibi_stride = 0;
   const uint32_t* keep_bits = nullptr;  // dropout keep bits drawn beforehand (device)
+  uint32_t* keep_out = nullptr;         // forward: record of the keep bits it draws (device)
 };
 Mask causal_mask(int is_causal) { return Mask{-1, is_causal ? 0 : -1, 0}; }
 
@@ -207,7 +208,9 @@ void set_window(const Mask& mk, int64_t s_q, int64_t s_kv, P* p) {
 // ALiBi slopes: 4-byte aligned; the stride between batch rows 0 (one row for
 // all) or at least h, and small enough for an int index.
 sdpa_status_t check_alibi(const Mask& mk, int64_t b, int64_t h) {
-  if ((reinterpret_cast<uintptr_t>(mk.keep_bits) & 3u) != 0) return SDPA_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(mk.keep_bits) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(mk.keep_out) & 3u) != 0)
+    return SDPA_ERR_MISALIGNED;
   if (mk.alibi == nullptr) return SDPA_OK;
   if ((reinterpret_cast<uintptr_t>(mk.alibi) & 3u) != 0) return SDPA_ERR_MISALIGNED;
   if (mk.alibi_stride < 0 || (mk.alibi_stride > 0 && mk.alibi_stride < h) ||
@@ -349,6 +352,11 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
   if (!kv_heads_ok(h, h_kv)) return fail(SDPA_ERR_INVALID_ARG, "h_kv must divide h");
   if (sdpa_status_t s = check_packing(pk, b, bias, &empty)) return s;
   if (sdpa_status_t s = check_alibi(mask, b, h)) return s;
+  if (dropout_p > 0.0f && mask.keep_out != nullptr) {  // a record of the keep bits drawn
+    if (mask.keep_bits != nullptr)
+      return fail(SDPA_ERR_INVALID_ARG, "keep_bits and keep_bits_out together");
+    if (s_kv % 32 != 0) return fail(SDPA_ERR_UNSUPPORTED, "keep_bits_out needs s_kv % 32 == 0");
+  }
   if (empty) return SDPA_OK;
   if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -375,6 +383,7 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
     p.keep_bits = mask.keep_bits;
     p.keep_words = (b * h * s_q * s_kv + 31) / 32;
   }
+  if (dropout_p > 0.0f) p.keep_out = mask.keep_out;  // record the bits drawn here (checked above)
   p.bias = bias;
   p.dropout = dropout_p > 0.0f ? 1 : 0;
   p.drop_threshold = drop_threshold(dropout_p);
@@ -688,11 +697,13 @@ sdpa_status_t sdpa_bwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_
 sdpa_status_t sdpa_fwd_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                               int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                               int64_t window_right, int bottom_right, const float* alibi_slopes,
-                              int64_t alibi_stride, const uint32_t* keep_bits, float dropout_p, uint64_t seed,
+                              int64_t alibi_stride, const uint32_t* keep_bits, uint32_t* keep_bits_out,
+                              float dropout_p, uint64_t seed,
                               uint64_t offset, sdpa_dtype_t dtype, const void* q, const void* k,
                               const void* v, const float* bias, void* o, float* lse, void* stream) {
   return fwd_impl(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits},
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits,
+                       keep_bits_out},
                   dropout_p, seed, offset, dtype, q, k, v, bias, o, lse, stream, Packing{});
 }
 
@@ -730,7 +741,7 @@ sdpa_status_t sdpa_fwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t tot
                                      int64_t d_qk, int64_t d_v, float scale, int64_t window_left,
                                      int64_t window_right, int bottom_right,
                                      const float* alibi_slopes, int64_t alibi_stride, const uint32_t* keep_bits,
-                                     float dropout_p, uint64_t seed, uint64_t offset,
+                                     uint32_t* keep_bits_out, float dropout_p, uint64_t seed, uint64_t offset,
                                      sdpa_dtype_t dtype, const int32_t* seqstart_q,
                                      const int32_t* seqstart_k, const void* q, const void* k,
                                      const void* v, void* o, float* lse, void* stream) {
@@ -740,7 +751,8 @@ sdpa_status_t sdpa_fwd_varlen_ex(int64_t b, int64_t h, int64_t h_kv, int64_t tot
     return fail(SDPA_ERR_INVALID_ARG, "seqstart_q and seqstart_k are required");
   }
   return fwd_impl(b, h, h_kv, max_seqlen_q, max_seqlen_k, d_qk, d_v, scale,
-                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits},
+                  Mask{window_left, window_right, bottom_right, alibi_slopes, alibi_stride, keep_bits,
+                       keep_bits_out},
                   dropout_p, seed, offset, dtype, q, k, v, nullptr, o, lse, stream, pk);
 }
 

@@ -114,6 +114,52 @@ __device__ __forceinline__ void keep_bits_transposed(uint64_t lin_quad, int S_kv
   }
 }
 
+// Bit r of x to bit 4 r (r < 8).
+__device__ __forceinline__ uint32_t spread4(uint32_t x) {
+  x = (x | (x << 12)) & 0x000F000Fu;
+  x = (x | (x << 6)) & 0x03030303u;
+  return (x | (x << 3)) & 0x11111111u;
+}
+
+// Keep flags of one key for the 32 query rows [q0, q0 + 32) as one word, bit
+// c = flag of query row q0 + c. The warp's lanes hold 32 consecutive keys
+// key0 + lane. With keep bits drawn beforehand (sdpa_dropout_mask's packing,
+// row-major: bit L % 32 of word L / 32), lane l reads the 32 flags of query
+// row q0 + l for keys key0 .. key0 + 31 (one word, or two joined) and 32
+// ballots transpose the warp's 32 words, so each lane gets its key's column;
+// otherwise the flags are drawn (keep_bits_transposed) and their bits, which
+// come grouped by query row modulo 4, are put in order.
+// lin_q0_key0 is the linear element index of (q0, key0).
+// The keep bits lane `lane` contributes to keep_flags_of_key: query row
+// q0 + lane, keys key0 .. key0 + 31 (kernels may load it a tile early).
+__device__ __forceinline__ uint32_t keep_row_word(const uint32_t* keep_bits, int64_t keep_words,
+                                                  uint64_t lin_q0_key0, int S_kv, int lane) {
+  return keep_word(keep_bits, keep_words, lin_q0_key0 + static_cast<uint64_t>(lane) * S_kv);
+}
+// The 32 words of a warp (lane l: keep_row_word of query row q0 + l)
+// transposed by 32 ballots: bit c of the result is lane c's bit `lane`.
+__device__ __forceinline__ uint32_t transpose_keep_words(uint32_t w, int lane) {
+  uint32_t mine = 0;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const uint32_t t = __ballot_sync(0xffffffffu, (w >> k) & 1u);
+    if (lane == k) mine = t;
+  }
+  return mine;
+}
+
+__device__ __forceinline__ uint32_t keep_flags_of_key(const uint32_t* keep_bits, int64_t keep_words,
+                                                      uint64_t lin_q0_key0, int S_kv, int lane,
+                                                      uint32_t thr, uint32_t seed_lo, uint32_t seed_hi,
+                                                      uint32_t off_lo, uint32_t off_hi) {
+  if (keep_bits != nullptr)
+    return transpose_keep_words(keep_row_word(keep_bits, keep_words, lin_q0_key0, S_kv, lane), lane);
+  uint32_t m[4];
+  keep_bits_transposed(lin_q0_key0 + (lane & ~3), S_kv, lane, thr, seed_lo, seed_hi, off_lo, off_hi, m);
+  // m[src] bit r = flag of query row q0 + 4 r + src
+  return spread4(m[0]) | (spread4(m[1]) << 1) | (spread4(m[2]) << 2) | (spread4(m[3]) << 3);
+}
+
 // Epilogue of a split key tile (BwdParams::kv_split > 1), run by all NCT
 // compute threads: this CTA's fp32 dK / dV sums go to its partial rows
 // [dK | dV]; after a fence, one atomic per key tile counts the CTA in, and the
@@ -460,21 +506,15 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         const int qc0 = q0 + CW * hf;  // first query row of this thread's columns
         const float* stat = rowbuf + (i & 1) * (2 * BM) + stat_off;
         const uint32_t nl2_s = smem_u32(stat), dd_s = smem_u32(stat + 64);
-        uint32_t km[CW / 32][4];
-#pragma unroll
-        for (int g = 0; g < CW / 32; ++g) {
-          km[g][0] = km[g][1] = km[g][2] = km[g][3] = 0xFFu;
-          // (keep bits drawn beforehand are not read here: this kernel needs
-          // them down a column, one word per query row, which measured slower
-          // than drawing them; both give the same bits)
-          if constexpr (DROP)
-            keep_bits_transposed(
-                (static_cast<uint64_t>(bh) * p.S_q + qc0 + 32 * g) * p.S_kv + k0 + (row & ~3),
-                p.S_kv, lane, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi,
-                km[g]);
-        }
+        // keep flags of this key for the thread's query columns (bit c: column c)
+        uint32_t kw = 0xFFFFFFFFu;
+        if constexpr (DROP)
+          kw = keep_flags_of_key(p.keep_bits, p.keep_words,
+                                 (static_cast<uint64_t>(bh) * p.S_q + qc0) * p.S_kv + k0 + (row & ~31),
+                                 p.S_kv, lane, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo,
+                                 p.offset_hi);
         auto zf = [&](int c) -> float {  // dropout factor of local column c
-          if constexpr (DROP) return ((km[c >> 5][c & 3] >> ((c & 31) >> 2)) & 1u) ? zk : 0.f;
+          if constexpr (DROP) return ((kw >> c) & 1u) ? zk : 0.f;
           return 1.0f;
         };
         // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)

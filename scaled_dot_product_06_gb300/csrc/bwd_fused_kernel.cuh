@@ -478,14 +478,16 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
         const int qc0 = q0 + CW * hf;
         const float* stat = rowbuf + (i & 1) * (2 * BM) + stat_off;
         const uint32_t nl2_s = smem_u32(stat), dd_s = smem_u32(stat + 64);
-        uint32_t km[4];
-        km[0] = km[1] = km[2] = km[3] = 0xFFu;
+        // keep flags of this key for the thread's query columns (bit c: column
+        // c), read from the keep bits drawn beforehand or drawn here
+        uint32_t kw = 0xFFFFFFFFu;
         if constexpr (DROP)
-          keep_bits_transposed((static_cast<uint64_t>(bh) * p.S_q + qc0) * p.S_kv + k0 + (row & ~3),
-                               p.S_kv, lane, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo,
-                               p.offset_hi, km);
+          kw = keep_flags_of_key(p.keep_bits, p.keep_words,
+                                 (static_cast<uint64_t>(bh) * p.S_q + qc0) * p.S_kv + k0 + (row & ~31),
+                                 p.S_kv, lane, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo,
+                                 p.offset_hi);
         auto zf = [&](int c) -> float {
-          if constexpr (DROP) return ((km[c & 3] >> (c >> 2)) & 1u) ? zk : 0.f;
+          if constexpr (DROP) return ((kw >> c) & 1u) ? zk : 0.f;
           return 1.0f;
         };
         float pr[CW];

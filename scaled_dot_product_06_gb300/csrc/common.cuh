@@ -42,6 +42,11 @@ struct FwdParams {
   // null to draw them here; keep_words is the array's length in words.
   const uint32_t* keep_bits;
   int64_t keep_words;
+  // Record of the keep bits drawn here (same packing; null: none), for the
+  // backward to read instead of drawing them again. Written only while
+  // drawing (keep_bits null), whole words of a row (the host requires
+  // S_kv % 32 == 0).
+  uint32_t* keep_out;
   // ALiBi (null: none): score of (i, j) gets -alibi[b * alibi_stride + h] *
   // |j - i - off|, off = S_kv - S_q when alibi_br, else 0 (a top-left mask).
   // Handled by the kernels compiled for general windows.

@@ -33,12 +33,18 @@
 // Registers: launched at 168 a thread (384 threads); the producer/MMA
 // warpgroup drops to 72 and the softmax warpgroups rise to 216, enough for a
 // row's 128 scores without spilling: 2 x 128 x 216 + 128 x 72 = 384 x 168.
-// GENERAL (a bias or dropout present) and WIN (a local window or the
-// bottom-right alignment) are template parameters so the plain kernel is
-// compiled without their registers. RAW (no bias, dropout or ALiBi, a nonzero
+// GENERAL (an additive bias present), DROP (dropout) and WIN (a local window
+// or the bottom-right alignment) are template parameters so the plain kernel
+// is compiled without their registers. RAW (no bias or ALiBi, a nonzero
 // scale) keeps the scores unscaled until the exponential, which takes the
-// scale and the row max in one FMA per score.
+// scale and the row max in one FMA per score; dropout leaves the softmax
+// statistics alone (it zeroes entries of P after the exponentials), so it
+// runs in the raw-score kernels too. Under dropout the kernel can also record
+// the keep bits it draws (FwdParams::keep_out, sdpa_dropout_mask's packing),
+// for the backward to read instead of drawing them again.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sdpa {
@@ -73,7 +79,7 @@ struct FwdCfg {
 enum : int { FB_Q = 0, FB_S, FB_P = FB_S + 2, FB_O = FB_P + 2, FB_DRAIN = FB_O + 2, FB_KF,
              FB_KE = FB_KF + 3, FB_VF = FB_KE + 3, FB_VE = FB_VF + 3, FB_COUNT = FB_VE + 3 };
 
-template <int DQK, int DV, bool BF16, bool GENERAL, bool WIN, bool RAW>
+template <int DQK, int DV, bool BF16, bool GENERAL, bool WIN, bool RAW, bool DROP>
 __global__ void __launch_bounds__(384, 1)
     sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -349,6 +355,39 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 128; ++i) x[i] = (k0 + i < p.S_kv) ? __ldg(bias_row + k0 + i) : 0.f;
         }
       }
+      // dropout keep flags of keys k0 .. k0 + 127 (word w: keys k0 + 32 w ..,
+      // bit i: key k0 + 32 w + i, the packing of sdpa_dropout_mask), read or
+      // drawn before the wait for the scores so the draws overlap it
+      uint32_t kw[4] = {~0u, ~0u, ~0u, ~0u};
+      if constexpr (DROP) {
+        if (p.keep_bits != nullptr) {  // drawn beforehand
+#pragma unroll
+          for (int w = 0; w < 4; ++w) kw[w] = keep_word(p.keep_bits, p.keep_words, lin_row + k0 + 32 * w);
+        } else {
+          const uint64_t g0 = (lin_row + k0) >> 2;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const uint4 d = dropout_draws(g0 + 8 * w + g, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi);
+              acc |= (static_cast<uint32_t>(d.x >= p.drop_threshold) << (4 * g)) |
+                     (static_cast<uint32_t>(d.y >= p.drop_threshold) << (4 * g + 1)) |
+                     (static_cast<uint32_t>(d.z >= p.drop_threshold) << (4 * g + 2)) |
+                     (static_cast<uint32_t>(d.w >= p.drop_threshold) << (4 * g + 3));
+            }
+            kw[w] = acc;
+          }
+          if (p.keep_out != nullptr && row_ok) {
+            // record them for the backward: whole words of this row only
+            // (the host requires S_kv % 32 == 0 for a record)
+            uint32_t* dst = p.keep_out + ((lin_row + k0) >> 5);
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              if (k0 + 32 * w < p.S_kv) dst[w] = kw[w];
+          }
+        }
+      }
       if (!(ok = mbar_wait(bar(FB_S + t), c & 1, ec, kSiteFwdSoftmax))) break;
       tc_fence_after();
 #pragma unroll
@@ -439,23 +478,12 @@ __global__ void __launch_bounds__(384, 1)
         const float2 u = f2split(sa), w = f2split(sb);
         l += (u.x + u.y) + (w.x + w.y);
       }
-      if (GENERAL && p.dropout && p.keep_bits != nullptr) {
+      if constexpr (DROP) {  // dropout: zero the dropped entries of P
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {  // keep bits drawn beforehand
-          const uint32_t kw = keep_word(p.keep_bits, p.keep_words, lin_row + k0 + 32 * w);
+        for (int w = 0; w < 4; ++w) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (!((kw >> i) & 1u)) x[32 * w + i] = 0.f;
-        }
-      } else if (GENERAL && p.dropout) {
-        const uint64_t g0 = (lin_row + k0) >> 2;
-#pragma unroll
-        for (int g = 0; g < 32; ++g) {
-          const uint4 w = dropout_draws(g0 + g, p.seed_lo, p.seed_hi, p.offset_lo, p.offset_hi);
-          if (w.x < p.drop_threshold) x[4 * g + 0] = 0.f;
-          if (w.y < p.drop_threshold) x[4 * g + 1] = 0.f;
-          if (w.z < p.drop_threshold) x[4 * g + 2] = 0.f;
-          if (w.w < p.drop_threshold) x[4 * g + 3] = 0.f;
+            if (!((kw[w] >> i) & 1u)) x[32 * w + i] = 0.f;
         }
       }
 #pragma unroll
@@ -472,7 +500,7 @@ __global__ void __launch_bounds__(384, 1)
     // ---- epilogue: O / l (times 1/(1-p) under dropout), LSE = m ln2 + ln l
     if (n_kv > 0 && ok && mbar_wait(bar(FB_O + t), 0, ec, kSiteFwdSoftmax)) {
       tc_fence_after();
-      const float inv = (l > 0.f) ? ((GENERAL && p.dropout) ? p.keep_scale : 1.0f) / l : 0.f;
+      const float inv = (l > 0.f) ? (DROP ? p.keep_scale : 1.0f) / l : 0.f;
       const size_t ri = static_cast<size_t>(zq) * p.rows_q + sl.row_q + (row_ok ? row : 0);
       uint8_t* orow = static_cast<uint8_t*>(p.o) + ri * DV * 2;
 #pragma unroll
@@ -516,16 +544,20 @@ template <int DQK, int DV, bool BF16>
 cudaError_t launch_fwd_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                          const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
-  const bool general = p.bias != nullptr || p.dropout != 0;
-  // raw scores (RAW) unless ALiBi or a zero scale; those take the windowed
-  // kernel, which also runs the plain masks
+  const bool general = p.bias != nullptr;
+  // raw scores (RAW) unless a bias, ALiBi or a zero scale; ALiBi and a zero
+  // scale take the windowed kernel, which also runs the plain masks
   const bool raw = !general && p.alibi == nullptr && p.scale_log2 != 0.f;
   const bool win = p.win_general || p.alibi != nullptr || (!general && !raw);
-  auto kern = general ? (win ? sdpa_fwd_kernel<DQK, DV, BF16, true, true, false>
-                             : sdpa_fwd_kernel<DQK, DV, BF16, true, false, false>)
-                      : !raw ? sdpa_fwd_kernel<DQK, DV, BF16, false, true, false>
-                             : (win ? sdpa_fwd_kernel<DQK, DV, BF16, false, true, true>
-                                    : sdpa_fwd_kernel<DQK, DV, BF16, false, false, true>);
+  auto pick = [&](auto drop) {
+    constexpr bool D = decltype(drop)::value;
+    return general ? (win ? sdpa_fwd_kernel<DQK, DV, BF16, true, true, false, D>
+                          : sdpa_fwd_kernel<DQK, DV, BF16, true, false, false, D>)
+                   : !raw ? sdpa_fwd_kernel<DQK, DV, BF16, false, true, false, D>
+                          : (win ? sdpa_fwd_kernel<DQK, DV, BF16, false, true, true, D>
+                                 : sdpa_fwd_kernel<DQK, DV, BF16, false, false, true, D>);
+  };
+  auto kern = p.dropout ? pick(std::true_type{}) : pick(std::false_type{});
   // The warpgroups' setmaxnreg shares add up to exactly 384 x REG_LAUNCH; had
   // the compiler given the kernel another launch register count, the softmax
   // warpgroups' increase could never be granted, so refuse to launch then.

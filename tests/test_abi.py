@@ -221,16 +221,31 @@ def test_alibi_arguments_validated_before_any_device_work(lib):
     P = ctypes.c_void_p(16)
 
     def fwd(slopes, stride, b=2, h=4):
-        return lib.sdpa_fwd_ex(b, h, h, 64, 64, 64, 64, 0.125, -1, 0, 0, slopes, stride, None, 0.0, 0,
-                               0, 0, P, P, P, None, P, P, None)
+        return lib.sdpa_fwd_ex(b, h, h, 64, 64, 64, 64, 0.125, -1, 0, 0, slopes, stride, None, None,
+                               0.0, 0, 0, 0, P, P, P, None, P, P, None)
     assert fwd(ctypes.c_void_p(18), 0) == _native.SDPA_ERR_MISALIGNED
     assert fwd(ctypes.c_void_p(64), -1) == _native.SDPA_ERR_INVALID_ARG
     assert fwd(ctypes.c_void_p(64), 3) == _native.SDPA_ERR_INVALID_ARG   # 0 < stride < h
     assert fwd(ctypes.c_void_p(64), 1 << 40) == _native.SDPA_ERR_INVALID_ARG
-    # dropout keep bits drawn beforehand must be 4-byte aligned
-    st = lib.sdpa_fwd_ex(2, 4, 4, 64, 64, 64, 64, 0.125, -1, 0, 0, None, 0, ctypes.c_void_p(66), 0.1, 0,
-                         0, 0, P, P, P, None, P, P, None)
+    # dropout keep bits drawn beforehand, and a forward's record of them, must
+    # be 4-byte aligned
+    st = lib.sdpa_fwd_ex(2, 4, 4, 64, 64, 64, 64, 0.125, -1, 0, 0, None, 0, ctypes.c_void_p(66), None,
+                         0.1, 0, 0, 0, P, P, P, None, P, P, None)
     assert st == _native.SDPA_ERR_MISALIGNED
+    st = lib.sdpa_fwd_ex(2, 4, 4, 64, 64, 64, 64, 0.125, -1, 0, 0, None, 0, None, ctypes.c_void_p(66),
+                         0.1, 0, 0, 0, P, P, P, None, P, P, None)
+    assert st == _native.SDPA_ERR_MISALIGNED
+
+
+def test_keep_bit_record_arguments_validated_before_any_device_work(lib):
+    P = ctypes.c_void_p(1 << 20)
+
+    def fwd(keep_in, keep_out, skv=64, p=0.1):
+        return lib.sdpa_fwd_ex(1, 2, 2, 64, skv, 64, 64, 0.125, -1, 0, 0, None, 0, keep_in, keep_out,
+                               p, 0, 0, 0, P, P, P, None, P, P, None)
+    # a record needs whole 32-key words per row, and cannot come with input bits
+    assert fwd(None, P, skv=68) == _native.SDPA_ERR_UNSUPPORTED
+    assert fwd(P, P) == _native.SDPA_ERR_INVALID_ARG
 
 
 def test_grouped_workspace_size(lib):

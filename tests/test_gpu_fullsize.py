@@ -72,12 +72,37 @@ def test_b2h16_s4096_d192x128_causal_bias():
     key_sum_invariants(case, outs, x)
 
 
+def same_bits_with_keep_bits(case, x, outs):
+    """The kernels' own Philox draws at this size give exactly the bits of
+    sdpa_dropout_mask: the forward and backward run again with the mask passed
+    in (the kernels then read it) and must agree bit for bit (O, LSE, dK, dV;
+    dQ in the deterministic backward, whose sums have a fixed order)."""
+    from scaled_dot_product_06_gb300 import sdpa_bwd, sdpa_fwd
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    kw = dict(scale=case.sc, is_causal=case.causal, dropout_p=case.p, seed=case.seed,
+              offset=case.offset)
+    mask = sdpa_dropout_mask(case.B, case.H, case.S_q, case.S_kv, case.p, case.seed, case.offset)
+    o, lse = sdpa_fwd(q, k, v, dropout_mask=mask, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o, outs[0]) and torch.equal(lse, outs[1])
+    _, dk, dv, _ = sdpa_bwd(q, k, v, o, do, lse, dropout_mask=mask, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, outs[3]) and torch.equal(dv, outs[4])
+    del dk, dv
+    det_a = sdpa_bwd(q, k, v, o, do, lse, deterministic=True, **kw)
+    det_b = sdpa_bwd(q, k, v, o, do, lse, dropout_mask=mask, deterministic=True, **kw)
+    torch.cuda.synchronize()
+    for a, b in zip(det_a[:3], det_b[:3]):
+        assert torch.equal(a, b)
+
+
 def test_b8h16_s1024x2048_d64_fp16_dropout():
     case = Case(8, 16, 1024, 2048, 64, 64, dtype="fp16", p=0.1)
     x = make_inputs(case.shape, case.dtype)
     outs = run_gpu(case, x)
     for b, h in ((0, 0), (7, 15), (3, 9)):
         slice_check(case, x, outs, b, h)
+    same_bits_with_keep_bits(case, x, outs)
     # keep bits of the sampled slices, bit-exact
     bits = sdpa_dropout_mask(case.B, case.H, case.S_q, case.S_kv, case.p, case.seed,
                              case.offset).cpu().numpy().view(np.uint32)
@@ -172,6 +197,7 @@ def test_dropout_element_index_past_2_pow_32():
     dq_r, _, _, _ = oracle.backward_head(pr, 0, h, x["q"], x["k"], x["v"], x["do"], rows=rows,
                                          cols=np.array([], dtype=np.int64))
     assert_close("dq rows", dq[0, h][r_t], dq_r)
+    same_bits_with_keep_bits(case, x, (o, lse, dq, dk, dv))
     total = 8 * 32768 * 32768
     words = sdpa_dropout_mask(1, 8, 32768, 32768, case.p, case.seed, case.offset)
     last = words[-64:].cpu().numpy().view(np.uint32)

@@ -226,3 +226,52 @@ def test_dropout_bits_drawn_beforehand_give_the_same_bits(case):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     for a, b in zip(g1, g2):
         assert (a is None and b is None) or torch.equal(a, b)
+
+
+@pytest.mark.parametrize("case", [
+    Case(2, 2, 256, 384, 64, 64, dtype="fp16", p=0.1),
+    Case(1, 4, 300, 320, 128, 128, causal=True, p=0.2, H_kv=2),
+    Case(1, 2, 200, 256, 192, 128, causal=True, bias=True, p=0.15),
+], ids=["d64-fp16", "d128-causal-gqa-ragged", "d192-bias"])
+def test_forward_keep_bit_record(case):
+    """A forward asked to record its dropout keep bits writes exactly
+    sdpa_dropout_mask's words (every query row sees every key tile here, or
+    the causal diagonal and below, which the comparison covers), its O and LSE
+    are those of the forward without a record, and a backward given the
+    record reproduces the backward that draws its own bits: every gradient of
+    the deterministic backward bit for bit, dK and dV of the default one bit
+    for bit and its dQ up to the order of its fp32 reductions."""
+    from parity_util import assert_close
+    from scaled_dot_product_06_gb300 import sdpa_bwd, sdpa_dropout_mask, sdpa_fwd
+    from scaled_dot_product_06_gb300.inputs import make_inputs
+    x = make_inputs(case.shape, case.dtype, with_bias=case.bias, device="cuda")
+    q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
+    kw = dict(scale=case.sc, is_causal=case.causal, dropout_p=case.p, seed=case.seed,
+              offset=case.offset, bias=bias)
+    words = (case.B * case.H * case.S_q * case.S_kv + 31) // 32
+    rec = torch.zeros(words, dtype=torch.int32, device="cuda")
+    o1, l1 = sdpa_fwd(q, k, v, **kw)
+    o2, l2 = sdpa_fwd(q, k, v, dropout_mask_out=rec, **kw)
+    ref = sdpa_dropout_mask(case.B, case.H, case.S_q, case.S_kv, case.p, case.seed, case.offset)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    got_w = rec.cpu().numpy().view(np.uint32).reshape(case.B * case.H, case.S_q, case.S_kv // 32)
+    ref_w = ref.cpu().numpy().view(np.uint32).reshape(case.B * case.H, case.S_q, case.S_kv // 32)
+    if case.causal:  # words holding a key at or below the diagonal: the forward visits their tile
+        rows = np.arange(case.S_q)[:, None]
+        first_key = 32 * np.arange(case.S_kv // 32)[None, :]
+        keep = np.broadcast_to((first_key // 128) * 128 <= rows, got_w.shape)
+        np.testing.assert_array_equal(got_w[keep], ref_w[keep])
+    else:
+        np.testing.assert_array_equal(got_w, ref_w)
+    for det in (True, False):
+        g1 = sdpa_bwd(q, k, v, o1, do, l1, deterministic=det, **kw)
+        g2 = sdpa_bwd(q, k, v, o1, do, l1, dropout_mask=rec, deterministic=det, **kw)
+        torch.cuda.synchronize()
+        for name, a, b in zip(("dq", "dk", "dv", "dbias"), g1, g2):
+            if a is None:
+                continue
+            if name == "dq" and not det and case.D_qk <= 128:
+                assert_close("dq with the record", b, a.double().cpu().numpy(), rel=1e-2)
+            else:
+                assert torch.equal(a, b), (name, det)
