@@ -125,8 +125,8 @@ __device__ __forceinline__ uint32_t spread4(uint32_t x) {
 // c = flag of query row q0 + c. The warp's lanes hold 32 consecutive keys
 // key0 + lane. With keep bits drawn beforehand (sdpa_dropout_mask's packing,
 // row-major: bit L % 32 of word L / 32), lane l reads the 32 flags of query
-// row q0 + l for keys key0 .. key0 + 31 (one word, or two joined) and 32
-// ballots transpose the warp's 32 words, so each lane gets its key's column;
+// row q0 + l for keys key0 .. key0 + 31 (one word, or two joined) and a warp
+// bit-matrix transpose hands each lane its key's column;
 // otherwise the flags are drawn (keep_bits_transposed) and their bits, which
 // come grouped by query row modulo 4, are put in order.
 // lin_q0_key0 is the linear element index of (q0, key0).
@@ -136,16 +136,20 @@ __device__ __forceinline__ uint32_t keep_row_word(const uint32_t* keep_bits, int
                                                   uint64_t lin_q0_key0, int S_kv, int lane) {
   return keep_word(keep_bits, keep_words, lin_q0_key0 + static_cast<uint64_t>(lane) * S_kv);
 }
-// The 32 words of a warp (lane l: keep_row_word of query row q0 + l)
-// transposed by 32 ballots: bit c of the result is lane c's bit `lane`.
+// The 32 words of a warp (lane l: keep_row_word of query row q0 + l) as a
+// 32 x 32 bit matrix (row = lane, column = bit), transposed: bit c of the
+// result is lane c's bit `lane`. Five rounds of the recursive block
+// transpose: in round s the lanes l and l ^ s swap the off-diagonal s x s
+// blocks of their 2s x 2s block (the lower lane's low column half moves up
+// into the upper lane, the upper lane's high half down into the lower lane).
 __device__ __forceinline__ uint32_t transpose_keep_words(uint32_t w, int lane) {
-  uint32_t mine = 0;
+  uint32_t m = 0x0000FFFFu;  // columns in the low half of each 2s-column group
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const uint32_t t = __ballot_sync(0xffffffffu, (w >> k) & 1u);
-    if (lane == k) mine = t;
+  for (int sh = 16; sh > 0; sh >>= 1, m ^= (m << sh)) {
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, w, sh);
+    w = (lane & sh) ? (((o >> sh) & m) | (w & ~m)) : ((w & m) | ((o & m) << sh));
   }
-  return mine;
+  return w;
 }
 
 __device__ __forceinline__ uint32_t keep_flags_of_key(const uint32_t* keep_bits, int64_t keep_words,
