@@ -33,6 +33,9 @@
 // Registers: launched at 168 a thread (384 threads); the producer/MMA
 // warpgroup drops to 72 and the softmax warpgroups rise to 216, enough for a
 // row's 128 scores without spilling: 2 x 128 x 216 + 128 x 72 = 384 x 168.
+// With a bias (its 128 values per row loaded ahead of the scores) or dropout
+// (the keep words) the softmax takes 224 and the issuing warpgroup 56, which
+// it fits in when its descriptors are built at each issue (opaque_u64).
 // GENERAL (an additive bias present), DROP (dropout) and WIN (a local window
 // or the bottom-right alignment) are template parameters so the plain kernel
 // is compiled without their registers. RAW (no bias or ALiBi, a nonzero
@@ -67,12 +70,16 @@ struct FwdCfg {
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_O = 256;
-  // measured with ptxas at d = 128: the softmax needs ~210 registers, the
-  // MMA issuer ~70; below either the kernel spills
+  // measured with ptxas: the plain softmax needs ~210 registers and the MMA
+  // issuer ~70; with a bias or dropout the softmax needs ~220, and the issuer
+  // fits in 56 once its base descriptors are opaque
   static constexpr int REG_LAUNCH = 168, REG_SOFTMAX = 216, REG_OTHER = 72;
+  static constexpr int REG_SOFTMAX_FLAGS = 224, REG_OTHER_FLAGS = 56;
   static_assert(STAGES >= 1 && SMEM <= 227 * 1024, "shared memory");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "unsupported head size");
   static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_OTHER == THREADS * REG_LAUNCH, "register split");
+  static_assert(2 * 128 * REG_SOFTMAX_FLAGS + 128 * REG_OTHER_FLAGS == THREADS * REG_LAUNCH,
+                "register split");
 };
 
 // Barrier slots (the K/V ring has at most 3 stages).
@@ -184,8 +191,10 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tbase = *tmem_slot;
   const ErrCtx ec{p.err, abort_flag, p.wait_ns};
 
+  // a bias or dropout moves registers from the issuing warpgroup to the softmax
+  constexpr bool FLAGS = GENERAL || DROP;
   if (warp >= 8) {
-    setmaxnreg_dec<C::REG_OTHER>();
+    setmaxnreg_dec<FLAGS ? C::REG_OTHER_FLAGS : C::REG_OTHER>();
     if (warp == 8) {
       // ---------------------------------------------------------- producer
       int issued = 0;
@@ -241,9 +250,13 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dV0 = sdesc_sw128(sV, C::BN * 128, 1024);
       uint32_t pph0 = 0, pph1 = 0;  // P phases consumed per query tile
+      // base descriptors opaque where the issuer runs at 56 registers or the
+      // ring has one stage (then nothing in them changes across iterations)
+      constexpr bool OPQ = FLAGS || ST == 1;
+      auto base = [](uint64_t d) { return OPQ ? opaque_u64(d) : d; };
       auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
-        const uint64_t dQ = desc_adv(dQ0, t * C::Q_BYTES);
-        const uint64_t dK = desc_adv(dK0, (j % ST) * C::K_BYTES);
+        const uint64_t dQ = base(desc_adv(dQ0, t * C::Q_BYTES));
+        const uint64_t dK = base(desc_adv(dK0, (j % ST) * C::K_BYTES));
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(384, 1)
         umma_commit_w(bar(FB_S + t));
       };
       auto issue_pv = [&](int t, int j, bool first) {  // O_t += P_t V_j
-        const uint64_t dV = desc_adv(dV0, (j % ST) * C::V_BYTES);
+        const uint64_t dV = base(desc_adv(dV0, (j % ST) * C::V_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           umma_ts_w(tbase + C::T_O + DV * t, tbase + C::T_S + 128 * t + kk * 8, desc_adv(dV, kk * 2048),
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_wait(bar(FB_DRAIN), 0, ec, kSiteDrain, false);
     }
   } else {
-    setmaxnreg_inc<C::REG_SOFTMAX>();
+    setmaxnreg_inc<FLAGS ? C::REG_SOFTMAX_FLAGS : C::REG_SOFTMAX>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;  // query tile of this warpgroup
     const int qt0 = q0 + t * C::BM;

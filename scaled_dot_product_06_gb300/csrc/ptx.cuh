@@ -227,6 +227,17 @@ __device__ __forceinline__ uint64_t desc_adv(uint64_t desc, uint32_t bytes) {
   return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
+// The same value, opaque to the compiler. An issue loop can pass its per-call
+// base descriptor through this so that the constant offsets are added where
+// each MMA is issued: left visible, descriptors that do not change from one
+// loop iteration to the next (a one-stage ring) are all computed ahead of
+// the loop and held in registers, which the issuing warpgroup does not have.
+__device__ __forceinline__ uint64_t opaque_u64(uint64_t x) {
+  uint64_t r;
+  asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(x));
+  return r;
+}
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 //   ab_bf16: operands are bf16 (else fp16); a_mn / b_mn: operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, bool ab_bf16, bool a_mn,
