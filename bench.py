@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "SDPA fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense BF16 tensor peak"
 UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1000 * 1000  # GB300 L2 (about 126 MiB)
 
 WORKLOADS = {
     "b1h2-s128-d64": dict(B=1, H=2, S_q=128, S_kv=128, D_qk=64, D_v=64, dtype="bf16",
@@ -567,13 +568,37 @@ def main():
         join.record(side)
         stream.wait_event(join)
 
+    def user_step(D):
+        # one step as a user runs it: the forward and the whole backward, one
+        # call each (plus this step's keep bits where they are drawn beforehand)
+        if mask_words:
+            sdpa_dropout_mask(w["B"], w["H"], w["S_q"], w["S_kv"], w["p"], DROP_SEED, DROP_OFFSET,
+                              out=kw["dropout_mask"])
+        t0 = time.perf_counter()
+        fwd_call(D)
+        t1 = time.perf_counter()
+        bwd_call(SDPA_BWD_ALL, D)
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
+
+    # Inputs that fit in L2 (the smallest workload) are flushed out of it
+    # between timed steps by writing a buffer twice its size; each step is
+    # then timed by its own pair of events, so the flush is not counted.
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do) if t is not None)
+    in_bytes += bias.numel() * bias.element_size() if bias is not None else 0
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if in_bytes < L2_BYTES else None
+
     for _ in range(max(args.warmup, 0)):
+        user_step(set0)
         step()
     torch.cuda.synchronize()
     if sdpa_device_error() != 0:
         raise SystemExit("a kernel wait ran out during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    # timed region: K user steps, bracketed by a barrier and synchronize
+    host_fwd = host_bwd = 0.0
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] if flush is not None else []
     sampler = ClockSampler(local)
     sampler.start()
     barrier()
@@ -581,15 +606,40 @@ def main():
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for s in range(args.steps):
-        step(evs[s])
+    for s_ in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+            step_ev[s_][0].record(stream)
+        hf, hb = user_step(set0)
+        host_fwd += hf
+        host_bwd += hb
+        if flush is not None:
+            step_ev[s_][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
     if sdpa_device_error() != 0:
         raise SystemExit("a kernel wait ran out during the timed steps")
-    total_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        total_ms = t_start.elapsed_time(t_end)
+    host_us = {"sdpa_fwd": host_fwd / args.steps * 1e6, "sdpa_bwd": host_bwd / args.steps * 1e6}
+
+    # per-kernel durations: the same K steps again, issued phase by phase with
+    # events between the kernels (on the stream each kernel runs on)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for s_ in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        step(evs[s_])
+    torch.cuda.synchronize()
+    barrier()
+    if sdpa_device_error() != 0:
+        raise SystemExit("a kernel wait ran out during the per-kernel steps")
     per_kernel = {n: 0.0 for n in names}
     spans = {"fwd": (0, 1), "bwd_pre": (1, 2), "bwd_dkdv": (4, 5),
              "bwd_dq": (5, 3) if fused else (2, 3)}
@@ -598,6 +648,60 @@ def main():
             per_kernel[n] += e[a].elapsed_time(e[b])
     per_kernel = {n: t / args.steps for n, t in per_kernel.items()}
     ms = max_over_ranks(total_ms / args.steps, world, dev)
+
+    # The smallest workload is bound by host time per call: a step issued call
+    # by call back to back (no flush, what a loop of calls sees), and the same
+    # step captured once in a CUDA graph and replayed.
+    latency = None
+    if fwd_flops(w) < 1e9:
+        n_l = 200
+        torch.cuda.synchronize()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        for _ in range(n_l):
+            user_step(set0)
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        loop_us = a_ev.elapsed_time(b_ev) / n_l * 1e3
+        graph_us = None
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            user_step(set0)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            user_step(set0)
+        for _ in range(10):
+            g.replay()
+        torch.cuda.synchronize()
+        a_ev.record(stream)
+        for _ in range(n_l):
+            g.replay()
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        graph_us = a_ev.elapsed_time(b_ev) / n_l * 1e3
+        # host time of each call with the device idle before it (the launch
+        # queue empty, so no call waits for room in it)
+        hf = hb = 0.0
+        for _ in range(n_l):
+            torch.cuda.synchronize()
+            a_, b_ = user_step(set0)
+            hf += a_
+            hb += b_
+        torch.cuda.synchronize()
+        if sdpa_device_error() != 0:
+            raise SystemExit("a kernel wait ran out during the latency loops")
+        host_us = {"sdpa_fwd": hf / n_l * 1e6, "sdpa_bwd": hb / n_l * 1e6}
+        latency = {"device_us_per_step_l2_flushed": ms * 1e3,
+                   "api_loop_us_per_step": loop_us,
+                   "graph_replay_us_per_step": graph_us,
+                   "host_us_per_call": host_us,
+                   "method": "api loop: sdpa_fwd + sdpa_bwd called back to back 200 times, no "
+                             "flush, events around the loop; graph: the same step captured once "
+                             "in a CUDA graph (torch.cuda.graph) and replayed 200 times; host: "
+                             "each call timed on the host with the device idle before it"}
 
     ff = fwd_flops(w)
     step_flops = 3.5 * ff
@@ -777,14 +881,17 @@ def main():
                        "backward": "fused (dQ by fp32 reductions)" if fused else "deterministic",
                        **({"dropout_bits": "drawn once by the forward, recorded, read by the "
                                            "backward"} if record_words else {}),
-                       "l2": "inputs larger than L2, no flush",
+                       "l2": ("inputs smaller than L2: a 2x L2 buffer written between timed "
+                              "steps, each step timed by its own events"
+                              if flush is not None else "inputs larger than L2, no flush"),
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "pct_of_peak": 100.0 * value / world / peak,
             "fwd_tflops": ff / (per_kernel["fwd"] * 1e-3) / 1e12,
             "bwd_tflops": 2.5 * ff / (bwd_ms * 1e-3) / 1e12,
             "kernels": kt,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            **({"latency_us_per_step": ms * 1e3} if ff < 1e9 else {}),
+            "host_us_per_call": host_us,
+            **({"latency_us_per_step": ms * 1e3, "latency": latency} if latency else {}),
             "gpu_launches": (5 if mask_words else 4) * args.steps,
         }
         print(json.dumps(out), flush=True)

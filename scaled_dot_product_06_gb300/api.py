@@ -7,6 +7,7 @@ tensor properties, allocate outputs with torch and pass raw pointers.
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 
 import torch
@@ -16,9 +17,18 @@ from . import _native
 _DTYPE_CODE = {torch.bfloat16: _native.SDPA_BF16, torch.float16: _native.SDPA_FP16}
 
 
-def _stream_ptr(stream) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return int(s.cuda_stream)
+# The current stream's handle without building a torch.cuda.Stream object
+# (which costs a few microseconds a call); the public route where the private
+# accessor is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_ptr(stream, t: torch.Tensor) -> int:
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if _raw_stream is not None:
+        return int(_raw_stream(t.get_device()))
+    return int(torch.cuda.current_stream(t.device).cuda_stream)
 
 
 def _check_io(name: str, t: torch.Tensor, shape, dtype) -> None:
@@ -33,7 +43,8 @@ def _check_io(name: str, t: torch.Tensor, shape, dtype) -> None:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # an int converts to void* through the functions' argtypes
+    return None if t is None else t.data_ptr()
 
 
 def _window(is_causal, window, bottom_right, alibi_slopes, n_batch, h, dropout_mask=None,
@@ -113,14 +124,14 @@ def sdpa_fwd(q, k, v, *, scale=None, is_causal=False, dropout_p=0.0, seed=0, off
         st = _native.lib().sdpa_fwd_gqa(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
                                         float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
                                         _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse),
-                                        ctypes.c_void_p(_stream_ptr(stream)))
+                                        _stream_ptr(stream, q))
         _native.check(st, "sdpa_fwd_gqa")
     else:
         rec = _mask_out(dropout_mask_out, (b * h * s_q * s_kv + 31) // 32)
         st = _native.lib().sdpa_fwd_ex(b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, *w, rec,
                                            float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
                                            _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out),
-                                           _ptr(lse), ctypes.c_void_p(_stream_ptr(stream)))
+                                           _ptr(lse), _stream_ptr(stream, q))
         _native.check(st, "sdpa_fwd_ex")
     return out, lse
 
@@ -130,8 +141,13 @@ def sdpa_bwd_workspace_size(b, h, s_q, s_kv, d_qk, d_v, h_kv=None, deterministic
     accumulator of the default backward at d_qk <= 128 (not with
     deterministic=True); with h_kv (grouped K/V heads) the room for splitting
     large groups over several CTAs per key tile is included."""
-    return int(_native.lib().sdpa_bwd_workspace_size_ex(b, h, h if h_kv is None else h_kv, s_q, s_kv,
-                                                        d_qk, d_v, int(bool(deterministic))))
+    return _workspace_size(int(b), int(h), int(h if h_kv is None else h_kv), int(s_q), int(s_kv),
+                           int(d_qk), int(d_v), int(bool(deterministic)))
+
+
+@functools.lru_cache(maxsize=256)
+def _workspace_size(b, h, h_kv, s_q, s_kv, d_qk, d_v, deterministic) -> int:
+    return int(_native.lib().sdpa_bwd_workspace_size_ex(b, h, h_kv, s_q, s_kv, d_qk, d_v, deterministic))
 
 
 def sdpa_bwd(q, k, v, o, dout, lse, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
@@ -187,14 +203,14 @@ def sdpa_bwd_phases(phases, q, k, v, o, dout, lse, *, scale=None, is_causal=Fals
             int(phases), b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, int(bool(is_causal)),
             float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt], _ptr(q), _ptr(k), _ptr(v),
             _ptr(bias), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
-            _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream_ptr(stream)))
+            _ptr(workspace), workspace.numel(), _stream_ptr(stream, q))
         _native.check(st, "sdpa_bwd_phases_gqa")
     else:
         st = _native.lib().sdpa_bwd_phases_ex(
             int(phases), b, h, h_kv, s_q, s_kv, d_qk, d_v, scale, *w, float(dropout_p), int(seed),
             int(offset), _DTYPE_CODE[dt], _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(o),
             _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
-            workspace.numel(), ctypes.c_void_p(_stream_ptr(stream)))
+            workspace.numel(), _stream_ptr(stream, q))
         _native.check(st, "sdpa_bwd_phases_ex")
     return dq, dk, dv, dbias
 
@@ -241,7 +257,7 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
             b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale,
             int(bool(is_causal)), float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
             _ptr(seqstart_q), _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-            ctypes.c_void_p(_stream_ptr(stream)))
+            _stream_ptr(stream, q))
         _native.check(st, "sdpa_fwd_varlen")
     else:
         rec = _mask_out(dropout_mask_out, (b * h * int(max_seqlen_q) * int(max_seqlen_k) + 31) // 32)
@@ -249,7 +265,7 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
             b, h, h_kv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d_qk, d_v, scale, *w,
             rec, float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt], _ptr(seqstart_q),
             _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-            ctypes.c_void_p(_stream_ptr(stream)))
+            _stream_ptr(stream, q))
         _native.check(st, "sdpa_fwd_varlen_ex")
     return out, lse
 
@@ -305,7 +321,7 @@ def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k
             d_v, scale, int(bool(is_causal)), float(dropout_p), int(seed), int(offset),
             _DTYPE_CODE[dt], _ptr(seqstart_q), _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
             _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
-            ctypes.c_void_p(_stream_ptr(stream)))
+            _stream_ptr(stream, q))
         _native.check(st, "sdpa_bwd_phases_varlen")
     else:
         st = _native.lib().sdpa_bwd_phases_varlen_ex(
@@ -313,7 +329,7 @@ def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k
             d_v, scale, *w, float(dropout_p), int(seed), int(offset), _DTYPE_CODE[dt],
             _ptr(seqstart_q), _ptr(seqstart_k), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
             _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
-            ctypes.c_void_p(_stream_ptr(stream)))
+            _stream_ptr(stream, q))
         _native.check(st, "sdpa_bwd_phases_varlen_ex")
     return dq, dk, dv
 
@@ -328,7 +344,7 @@ def sdpa_dropout_mask(b, h, s_q, s_kv, dropout_p, seed, offset, device="cuda", s
     if out is not None and (out.dtype != torch.int32 or out.numel() < words or not out.is_cuda):
         raise ValueError(f"out must be an int32 CUDA tensor of at least {words} words")
     st = _native.lib().sdpa_dropout_mask(b, h, s_q, s_kv, float(dropout_p), int(seed), int(offset),
-                                         _ptr(bits), ctypes.c_void_p(_stream_ptr(stream)))
+                                         _ptr(bits), _stream_ptr(stream, bits))
     _native.check(st, "sdpa_dropout_mask")
     return bits[:words]
 

@@ -79,9 +79,53 @@ sdpa_status_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return SDPA_OK;
 }
 
+// Maps encoded by this host thread's recent calls. A training or serving
+// loop passes the same tensors step after step, and a lookup costs far less
+// host time than an encode; a map depends on nothing but these fields.
+struct MapKey {
+  const void* ptr;
+  int64_t inner, rows, outer;
+  uint32_t box_rows;
+  int type, elem_bytes, swizzle;
+  bool same(const MapKey& o) const {
+    return ptr == o.ptr && inner == o.inner && rows == o.rows && outer == o.outer &&
+           box_rows == o.box_rows && type == o.type && elem_bytes == o.elem_bytes && swizzle == o.swizzle;
+  }
+};
+struct MapSlot {
+  CUtensorMap map;
+  MapKey key;
+  bool used;
+};
+constexpr int kMapSlots = 32;
+thread_local MapSlot g_maps[kMapSlots];
+thread_local int g_map_next = 0;
+
+sdpa_status_t encode_map(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* ptr,
+                         int64_t inner, int64_t rows, int64_t outer, uint32_t box_rows, bool swizzle);
+
 // 3-D map over a [outer][rows][inner] tensor, box {64, box_rows, 1}.
 sdpa_status_t make_map(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* ptr,
                        int64_t inner, int64_t rows, int64_t outer, uint32_t box_rows, bool swizzle) {
+  const MapKey key{ptr, inner, rows, outer, box_rows, static_cast<int>(type), elem_bytes, swizzle ? 1 : 0};
+  for (int i = 0; i < kMapSlots; ++i) {
+    if (g_maps[i].used && g_maps[i].key.same(key)) {
+      *m = g_maps[i].map;
+      return SDPA_OK;
+    }
+  }
+  if (sdpa_status_t s = encode_map(m, type, elem_bytes, ptr, inner, rows, outer, box_rows, swizzle))
+    return s;
+  MapSlot& slot = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapSlots;
+  slot.map = *m;
+  slot.key = key;
+  slot.used = true;
+  return SDPA_OK;
+}
+
+sdpa_status_t encode_map(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* ptr,
+                         int64_t inner, int64_t rows, int64_t outer, uint32_t box_rows, bool swizzle) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   if (sdpa_status_t s = encoder(&enc)) return s;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
