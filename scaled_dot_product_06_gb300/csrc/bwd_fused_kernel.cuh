@@ -56,7 +56,9 @@
 //             the next tile's products.
 //   (warps 18, 19 idle.) Registers: launched at 80 a thread, the compute
 //   warpgroups raise theirs to 96 (setmaxnreg), the producer/MMA warpgroup
-//   drops to 72 and the drain warpgroup to 24.
+//   drops to 56 (its base descriptors rebuilt at each use through
+//   opaque_u64 instead of all held in registers) and the drain warpgroup to
+//   40.
 // Tensor memory (512 columns): S^T / dP^T / P~^T [0,128), dQ_i [128,128+Dk),
 // dV [128+Dk, 128+Dk+Dv), dK after it, then K and V (two elements per column)
 // when they fit (d = 64).
@@ -96,7 +98,7 @@ struct FusedCfg {
   static constexpr int kLoadWarp = 16, kMmaWarp = 17, kDrainWarp0 = 20;
   // registers: launched at REG_LAUNCH; compute warpgroups raise theirs, the
   // producer/MMA and drain warpgroups lower theirs, within the launch total
-  static constexpr int REG_LAUNCH = 80, REG_COMPUTE = 96, REG_ISSUE = 72, REG_DRAIN = 24;
+  static constexpr int REG_LAUNCH = 80, REG_COMPUTE = 96, REG_ISSUE = 56, REG_DRAIN = 40;
   static_assert(4 * 128 * REG_COMPUTE + 128 * REG_ISSUE + 128 * REG_DRAIN == THREADS * REG_LAUNCH,
                 "register split");
   static constexpr uint32_t TMEM_COLS = 512;
@@ -321,26 +323,31 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
       // MN-major (queries in M, 16 KB between the two 64-query boxes) for dQ
       const uint64_t dSk0 = sdesc_sw128(sdS, 16, 1024), dSm0 = sdesc_sw128(sdS, C::BN * 128, 1024);
       const uint64_t dKm0 = sdesc_sw128(sK, C::BN * 128, 1024);  // K_j with d in N
+      // the loop-invariant base descriptors (K, V, the dS^T tile) pass through
+      // opaque_u64 at each product, so the issuer adds the constant offsets
+      // where it issues instead of holding every descriptor in registers
       auto issue_s = [&](int s) {  // S^T = K Q^T
         const uint64_t dq = desc_adv(dQk0, s * C::Q_BYTES);
+        const uint64_t dKb = opaque_u64(dK0);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint64_t bq = desc_adv(dq, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
           if constexpr (C::OPS_IN_TMEM)
             umma_ts_w(tS, tbase + C::T_K + kk * 8, bq, kIdS, kk > 0);
           else
-            umma_ss_w(tS, desc_adv(dK0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bq, kIdS, kk > 0);
+            umma_ss_w(tS, desc_adv(dKb, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bq, kIdS, kk > 0);
         }
       };
       auto issue_dp = [&](int s) {  // dP^T = V dO^T, into the S^T columns
         const uint64_t dob = desc_adv(dOk0, s * C::DO_BYTES);
+        const uint64_t dVb = opaque_u64(dV0);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint64_t bo = desc_adv(dob, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
           if constexpr (C::OPS_IN_TMEM)
             umma_ts_w(tS, tbase + C::T_V + kk * 8, bo, kIdS, kk > 0);
           else
-            umma_ss_w(tS, desc_adv(dV0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bo, kIdS, kk > 0);
+            umma_ss_w(tS, desc_adv(dVb, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32), bo, kIdS, kk > 0);
         }
       };
       bool ok = n_it > 0;
@@ -377,9 +384,10 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
             }
           }
           tc_fence_after();
+          const uint64_t dSm = opaque_u64(dSm0), dKm = opaque_u64(dKm0);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
-            umma_ss_w(tDQ, desc_adv(dSm0, kk * 2048), desc_adv(dKm0, kk * 2048), kIdDQ, kk > 0);
+            umma_ss_w(tDQ, desc_adv(dSm, kk * 2048), desc_adv(dKm, kk * 2048), kIdDQ, kk > 0);
           umma_commit_w(bar(FB_DQ));
           dq_in = true;
           return true;
@@ -429,9 +437,10 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
         tc_fence_after();
         {  // dK += dS^T Q_i
           const uint64_t dqb = desc_adv(dQm0, s * C::Q_BYTES);
+          const uint64_t dSk = opaque_u64(dSk0);
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            umma_ss_w(tDK, desc_adv(dSk0, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32),
+            umma_ss_w(tDK, desc_adv(dSk, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32),
                       desc_adv(dqb, kk * 2048), kIdDK, (i > 0 || kk > 0));
         }
         umma_commit_w(bar(FB_QE + s));  // Q_i and dO_i are no longer read
