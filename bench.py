@@ -892,7 +892,12 @@ def main():
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "host_us_per_call": host_us,
             **({"latency_us_per_step": ms * 1e3, "latency": latency} if latency else {}),
-            "gpu_launches": (5 if mask_words else 4) * args.steps,
+            # per step: forward, preprocess, two backward kernels, plus the keep
+            # bits' kernel where the step draws them beforehand or the forward
+            # draws its record with it (no mask)
+            "gpu_launches": (5 if (mask_words or (record_words and not w["causal"]
+                                                  and w.get("window") is None))
+                             else 4) * args.steps,
         }
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -306,7 +306,9 @@ sdpa_status_t sdpa_bwd_phases_varlen(int phases, int64_t b, int64_t h, int64_t h
  *            drawing them again (CK tile's kIsStoreRandval keeps its random
  *            values for the same reason). Only the words of (query row, key
  *            tile) pairs the forward visits are written; a backward with the
- *            same mask reads no other. Requires s_kv % 32 == 0
+ *            same mask reads no other. With no mask (window (-1, -1), batch
+ *            mode) every word is written, by sdpa_dropout_mask's kernel on the
+ *            same stream before the forward, which then reads them. Requires s_kv % 32 == 0
  *            (SDPA_ERR_UNSUPPORTED) and keep_bits null (SDPA_ERR_INVALID_ARG);
  *            ignored when dropout_p is 0.
  * Causal is (-1, 0, 0), bottom-right causal (-1, 0, 1), a sliding window of

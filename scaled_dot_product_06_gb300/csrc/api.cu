@@ -445,8 +445,21 @@ sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t 
   p.fault = static_cast<uint32_t>(g_debug_fault.load());
   const uint64_t wait_ns = g_debug_wait_ns.load();
   p.wait_ns = wait_ns != 0 ? wait_ns : kWaitLimitNs;
-  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // A record over a mask that hides no element (no causal mask or window,
+  // batch mode) holds every bit of the frame: the mask kernel draws them at
+  // full occupancy, faster than the softmax warps draw them between their
+  // other work, and the forward then reads the record it would have written.
+  if (p.keep_out != nullptr && pk.seqstart_q == nullptr && p.win_left < 0 && p.win_right < 0) {
+    const int64_t total = b * h * s_q * s_kv;
+    const cudaError_t me = launch_dropout_mask(total, p.drop_threshold, p.seed_lo, p.seed_hi, p.offset_lo,
+                                               p.offset_hi, p.keep_out, st);
+    if (me != cudaSuccess) return fail(SDPA_ERR_CUDA, "dropout mask launch", me);
+    p.keep_bits = p.keep_out;
+    p.keep_words = (total + 31) / 32;
+    p.keep_out = nullptr;
+  }
+  if (sdpa_status_t s = error_word_ptr(&p.err)) return s;
   const cudaError_t e = bf16 ? launch_fwd_bf16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st)
                              : launch_fwd_fp16(static_cast<int>(d_qk), static_cast<int>(d_v), mq, mk, mv, p, st);
   return cuda_status(e, "forward kernel launch");
