@@ -434,6 +434,32 @@ sdpa_status_t sdpa_device_error(uint32_t* word, int clear);
  */
 sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns);
 
+/*
+ * Test hook, host only (no device work, no CUDA call): the (query tile, key
+ * tile) pairs a kernel of this library processes for one sequence of s_q
+ * query rows and s_kv keys under a mask given as for sdpa_fwd_ex (window
+ * (-1, 0) is the plain causal mask, (-1, -1) none), computed by the functions
+ * the kernels themselves call, so that a host test can check them against
+ * the visibility rule. The kernels' other cases (packed sequences, grouped
+ * heads) walk the same ranges per sequence and head.
+ *   kernel      0 the forward, 1 the key/value-stationary backward kernels
+ *               (dK/dV and the fused one), 2 the query-stationary dQ kernel
+ *   windowed    nonzero: the band arithmetic the kernels use for any
+ *               window that is not plain (and, with ALiBi, for the plain ones
+ *               too); zero: the mask decides, as without ALiBi
+ *   query_rows  the kernel's query tile height: 128, or 64 for the dK/dV
+ *               kernel at d_qk = 192
+ *   out         HOST memory for up to cap triples (first query row of the
+ *               tile, query rows of the tile, key tile index of 128 keys),
+ *               in the order the kernels' CTAs walk them
+ * Returns the number of triples (written up to cap), or -1 for an invalid
+ * argument (kernel, query_rows, negative or out-of-range sizes, out null with
+ * cap > 0).
+ */
+int64_t sdpa_tile_ranges(int kernel, int64_t s_q, int64_t s_kv, int64_t window_left,
+                         int64_t window_right, int bottom_right, int windowed, int query_rows,
+                         int32_t* out, int64_t cap);
+
 /* Detail of the calling thread's most recent failure (the step and, for
  * SDPA_ERR_CUDA, the CUDA error string); "" if none. Valid until the thread's
  * next call into the library. */

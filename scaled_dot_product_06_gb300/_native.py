@@ -79,6 +79,7 @@ SIGNATURES = {
     "sdpa_dropout_mask": (_int, [_i64, _i64, _i64, _i64, _f32, _u64, _u64, _ptr, _ptr]),
     "sdpa_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
     "sdpa_debug_fault": (_int, [_int, ctypes.c_uint64]),
+    "sdpa_tile_ranges": (_i64, [_int, _i64, _i64, _i64, _i64, _int, _int, _int, _ptr, _i64]),
     "sdpa_last_error": (ctypes.c_char_p, []),
     "sdpa_status_string": (ctypes.c_char_p, [_int]),
     "sdpa_version": (_int, []),

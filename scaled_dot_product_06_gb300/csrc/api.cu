@@ -651,6 +651,55 @@ sdpa_status_t sdpa_debug_fault(int fault, uint64_t wait_limit_ns) {
   return SDPA_OK;
 }
 
+int64_t sdpa_tile_ranges(int kernel, int64_t s_q, int64_t s_kv, int64_t window_left,
+                         int64_t window_right, int bottom_right, int windowed, int query_rows,
+                         int32_t* out, int64_t cap) {
+  if (kernel < 0 || kernel > 2 || (query_rows != 64 && query_rows != 128) || s_q < 0 || s_kv < 0 ||
+      s_q > kMaxSeq || s_kv > kMaxSeq || cap < 0 || (cap > 0 && out == nullptr))
+    return -1;
+  // the window as the launchers hand it to the kernels
+  FwdParams w{};
+  set_window(Mask{window_left, window_right, bottom_right}, s_q, s_kv, &w);
+  const int S_q = static_cast<int>(s_q), S_kv = static_cast<int>(s_kv);
+  const bool win = w.win_general != 0 || windowed != 0;
+  const Band bd = win ? band_of(w.win_left, w.win_right, w.win_br, S_q, S_kv) : plain_band(w.win_right);
+  constexpr int kTile = 128;  // forward and dQ query tiles; key tiles everywhere
+  int64_t n = 0;
+  auto emit = [&](int q0, int rows, int kt) {
+    if (n < cap) {
+      out[3 * n] = q0;
+      out[3 * n + 1] = rows;
+      out[3 * n + 2] = kt;
+    }
+    ++n;
+  };
+  if (kernel == 0) {  // forward: pairs of query tiles, key tiles from the diagonal down
+    const int n_pairs = ((S_q + kTile - 1) / kTile + 1) / 2;
+    for (int qt = 0; qt < n_pairs; ++qt) {
+      const QueryPair qp = query_pair(qt, S_q, kTile);
+      const TileRange kr[2] = {key_tiles_of_rows(bd, qp.q0, kTile, kTile, S_q, S_kv),
+                               key_tiles_of_rows(bd, qp.lone ? S_q : qp.q0 + kTile, kTile, kTile, S_q, S_kv)};
+      const FwdIters it = fwd_iters(kr[0], kr[1]);
+      const IterSpan sp[2] = {fwd_tile_iters(kr[0], it), fwd_tile_iters(kr[1], it)};
+      for (int j = 0; j < it.n_it; ++j)
+        for (int t = 0; t < 2; ++t)
+          if (sp[t].first <= j && j <= sp[t].last) emit(qp.q0 + t * kTile, kTile, it.khi - j);
+    }
+  } else if (kernel == 1) {  // key/value-stationary: a CTA per key tile
+    for (int kt = 0; kt * kTile < S_kv; ++kt) {
+      const TileRange qr = query_tiles_of_keys(win, bd, w.win_right, kt * kTile, kTile, query_rows, S_q, S_kv);
+      for (int i = qr.lo; i <= qr.hi; ++i) emit(i * query_rows, query_rows, kt);
+    }
+  } else {  // query-stationary dQ: a CTA per query tile, key tiles from the diagonal down
+    for (int q0 = 0; q0 < S_q; q0 += kTile) {
+      const TileRange kr = win ? key_tiles_of_rows(bd, q0, kTile, kTile, S_q, S_kv)
+                               : key_tiles_plain(w.win_right >= 0, q0, kTile, kTile, S_kv);
+      for (int j = 0; j <= kr.hi - kr.lo; ++j) emit(q0, kTile, kr.hi - j);
+    }
+  }
+  return n;
+}
+
 size_t sdpa_bwd_workspace_size_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv,
                                   int64_t d_qk, int64_t d_v, int deterministic) {
   bool empty = false;

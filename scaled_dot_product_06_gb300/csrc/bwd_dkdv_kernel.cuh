@@ -284,18 +284,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   if (k0 >= S_kv) return;
   // query tiles [it0, it0 + n_per) holding a row that sees a key of this tile
   // (WIN: a general window; else top-left, causal when win_right >= 0)
-  const Band bd = WIN ? band_of(p.win_left, p.win_right, p.win_br, S_q, S_kv)
-                      : Band{-kUnbounded, p.win_right >= 0 ? 0 : kUnbounded};
-  int it0, n_per;
-  if constexpr (WIN) {
-    const int qlo = max(k0 - bd.hi, 0), qhi = min(min(k0 + C::BN, S_kv) - 1 - bd.lo, S_q - 1);
-    it0 = qlo / BM;
-    n_per = qlo <= qhi ? qhi / BM - it0 + 1 : 0;
-  } else {
-    const int n_qt = (S_q + BM - 1) / BM;
-    it0 = p.win_right >= 0 ? min(n_qt, k0 / BM) : 0;
-    n_per = n_qt - it0;
-  }
+  const Band bd = WIN ? band_of(p.win_left, p.win_right, p.win_br, S_q, S_kv) : plain_band(p.win_right);
+  const TileRange qr_t = query_tiles_of_keys(WIN, bd, p.win_right, k0, C::BN, BM, S_q, S_kv);
+  const int it0 = qr_t.lo, n_per = qr_t.hi - qr_t.lo + 1;
   // A key tile no query sees: its first split writes the zeros alone.
   if (SPLIT && n_per == 0 && sp != 0) return;
   // One loop over (query head of the split, query tile): iteration i visits

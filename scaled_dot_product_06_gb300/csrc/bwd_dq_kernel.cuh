@@ -118,19 +118,10 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   const int q0 = qt * BM;
   // key tiles [khi - n_kv + 1, khi] holding a key some row of the tile sees
   // (WIN: a general window; else top-left, causal when win_right >= 0)
-  const bool causal = p.win_right >= 0;
-  const Band bd = WIN ? band_of(p.win_left, p.win_right, p.win_br, S_q, S_kv)
-                      : Band{-kUnbounded, causal ? 0 : kUnbounded};
-  int khi, n_kv;
-  if constexpr (WIN) {
-    const int klo_key = max(q0 + bd.lo, 0), khi_key = min(min(q0 + BM, S_q) - 1 + bd.hi, S_kv - 1);
-    khi = khi_key / BN;
-    n_kv = (q0 < S_q && klo_key <= khi_key) ? khi - klo_key / BN + 1 : 0;
-  } else {
-    const int n_kv_all = (S_kv + BN - 1) / BN;
-    n_kv = causal ? min(n_kv_all, (q0 + BM - 1) / BN + 1) : n_kv_all;
-    khi = n_kv - 1;
-  }
+  const Band bd = WIN ? band_of(p.win_left, p.win_right, p.win_br, S_q, S_kv) : plain_band(p.win_right);
+  const TileRange kr = WIN ? key_tiles_of_rows(bd, q0, BM, BN, S_q, S_kv)
+                           : key_tiles_plain(p.win_right >= 0, q0, BM, BN, S_kv);
+  const int khi = kr.hi, n_kv = kr.hi - kr.lo + 1;
   // Uniform over the CTA: a tile past the end of a shorter packed sequence has
   // nothing to do, and rows that see no key (a sequence without keys, or the
   // window) have dQ = 0.

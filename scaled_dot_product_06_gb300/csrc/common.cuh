@@ -93,9 +93,103 @@ constexpr int kUnbounded = 1 << 30;
 struct Band {
   int lo, hi;
 };
-__device__ __forceinline__ Band band_of(int win_left, int win_right, int win_br, int S_q, int S_kv) {
+__host__ __device__ __forceinline__ Band band_of(int win_left, int win_right, int win_br, int S_q, int S_kv) {
   const int off = win_br ? S_kv - S_q : 0;
   return Band{win_left < 0 ? -kUnbounded : off - win_left, win_right < 0 ? kUnbounded : off + win_right};
+}
+
+// ---- tile ranges: which tiles each kernel walks. The kernels and the
+// library's host-side range check (sdpa_tile_ranges) call these same
+// functions, so a test of the one tests the other.
+__host__ __device__ __forceinline__ int imin(int a, int b) {
+#ifdef __CUDA_ARCH__
+  return min(a, b);
+#else
+  return a < b ? a : b;
+#endif
+}
+__host__ __device__ __forceinline__ int imax(int a, int b) {
+#ifdef __CUDA_ARCH__
+  return max(a, b);
+#else
+  return a > b ? a : b;
+#endif
+}
+
+// The band of the plain kernels: top-left, causal when win_right >= 0.
+__host__ __device__ __forceinline__ Band plain_band(int win_right) {
+  return Band{-kUnbounded, win_right >= 0 ? 0 : kUnbounded};
+}
+
+// Tiles [lo, hi] of a range; lo > hi when empty.
+struct TileRange {
+  int lo, hi;
+};
+
+// Key tiles (bn keys each) holding a key that some row of [q0, q0 + rows)
+// sees under the band; empty when q0 >= S_q or no row sees a key.
+__host__ __device__ __forceinline__ TileRange key_tiles_of_rows(Band bd, int q0, int rows, int bn, int S_q,
+                                                              int S_kv) {
+  TileRange r{0, -1};
+  if (q0 < S_q) {
+    const int lo = imax(q0 + bd.lo, 0), hi = imin(imin(q0 + rows, S_q) - 1 + bd.hi, S_kv - 1);
+    if (lo <= hi) r = TileRange{lo / bn, hi / bn};
+  }
+  return r;
+}
+
+// The same for the plain masks in closed form (the dQ kernel's plain
+// instances): every key tile, or those up to the tile holding the last row's
+// diagonal key under the causal mask.
+__host__ __device__ __forceinline__ TileRange key_tiles_plain(bool causal, int q0, int rows, int bn, int S_kv) {
+  const int n_all = (S_kv + bn - 1) / bn;
+  return TileRange{0, (causal ? imin(n_all, (q0 + rows - 1) / bn + 1) : n_all) - 1};
+}
+
+// Query tiles (bm rows each) holding a row that sees some key of
+// [k0, k0 + bn): under a general band (win), else the plain masks' closed
+// form (from the diagonal tile down, or every tile).
+__host__ __device__ __forceinline__ TileRange query_tiles_of_keys(bool win, Band bd, int win_right, int k0,
+                                                                 int bn, int bm, int S_q, int S_kv) {
+  if (win) {
+    const int qlo = imax(k0 - bd.hi, 0), qhi = imin(imin(k0 + bn, S_kv) - 1 - bd.lo, S_q - 1);
+    return qlo <= qhi ? TileRange{qlo / bm, qhi / bm} : TileRange{qlo / bm, qlo / bm - 1};
+  }
+  const int n_qt = (S_q + bm - 1) / bm;
+  return TileRange{win_right >= 0 ? imin(n_qt, k0 / bm) : 0, n_qt - 1};
+}
+
+// The forward's pair of query tiles number qt of a sequence of S_q rows:
+// tiles (0,1), (2,3), ... for an even tile count; tile 0 alone and then
+// (1,2), (3,4), ... for an odd one, so the tile without a partner is the one
+// with the fewest causal key tiles. q0 is the first row of the pair's tile 0.
+struct QueryPair {
+  int q0;
+  bool lone;  // tile 1 of the pair does not exist
+};
+__host__ __device__ __forceinline__ QueryPair query_pair(int qt, int S_q, int bm) {
+  const int n = (S_q + bm - 1) / bm;
+  const bool odd = (n & 1) != 0;
+  return QueryPair{(odd ? imax(2 * qt - 1, 0) : 2 * qt) * bm, odd && qt == 0};
+}
+
+// The forward's walk over a pair whose tiles see key tiles k0 and k1:
+// iteration j (of n_it) visits key tile khi - j, from the diagonal down, and
+// a query tile takes part in the iterations [first, last] of its own range
+// (first > last when it sees no key).
+struct FwdIters {
+  int khi, n_it;
+};
+__host__ __device__ __forceinline__ FwdIters fwd_iters(TileRange k0, TileRange k1) {
+  const bool has0 = k0.lo <= k0.hi, has1 = k1.lo <= k1.hi;
+  const int khi = imax(k0.hi, k1.hi);
+  return FwdIters{khi, (has0 || has1) ? khi - (has0 ? k0.lo : k1.lo) + 1 : 0};
+}
+struct IterSpan {
+  int first, last;
+};
+__host__ __device__ __forceinline__ IterSpan fwd_tile_iters(TileRange k, FwdIters it) {
+  return k.lo <= k.hi ? IterSpan{it.khi - k.hi, it.khi - k.lo} : IterSpan{it.n_it, -1};
 }
 
 // The band kept in shared memory and re-read where a loop needs it, so that

@@ -1,36 +1,50 @@
-"""The tile ranges the three kernels walk, restated here from the kernels and
+"""The tile ranges the kernels walk, taken from the library itself and
 checked against the oracle's visibility rule: every visible (query, key) pair
-lies in a tile the kernel processes, and every tile coordinate it loads lies
-inside the problem.
+lies in a tile the kernel processes, every tile coordinate lies inside the
+problem, and the plain causal ranges skip the tiles wholly above the
+diagonal.
 
-* Forward (fwd_kernel.cuh): a CTA owns a pair of 128-row query tiles (with an
-  odd number of tiles, tile 0 alone and pairs (1, 2), (3, 4), ...) and walks
-  the 128-key tiles from the highest one either query tile sees down to the
-  lowest one of tile 0 (of tile 1 when tile 0 sees none); query tile t joins
-  the iterations of its own key range.
-* dK / dV (bwd_dkdv_kernel.cuh): a CTA owns a 128-key tile and walks the
-  query tiles (128 rows, 64 at d_qk = 192) holding a row that sees one of its
-  keys.
-* dQ (bwd_dq_kernel.cuh): a CTA owns a 128-row query tile and walks the key
-  tiles holding a key that one of its rows sees.
+sdpa_tile_ranges (a host-only test hook of the C ABI) enumerates the
+(query tile, key tile) pairs of each kernel with the functions of
+common.cuh that the backward kernels call (key_tiles_of_rows,
+key_tiles_plain, query_tiles_of_keys) and whose arithmetic the forward
+writes out (query_pair, key_tiles_of_rows, fwd_iters / fwd_tile_iters; the
+calls themselves changed its compiled code):
 
-The windowed kernels take these ranges from the band [i + lo, i + hi] of
-visible keys of row i; the plain kernels (top-left causal or unmasked) from
-the closed forms below. These are CPU restatements of the kernels' integer
-arithmetic: a change to a kernel's ranges has to be made here too.
+* the forward: a CTA owns a pair of 128-row query tiles (with an odd number
+  of tiles, tile 0 alone and pairs (1, 2), (3, 4), ...) and walks the key
+  tiles from the highest one either query tile sees down; query tile t joins
+  the iterations of its own key range;
+* the key/value-stationary backward (dK/dV, fused): a CTA owns a 128-key
+  tile and walks the query tiles (128 rows, 64 at d_qk = 192) holding a row
+  that sees one of its keys;
+* the dQ kernel: a CTA owns a 128-row query tile and walks the key tiles
+  holding a key one of its rows sees.
+
+Windows take the band [i + lo, i + hi] of visible keys of row i; the plain
+masks (top-left causal or none) closed forms, or the band as well when
+`windowed` is set (the kernels' ALiBi instances).
 """
+import ctypes
+
 import numpy as np
 import pytest
 
 import oracle
+from scaled_dot_product_06_gb300 import _native
 
-U = 1 << 30  # an unbounded side of the band
 BM = BN = 128
 
 
-def band(wl, wr, br, S_q, S_kv):
-    off = S_kv - S_q if br else 0
-    return (-U if wl < 0 else off - wl, U if wr < 0 else off + wr)
+def tiles(kernel, S_q, S_kv, wl, wr, br, windowed=False, rows=128):
+    """(first query row, query rows, key tile) triples from the library."""
+    lib = _native.lib()
+    n = lib.sdpa_tile_ranges(kernel, S_q, S_kv, wl, wr, int(br), int(windowed), rows, None, 0)
+    assert n >= 0
+    buf = (ctypes.c_int32 * max(3 * n, 1))()
+    assert lib.sdpa_tile_ranges(kernel, S_q, S_kv, wl, wr, int(br), int(windowed), rows,
+                                ctypes.addressof(buf), n) == n
+    return np.frombuffer(buf, dtype=np.int32, count=3 * n).reshape(n, 3)
 
 
 def visible(S_q, S_kv, wl, wr, br):
@@ -38,90 +52,17 @@ def visible(S_q, S_kv, wl, wr, br):
     return oracle.sdpa_oracle.visible(pr, np.arange(S_q), np.arange(S_kv))
 
 
-def fwd_tiles(S_q, S_kv, lo, hi):
-    """(query tile start, key tile) pairs the forward processes."""
-    out = []
-    n_qt = (S_q + BM - 1) // BM
-    odd = n_qt & 1
-    for qt in range((n_qt + 1) // 2):
-        lone = odd and qt == 0
-        q0 = (max(2 * qt - 1, 0) if odd else 2 * qt) * BM
-        rng = []
-        for t in (0, 1):
-            qs = q0 + t * BM
-            if (t == 1 and lone) or qs >= S_q:
-                rng.append(None)
-                continue
-            l, h = max(qs + lo, 0), min(min(qs + BM, S_q) - 1 + hi, S_kv - 1)
-            rng.append((l // BN, h // BN) if l <= h else None)
-        if rng[0] is None and rng[1] is None:
-            continue
-        khi = max(r[1] for r in rng if r)
-        klo = rng[0][0] if rng[0] else rng[1][0]
-        for j in range(khi - klo + 1):
-            kt = khi - j
-            assert 0 <= kt * BN < S_kv
-            users = [t for t in (0, 1) if rng[t] and rng[t][0] <= kt <= rng[t][1]]
-            assert users, "an iteration without a query tile"
-            out += [(q0 + t * BM, kt) for t in users]
-    return out
-
-
-def dkdv_tiles(S_q, S_kv, lo, hi, bm, plain_causal=None):
-    out = []
-    n_qt = (S_q + bm - 1) // bm
-    for kt in range((S_kv + BN - 1) // BN):
-        k0 = kt * BN
-        if plain_causal is None:
-            qlo, qhi = max(k0 - hi, 0), min(min(k0 + BN, S_kv) - 1 - lo, S_q - 1)
-            it0 = qlo // bm
-            n_per = qhi // bm - it0 + 1 if qlo <= qhi else 0
-        else:
-            it0 = min(n_qt, k0 // bm) if plain_causal else 0
-            n_per = n_qt - it0
-        for i in range(n_per):
-            q0 = (it0 + i) * bm
-            assert 0 <= q0 < S_q
-            out.append((q0, bm, kt))
-    return out
-
-
-def dq_tiles(S_q, S_kv, lo, hi, plain_causal=None):
-    out = []
-    n_kv_all = (S_kv + BN - 1) // BN
-    for qt in range((S_q + BM - 1) // BM):
-        q0 = qt * BM
-        if plain_causal is None:
-            l, h = max(q0 + lo, 0), min(min(q0 + BM, S_q) - 1 + hi, S_kv - 1)
-            khi = h // BN
-            n_kv = khi - l // BN + 1 if l <= h else 0
-        else:
-            n_kv = min(n_kv_all, (q0 + BM - 1) // BN + 1) if plain_causal else n_kv_all
-            khi = n_kv - 1
-        for j in range(n_kv):
-            kt = khi - j
-            assert 0 <= kt * BN < S_kv
-            out.append((q0, kt))
-    return out
-
-
-def cover(shape, tiles_q_k, bm=BM):
-    cov = np.zeros(shape, dtype=bool)
-    for q0, kt in tiles_q_k:
-        cov[q0:q0 + bm, kt * BN:kt * BN + BN] = True
-    return cov
-
-
-def check(S_q, S_kv, wl, wr, br):
+def check(S_q, S_kv, wl, wr, br, windowed=False):
     vis = visible(S_q, S_kv, wl, wr, br)
-    lo, hi = band(wl, wr, br, S_q, S_kv)
-    assert not (vis & ~cover(vis.shape, fwd_tiles(S_q, S_kv, lo, hi))).any(), "forward"
-    for bm in (128, 64):
+    for kernel, rows in ((0, 128), (1, 128), (1, 64), (2, 128)):
         cov = np.zeros_like(vis)
-        for q0, b, kt in dkdv_tiles(S_q, S_kv, lo, hi, bm):
-            cov[q0:q0 + b, kt * BN:kt * BN + BN] = True
-        assert not (vis & ~cov).any(), f"dK/dV, {bm}-row query tiles"
-    assert not (vis & ~cover(vis.shape, dq_tiles(S_q, S_kv, lo, hi))).any(), "dQ"
+        t = tiles(kernel, S_q, S_kv, wl, wr, br, windowed, rows)
+        for q0, nr, kt in t:
+            assert nr == rows and 0 <= q0 < S_q and q0 % rows == 0, (kernel, q0, nr)
+            assert 0 <= kt * BN < S_kv, (kernel, kt)
+            cov[q0:q0 + nr, kt * BN:kt * BN + BN] = True
+        assert len({tuple(x) for x in t}) == len(t), f"kernel {kernel}: a tile pair visited twice"
+        assert not (vis & ~cov).any(), f"kernel {kernel} ({rows}-row query tiles) misses a visible pair"
 
 
 @pytest.mark.parametrize("S_q,S_kv,wl,wr,br", [
@@ -146,28 +87,31 @@ def test_windowed_ranges_on_random_shapes():
 @pytest.mark.parametrize("S_q,S_kv", [(1, 1), (128, 128), (129, 257), (700, 300), (640, 1000),
                                       (383, 383)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_plain_ranges_cover_every_visible_pair(S_q, S_kv, causal):
-    """The plain kernels: top-left causal (window (-1, 0)) or unmasked."""
-    vis = visible(S_q, S_kv, -1, 0 if causal else -1, False)
-    lo, hi = -U, (0 if causal else U)  # the forward's plain band
-    assert not (vis & ~cover(vis.shape, fwd_tiles(S_q, S_kv, lo, hi))).any()
-    for bm in (128, 64):
-        cov = np.zeros_like(vis)
-        for q0, b, kt in dkdv_tiles(S_q, S_kv, lo, hi, bm, plain_causal=causal):
-            cov[q0:q0 + b, kt * BN:kt * BN + BN] = True
-        assert not (vis & ~cov).any()
-    assert not (vis & ~cover(vis.shape, dq_tiles(S_q, S_kv, lo, hi, plain_causal=causal))).any()
+@pytest.mark.parametrize("windowed", [False, True])
+def test_plain_ranges_cover_every_visible_pair(S_q, S_kv, causal, windowed):
+    """The plain masks (top-left causal or none), by the closed forms of the
+    plain instances and by the band arithmetic of the ALiBi instances."""
+    check(S_q, S_kv, -1, 0 if causal else -1, False, windowed)
 
 
-def test_causal_ranges_skip_tiles_above_the_diagonal():
+@pytest.mark.parametrize("windowed", [False, True])
+def test_causal_ranges_skip_tiles_above_the_diagonal(windowed):
     """The plain causal ranges are tight: no processed tile lies wholly above
     the diagonal (where no key is visible)."""
     S = 1000
     vis = visible(S, S, -1, 0, False)
-    for q0, kt in fwd_tiles(S, S, -U, 0) + dq_tiles(S, S, -U, 0, plain_causal=True):
-        assert vis[q0:q0 + BM, kt * BN:kt * BN + BN].any()
-    for q0, b, kt in dkdv_tiles(S, S, -U, 0, 128, plain_causal=True):
-        assert vis[q0:q0 + b, kt * BN:kt * BN + BN].any()
+    for kernel, rows in ((0, 128), (1, 128), (1, 64), (2, 128)):
+        for q0, nr, kt in tiles(kernel, S, S, -1, 0, False, windowed, rows):
+            assert vis[q0:q0 + nr, kt * BN:kt * BN + BN].any(), (kernel, q0, kt)
+
+
+def test_tile_ranges_hook_rejects_bad_arguments():
+    lib = _native.lib()
+    assert lib.sdpa_tile_ranges(3, 128, 128, -1, 0, 0, 0, 128, None, 0) == -1
+    assert lib.sdpa_tile_ranges(0, 128, 128, -1, 0, 0, 0, 96, None, 0) == -1
+    assert lib.sdpa_tile_ranges(0, -1, 128, -1, 0, 0, 0, 128, None, 0) == -1
+    assert lib.sdpa_tile_ranges(0, 128, 128, -1, 0, 0, 0, 128, None, 4) == -1
+    assert lib.sdpa_tile_ranges(2, 0, 128, -1, 0, 0, 0, 128, None, 0) == 0
 
 
 def test_packed_statistics_blocks_are_disjoint_and_inside_the_pad():
