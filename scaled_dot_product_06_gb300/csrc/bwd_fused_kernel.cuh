@@ -58,7 +58,7 @@
 //   warpgroups raise theirs to 96 (setmaxnreg), the producer/MMA warpgroup
 //   drops to 56 (its base descriptors rebuilt at each use through
 //   opaque_u64 instead of all held in registers) and the drain warpgroup to
-//   40.
+//   40; in the split instances 72 and 24, with the descriptors held.
 // Tensor memory (512 columns): S^T / dP^T / P~^T [0,128), dQ_i [128,128+Dk),
 // dV [128+Dk, 128+Dk+Dv), dK after it, then K and V (two elements per column)
 // when they fit (d = 64).
@@ -99,7 +99,13 @@ struct FusedCfg {
   // registers: launched at REG_LAUNCH; compute warpgroups raise theirs, the
   // producer/MMA and drain warpgroups lower theirs, within the launch total
   static constexpr int REG_LAUNCH = 80, REG_COMPUTE = 96, REG_ISSUE = 56, REG_DRAIN = 40;
+  // the split instances (grouped K/V heads over several CTAs per key tile)
+  // keep plain descriptors and the issuer at 72: measured, the opaque form
+  // there took the grouped workloads' kernel from 4.50 to 4.61 ms
+  static constexpr int REG_ISSUE_SPLIT = 72, REG_DRAIN_SPLIT = 24;
   static_assert(4 * 128 * REG_COMPUTE + 128 * REG_ISSUE + 128 * REG_DRAIN == THREADS * REG_LAUNCH,
+                "register split");
+  static_assert(4 * 128 * REG_COMPUTE + 128 * REG_ISSUE_SPLIT + 128 * REG_DRAIN_SPLIT == THREADS * REG_LAUNCH,
                 "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DQ = 128, T_DV = 128 + DQK, T_DK = T_DV + DV;
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
     // ------------------------------------------------------------ drain
     // (each warpgroup's register change directly precedes its own code, so
     // the compiler holds each role to its own budget)
-    setmaxnreg_dec<C::REG_DRAIN>();
+    setmaxnreg_dec<SPLIT ? C::REG_DRAIN_SPLIT : C::REG_DRAIN>();
     // lanes of warp kDrainWarp0 + r: query rows 32 r .. 32 r + 31 of dQ_i
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int i = 0; i < n_it; ++i) {
@@ -250,7 +256,7 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
       }
     }
   } else if (warp >= NCT / 32) {
-    setmaxnreg_dec<C::REG_ISSUE>();
+    setmaxnreg_dec<SPLIT ? C::REG_ISSUE_SPLIT : C::REG_ISSUE>();
     if (warp == kLoadWarp) {
       // ---------------------------------------------------------- producer
       int issued = 0;
@@ -317,9 +323,11 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
       // the loop-invariant base descriptors (K, V, the dS^T tile) pass through
       // opaque_u64 at each product, so the issuer adds the constant offsets
       // where it issues instead of holding every descriptor in registers
+      // (not in the split instances, see REG_ISSUE_SPLIT)
+      auto opq = [](uint64_t d) { return SPLIT ? d : opaque_u64(d); };
       auto issue_s = [&](int s) {  // S^T = K Q^T
         const uint64_t dq = desc_adv(dQk0, s * C::Q_BYTES);
-        const uint64_t dKb = opaque_u64(dK0);
+        const uint64_t dKb = opq(dK0);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint64_t bq = desc_adv(dq, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
@@ -331,7 +339,7 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
       };
       auto issue_dp = [&](int s) {  // dP^T = V dO^T, into the S^T columns
         const uint64_t dob = desc_adv(dOk0, s * C::DO_BYTES);
-        const uint64_t dVb = opaque_u64(dV0);
+        const uint64_t dVb = opq(dV0);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint64_t bo = desc_adv(dob, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
@@ -375,7 +383,7 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
             }
           }
           tc_fence_after();
-          const uint64_t dSm = opaque_u64(dSm0), dKm = opaque_u64(dKm0);
+          const uint64_t dSm = opq(dSm0), dKm = opq(dKm0);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)
             umma_ss_w(tDQ, desc_adv(dSm, kk * 2048), desc_adv(dKm, kk * 2048), kIdDQ, kk > 0);
@@ -428,7 +436,7 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
         tc_fence_after();
         {  // dK += dS^T Q_i
           const uint64_t dqb = desc_adv(dQm0, s * C::Q_BYTES);
-          const uint64_t dSk = opaque_u64(dSk0);
+          const uint64_t dSk = opq(dSk0);
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
             umma_ss_w(tDK, desc_adv(dSk, (kk >> 2) * (C::BN * 128) + (kk & 3) * 32),
