@@ -134,7 +134,9 @@ def kernel_bytes(w: dict, fused: bool) -> dict:
     kv = rk * (Dk + Dv) * e
     bias = H * visible_pairs_per_head(w) * 4 if w["bias"] else 0  # read over the visible pairs
     dbias = H * w["S_q"] * w["S_kv"] * 4 if w["bias"] else 0       # written in full (0 where masked)
-    acc = B * H * ((w["S_q"] + 127) // 128) * 128 * Dk * 4  # fp32, rows padded to 128 per (b, h)
+    # the fp32 dQ accumulator: rows padded to 128 per (b, h), or per head over the packed rows
+    acc = (H * ((sum(w["lens"]) + 127) // 128) if w.get("lens") else B * H * ((w["S_q"] + 127) // 128)) \
+        * 128 * Dk * 4
     out = {"fwd": q + kv + o + lse + bias, "bwd_pre": 2 * o + lse + st}
     main = q + o + kv + st + kv + bias + dbias  # Q, dO, K, V, stats, Bias in; dK, dV, dBias out
     if fused:
@@ -458,8 +460,9 @@ def main():
         starts = torch.tensor(seqstarts(w["lens"]), dtype=torch.int32, device=dev)
         o = torch.empty(w["H"], total, w["D_v"], dtype=x["q"].dtype, device=dev)
         lse = torch.empty(w["H"], total, dtype=torch.float32, device=dev)
-        ws = torch.empty(sdpa_bwd_varlen_workspace_size(w["B"], w["H"], total), dtype=torch.uint8,
-                         device=dev)
+        ws = torch.empty(sdpa_bwd_varlen_workspace_size(w["B"], w["H"], total, w["D_qk"],
+                                                        args.deterministic),
+                         dtype=torch.uint8, device=dev)
         mx = w["S_q"]
 
         def fwd_call(D):
@@ -469,7 +472,8 @@ def main():
         def bwd_call(ph, D, stream=None):
             sdpa_bwd_phases_varlen(ph, D["q"], D["k"], D["v"], D["o"], D["do"], D["lse"], starts,
                                    starts, mx, mx, workspace=ws, dq=D["dq"], dk=D["dk"],
-                                   dv=D["dv"], stream=stream, **kw)
+                                   dv=D["dv"], stream=stream, deterministic=args.deterministic,
+                                   **kw)
     else:
         shp = Shape(w["B"], w["H"], w["S_q"], w["S_kv"], w["D_qk"], w["D_v"], w.get("H_kv", 0))
         x = make_inputs(shp, w["dtype"], with_bias=w["bias"], seed_base=rank, device=dev)
@@ -491,12 +495,12 @@ def main():
             sdpa_bwd_phases(ph, D["q"], D["k"], D["v"], D["o"], D["do"], D["lse"], workspace=ws,
                             dq=D["dq"], dk=D["dk"], dv=D["dv"], bias=D["bias"], dbias=D["dbias"],
                             stream=stream, deterministic=args.deterministic, **kw, **rec_bwd)
-    # The default backward at d_qk <= 128 in batch mode is the fused one: the
-    # preprocess, one key/value-stationary kernel that also accumulates dQ,
-    # and the dQ convert pass, one after the other. Otherwise (d_qk = 192,
-    # packed sequences, --deterministic) the dK/dV and dQ kernels run
-    # concurrently after the preprocess.
-    fused = not args.deterministic and w["D_qk"] <= 128 and not packed
+    # The default backward at d_qk <= 128 is the fused one: the preprocess,
+    # one key/value-stationary kernel that also accumulates dQ, and the dQ
+    # convert pass, one after the other. Otherwise (d_qk = 192,
+    # --deterministic) the dK/dV and dQ kernels run concurrently after the
+    # preprocess.
+    fused = not args.deterministic and w["D_qk"] <= 128
     q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 

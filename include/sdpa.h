@@ -243,12 +243,22 @@ sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv
  *   Inputs   K/V rows of the neighbouring sequence can enter a tile before
  *            their scores are masked: inputs must be finite.
  *   Bias     not supported with packed sequences (no bias argument).
- *   Workspace  sdpa_bwd_varlen_workspace_size(b, h, total_q) bytes, 256-byte
- *            aligned (0 for invalid sizes).
+ *   Workspace  256-byte aligned. sdpa_bwd_varlen_workspace_size_ex(b, h,
+ *            total_q, d_qk, 0) bytes run the default backward (at d_qk <= 128
+ *            the fused one, with its fp32 dQ accumulator over the packed rows:
+ *            4 * h * ceil(total_q / 128) * 128 * d_qk bytes after the
+ *            statistics); a workspace of fewer bytes but at least
+ *            sdpa_bwd_varlen_workspace_size(b, h, total_q) (the row statistics
+ *            alone, = the _ex size with deterministic != 0) runs the
+ *            deterministic backward. The fused backward's convert pass writes
+ *            every row of dq: rows of no sequence get dQ = 0. Both sizes are 0
+ *            for invalid sizes.
  * h_kv as in the grouped calls. Zero b, h, total_q, total_k, max_seqlen_q or
  * max_seqlen_k is a no-op returning SDPA_OK.
  */
 size_t sdpa_bwd_varlen_workspace_size(int64_t b, int64_t h, int64_t total_q);
+size_t sdpa_bwd_varlen_workspace_size_ex(int64_t b, int64_t h, int64_t total_q, int64_t d_qk,
+                                         int deterministic);
 sdpa_status_t sdpa_fwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,
                               int64_t max_seqlen_q, int64_t max_seqlen_k, int64_t d_qk, int64_t d_v,
                               float scale, int is_causal, float dropout_p, uint64_t seed,

@@ -270,30 +270,44 @@ def sdpa_fwd_varlen(q, k, v, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k,
     return out, lse
 
 
-def sdpa_bwd_varlen_workspace_size(b, h, total_q) -> int:
-    return int(_native.lib().sdpa_bwd_varlen_workspace_size(b, h, total_q))
+def sdpa_bwd_varlen_workspace_size(b, h, total_q, d_qk=None, deterministic=False) -> int:
+    """Workspace bytes of the packed backward. Without d_qk: the row
+    statistics alone, which run the deterministic backward; with d_qk: the
+    bytes of the backward ``deterministic`` selects (the default one at
+    d_qk <= 128 adds its fp32 dQ accumulator)."""
+    if d_qk is None:
+        return int(_native.lib().sdpa_bwd_varlen_workspace_size(b, h, total_q))
+    return int(_native.lib().sdpa_bwd_varlen_workspace_size_ex(b, h, total_q, int(d_qk),
+                                                               int(bool(deterministic))))
 
 
 def sdpa_bwd_varlen(q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q, max_seqlen_k, *,
                     scale=None, is_causal=False, dropout_p=0.0, seed=0, offset=0, workspace=None,
                     dq=None, dk=None, dv=None, stream=None, window=None, bottom_right=False,
-                    alibi_slopes=None, dropout_mask=None):
+                    alibi_slopes=None, dropout_mask=None, deterministic=False):
     """Backward pass over packed sequences (layouts as sdpa_fwd_varlen).
-    Returns (dq, dk, dv) shaped like q, k, v."""
+    Returns (dq, dk, dv) shaped like q, k, v. deterministic=True runs the
+    deterministic backward, as sdpa_bwd."""
     return sdpa_bwd_phases_varlen(_native.SDPA_BWD_ALL, q, k, v, o, dout, lse, seqstart_q,
                                   seqstart_k, max_seqlen_q, max_seqlen_k, scale=scale,
                                   is_causal=is_causal, dropout_p=dropout_p, seed=seed,
                                   offset=offset, workspace=workspace, dq=dq, dk=dk, dv=dv,
                                   stream=stream, window=window, bottom_right=bottom_right,
-                                  alibi_slopes=alibi_slopes, dropout_mask=dropout_mask)
+                                  alibi_slopes=alibi_slopes, dropout_mask=dropout_mask,
+                                  deterministic=deterministic)
 
 
 def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k, max_seqlen_q,
                            max_seqlen_k, *, scale=None, is_causal=False, dropout_p=0.0, seed=0,
                            offset=0, workspace=None, dq=None, dk=None, dv=None, stream=None,
                            window=None, bottom_right=False, alibi_slopes=None,
-                           dropout_mask=None):
-    """The packed-sequence backward phases selected by ``phases``."""
+                           dropout_mask=None, deterministic=False):
+    """The packed-sequence backward phases selected by ``phases`` (the
+    SDPA_BWD_DETERMINISTIC bit, or deterministic=True, selects the
+    deterministic backward). A caller-given workspace smaller than the
+    default backward's size runs the deterministic one."""
+    deterministic = bool(deterministic) or bool(int(phases) & _native.SDPA_BWD_DETERMINISTIC)
+    phases = int(phases) | (_native.SDPA_BWD_DETERMINISTIC if deterministic else 0)
     h, total_q, d_qk = q.shape
     h_kv, total_k, d_v = k.shape[0], k.shape[1], v.shape[2]
     dt = q.dtype
@@ -311,7 +325,7 @@ def sdpa_bwd_phases_varlen(phases, q, k, v, o, dout, lse, seqstart_q, seqstart_k
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = sdpa_bwd_varlen_workspace_size(b, h, total_q)
+    need = sdpa_bwd_varlen_workspace_size(b, h, total_q, d_qk, deterministic)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     w = _window(is_causal, window, bottom_right, alibi_slopes, b, h, dropout_mask)

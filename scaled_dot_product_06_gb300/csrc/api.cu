@@ -377,12 +377,19 @@ size_t dq_acc_bytes(int64_t b, int64_t h, int64_t s_q, int64_t d_qk) {
 }
 
 // The fused backward (one key/value-stationary kernel that also accumulates
-// dQ) serves batch mode with d_qk <= 128 unless the caller asks for the
-// deterministic backward; tensor memory has no room for its dQ tile beside
-// dK at d_qk = 192, and the packed entry points size their workspace without
-// d_qk.
-bool use_fused(int phases, int64_t d_qk, const Packing& pk) {
-  return (phases & SDPA_BWD_DETERMINISTIC) == 0 && d_qk <= 128 && pk.seqstart_q == nullptr;
+// dQ) serves d_qk <= 128 unless the caller asks for the deterministic
+// backward; tensor memory has no room for its dQ tile beside dK at d_qk = 192.
+// (Packed calls also need a workspace with room for the accumulator; see
+// bwd_impl.)
+bool use_fused(int phases, int64_t d_qk) {
+  return (phases & SDPA_BWD_DETERMINISTIC) == 0 && d_qk <= 128;
+}
+
+// Bytes of the packed statistics: per head, each sequence's rows in a block
+// of its own (packed_stat_pad), two floats a row, rounded up to 256.
+size_t packed_stats_bytes(int64_t b, int64_t h, int64_t total_q) {
+  const size_t prows = static_cast<size_t>(h) * static_cast<size_t>(packed_stat_pad(total_q, b));
+  return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
 }
 
 sdpa_status_t fwd_impl(int64_t b, int64_t h, int64_t h_kv, int64_t s_q, int64_t s_kv, int64_t d_qk,
@@ -475,7 +482,6 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
                        const Packing& pk) {
   if ((phases & SDPA_BWD_ALL) == 0 || (phases & ~(SDPA_BWD_ALL | SDPA_BWD_DETERMINISTIC)) != 0)
     return fail(SDPA_ERR_INVALID_ARG, "phases");
-  const bool fused = use_fused(phases, d_qk, pk);
   bool empty = false;
   if (sdpa_status_t s = check_sizes(b, h, s_q, s_kv, d_qk, d_v, dropout_p, dtype, &empty)) return s;
   if (!scale_ok(scale)) return fail(SDPA_ERR_INVALID_ARG, "scale must be finite");
@@ -489,10 +495,14 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (bias && !aligned16(bias)) || (dbias && !aligned16(dbias)))
     return SDPA_ERR_MISALIGNED;
-  const size_t stat_bytes = pk.seqstart_q ? sdpa_bwd_varlen_workspace_size(b, h, pk.total_q)
-                                          : stats_bytes(b, h, s_q);
-  // the fused backward's fp32 dQ accumulator follows the statistics
-  const size_t need = stat_bytes + (fused ? dq_acc_bytes(b, h, s_q, d_qk) : 0);
+  const size_t stat_bytes = pk.seqstart_q ? packed_stats_bytes(b, h, pk.total_q) : stats_bytes(b, h, s_q);
+  // the fused backward's fp32 dQ accumulator follows the statistics (packed:
+  // per head, over the packed rows); a packed call whose workspace holds only
+  // the statistics runs the deterministic backward
+  const size_t acc_bytes = pk.seqstart_q ? dq_acc_bytes(1, h, pk.total_q, d_qk) : dq_acc_bytes(b, h, s_q, d_qk);
+  const bool fused = use_fused(phases, d_qk) &&
+                     (pk.seqstart_q == nullptr || workspace_bytes >= stat_bytes + acc_bytes);
+  const size_t need = stat_bytes + (fused ? acc_bytes : 0);
   if (workspace == nullptr || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SDPA_ERR_MISALIGNED;
   // A split dK/dV when the group is large for the grid and the workspace has
@@ -707,7 +717,7 @@ size_t sdpa_bwd_workspace_size_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_
   if (!kv_heads_ok(h, h_kv)) return 0;
   const int phases = SDPA_BWD_ALL | (deterministic ? SDPA_BWD_DETERMINISTIC : 0);
   const size_t base = stats_bytes(b, h, s_q) +
-                      (use_fused(phases, d_qk, Packing{}) ? dq_acc_bytes(b, h, s_q, d_qk) : 0);
+                      (use_fused(phases, d_qk) ? dq_acc_bytes(b, h, s_q, d_qk) : 0);
   return base + split_bytes(b, h, h_kv, s_kv, d_qk, d_v);
 }
 
@@ -748,8 +758,16 @@ sdpa_status_t sdpa_bwd_phases_gqa(int phases, int64_t b, int64_t h, int64_t h_kv
 // the place of s_q / s_kv.
 size_t sdpa_bwd_varlen_workspace_size(int64_t b, int64_t h, int64_t total_q) {
   if (b < 0 || h < 0 || total_q < 0 || total_q > kMaxSeq || b > (int64_t{1} << 24)) return 0;
-  const size_t prows = static_cast<size_t>(h) * static_cast<size_t>(packed_stat_pad(total_q, b));
-  return (prows * 2 * sizeof(float) + 255) & ~size_t(255);
+  return packed_stats_bytes(b, h, total_q);
+}
+
+size_t sdpa_bwd_varlen_workspace_size_ex(int64_t b, int64_t h, int64_t total_q, int64_t d_qk,
+                                         int deterministic) {
+  if (h > (int64_t{1} << 24) || (d_qk != 64 && d_qk != 128 && d_qk != 192)) return 0;
+  const size_t base = sdpa_bwd_varlen_workspace_size(b, h, total_q);
+  if (base == 0) return 0;
+  const int phases = SDPA_BWD_ALL | (deterministic ? SDPA_BWD_DETERMINISTIC : 0);
+  return base + (use_fused(phases, d_qk) ? dq_acc_bytes(1, h, total_q, d_qk) : 0);
 }
 
 sdpa_status_t sdpa_fwd_varlen(int64_t b, int64_t h, int64_t h_kv, int64_t total_q, int64_t total_k,

@@ -185,6 +185,18 @@ def test_varlen_workspace_size(lib):
         assert lib.sdpa_bwd_varlen_workspace_size(b, h, tq) == expect(b, h, tq)
     assert lib.sdpa_bwd_varlen_workspace_size(-1, 2, 10) == 0
     assert lib.sdpa_bwd_varlen_workspace_size(2, 2, -10) == 0
+    # the default backward at d_qk <= 128 adds its fp32 dQ accumulator over
+    # the packed rows (per head, rows padded to 128); deterministic and d_qk =
+    # 192 need the statistics alone
+    for b, h, tq in ((1, 1, 1), (3, 4, 1000), (16, 32, 65536)):
+        for d in (64, 128):
+            acc = h * ((tq + 127) // 128) * 128 * d * 4
+            assert lib.sdpa_bwd_varlen_workspace_size_ex(b, h, tq, d, 0) == expect(b, h, tq) + acc
+            assert lib.sdpa_bwd_varlen_workspace_size_ex(b, h, tq, d, 1) == expect(b, h, tq)
+        assert lib.sdpa_bwd_varlen_workspace_size_ex(b, h, tq, 192, 0) == expect(b, h, tq)
+    assert lib.sdpa_bwd_varlen_workspace_size_ex(2, 2, 10, 96, 0) == 0
+    assert lib.sdpa_bwd_varlen_workspace_size_ex(-1, 2, 10, 64, 0) == 0
+    assert lib.sdpa_bwd_varlen_workspace_size_ex(2, 1 << 25, 10, 64, 0) == 0
 
 
 def test_varlen_arguments_validated_before_any_device_work(lib):

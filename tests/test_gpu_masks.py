@@ -90,7 +90,8 @@ def test_window_with_negative_or_zero_scale(scale):
     assert_close("dv", dv, dv_r)
 
 
-def test_packed_window_bottom_right_matches_oracle():
+@pytest.mark.parametrize("deterministic", [False, True], ids=["fused", "deterministic"])
+def test_packed_window_bottom_right_matches_oracle(deterministic):
     lq, lk = (100, 300, 7, 256), (200, 150, 64, 256)
     H, H_kv, D = 4, 2, 128
     win, br = (50, 10), True
@@ -104,7 +105,8 @@ def test_packed_window_bottom_right_matches_oracle():
     sk = torch.tensor(seqstarts(lk), dtype=torch.int32, device=dev)
     kw = dict(scale=scale, window=win, bottom_right=br)
     o, lse = sdpa_fwd_varlen(q, k, v, sq, sk, max(lq), max(lk), **kw)
-    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, sq, sk, max(lq), max(lk), **kw)
+    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, sq, sk, max(lq), max(lk),
+                                 deterministic=deterministic, **kw)
     torch.cuda.synchronize()
     assert sdpa_device_error() == 0
     o_ref, lse_ref = ovl.forward(pk, x["q"], x["k"], x["v"])
@@ -201,7 +203,8 @@ def test_alibi_matches_oracle(c):
     assert_close("dv", dv, dv_r)
 
 
-def test_packed_alibi_causal_matches_oracle():
+@pytest.mark.parametrize("deterministic", [False, True], ids=["fused", "deterministic"])
+def test_packed_alibi_causal_matches_oracle(deterministic):
     lq = lk = (130, 257, 64)
     H, D = 4, 128
     sl = np.array([[s * (i + 1) for s in alibi_slopes(H)] for i in range(3)], dtype=np.float32)
@@ -213,7 +216,8 @@ def test_packed_alibi_causal_matches_oracle():
     st = torch.tensor(seqstarts(lq), dtype=torch.int32, device="cuda")
     kw = dict(scale=scale, is_causal=True, alibi_slopes=torch.tensor(sl, device="cuda"))
     o, lse = sdpa_fwd_varlen(q, k, v, st, st, max(lq), max(lk), **kw)
-    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, st, st, max(lq), max(lk), **kw)
+    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, st, st, max(lq), max(lk),
+                                 deterministic=deterministic, **kw)
     torch.cuda.synchronize()
     assert sdpa_device_error() == 0
     o_ref, lse_ref = ovl.forward(pk, x["q"], x["k"], x["v"])

@@ -4,7 +4,9 @@ its bitwise agreement with batch mode when every sequence has the same length.
 
 Cases cover ragged lengths with tails inside a tile, cross-attention lengths,
 grouped and single K/V heads, dropout with max lengths above the real ones,
-sequences without queries or without keys, d 64 / 128 / 192, bf16 and fp16.
+sequences without queries or without keys, d 64 / 128 / 192, bf16 and fp16,
+through both backwards (the default fused one, whose fp32 dQ accumulator spans
+the packed rows, and the deterministic one).
 """
 from __future__ import annotations
 
@@ -55,7 +57,7 @@ class VCase:
                           mq, mk)
 
 
-def run_varlen(c: VCase, x: dict):
+def run_varlen(c: VCase, x: dict, deterministic=False):
     dev = "cuda"
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     sq = torch.tensor(seqstarts(c.lq), dtype=torch.int32, device=dev)
@@ -63,7 +65,8 @@ def run_varlen(c: VCase, x: dict):
     mq, mk = c.maxes
     kw = dict(scale=c.sc, is_causal=c.causal, dropout_p=c.p, seed=c.seed, offset=c.offset)
     o, lse = sdpa_fwd_varlen(q, k, v, sq, sk, mq, mk, **kw)
-    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, sq, sk, mq, mk, **kw)
+    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, sq, sk, mq, mk, deterministic=deterministic,
+                                 **kw)
     torch.cuda.synchronize()
     assert sdpa_device_error() == 0, "a kernel wait ran out"
     return o, lse, dq, dk, dv
@@ -79,13 +82,14 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("deterministic", [False, True], ids=["fused", "deterministic"])
 @pytest.mark.parametrize("c", CASES, ids=lambda c: f"H{c.H}kv{c.H_kv}-d{c.D_qk}-{c.dtype}"
                          f"{'-causal' if c.causal else ''}{'-p' + str(c.p) if c.p else ''}-"
                          f"{len(c.lq)}seq")
-def test_varlen_matches_oracle(c):
+def test_varlen_matches_oracle(c, deterministic):
     pk = c.packed()
     x = make_packed_inputs(c.H, sum(c.lq), sum(c.lk), c.D_qk, c.D_v, c.dtype, c.H_kv)
-    o, lse, dq, dk, dv = run_varlen(c, x)
+    o, lse, dq, dk, dv = run_varlen(c, x, deterministic)
     o_ref, lse_ref = ovl.forward(pk, x["q"], x["k"], x["v"])
     assert_close("o", o, o_ref)
     assert_lse(lse, lse_ref)
@@ -95,40 +99,45 @@ def test_varlen_matches_oracle(c):
     assert_close("dv", dv, dv_ref)
 
 
+@pytest.mark.parametrize("deterministic", [False, True], ids=["fused", "deterministic"])
 @pytest.mark.parametrize("p", [0.0, 0.15])
-def test_uniform_lengths_bitwise_equal_batch_mode(p):
+def test_uniform_lengths_bitwise_equal_batch_mode(p, deterministic):
     """Equal lengths: the packed path computes exactly the batch-mode numbers
-    (same tiles, same accumulation order, same dropout bits)."""
+    (same tiles, same accumulation order, same dropout bits); the fused
+    backward's dQ within fp32 summation order (its reductions add in arrival
+    order)."""
     B, H, S, D = 3, 4, 384, 128
     c = VCase(H, (S,) * B, (S,) * B, D, D, causal=True, p=p)
     x = make_packed_inputs(H, B * S, B * S, D, D)
-    o, lse, dq, dk, dv = run_varlen(c, x)
+    o, lse, dq, dk, dv = run_varlen(c, x, deterministic)
     to_b = lambda t: t.reshape(t.shape[0], B, S, t.shape[-1]).transpose(0, 1).contiguous().cuda()
     kw = dict(scale=c.sc, is_causal=True, dropout_p=p, seed=c.seed, offset=c.offset)
     qb, kb, vb, dob = (to_b(x[n]) for n in ("q", "k", "v", "do"))
     ob, lseb = sdpa_fwd(qb, kb, vb, **kw)
-    # packed sequences run the deterministic backward; batch mode matches it
-    dqb, dkb, dvb, _ = sdpa_bwd(qb, kb, vb, ob, dob, lseb, deterministic=True, **kw)
+    dqb, dkb, dvb, _ = sdpa_bwd(qb, kb, vb, ob, dob, lseb, deterministic=deterministic, **kw)
     torch.cuda.synchronize()
     from_b = lambda t: t.transpose(0, 1).reshape(t.shape[1], B * S, t.shape[-1])
     assert torch.equal(from_b(ob), o)
     assert torch.equal(lseb.transpose(0, 1).reshape(H, B * S), lse)
-    assert torch.equal(from_b(dqb), dq)
+    if deterministic:
+        assert torch.equal(from_b(dqb), dq)
+    else:
+        assert_close("dq packed vs batch", dq, from_b(dqb).double().cpu().numpy(), rel=1e-2)
     assert torch.equal(from_b(dkb), dk)
     assert torch.equal(from_b(dvb), dv)
 
 
 def test_packed_h32_d128_causal_16_sequences_sampled():
     """The packed-sequence workload the benchmark times (16 sequences of
-    512..8192 tokens, 32 heads, d 128, causal): two sequences checked on
-    sampled rows and key columns of one head, the others through the key-sum
-    invariants (dK sums to 0 over each sequence's keys, dV to the sequence's
-    query-sum of dO)."""
+    512..8192 tokens, 32 heads, d 128, causal), through the fused and the
+    deterministic backward: two sequences checked on sampled rows and key
+    columns of one head, the others through the key-sum invariants (dK sums to
+    0 over each sequence's keys, dV to the sequence's query-sum of dO)."""
     lens = tuple(packed_lengths(16, 512, 8192, seed=2024))
     c = VCase(32, lens, lens, 128, 128, causal=True)
     pk = c.packed()
     x = make_packed_inputs(32, sum(lens), sum(lens), 128, 128)
-    o, lse, dq, dk, dv = run_varlen(c, x)
+    runs = {"fused": run_varlen(c, x), "deterministic": run_varlen(c, x, deterministic=True)}
     rng = np.random.default_rng(9)
     for i, h in ((int(np.argmax(lens)), 5), (3, 30)):
         pr = pk.sequence(i)
@@ -139,23 +148,32 @@ def test_packed_h32_d128_causal_16_sequences_sampled():
                                          rng.integers(0, n, 40)]))
         cols = np.unique(np.concatenate([np.arange(min(n, 24)), np.arange(max(0, n - 24), n),
                                          rng.integers(0, n, 24)]))
-        r_t, c_t = (torch.as_tensor(a + r, device=o.device) for r in (rows, cols))
         o_ref, lse_ref = oracle.forward_head(pr, 0, h, xs["q"], xs["k"], xs["v"], rows=rows)
-        assert_close(f"o seq {i}", o[h][r_t], o_ref)
-        assert_lse(lse[h][r_t], lse_ref)
         dq_r, dk_c, dv_c, _ = oracle.backward_head(pr, 0, h, xs["q"], xs["k"], xs["v"], xs["do"],
                                                    rows=rows, cols=cols, row_chunk=2048)
-        assert_close(f"dq seq {i}", dq[h][r_t], dq_r)
-        assert_close(f"dk seq {i}", dk[h][c_t], dk_c)
-        assert_close(f"dv seq {i}", dv[h][c_t], dv_c)
+        for tag, (o, lse, dq, dk, dv) in runs.items():
+            r_t, c_t = (torch.as_tensor(a + r, device=o.device) for r in (rows, cols))
+            assert_close(f"o seq {i}", o[h][r_t], o_ref)
+            assert_lse(lse[h][r_t], lse_ref)
+            assert_close(f"dq seq {i} ({tag})", dq[h][r_t], dq_r)
+            assert_close(f"dk seq {i} ({tag})", dk[h][c_t], dk_c)
+            assert_close(f"dv seq {i} ({tag})", dv[h][c_t], dv_c)
     starts = pk.seqstart_q
-    for i in range(16):
-        a, b = starts[i], starts[i + 1]
-        dk64 = dk[:, a:b].double()
-        rel = dk64.sum(dim=1).abs().max().item() / dk64.abs().sum(dim=1).max().item()
-        assert rel < 2e-2, f"sequence {i}: key-sum of dK is not ~0 (relative {rel:.3e})"
-        assert_close(f"sum_j dV seq {i}", dv[:, a:b].double().sum(dim=1).cpu(),
-                     x["do"][:, a:b].double().sum(dim=1).numpy(), rel=3e-2)
+    for tag, (o, lse, dq, dk, dv) in runs.items():
+        for i in range(16):
+            a, b = starts[i], starts[i + 1]
+            dk64 = dk[:, a:b].double()
+            rel = dk64.sum(dim=1).abs().max().item() / dk64.abs().sum(dim=1).max().item()
+            assert rel < 2e-2, f"{tag}, sequence {i}: key-sum of dK is not ~0 (relative {rel:.3e})"
+            assert_close(f"sum_j dV seq {i} ({tag})", dv[:, a:b].double().sum(dim=1).cpu(),
+                         x["do"][:, a:b].double().sum(dim=1).numpy(), rel=3e-2)
+    # the two backwards agree on every element, within the bf16 rounding of
+    # the outputs
+    f, d = runs["fused"], runs["deterministic"]
+    for name, k in (("dq", 2), ("dk", 3), ("dv", 4)):
+        diff = (f[k].float() - d[k].float()).abs().max().item()
+        top = d[k].float().abs().max().item()
+        assert diff <= 1e-2 * top, f"{name}: fused vs deterministic max|diff| {diff:.3e} (max {top:.3e})"
 
 
 def test_packed_dropout_bits_drawn_beforehand_give_the_same_bits():
@@ -175,6 +193,15 @@ def test_packed_dropout_bits_drawn_beforehand_give_the_same_bits():
               dropout_mask=mask)
     o, lse = sdpa_fwd_varlen(q, k, v, sq, sk, mq, mk, **kw)
     dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, sq, sk, mq, mk, **kw)
+    torch.cuda.synchronize()
+    for name, x1, x2 in zip(("o", "lse", "dq", "dk", "dv"), a, (o, lse, dq, dk, dv)):
+        if name == "dq":  # the fused backward's reductions add in arrival order
+            assert_close("dq drawn vs given bits", x2, x1.double().cpu().numpy(), rel=1e-2)
+        else:
+            assert torch.equal(x1, x2), name
+    # the deterministic backward: every result bitwise
+    a = run_varlen(c, x, deterministic=True)
+    dq, dk, dv = sdpa_bwd_varlen(q, k, v, o, do, lse, sq, sk, mq, mk, deterministic=True, **kw)
     torch.cuda.synchronize()
     for x1, x2 in zip(a, (o, lse, dq, dk, dv)):
         assert torch.equal(x1, x2)
