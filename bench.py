@@ -384,7 +384,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--cpu-sample", type=int, default=16384,
                     help="query positions of the one-head oracle sample (cpu_baseline); the "
                          "default is a whole head of the long-context workload, ~15 s of CPU")
@@ -781,7 +781,11 @@ def main():
     # back its results. Two sets of device tensors and two copy streams let the
     # upload of step n+1 and the read-back of step n-1 overlap step n's
     # compute, the way a serving loop would run; each step still moves all its
-    # bytes through the host link.
+    # bytes through the host link. A set's inputs are refilled once the step
+    # two back has read them (its kernels are done), and its outputs are
+    # rewritten once that step's read-back is done, so an upload and a
+    # read-back need not follow one another within one step's compute. The
+    # first upload and the last read-back are inside the timed region too.
     e2e = None
     if args.e2e_steps > 0:
         in_names = ["q", "k", "v", "do"] + (["bias"] if bias is not None else [])
@@ -806,12 +810,14 @@ def main():
             D = sets[i % 2]
             with torch.cuda.stream(s_in):
                 if i >= 2:
-                    s_in.wait_event(ev_out[i - 2])  # step i-2 read back from this set
+                    s_in.wait_event(ev_cmp[i - 2])  # step i-2's kernels have read this set's inputs
                 for n in in_names:
                     D[n].copy_(hin[n], non_blocking=True)
                 ev_in[i].record(s_in)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in[i])
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[i - 2])  # step i-2's results are read back from this set
                 if mask_words:
                     sdpa_dropout_mask(w["B"], w["H"], w["S_q"], w["S_kv"], w["p"], DROP_SEED,
                                       DROP_OFFSET, out=kw["dropout_mask"], stream=s_cmp)

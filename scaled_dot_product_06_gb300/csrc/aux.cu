@@ -102,34 +102,41 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const uint4* __res
   for (int64_t i = tid; i < dq_acc_vec; i += nthreads) dq_acc[i] = z;    // fused dQ accumulator
 }
 
-// dQ = scale * dQacc in the io dtype: one thread per (z, row, 8 columns); the
-// threads of a warp take 32 consecutive rows of one 8-column block, so each of
-// their two 16-byte accumulator reads is one 512-byte run of the tiled layout
-// (dq_acc_index: per z and 128-row tile, per group of 4 columns, 128 rows of
-// 16 bytes).
-template <bool BF16>
+// dQ = scale * dQacc in the io dtype, transposed through shared memory so
+// that both sides move whole lines: a block takes one 32-row slab of a
+// 128-row tile of one z at a time, reads its D/4 column groups (each a
+// 512-byte run of the tiled layout of dq_acc_index: per z and tile, per group
+// of 4 columns, 128 rows of 16 bytes; one warp a run) into a row-major
+// shared buffer, then writes whole dQ rows of the slab, D/8 consecutive
+// threads a row, 16 bytes each.
+template <bool BF16, int D>
 __global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const float4* __restrict__ acc,
                                                                  uint4* __restrict__ dq, int64_t z_count,
-                                                                 int rows, int dq_tiles, int d,
-                                                                 float scale) {
-  const int c8n = d / 8;  // 8-column blocks per row
-  const int64_t per_z = static_cast<int64_t>(dq_tiles) * 128 * c8n;
-  const int64_t total = z_count * per_z;
-  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += nthreads) {
-    const int64_t z = t / per_z;
-    const int64_t r0 = t - z * per_z;
-    const int tile = static_cast<int>(r0 / (128 * c8n));
-    const int r1 = static_cast<int>(r0 - static_cast<int64_t>(tile) * 128 * c8n);
-    const int c8 = r1 / 128, rr = r1 % 128;
-    const int row = tile * 128 + rr;
-    if (row >= rows) continue;
-    // groups 2 c8 and 2 c8 + 1 of the row, 128 rows apart in float4 units
-    const int64_t g0 = ((z * dq_tiles + tile) * (d / 4) + 2 * c8) * 128 + rr;
-    const float4 a = acc[g0], b = acc[g0 + 128];
-    dq[(z * rows + row) * c8n + c8] =
-        make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
-                   pack2<BF16>(b.x * scale, b.y * scale), pack2<BF16>(b.z * scale, b.w * scale));
+                                                                 int rows, int dq_tiles, float scale) {
+  constexpr int G = D / 4;      // float4 column groups a row
+  constexpr int LDV = G + 1;    // shared row stride in float4: 8 consecutive rows hit all 32 banks
+  constexpr int C8 = D / 8;     // 16-byte output chunks a row
+  __shared__ float4 slab_buf[32 * LDV];
+  const int64_t n_slabs = z_count * dq_tiles * 4;
+  for (int64_t sl = blockIdx.x; sl < n_slabs; sl += gridDim.x) {  // uniform over the block
+    const int64_t zt = sl >> 2;  // z * dq_tiles + tile
+    const int64_t z = zt / dq_tiles;
+    const int row0 = static_cast<int>(zt - z * dq_tiles) * 128 + static_cast<int>(sl & 3) * 32;
+    const float4* src = acc + zt * G * 128 + (sl & 3) * 32;
+#pragma unroll
+    for (int i = threadIdx.x; i < G * 32; i += kAuxThreads) slab_buf[(i & 31) * LDV + (i >> 5)] = src[(i >> 5) * 128 + (i & 31)];
+    __syncthreads();
+#pragma unroll
+    for (int i = threadIdx.x; i < 32 * C8; i += kAuxThreads) {
+      const int r = i / C8, c8 = i % C8;
+      if (row0 + r < rows) {
+        const float4 a = slab_buf[r * LDV + 2 * c8], b = slab_buf[r * LDV + 2 * c8 + 1];
+        dq[(z * rows + row0 + r) * C8 + c8] =
+            make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
+                       pack2<BF16>(b.x * scale, b.y * scale), pack2<BF16>(b.z * scale, b.w * scale));
+      }
+    }
+    __syncthreads();  // the buffer is read before the next slab overwrites it
   }
 }
 
@@ -175,11 +182,14 @@ cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const flo
 
 cudaError_t launch_dq_convert(bool bf16, const float* dq_acc, void* dq, int64_t z_count, int rows,
                               int dq_tiles, int d_qk, float scale, cudaStream_t st) {
-  const int64_t work = z_count * dq_tiles * 128 * (d_qk / 8);
-  auto kern = bf16 ? dq_convert_kernel<true> : dq_convert_kernel<false>;
-  kern<<<aux_grid(work), kAuxThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
-                                               static_cast<uint4*>(dq), z_count, rows, dq_tiles,
-                                               d_qk, scale);
+  const int64_t slabs = z_count * dq_tiles * 4;
+  const int grid = static_cast<int>(slabs < 152 * 8 ? slabs : 152 * 8);  // 8 resident blocks an SM
+  auto kern = d_qk == 64 ? (bf16 ? dq_convert_kernel<true, 64> : dq_convert_kernel<false, 64>)
+                         : (bf16 ? dq_convert_kernel<true, 128> : dq_convert_kernel<false, 128>);
+  if (d_qk != 64 && d_qk != 128) return cudaErrorInvalidValue;
+  if (slabs == 0) return cudaSuccess;
+  kern<<<grid, kAuxThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc), static_cast<uint4*>(dq),
+                                     z_count, rows, dq_tiles, scale);
   return cudaGetLastError();
 }
 
