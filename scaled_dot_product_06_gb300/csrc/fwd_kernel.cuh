@@ -408,23 +408,37 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!(ok = mbar_wait(bar(FB_S + t), c & 1, ec, kSiteFwdSoftmax))) break;
       tc_fence_after();
+      if constexpr (GENERAL) {
+        // a quarter at a time (the scores join the bias values held in x)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t rr[32];
-        tmem_ld32(tS + lane_off + q * 32, rr);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t rr[32];
+          tmem_ld32(tS + lane_off + q * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t s2 = f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+            float2 v;
+            if (bias_row != nullptr)
+              v = f2split(fma2(s2, sl22, mul2(f2(x[q * 32 + 2 * i], x[q * 32 + 2 * i + 1]), f2(kLog2e, kLog2e))));
+            else
+              v = f2split(mul2(s2, sl22));
+            x[q * 32 + 2 * i] = v.x;
+            x[q * 32 + 2 * i + 1] = v.y;
+          }
+        }
+      } else {
+        // the four quarters' loads in flight together, one wait
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32f(tS + lane_off + q * 32, x + q * 32);
         tmem_wait_ld();
+        if constexpr (!RAW) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t s2 = f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
-          float2 v;
-          if (GENERAL && bias_row != nullptr)
-            v = f2split(fma2(s2, sl22, mul2(f2(x[q * 32 + 2 * i], x[q * 32 + 2 * i + 1]), f2(kLog2e, kLog2e))));
-          else if (!RAW)
-            v = f2split(mul2(s2, sl22));
-          else
-            v = f2split(s2);
-          x[q * 32 + 2 * i] = v.x;
-          x[q * 32 + 2 * i + 1] = v.y;
+          for (int i = 0; i < 128; i += 2) {
+            const float2 v = f2split(mul2(f2(x[i], x[i + 1]), sl22));
+            x[i] = v.x;
+            x[i + 1] = v.y;
+          }
         }
       }
       if constexpr (WIN && !RAW) {
