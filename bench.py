@@ -501,6 +501,11 @@ def main():
     # --deterministic) the dK/dV and dQ kernels run concurrently after the
     # preprocess.
     fused = not args.deterministic and w["D_qk"] <= 128
+    # With one key tile that every query tile meets (here: s_kv <= 128 under a
+    # plain mask, no grouped heads) the fused kernel writes dQ itself: no
+    # accumulator, no convert pass (sdpa_bwd decides the same way).
+    direct = (fused and not packed and w["S_kv"] <= 128 and w.get("window") is None
+              and not w.get("bottom_right") and w.get("H_kv", w["H"]) == w["H"])
     q, k, v, do, bias = x["q"], x["k"], x["v"], x["do"], x["bias"]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
@@ -717,6 +722,8 @@ def main():
     if fused:
         per_kernel = {{"bwd_dkdv": "bwd_fused", "bwd_dq": "dq_convert"}.get(n, n): t
                       for n, t in per_kernel.items()}
+        if direct:  # the DQ phase launches nothing
+            per_kernel.pop("dq_convert")
 
     # algorithmic FLOPs per launch: the dK/dV kernel forms S^T, dP^T, dV, dK
     # (2x the forward), the fused one dQ as well; the deterministic dQ
@@ -729,6 +736,9 @@ def main():
     else:
         kernel_flops = {"fwd": ff, "bwd_dkdv": 2.0 * ff, "bwd_dq": dq_share}
     kbytes = kernel_bytes(w, fused)
+    if direct:  # the fused kernel writes dQ; no accumulator
+        kbytes["bwd_fused"] += kbytes.pop("dq_convert") - (
+            w["B"] * w["H"] * ((w["S_q"] + 127) // 128) * 128 * w["D_qk"] * 4)
     # Philox4x32-10 blocks (four elements each) a kernel draws per launch:
     # every visible element once in the forward and, unless the forward
     # recorded its keep bits for it, once in the main backward kernel(s)
@@ -862,7 +872,10 @@ def main():
                 kt[n]["hbm_frac"] = gbs / hbm
             if kernel_blocks.get(n):
                 kt[n]["philox_gblocks_per_s"] = kernel_blocks[n] / (t * 1e-3) / 1e9
-        if fused:
+        if fused and direct:
+            kt["bwd_fused"]["note"] = ("fused key/value-stationary kernel: S^T, dP^T, dV, dK and dQ "
+                                       "(one key tile: dQ written directly, no convert pass)")
+        elif fused:
             kt["bwd_fused"]["note"] = ("fused key/value-stationary kernel: S^T, dP^T, dV, dK and dQ "
                                        "(fp32 reductions into the workspace accumulator)")
             kt["dq_convert"]["note"] = "dQ = scale * dQacc convert pass"
@@ -905,9 +918,9 @@ def main():
             # per step: forward, preprocess, two backward kernels, plus the keep
             # bits' kernel where the step draws them beforehand or the forward
             # draws its record with it (no mask)
-            "gpu_launches": (5 if (mask_words or (record_words and not w["causal"]
-                                                  and w.get("window") is None))
-                             else 4) * args.steps,
+            "gpu_launches": ((5 if (mask_words or (record_words and not w["causal"]
+                                                   and w.get("window") is None))
+                              else 4) - (1 if direct else 0)) * args.steps,
         }
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -118,12 +118,15 @@ size_t sdpa_bwd_workspace_size_ex(int64_t b, int64_t h, int64_t h_kv, int64_t s_
  *   workspace caller-owned device memory of at least
  *             sdpa_bwd_workspace_size(...) bytes, 256-byte aligned; its
  *             contents on entry are ignored and on exit are unspecified.
- * Runs three kernels on `stream`. At d_qk <= 128 (the default backward):
+ * Runs up to three kernels on `stream`. At d_qk <= 128 (the default backward):
  * preprocess (row statistics; zero dBias and the dQ accumulator), one
  * key/value-stationary kernel that forms every product of each (query tile,
  * key tile) pair once (dK, dV, dBias, and dQ added into the fp32 accumulator
  * with fp32 reductions, as CK tile's FmhaBwdDQDKDVKernel and oneDNN's backward
- * kernel do), and a convert pass dQ = scale * dQacc. dK and dV are bitwise
+ * kernel do), and a convert pass dQ = scale * dQacc (with s_kv <= 128 under a
+ * mask where every query tile meets the one key tile, and no split of
+ * grouped heads, the kernel writes dQ itself: two kernels, dQ reproducible
+ * too). dK and dV are bitwise
  * reproducible; dQ's fp32 sums depend on the order the reductions arrive in
  * (results of two calls may differ in the last bits), as does dBias for
  * b > 2. At d_qk = 192, and with SDPA_BWD_DETERMINISTIC, the deterministic

@@ -548,11 +548,26 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
   p.rows_q = static_cast<int>(rw.q);
   p.rows_k = static_cast<int>(rw.k);
   p.kv_split = static_cast<int>(kv_split);
-  if (fused) {
+  // One key tile per (b, h) that every query tile meets (the tile range the
+  // fused kernel walks for key tile 0 covers them all): each dQ row then has
+  // a single contribution, written directly, and the accumulator, its zeroing
+  // and the convert pass drop out. Batch mode only (packed lengths live on
+  // the device), and not with split key tiles (whose drain warps hold 24
+  // registers).
+  bool dq_direct = false;
+  if (fused && pk.seqstart_q == nullptr && s_kv <= 128 && kv_split <= 1) {
+    const bool win = p.win_general || p.alibi != nullptr;  // the kernel instance's band
+    const sdpa::Band bd = win ? sdpa::band_of(p.win_left, p.win_right, p.win_br, p.S_q, p.S_kv)
+                              : sdpa::plain_band(p.win_right);
+    const sdpa::TileRange r = sdpa::query_tiles_of_keys(win, bd, p.win_right, 0, 128, 128, p.S_q, p.S_kv);
+    dq_direct = r.lo == 0 && r.hi == (p.S_q + 127) / 128 - 1;
+  }
+  p.dq_direct = dq_direct ? 1 : 0;
+  if (fused && !dq_direct) {
     p.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + stat_bytes);
     p.dq_tiles = static_cast<int>((rw.q + 127) / 128);
   }
-  const int64_t dq_acc_elems = fused ? rw.zq * p.dq_tiles * 128 * d_qk : 0;
+  const int64_t dq_acc_elems = (fused && !dq_direct) ? rw.zq * p.dq_tiles * 128 * d_qk : 0;
   const int n_counters = kv_split > 1 ? static_cast<int>(((s_kv + 127) / 128) * b * h_kv) : 0;
   if (kv_split > 1) {
     uint8_t* extra = static_cast<uint8_t*>(workspace) + need;
@@ -610,8 +625,10 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
     }
   }
   if ((phases & SDPA_BWD_DQ) && fused) {  // dQ = scale * dQacc in the io dtype
-    e = launch_dq_convert(bf16, p.dq_acc, dq, rw.zq, static_cast<int>(rw.q), p.dq_tiles, di, scale, st);
-    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dQ convert launch", e);
+    if (!dq_direct) {
+      e = launch_dq_convert(bf16, p.dq_acc, dq, rw.zq, static_cast<int>(rw.q), p.dq_tiles, di, scale, st);
+      if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "backward dQ convert launch", e);
+    }
   } else if (phases & SDPA_BWD_DQ) {
     CUtensorMap mq, mk, mv, mdo;
     sdpa_status_t ms = make_map(&mq, tt, 2, q, d_qk, rw.q, rw.zq, 128, true);

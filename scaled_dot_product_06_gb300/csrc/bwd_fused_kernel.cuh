@@ -235,8 +235,32 @@ __global__ void __launch_bounds__(FusedCfg<DQK, DV>::THREADS, 1)
       tc_fence_after();
       const int qr = qtile0(i) + (warp & 3) * 32 + lane;  // local query row
       const bool live = qr < S_q;
-      float* dst = p.dq_acc + dq_acc_index(static_cast<size_t>(sl.zq0 + qhead(i)), p.dq_tiles, DQK,
-                                           sl.row_q + (live ? qr : 0), 0);
+      const int zr = sl.row_q + (live ? qr : 0);  // tensor row of the query
+      if (!SPLIT && p.dq_direct) {  // the row's only contribution: dQ = scale * dQ_i, written out
+        uint8_t* drow = static_cast<uint8_t*>(p.dq) +
+                        (static_cast<size_t>(sl.zq0 + qhead(i)) * p.rows_q + zr) * DQK * 2;
+#pragma unroll 1
+        for (int c = 0; c < DQK / 16; ++c) {
+          uint32_t a[16];
+          tmem_ld16(tbase + C::T_DQ + lane_off + 16 * c, a);
+          tmem_wait_ld();
+          if (c == DQK / 16 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(FB_DQFREE));
+          }
+          if (live) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
+            uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+        continue;
+      }
+      float* dst = p.dq_acc + dq_acc_index(static_cast<size_t>(sl.zq0 + qhead(i)), p.dq_tiles, DQK, zr, 0);
 #pragma unroll 1
       for (int c = 0; c < DQK / 16; ++c) {
         uint32_t a[16];

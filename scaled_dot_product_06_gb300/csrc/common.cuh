@@ -297,6 +297,10 @@ struct BwdParams {
   // dq_acc_index): dq_tiles 128-row tiles per tensor-map z; null otherwise.
   float* dq_acc;
   int dq_tiles;
+  // fused backward with one key tile per (b, h) that every query tile meets:
+  // each dQ row has one contribution, which the drain writes to dq directly
+  // (scaled, in the io dtype) with no accumulator and no convert pass
+  int dq_direct;
 };
 
 // ---------------------------------------------------------------- Philox4x32-10

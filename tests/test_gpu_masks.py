@@ -29,6 +29,11 @@ CASES = [
     (1, 2, 1, 384, 384, 64, 64, "bf16", (1, 0), False, 0.0, False),       # two keys per row
     (2, 2, 2, 512, 512, 128, 128, "bf16", (256, 32), False, 0.0, True),   # window and bias
     (1, 2, 2, 333, 1000, 128, 128, "bf16", (130, 130), True, 0.0, False), # ragged, bottom-right
+    # one key tile: query tiles without keys keep the accumulator path (dQ = 0
+    # there); a window every query tile meets takes the direct dQ write
+    (1, 2, 2, 300, 100, 128, 128, "bf16", (-1, 0), True, 0.0, False),     # bottom-right, s_kv < 128
+    (1, 2, 2, 260, 128, 64, 64, "bf16", (40, 0), False, 0.0, False),      # late rows see no key
+    (1, 2, 2, 200, 128, 64, 64, "bf16", (300, 0), False, 0.0, True),      # wide window, bias
 ]
 
 

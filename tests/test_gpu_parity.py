@@ -43,6 +43,12 @@ CASES = [
     Case(1, 2, 300, 300, 128, 128, causal=True, scale=-0.09),
     Case(1, 1, 200, 260, 64, 64, scale=-0.125, dtype="fp16"),
     Case(1, 2, 256, 300, 128, 128, causal=True, scale=0.0),
+    # one key tile that every query tile meets: the fused kernel writes dQ
+    # directly (no accumulator, no convert pass)
+    Case(2, 2, 300, 100, 128, 128),
+    Case(1, 3, 200, 128, 64, 64, causal=True, p=0.1, dtype="fp16"),
+    Case(2, 2, 256, 64, 128, 128, causal=True, bias=True),
+    Case(1, 4, 130, 96, 128, 128, H_kv=2),
 ]
 
 
