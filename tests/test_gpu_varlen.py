@@ -205,3 +205,26 @@ def test_packed_dropout_bits_drawn_beforehand_give_the_same_bits():
     torch.cuda.synchronize()
     for x1, x2 in zip(a, (o, lse, dq, dk, dv)):
         assert torch.equal(x1, x2)
+
+
+def test_statistics_only_workspace_runs_the_deterministic_backward():
+    """A caller's workspace of sdpa_bwd_varlen_workspace_size(b, h, total_q)
+    bytes (the row statistics alone, no room for the fused backward's dQ
+    accumulator) runs the deterministic backward: its bits, exactly."""
+    from scaled_dot_product_06_gb300 import sdpa_bwd_varlen_workspace_size
+    c = VCase(4, (130, 1, 300, 77), (130, 1, 300, 77), 128, 128, causal=True)
+    x = make_packed_inputs(c.H, sum(c.lq), sum(c.lk), c.D_qk, c.D_v, c.dtype)
+    det = run_varlen(c, x, deterministic=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    sq = torch.tensor(seqstarts(c.lq), dtype=torch.int32, device="cuda")
+    mq, mk = c.maxes
+    small = sdpa_bwd_varlen_workspace_size(len(c.lq), c.H, sum(c.lq))
+    full = sdpa_bwd_varlen_workspace_size(len(c.lq), c.H, sum(c.lq), c.D_qk)
+    assert small < full
+    ws = torch.empty(small, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = sdpa_bwd_varlen(q, k, v, det[0], do, det[1], sq, sq, mq, mk, scale=c.sc,
+                                 is_causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert sdpa_device_error() == 0
+    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), det[2:]):
+        assert torch.equal(a, b), name
