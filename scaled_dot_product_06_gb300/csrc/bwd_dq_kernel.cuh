@@ -49,7 +49,15 @@ struct DqCfg {
   static constexpr int OFF_DO = OFF_Q + Q_BYTES;
   static constexpr int OFF_K = OFF_DO + DO_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
-  static constexpr int OFF_BAR = OFF_V + STAGES * V_BYTES;
+  // The bias tile of a key tile ([BM query rows][BN keys] fp32, four
+  // 32-key column blocks of BM 128-byte rows, 128-byte swizzle), loaded by
+  // TMA one tile ahead, where it fits beside the operands (d_qk = 64 and
+  // 192; at d_qk = 128 the two K/V stages leave no room and the bias is read
+  // from global memory).
+  static constexpr int BIAS_BYTES = BM * BN * 4;
+  static constexpr int OFF_BIAS = OFF_V + STAGES * V_BYTES;
+  static constexpr bool BIAS_TMA_OK = OFF_BIAS + BIAS_BYTES + 256 + 1024 <= 227 * 1024;
+  static constexpr int OFF_BAR = OFF_BIAS + (BIAS_TMA_OK ? BIAS_BYTES : 0);
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int THREADS = NCT + 64;  // + producer warp + MMA warp
   static constexpr uint32_t TMEM_COLS = 512;
@@ -76,7 +84,7 @@ struct DqCfg {
 
 enum : int { QB_Q = 0, QB_KF, QB_KE = QB_KF + 2, QB_VF = QB_KE + 2, QB_VE = QB_VF + 2,
              QB_S = QB_VE + 2, QB_SFREE, QB_DP, QB_DSL = QB_DP + 2, QB_DSH = QB_DSL + 2,
-             QB_DONE = QB_DSH + 2, QB_DRAIN, QB_OPS, QB_COUNT };
+             QB_DONE = QB_DSH + 2, QB_DRAIN, QB_OPS, QB_BF, QB_BE, QB_COUNT };
 
 // DROP, BIAS and WIN (a local window or the bottom-right alignment) are
 // template parameters so the kernel without them is compiled alone and stays
@@ -86,13 +94,17 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ CUtensorMap tmB, const BwdParams p) {
   using C = DqCfg<DQK, DV>;
   constexpr int BM = C::BM, BN = C::BN, CW = C::CW, ST = C::STAGES, NCT = C::NCT;
+  // the bias of each key tile by TMA into shared memory (see DqCfg::OFF_BIAS)
+  const bool bias_tma = BIAS && C::BIAS_TMA_OK && p.bias_tma != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
   const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+  const uint32_t sB = smem_u32(smem + C::OFF_BIAS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + QB_COUNT);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB_COUNT; ++i)
       mbar_init(bar(i), (i == QB_SFREE || i == QB_DSL || i == QB_DSL + 1 || i == QB_DSH ||
-                         i == QB_DSH + 1 || i == QB_OPS)
+                         i == QB_DSH + 1 || i == QB_OPS || i == QB_BE)
                             ? static_cast<uint32_t>(NCT)
                             : 1u);
     *abort_flag = 0u;
@@ -159,6 +171,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
+    if (bias_tma) tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
   __syncthreads();
@@ -168,7 +181,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
+    int issued = 0, bias_issued = 0;
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(QB_Q), C::Q_BYTES + C::DO_BYTES);
 #pragma unroll
@@ -179,6 +192,18 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     for (int j = 0; j < n_kv; ++j) {
       const int s = j % ST;
       const uint32_t ph = (j / ST) & 1;
+      // the tile's bias first, as soon as the compute threads have read the
+      // last tile's (early in that tile), so a whole tile hides its latency
+      if (bias_tma) {
+        if (!mbar_wait(bar(QB_BE), (j & 1) ^ 1, ec, kSiteBwdLoad, true, true)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(QB_BF), C::BIAS_BYTES);
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            tma_load_3d(sB + c * (BM * 128), &tmB, bar(QB_BF), (khi - j) * BN + 32 * c, q0, h);
+        }
+        bias_issued = j + 1;
+      }
       if (!mbar_wait(bar(QB_KE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(QB_KF + s), C::K_BYTES);
@@ -205,6 +230,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
         const int j = i >> 1, s = j % ST;
         mbar_wait(bar(((i & 1) ? QB_VF : QB_KF) + s), (j / ST) & 1, ec, kSiteDrain, false);
       }
+      // one bias tile at a time: only the last one can be in flight
+      if (bias_issued > 0) mbar_wait(bar(QB_BF), (bias_issued - 1) & 1, ec, kSiteDrain, false);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -385,9 +412,23 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)
       float pr[CW];
       if constexpr (BIAS) {
-        // this row's Bias for the thread's keys, loaded before the wait so its
-        // latency overlaps it (keys past S_kv or a missing row read 0)
-        if (bias_row != nullptr && bias_vec && kc0 + CW <= p.S_kv) {
+        // this row's Bias for the thread's keys (keys past S_kv or a missing
+        // row read 0): from the TMA tile in shared memory, block hf, the
+        // row's eight 16-byte chunks in their swizzled places; else loaded
+        // from global memory before the wait so its latency overlaps it
+        if (bias_tma) {
+          if (!(ok = mbar_wait(bar(QB_BF), j & 1, ec, kSiteBwdCompute))) break;
+          const uint32_t brow = sB + hf * (BM * 128) + row * 128;
+#pragma unroll
+          for (int c8 = 0; c8 < CW / 4; ++c8) {
+            const float4 v = lds128(brow + ((c8 ^ (row & 7)) << 4));
+            pr[4 * c8 + 0] = v.x;
+            pr[4 * c8 + 1] = v.y;
+            pr[4 * c8 + 2] = v.z;
+            pr[4 * c8 + 3] = v.w;
+          }
+          mbar_arrive(bar(QB_BE));
+        } else if (bias_row != nullptr && bias_vec && kc0 + CW <= p.S_kv) {
           const float4* b4 = reinterpret_cast<const float4*>(bias_row + kc0);
 #pragma unroll
           for (int i = 0; i < CW / 4; ++i) {
@@ -525,7 +566,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
 
 template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
+                            const CUtensorMap& dout, const CUtensorMap& bias_map, const BwdParams& p,
+                            cudaStream_t st) {
   using C = DqCfg<DQK, DV>;
   const bool bias = p.bias != nullptr;
   auto pick = [&](auto win) {
@@ -540,7 +582,7 @@ cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CU
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
   const long long grid = static_cast<long long>(n_qt) * p.B * p.H;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, p);
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, bias_map, p);
   return cudaGetLastError();
 }
 

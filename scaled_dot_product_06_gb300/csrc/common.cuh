@@ -301,6 +301,10 @@ struct BwdParams {
   // each dQ row has one contribution, which the drain writes to dq directly
   // (scaled, in the io dtype) with no accumulator and no convert pass
   int dq_direct;
+  // the dQ kernel's bias tiles come by TMA into shared memory (the map
+  // passed beside the operands' maps is valid): set where the bias is
+  // present, its row is a multiple of 16 bytes and the buffer fits
+  int bias_tma;
 };
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -486,10 +490,10 @@ cudaError_t launch_bwd_dkdv_fp16(int d_qk, int d_v, const CUtensorMap& q, const 
                                  const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
                                  cudaStream_t st);
 cudaError_t launch_bwd_dq_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias, const BwdParams& p,
                                cudaStream_t st);
 cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias, const BwdParams& p,
                                cudaStream_t st);
 cudaError_t launch_bwd_fused_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
                                   const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,

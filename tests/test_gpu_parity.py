@@ -49,6 +49,10 @@ CASES = [
     Case(1, 3, 200, 128, 64, 64, causal=True, p=0.1, dtype="fp16"),
     Case(2, 2, 256, 64, 128, 128, causal=True, bias=True),
     Case(1, 4, 130, 96, 128, 128, H_kv=2),
+    # a bias whose rows are not a multiple of 16 bytes: the deterministic dQ
+    # kernel reads it from global memory instead of by TMA
+    Case(1, 2, 130, 130, 192, 128, causal=True, bias=True),
+    Case(2, 1, 100, 70, 64, 64, bias=True, dtype="fp16"),
 ]
 
 
