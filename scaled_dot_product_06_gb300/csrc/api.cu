@@ -148,19 +148,22 @@ sdpa_status_t encode_map(CUtensorMap* m, CUtensorMapDataType type, int elem_byte
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Map over the fp32 bias [h][s_q][s_kv] for the dQ kernel's bias tiles: box
-// {32 keys, 128 query rows, 1 head} (128-byte rows, 128-byte swizzle),
-// out-of-range elements read as zero. Needs s_kv % 4 == 0 (row strides are
-// multiples of 16 bytes) and a 16-byte-aligned base.
-sdpa_status_t encode_bias_map(CUtensorMap* m, const float* bias, int64_t h, int64_t s_q, int64_t s_kv) {
+// Map over the fp32 bias [h][s_q][s_kv] for the backward kernels' bias
+// tiles, box {box_keys, box_rows, 1 head}: the dQ kernel's {32, 128} with
+// the 128-byte swizzle, the dK/dV kernel's {128, query tile rows} plain
+// row-major; out-of-range elements read as zero. Needs s_kv % 4 == 0 (row
+// strides are multiples of 16 bytes) and a 16-byte-aligned base.
+sdpa_status_t encode_bias_map(CUtensorMap* m, const float* bias, int64_t h, int64_t s_q, int64_t s_kv,
+                              uint32_t box_keys, uint32_t box_rows, bool swizzle) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   if (sdpa_status_t s = encoder(&enc)) return s;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(s_kv), static_cast<cuuint64_t>(s_q), static_cast<cuuint64_t>(h)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(s_kv * 4), static_cast<cuuint64_t>(s_kv * s_q * 4)};
-  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t box[3] = {box_keys, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(bias), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (bias) failed (CUresult %d)",
@@ -638,9 +641,18 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
     if (fused)
       e = bf16 ? launch_bwd_fused_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
                : launch_bwd_fused_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
-    else
-      e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
-               : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
+    else {
+      // the bias blocks by TMA where the kernel has room for them (d_qk 64
+      // and 192: query tiles of 128 and 64 rows) and the rows are 16-byte
+      // multiples; else the kernel reads them from global memory
+      CUtensorMap mb{};
+      p.bias_tma = 0;
+      if (bias != nullptr && d_qk != 128 && s_kv % 4 == 0 &&
+          encode_bias_map(&mb, bias, h, s_q, s_kv, 128, q_rows, false) == SDPA_OK)
+        p.bias_tma = 1;
+      e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, mb, p, st_dkdv)
+               : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, mb, p, st_dkdv);
+    }
     if (e != cudaSuccess) {
       join();
       return fail(SDPA_ERR_CUDA, "backward dK/dV kernel launch", e);
@@ -666,7 +678,8 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
     // from global memory
     CUtensorMap mb{};
     p.bias_tma = 0;
-    if (bias != nullptr && d_qk != 128 && s_kv % 4 == 0 && encode_bias_map(&mb, bias, h, s_q, s_kv) == SDPA_OK)
+    if (bias != nullptr && d_qk != 128 && s_kv % 4 == 0 &&
+        encode_bias_map(&mb, bias, h, s_q, s_kv, 32, 128, true) == SDPA_OK)
       p.bias_tma = 1;
     e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, mb, p, st)
              : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, mb, p, st);

@@ -70,7 +70,14 @@ struct DkdvCfg {
   static constexpr int OFF_DO = OFF_Q + STAGES * Q_BYTES;
   static constexpr int STAT_BYTES = 2 * BM * 4;       // -LSE log2e and D of BM query rows
   static constexpr int OFF_ROW = OFF_DO + STAGES * DO_BYTES;  // [STAGES] row statistics
-  static constexpr int OFF_BAR = OFF_ROW + STAGES * STAT_BYTES;
+  // The bias block of a query tile ([BM query rows][BN keys] fp32, row-major,
+  // so a warp's 32 keys of one query row are one 128-byte run), loaded by
+  // TMA one tile ahead, where it fits (d_qk = 64 and 192; at d_qk = 128 the
+  // bias is read from global memory).
+  static constexpr int BIAS_BYTES = BM * BN * 4;
+  static constexpr int OFF_BIAS = (OFF_ROW + STAGES * STAT_BYTES + 1023) & ~1023;
+  static constexpr bool BIAS_TMA_OK = OFF_BIAS + BIAS_BYTES + 256 + 1024 <= 227 * 1024;
+  static constexpr int OFF_BAR = BIAS_TMA_OK ? OFF_BIAS + BIAS_BYTES : OFF_ROW + STAGES * STAT_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr int THREADS = NCT + 64;            // + producer warp + MMA warp
   static constexpr uint32_t TMEM_COLS = 512;
@@ -86,7 +93,7 @@ struct DkdvCfg {
 };
 
 enum : int { AB_KV = 0, AB_QF, AB_DOF = AB_QF + 2, AB_QE = AB_DOF + 2, AB_S = AB_QE + 2, AB_SFREE,
-             AB_P, AB_DP, AB_DSL, AB_DSH, AB_DKDV, AB_DRAIN, AB_OPS, AB_COUNT };
+             AB_P, AB_DP, AB_DSL, AB_DSH, AB_DKDV, AB_DRAIN, AB_OPS, AB_BF, AB_BE, AB_COUNT };
 
 // Keep bits of key row k for the 32 query rows [row0, row0 + 32) of a tile.
 // One Philox block covers four consecutive keys of one query row, i.e. the
@@ -237,14 +244,18 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmdO, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ CUtensorMap tmB, const BwdParams p) {
   using C = DkdvCfg<DQK, DV>;
   constexpr int BM = C::BM, CW = C::CW, NCT = C::NCT;
+  // the bias of each query tile by TMA into shared memory (see DkdvCfg::OFF_BIAS)
+  const bool bias_tma = BIAS && C::BIAS_TMA_OK && p.bias_tma != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
   const uint32_t sQ = smem_u32(smem + C::OFF_Q), sdO = smem_u32(smem + C::OFF_DO);
   float* rowbuf = reinterpret_cast<float*>(smem + C::OFF_ROW);
+  const uint32_t sB = smem_u32(smem + C::OFF_BIAS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + AB_COUNT);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -299,7 +310,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < AB_COUNT; ++i)
-      mbar_init(bar(i), (i == AB_SFREE || i == AB_P || i == AB_DSL || i == AB_DSH || i == AB_OPS)
+      mbar_init(bar(i), (i == AB_SFREE || i == AB_P || i == AB_DSL || i == AB_DSH || i == AB_OPS ||
+                         i == AB_BE)
                             ? static_cast<uint32_t>(NCT)
                             : 1u);
     *abort_flag = 0u;
@@ -320,6 +332,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
+    if (bias_tma) tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
   __syncthreads();
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
+    int issued = 0, bias_issued = 0;
     if (n_it > 0) {
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(AB_KV), C::K_BYTES + C::V_BYTES);
@@ -343,8 +356,18 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
       for (int i = 0; i < n_it; ++i) {
         const int s = i & 1;
         const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) break;
         const int q0 = qtile0(i);
+        // the tile's bias first, as soon as the compute threads have read the
+        // last tile's (early in that tile), so a whole tile hides its latency
+        if (bias_tma) {
+          if (!mbar_wait(bar(AB_BE), (i & 1) ^ 1, ec, kSiteBwdLoad, true, true)) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(AB_BF), C::BIAS_BYTES);
+            tma_load_3d(sB, &tmB, bar(AB_BF), k0, q0, qhead(i));
+          }
+          bias_issued = i + 1;
+        }
+        if (!mbar_wait(bar(AB_QE + s), ph ^ 1, ec, kSiteBwdLoad, true, true)) break;
         const int zq = sl.zq0 + qhead(i);  // tensor-map z of the query head
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(AB_QF + s), C::Q_BYTES + C::STAT_BYTES);
@@ -369,6 +392,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         mbar_wait(bar(AB_QF + (i & 1)), ph, ec, kSiteDrain, false);
         mbar_wait(bar(AB_DOF + (i & 1)), ph, ec, kSiteDrain, false);
       }
+      // one bias block at a time: only the last one can be in flight
+      if (bias_issued > 0) mbar_wait(bar(AB_BF), (bias_issued - 1) & 1, ec, kSiteDrain, false);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -515,12 +540,25 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         // exponent in the log2 domain: S * scale * log2e - LSE * log2e (+ Bias * log2e)
         float pr[CW];
         if constexpr (BIAS) {
-          // Bias of this key and the thread's queries, loaded before the wait so
-          // its latency overlaps it (columns past S_q or a missing key read 0)
-          const float* bias_col = p.bias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + (kv_ok ? kv : 0);
-          const int lim = kv_ok ? min(CW, p.S_q - qc0) : 0;
+          // Bias of this key and the thread's queries (columns past S_q or a
+          // missing key read 0): from the TMA block in shared memory (query
+          // row 32 hf + c, key `row`: a warp reads 128 contiguous bytes a
+          // column), else loaded from global memory before the wait so its
+          // latency overlaps it
+          if (bias_tma) {
+            if (!(ok = mbar_wait(bar(AB_BF), i & 1, ec, kSiteBwdCompute))) break;
+            const float* bcol = reinterpret_cast<const float*>(smem + C::OFF_BIAS) + (CW * hf) * C::BN + row;
 #pragma unroll
-          for (int c = 0; c < CW; ++c) pr[c] = (c < lim) ? __ldg(bias_col + static_cast<size_t>(c) * p.S_kv) : 0.f;
+            for (int c = 0; c < CW; ++c) pr[c] = bcol[c * C::BN];
+            mbar_arrive(bar(AB_BE));
+          } else {
+            const float* bias_col =
+                p.bias + (static_cast<size_t>(h) * p.S_q + qc0) * p.S_kv + (kv_ok ? kv : 0);
+            const int lim = kv_ok ? min(CW, p.S_q - qc0) : 0;
+#pragma unroll
+            for (int c = 0; c < CW; ++c)
+              pr[c] = (c < lim) ? __ldg(bias_col + static_cast<size_t>(c) * p.S_kv) : 0.f;
+          }
         }
         if (!(ok = mbar_wait(bar(AB_S), i & 1, ec, kSiteBwdCompute))) break;
         // S^T(i) was issued after Q_i and the statistics landed; the wait on the
@@ -708,7 +746,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 
 template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                              const CUtensorMap& dout, const BwdParams& p, cudaStream_t st) {
+                              const CUtensorMap& dout, const CUtensorMap& bias_map, const BwdParams& p,
+                              cudaStream_t st) {
   using C = DkdvCfg<DQK, DV>;
   const bool bias = p.bias != nullptr;
   auto pick = [&](auto win, auto split) {
@@ -727,7 +766,7 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(n_kt) * p.B * p.H_kv * p.kv_split;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, p);
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, bias_map, p);
   return cudaGetLastError();
 }
 
