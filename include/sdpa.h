@@ -144,9 +144,11 @@ sdpa_status_t sdpa_bwd(int64_t b, int64_t h, int64_t s_q, int64_t s_kv, int64_t 
 /* Phases of the backward pass, in the order they must run, and the flag that
  * selects the deterministic backward. */
 typedef enum {
-  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O) and -LSE*log2e; zero dBias (and dQacc) */
-  SDPA_BWD_DKDV = 2,       /* key/value-stationary kernel: dK, dV, dBias (and dQacc, or
-                              dQ itself where each dQ row has one key tile) */
+  SDPA_BWD_PREPROCESS = 1, /* D = rowsum(dO * O) and -LSE*log2e; zero dQacc (and dBias,
+                              for the fused backward) */
+  SDPA_BWD_DKDV = 2,       /* key/value-stationary kernel: dK, dV, dBias (the deterministic
+                              backward zeroes dBias first) (and dQacc, or dQ itself where
+                              each dQ row has one key tile) */
   SDPA_BWD_DQ = 4,         /* dQ: convert dQacc (nothing left to do when the fused
                               kernel wrote dQ), or the query-stationary kernel */
   SDPA_BWD_ALL = 7,

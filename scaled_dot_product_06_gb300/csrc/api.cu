@@ -604,7 +604,10 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
 
   cudaError_t e = cudaSuccess;
   if (phases & SDPA_BWD_PREPROCESS) {
-    const int64_t dbias_elems = bias ? h * s_q * s_kv : 0;
+    // dBias is zeroed here for the fused backward; the deterministic one zeroes
+    // it in its dK/dV phase, on the dK/dV kernel's stream, so that the zero
+    // pass runs beside the dQ kernel instead of ahead of both
+    const int64_t dbias_elems = (bias && fused) ? h * s_q * s_kv : 0;
     e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, rw.zq, static_cast<int>(s_q), p.S_pad, p.rows_q,
                        pk.seqstart_q, static_cast<int>(b), dvi, dbias_elems, p.dkdv_count, n_counters,
                        p.dq_acc, dq_acc_elems, st);
@@ -642,6 +645,14 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
       e = bf16 ? launch_bwd_fused_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
                : launch_bwd_fused_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
     else {
+      if (bias != nullptr) {  // dBias = 0 ahead of the kernel's fp32 reductions into it
+        e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, 0, static_cast<int>(s_q), p.S_pad, p.rows_q,
+                           nullptr, static_cast<int>(b), dvi, h * s_q * s_kv, nullptr, 0, nullptr, 0, st_dkdv);
+        if (e != cudaSuccess) {
+          join();
+          return fail(SDPA_ERR_CUDA, "backward dBias zero pass launch", e);
+        }
+      }
       // the bias blocks by TMA where the kernel has room for them (d_qk 64
       // and 192: query tiles of 128 and 64 rows) and the rows are 16-byte
       // multiples; else the kernel reads them from global memory
