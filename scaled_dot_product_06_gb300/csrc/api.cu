@@ -641,10 +641,19 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
       join();
       return ms;
     }
-    if (fused)
-      e = bf16 ? launch_bwd_fused_bf16(di, dvi, mq, mk, mv, mdo, p, st_dkdv)
-               : launch_bwd_fused_fp16(di, dvi, mq, mk, mv, mdo, p, st_dkdv);
-    else {
+    if (fused) {
+      // dK and dV leave the fused kernel by TMA stores, through maps of K's
+      // and V's geometry
+      CUtensorMap mdk, mdv;
+      ms = make_map(&mdk, tt, 2, dk, d_qk, rw.k, rw.zk, 128, true);
+      if (!ms) ms = make_map(&mdv, tt, 2, dv, d_v, rw.k, rw.zk, 128, true);
+      if (ms) {
+        join();
+        return ms;
+      }
+      e = bf16 ? launch_bwd_fused_bf16(di, dvi, mq, mk, mv, mdo, mdk, mdv, p, st_dkdv)
+               : launch_bwd_fused_fp16(di, dvi, mq, mk, mv, mdo, mdk, mdv, p, st_dkdv);
+    } else {
       if (bias != nullptr) {  // dBias = 0 ahead of the kernel's fp32 reductions into it
         e = launch_bwd_pre(bf16, o, dout, lse, stats, dbias, 0, static_cast<int>(s_q), p.S_pad, p.rows_q,
                            nullptr, static_cast<int>(b), dvi, h * s_q * s_kv, nullptr, 0, nullptr, 0, st_dkdv);

@@ -496,11 +496,11 @@ cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CU
                                const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias, const BwdParams& p,
                                cudaStream_t st);
 cudaError_t launch_bwd_fused_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                                  const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
-                                  cudaStream_t st);
+                                  const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dk,
+                                  const CUtensorMap& dv, const BwdParams& p, cudaStream_t st);
 cudaError_t launch_bwd_fused_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                                  const CUtensorMap& v, const CUtensorMap& dout, const BwdParams& p,
-                                  cudaStream_t st);
+                                  const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dk,
+                                  const CUtensorMap& dv, const BwdParams& p, cudaStream_t st);
 cudaError_t launch_bwd_pre(bool bf16, const void* o, const void* dout, const float* lse, float* stats,
                            float* dbias, int64_t z_count, int s_q, int s_pad, int rows,
                            const int* seqstart, int n_seq, int d_v, int64_t dbias_elems,
