@@ -637,20 +637,16 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
     if (!ms) ms = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true);
     if (!ms) ms = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true);
     if (!ms) ms = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, q_rows, true);
+    // dK and dV leave either kernel by TMA stores, through maps of K's and
+    // V's geometry
+    CUtensorMap mdk, mdv;
+    if (!ms) ms = make_map(&mdk, tt, 2, dk, d_qk, rw.k, rw.zk, 128, true);
+    if (!ms) ms = make_map(&mdv, tt, 2, dv, d_v, rw.k, rw.zk, 128, true);
     if (ms) {
       join();
       return ms;
     }
     if (fused) {
-      // dK and dV leave the fused kernel by TMA stores, through maps of K's
-      // and V's geometry
-      CUtensorMap mdk, mdv;
-      ms = make_map(&mdk, tt, 2, dk, d_qk, rw.k, rw.zk, 128, true);
-      if (!ms) ms = make_map(&mdv, tt, 2, dv, d_v, rw.k, rw.zk, 128, true);
-      if (ms) {
-        join();
-        return ms;
-      }
       e = bf16 ? launch_bwd_fused_bf16(di, dvi, mq, mk, mv, mdo, mdk, mdv, p, st_dkdv)
                : launch_bwd_fused_fp16(di, dvi, mq, mk, mv, mdo, mdk, mdv, p, st_dkdv);
     } else {
@@ -670,8 +666,8 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
       if (bias != nullptr && d_qk != 128 && s_kv % 4 == 0 &&
           encode_bias_map(&mb, bias, h, s_q, s_kv, 128, q_rows, false) == SDPA_OK)
         p.bias_tma = 1;
-      e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, mb, p, st_dkdv)
-               : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, mb, p, st_dkdv);
+      e = bf16 ? launch_bwd_dkdv_bf16(di, dvi, mq, mk, mv, mdo, mb, mdk, mdv, p, st_dkdv)
+               : launch_bwd_dkdv_fp16(di, dvi, mq, mk, mv, mdo, mb, mdk, mdv, p, st_dkdv);
     }
     if (e != cudaSuccess) {
       join();

@@ -5,10 +5,11 @@ namespace sdpa {
 
 cudaError_t launch_bwd_dkdv_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
                                const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias,
-                               const BwdParams& p, cudaStream_t st) {
-  if (d_qk == 64 && d_v == 64) return launch_bwd_dkdv_t<64, 64, true>(q, k, v, dout, bias, p, st);
-  if (d_qk == 128 && d_v == 128) return launch_bwd_dkdv_t<128, 128, true>(q, k, v, dout, bias, p, st);
-  if (d_qk == 192 && d_v == 128) return launch_bwd_dkdv_t<192, 128, true>(q, k, v, dout, bias, p, st);
+                               const CUtensorMap& dk, const CUtensorMap& dv, const BwdParams& p,
+                               cudaStream_t st) {
+  if (d_qk == 64 && d_v == 64) return launch_bwd_dkdv_t<64, 64, true>(q, k, v, dout, bias, dk, dv, p, st);
+  if (d_qk == 128 && d_v == 128) return launch_bwd_dkdv_t<128, 128, true>(q, k, v, dout, bias, dk, dv, p, st);
+  if (d_qk == 192 && d_v == 128) return launch_bwd_dkdv_t<192, 128, true>(q, k, v, dout, bias, dk, dv, p, st);
   return cudaErrorInvalidValue;
 }
 

@@ -245,7 +245,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmdO,
-                         const __grid_constant__ CUtensorMap tmB, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmdK,
+                         const __grid_constant__ CUtensorMap tmdV, const BwdParams p) {
   using C = DkdvCfg<DQK, DV>;
   constexpr int BM = C::BM, CW = C::CW, NCT = C::NCT;
   // the bias of each query tile by TMA into shared memory (see DkdvCfg::OFF_BIAS)
@@ -267,7 +269,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
   // key tile index and split of this CTA for a split epilogue, set at start-up
   // (kept out of the registers of the compute loop)
   int* split_tile = reinterpret_cast<int*>(bars + AB_COUNT + 4);
-  static_assert((AB_COUNT + 5) * 8 <= 256, "barrier region");
+  // the TMA stores of dK and dV: {key row of the tile in its tensor-map
+  // plane, plane, staged (1) or written row by row (0)}
+  int* out_slot = reinterpret_cast<int*>(bars + AB_COUNT + 5);
+  static_assert((AB_COUNT + 7) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -321,6 +326,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
       split_tile[1] = sp;
     }
     if (WIN) *band_slot = bd;
+    out_slot[0] = sl.row_k + k0;
+    out_slot[1] = zk;
+    out_slot[2] = !SPLIT && (p.seqstart_k == nullptr || k0 + C::BN <= S_kv);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -333,6 +341,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
     if (bias_tma) tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmdK);
+    tma_prefetch_desc(&tmdV);
   }
   tc_fence_before();
   __syncthreads();
@@ -692,11 +702,66 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
         mbar_arrive(bar(AB_DSH));
       }
     }
-    // ---- epilogue: warps 0-3 write dV, warps 4-7 write dK * scale (zeros for
-    // a key tile that no query sees)
+    // ---- epilogue: dV and dK * scale (zeros for a key tile that no query
+    // sees). Whole tiles, and the ragged last tile of an unpacked tensor (the
+    // tensor maps drop its rows past the end), are staged in shared memory
+    // and stored by TMA; a packed sequence's ragged tile is written row by
+    // row, so that it stops at the sequence's end.
     const bool have = n_it > 0;
     const bool ready = have && ok && mbar_wait(bar(AB_DKDV), 0, ec, kSiteBwdCompute);
-    if (SPLIT && have) {
+    if (!SPLIT && out_slot[2]) {
+      // [dV | dK] lie side by side in tensor memory: column group hf takes its
+      // 32-column chunks hf, hf + NQ, ... into 64-column boxes (dV's first)
+      // with the 128-byte swizzle, in the Q / dO stages, idle once dK and dV
+      // are complete
+      constexpr int NCH = (DV + DQK) / 32;
+      static_assert(NCH % C::NQ == 0 && DV % 64 == 0 && DQK % 64 == 0 &&
+                        C::STAGES * (C::Q_BYTES + C::DO_BYTES) >= C::BN * (DV + DQK) * 2,
+                    "staging of dK and dV");
+      const bool write = !have || ready;
+      if (ready) tc_fence_after();
+      if (write) {
+#pragma unroll 1
+        for (int j = 0; j < NCH / C::NQ; ++j) {
+          const int c = hf + C::NQ * j;
+          const float mul = c * 32 < DV ? 1.0f : p.scale;
+          const uint32_t dst = sQ + (c >> 1) * (C::BN * 128) + row * 128;
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {  // 16 columns: two 16-byte chunks
+            uint32_t a[16];
+            if (ready) {
+              tmem_ld16(tbase + C::T_DV + lane_off + c * 32 + hc * 16, a);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) a[e] = 0u;
+            }
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               dst + ((static_cast<uint32_t>(4 * (c & 1) + 2 * hc + e) ^ (row & 7)) << 4)),
+                           "r"(pk[4 * e]), "r"(pk[4 * e + 1]), "r"(pk[4 * e + 2]), "r"(pk[4 * e + 3])
+                           : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      // stored only when every compute thread wrote its share
+      if (named_bar_and(2, NCT, write) && threadIdx.x == 0) {
+        const int r0 = out_slot[0], z = out_slot[1];
+#pragma unroll
+        for (int bx = 0; bx < DV / 64; ++bx) tma_store_3d(&tmdV, sQ + bx * (C::BN * 128), bx * 64, r0, z);
+#pragma unroll
+        for (int bx = 0; bx < DQK / 64; ++bx)
+          tma_store_3d(&tmdK, sQ + (DV / 64 + bx) * (C::BN * 128), bx * 64, r0, z);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the boxes leave shared memory before the CTA does
+      }
+    } else if (SPLIT && have) {
       if (ready) tc_fence_after();
       split_epilogue<C, BF16>(p.dkdv_part, p.dkdv_count, nsp, split_tile[0], split_tile[1], ready,
                               kv_ok, row, hf, tbase + lane_off, *key_row0 + row, p.scale, p.dv,
@@ -746,8 +811,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1)
 
 template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                              const CUtensorMap& dout, const CUtensorMap& bias_map, const BwdParams& p,
-                              cudaStream_t st) {
+                              const CUtensorMap& dout, const CUtensorMap& bias_map, const CUtensorMap& dk,
+                              const CUtensorMap& dv, const BwdParams& p, cudaStream_t st) {
   using C = DkdvCfg<DQK, DV>;
   const bool bias = p.bias != nullptr;
   auto pick = [&](auto win, auto split) {
@@ -766,7 +831,7 @@ cudaError_t launch_bwd_dkdv_t(const CUtensorMap& q, const CUtensorMap& k, const 
   if (e != cudaSuccess) return e;
   const int n_kt = (p.S_kv + C::BN - 1) / C::BN;
   const long long grid = static_cast<long long>(n_kt) * p.B * p.H_kv * p.kv_split;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, bias_map, p);
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, bias_map, dk, dv, p);
   return cudaGetLastError();
 }
 
