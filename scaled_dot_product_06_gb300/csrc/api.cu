@@ -685,6 +685,8 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
     if (!ms) ms = make_map(&mk, tt, 2, k, d_qk, rw.k, rw.zk, 128, true);
     if (!ms) ms = make_map(&mv, tt, 2, v, d_v, rw.k, rw.zk, 128, true);
     if (!ms) ms = make_map(&mdo, tt, 2, dout, d_v, rw.q, rw.zq, 128, true);
+    CUtensorMap mdq;  // dQ leaves the kernel by TMA stores, through a map of Q's geometry
+    if (!ms) ms = make_map(&mdq, tt, 2, dq, d_qk, rw.q, rw.zq, 128, true);
     if (ms) {
       join();
       return ms;
@@ -697,8 +699,8 @@ sdpa_status_t bwd_impl(int phases, int64_t b, int64_t h, int64_t h_kv, int64_t s
     if (bias != nullptr && d_qk != 128 && s_kv % 4 == 0 &&
         encode_bias_map(&mb, bias, h, s_q, s_kv, 32, 128, true) == SDPA_OK)
       p.bias_tma = 1;
-    e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, mb, p, st)
-             : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, mb, p, st);
+    e = bf16 ? launch_bwd_dq_bf16(di, dvi, mq, mk, mv, mdo, mb, mdq, p, st)
+             : launch_bwd_dq_fp16(di, dvi, mq, mk, mv, mdo, mb, mdq, p, st);
     if (e != cudaSuccess) {
       join();
       return fail(SDPA_ERR_CUDA, "backward dQ kernel launch", e);

@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmdO,
-                       const __grid_constant__ CUtensorMap tmB, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
   using C = DqCfg<DQK, DV>;
   constexpr int BM = C::BM, BN = C::BN, CW = C::CW, ST = C::STAGES, NCT = C::NCT;
   // the bias of each key tile by TMA into shared memory (see DqCfg::OFF_BIAS)
@@ -109,7 +110,10 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + QB_COUNT);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   Band* band_slot = reinterpret_cast<Band*>(bars + QB_COUNT + 1);  // see lds_band
-  static_assert((QB_COUNT + 2) * 8 <= 256, "barrier region");
+  // the TMA store of dQ: {query row of the tile in its tensor-map plane,
+  // plane, staged (1) or written row by row (0)}
+  int* out_slot = reinterpret_cast<int*>(bars + QB_COUNT + 2);
+  static_assert((QB_COUNT + 4) * 8 <= 256, "barrier region");
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,6 +164,9 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
                             : 1u);
     *abort_flag = 0u;
     if (WIN) *band_slot = bd;
+    out_slot[0] = sl.row_q + q0;
+    out_slot[1] = zq;
+    out_slot[2] = p.seqstart_q == nullptr || q0 + BM <= S_q;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -172,6 +179,7 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmdO);
     if (bias_tma) tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmdQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -532,8 +540,49 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(QB_DSH + b));
     }
-    // ---- epilogue: dQ * scale; the first two groups write half of the columns each
-    if (hf < 2 && ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute)) {
+    // ---- epilogue: dQ * scale. A tile whose rows all lie in its sequence,
+    // or any tile of an unpacked tensor (the tensor map drops its rows past
+    // the end), is staged in Q's shared memory (idle once dQ is complete) as
+    // 64-column boxes with the 128-byte swizzle, each column group taking
+    // every fourth 32-column chunk, and stored by TMA; a packed sequence's
+    // ragged tile is written row by row, so that it stops at the sequence's
+    // end.
+    if (out_slot[2]) {
+      const bool ready = ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute);
+      if (ready) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = hf; c < DQK / 32; c += C::NQ) {
+          const uint32_t dst = sQ + (c >> 1) * (BM * 128) + row * 128;
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {  // 16 columns: two 16-byte chunks
+            uint32_t a[16];
+            tmem_ld16(tbase + C::T_DQ + lane_off + c * 32 + hc * 16, a);
+            tmem_wait_ld();
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk[e] = pack2<BF16>(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               dst + ((static_cast<uint32_t>(4 * (c & 1) + 2 * hc + e) ^ (row & 7)) << 4)),
+                           "r"(pk[4 * e]), "r"(pk[4 * e + 1]), "r"(pk[4 * e + 2]), "r"(pk[4 * e + 3])
+                           : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      // stored only when every compute thread wrote its share
+      if (named_bar_and(1, NCT, ready) && threadIdx.x == 0) {
+        const int r0 = out_slot[0], z = out_slot[1];
+#pragma unroll
+        for (int bx = 0; bx < DQK / 64; ++bx) tma_store_3d(&tmdQ, sQ + bx * (BM * 128), bx * 64, r0, z);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the boxes leave shared memory before the CTA does
+      }
+    } else if (hf < 2 && ok && mbar_wait(bar(QB_DONE), 0, ec, kSiteBwdCompute)) {
+      // the first two groups write half of the columns each
       tc_fence_after();
       constexpr int HW = DQK / 2;  // columns per thread
       uint8_t* dst_row = static_cast<uint8_t*>(p.dq) + ridx * DQK * 2 + hf * HW * 2;
@@ -566,8 +615,8 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV>::THREADS, 1)
 
 template <int DQK, int DV, bool BF16>
 cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& dout, const CUtensorMap& bias_map, const BwdParams& p,
-                            cudaStream_t st) {
+                            const CUtensorMap& dout, const CUtensorMap& bias_map, const CUtensorMap& dq,
+                            const BwdParams& p, cudaStream_t st) {
   using C = DqCfg<DQK, DV>;
   const bool bias = p.bias != nullptr;
   auto pick = [&](auto win) {
@@ -582,7 +631,7 @@ cudaError_t launch_bwd_dq_t(const CUtensorMap& q, const CUtensorMap& k, const CU
   if (e != cudaSuccess) return e;
   const int n_qt = (p.S_q + C::BM - 1) / C::BM;
   const long long grid = static_cast<long long>(n_qt) * p.B * p.H;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, bias_map, p);
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, st>>>(q, k, v, dout, bias_map, dq, p);
   return cudaGetLastError();
 }
 

@@ -492,10 +492,12 @@ cudaError_t launch_bwd_dkdv_fp16(int d_qk, int d_v, const CUtensorMap& q, const 
                                  const CUtensorMap& dk, const CUtensorMap& dv, const BwdParams& p,
                                  cudaStream_t st);
 cudaError_t launch_bwd_dq_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias, const BwdParams& p,
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias,
+                               const CUtensorMap& dq, const BwdParams& p,
                                cudaStream_t st);
 cudaError_t launch_bwd_dq_fp16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
-                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias, const BwdParams& p,
+                               const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& bias,
+                               const CUtensorMap& dq, const BwdParams& p,
                                cudaStream_t st);
 cudaError_t launch_bwd_fused_bf16(int d_qk, int d_v, const CUtensorMap& q, const CUtensorMap& k,
                                   const CUtensorMap& v, const CUtensorMap& dout, const CUtensorMap& dk,
