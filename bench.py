@@ -785,6 +785,12 @@ def main():
                 "bytes_per_launch": kbytes[dom]}
     if bound != "tensor":
         roof["tensor_frac"] = (kernel_flops.get(dom, 0.0) / sec / 1e12) / peak
+    if dom == "bwd_dkdv" and w["bias"]:
+        # the deterministic backward zeroes dBias inside its dK/dV phase, on
+        # the kernel's stream right before it (so that the pass overlaps the
+        # dQ kernel); the events around the phase hold both launches
+        roof["span"] = ("the dK/dV phase: the dBias zero pass, then the dK/dV kernel, on one stream; "
+                        "achieved and frac are lower bounds for the kernel alone")
 
     # End to end through the public API (sdpa_fwd + sdpa_bwd, or their packed
     # forms: the calls a user makes) with pinned host buffers: every step uploads its inputs and reads
