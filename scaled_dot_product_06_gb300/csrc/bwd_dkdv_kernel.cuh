@@ -44,6 +44,8 @@
 //              dP^T(i+1).
 // Tensor memory (512 columns): S^T [0,BM), dP^T [BM,2BM), dV [2BM,2BM+Dv),
 // dK [2BM+Dv, 2BM+Dv+Dk), then K and V (two elements per column) if they fit.
+// At the end the compute warps stage dV and dK in the Q / dO stages, idle by
+// then, and one thread stores them by TMA.
 #pragma once
 #include <type_traits>
 

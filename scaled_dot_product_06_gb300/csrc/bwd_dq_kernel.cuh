@@ -27,6 +27,8 @@
 // then Q and dO (two elements per column) when they fit (d_qk <= 128): the S
 // and dP products then take A from TMEM and read only K_j / V_j from shared
 // memory, which keeps the tensor core within the shared-memory read rate.
+// At the end the compute warps stage dQ in Q's shared memory, idle by then,
+// and one thread stores it by TMA.
 #pragma once
 #include <type_traits>
 

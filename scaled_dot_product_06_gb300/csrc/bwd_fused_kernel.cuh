@@ -61,7 +61,8 @@
 //   40; in the split instances 72 and 24, with the descriptors held.
 // Tensor memory (512 columns): S^T / dP^T / P~^T [0,128), dQ_i [128,128+Dk),
 // dV [128+Dk, 128+Dk+Dv), dK after it, then K and V (two elements per column)
-// when they fit (d = 64).
+// when they fit (d = 64). At the end the compute warps stage dV and dK in the
+// Q / dO stages, idle by then, and one thread stores them by TMA.
 #pragma once
 #include <type_traits>
 
